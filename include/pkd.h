@@ -1,0 +1,245 @@
+/*
+ * pkd.h -- batched paged-KV decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libpkd.so.  Every argument is a plain host value or pointer; device
+ * buffers are raw device addresses; a stream is a cudaStream_t passed as
+ * `void*` (NULL = the legacy default stream).  No call throws or aborts: each
+ * returns a pkd_status, and pkd_last_error() gives the calling thread's last
+ * message.
+ *
+ * Problem statement (FlashInfer pages):
+ *   - plan/run split of the batched decode wrapper: plan takes the page table
+ *     and the static geometry and runs on the host before CUDA-graph capture;
+ *     run takes q and the paged K/V (aquanode.io 2026 guide, "Quickstart",
+ *     paragraph on BatchDecodeWithPagedKVCacheWrapper; snackonai.com deep dive,
+ *     "The Code, Annotated", snippet one, and "It In Action", step 1);
+ *   - the KV pool: fixed-size pages in the NHD layout
+ *     [num_pages, page_size, num_kv_heads, head_dim], a request's pages named by
+ *     a CSR table (kv_indptr, kv_page_indices, kv_last_page_len) (deep dive,
+ *     snippet one; 2026 guide, "What FlashInfer is", idea 1 "block-sparse KV
+ *     cache format");
+ *   - merge_state / merge_states and cascade (shared-prefix) decode
+ *     (2026 guide, "Cascade attention for shared prefixes");
+ *   - single-request decode with contiguous K/V (ai-tldr.dev tool card,
+ *     "Getting started", step 4).
+ *
+ * Conventions shared by all calls:
+ *   - head_dim must be 128.  num_qo_heads must be a multiple of num_kv_heads,
+ *     with a group size g = num_qo_heads / num_kv_heads of at most 8; qo head h
+ *     reads kv head h / g.
+ *   - q is [batch, num_qo_heads, head_dim], contiguous.  out has q's shape and
+ *     dtype; lse is fp32 [batch, num_qo_heads], the natural-log log-sum-exp of
+ *     the scaled scores sm_scale * <q, k>.  An empty request gives out = 0 and
+ *     lse = -inf.
+ *   - sm_scale <= 0 selects 1/sqrt(head_dim).
+ *   - Supported (q, kv) dtypes: (F16, F16), (BF16, BF16), (BF16, E4M3),
+ *     (F16, E4M3).  An E4M3 cache takes one fp32 scale per kv head for K and for
+ *     V (k_scale, v_scale: device arrays [num_kv_heads]); the attended values are
+ *     code * scale.
+ *   - Device pointers handed to run / cascade_decode must stay valid until the
+ *     work on the stream has finished.  Base addresses of q, the caches, out,
+ *     and page_stride_elems * element size must be 16-byte multiples.
+ */
+#ifndef PKD_H
+#define PKD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkd_status {
+  PKD_OK = 0,
+  PKD_ERR_INVALID_ARG = 1,         /* a NULL, negative or inconsistent argument */
+  PKD_ERR_UNSUPPORTED = 2,         /* head_dim, group size, dtype pair or page size not built */
+  PKD_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below pkd_workspace_bytes(...) */
+  PKD_ERR_CAPACITY_EXCEEDED = 4,   /* batch above the plan's max_batch, or prefix splits above max */
+  PKD_ERR_CUDA = 5,                /* a CUDA runtime or driver call failed (message has the name) */
+  PKD_ERR_DEVICE_CHECK = 6,        /* a kernel recorded an error (see pkd_check_device_errors) */
+  PKD_ERR_NO_PLAN = 7              /* run / cascade_decode before a successful pkd_plan */
+} pkd_status;
+
+typedef enum pkd_dtype {
+  PKD_F16 = 0,
+  PKD_BF16 = 1,
+  PKD_E4M3 = 2, /* OCP FP8 E4M3 ("fn"), KV cache only */
+  PKD_F32 = 3   /* merge_state / merge_states values only */
+} pkd_dtype;
+
+/* Device error bits recorded by the kernels (pkd_check_device_errors). */
+#define PKD_DEVERR_PAGE_INDEX 1u    /* a page index outside [0, num_pages): page 0 was read instead */
+#define PKD_DEVERR_WAIT_TIMEOUT 2u  /* a pipeline wait gave up after ~2 s; outputs are invalid */
+
+/* Opaque plan: host-side state plus views into the caller's device workspace. */
+typedef struct pkd_plan_s* pkd_plan_t;
+
+/* Library version string, e.g. "pkd 0.1.0 sm_103a". */
+const char* pkd_version(void);
+
+/* Static text for a status code. */
+const char* pkd_status_string(int status);
+
+/* The calling thread's last error message ("" if none).  Valid until the next
+ * failing call on this thread. */
+const char* pkd_last_error(void);
+
+/*
+ * Number of CTAs of the decode launch on `device` (a fixed multiple of its SM
+ * count).  The plan partitions work over exactly this many CTAs.  Needs a GPU.
+ */
+pkd_status pkd_num_ctas(int device, int* num_ctas_out);
+
+/*
+ * Bytes of device workspace a plan with these limits needs.  Pure host
+ * arithmetic (no GPU needed).  num_ctas: the value pkd_num_ctas returns for
+ * the device the plan will run on.  max_prefix_splits: how many pieces
+ * pkd_cascade_decode may split the shared prefix into (0 = no cascade; the
+ * library uses at most 16).  Returns 0 for invalid arguments.
+ */
+size_t pkd_workspace_bytes(int max_batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                           int num_ctas, int max_prefix_splits);
+
+/*
+ * Create a plan object.  d_workspace (device, caller-owned, >= the size above,
+ * 256-byte aligned) holds the schedule, split-KV partial results and cascade
+ * prefix partials; it must outlive the plan and must not be shared by two
+ * plans whose work can overlap on the GPU.  Host-only: no device call is made.
+ */
+pkd_status pkd_plan_create(pkd_plan_t* plan_out, int max_batch, int num_qo_heads,
+                           int num_kv_heads, int head_dim, int num_ctas, int max_prefix_splits,
+                           void* d_workspace, size_t workspace_bytes);
+
+/* Free the host-side plan object (the workspace stays the caller's). */
+pkd_status pkd_plan_destroy(pkd_plan_t plan);
+
+/*
+ * Plan one decode step (the host "plan" of the pages' plan/run split).
+ *   h_kv_indptr        host int32 [batch + 1]: kv_indptr[0] = 0, non-decreasing;
+ *                      request b owns kv_page_indices[kv_indptr[b] .. kv_indptr[b+1]).
+ *   d_kv_page_indices  device int32 [kv_indptr[batch]]: physical page ids.
+ *                      Borrowed: it must hold the same contents at every
+ *                      pkd_run / pkd_cascade_decode until the next pkd_plan.
+ *   h_kv_last_page_len host int32 [batch]: valid tokens in each request's last
+ *                      page, 1..page_size (ignored for a request with no page).
+ *   page_size          tokens per page: 1..64, or a multiple of 64.
+ * The split-KV rule: each (request, kv head) row is cut into chunks of up to 64
+ * keys (whole pages for page_size <= 64); the list of all chunks, rows in
+ * order r = b * num_kv_heads + h, is divided into num_ctas equal contiguous
+ * runs of ceil(total / num_ctas) chunks, one per CTA.  A row that falls to one
+ * CTA is written directly; rows split across CTAs are merged by a second pass.
+ * The schedule is copied into the workspace with one cudaMemcpyAsync from
+ * pageable host memory on `stream`, so plan must not be called during stream
+ * capture; the launch shape of run never changes, so a graph captured around
+ * run stays valid across re-plans of the same plan object.
+ */
+pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* d_kv_page_indices,
+                    const int32_t* h_kv_last_page_len, int batch, int num_qo_heads,
+                    int num_kv_heads, int head_dim, int page_size, int q_dtype, int kv_dtype,
+                    void* stream);
+
+/*
+ * Run batched paged decode with the last plan: (out, lse) for every request
+ * and qo head.
+ *   d_q        [batch, num_qo_heads, 128] in the planned q dtype.
+ *   d_k_cache, d_v_cache  the K and V pools: page p, slot t, kv head h, dim d at
+ *              element p * page_stride_elems + (t * num_kv_heads + h) * 128 + d.
+ *              page_stride_elems = page_size * num_kv_heads * 128 for separate
+ *              pools, 2 * that for one interleaved [pages, 2, P, Hk, D] pool
+ *              (then d_v_cache = d_k_cache + page_size * num_kv_heads * 128).
+ *   num_pages  pages in each pool; page ids must lie in [0, num_pages).
+ *   d_k_scale, d_v_scale  fp32 [num_kv_heads] for an E4M3 cache, else NULL.
+ *   d_out      [batch, num_qo_heads, 128] q dtype;  d_lse fp32 [batch, num_qo_heads] or NULL.
+ * Enqueues two kernels on `stream` (decode, then the split-KV merge) with a
+ * grid that depends only on the plan object; no allocation, no host sync:
+ * capturable in a CUDA graph.
+ */
+pkd_status pkd_run(pkd_plan_t plan, const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                   int64_t num_pages, int64_t page_stride_elems, const float* d_k_scale,
+                   const float* d_v_scale, float sm_scale, void* d_out, float* d_lse, void* stream);
+
+/*
+ * Cascade (shared-prefix) decode: every request attends one shared prefix page
+ * list and its own pages (the last plan's table, which holds only the private
+ * suffixes); the two attention states are merged per (request, qo head).
+ *   d_prefix_page_indices  device int32 [prefix_num_pages] (prefix_num_pages >= 0).
+ *   prefix_last_page_len   valid tokens in the prefix's last page (1..page_size).
+ * The prefix is attended once per kv head for all requests (a dense
+ * [batch * g, 128] x [128, prefix_len] product on the tensor cores), not once
+ * per request.  Other arguments as pkd_run.  The plan must have been created
+ * with max_prefix_splits >= 1.  Capturable like pkd_run.
+ */
+pkd_status pkd_cascade_decode(pkd_plan_t suffix_plan, const int32_t* d_prefix_page_indices,
+                              int prefix_num_pages, int prefix_last_page_len, const void* d_q,
+                              const void* d_k_cache, const void* d_v_cache, int64_t num_pages,
+                              int64_t page_stride_elems, const float* d_k_scale,
+                              const float* d_v_scale, float sm_scale, void* d_out, float* d_lse,
+                              void* stream);
+
+/*
+ * Single-request decode with contiguous K/V (the quickstart call):
+ *   d_q [num_qo_heads, 128]; d_k, d_v [kv_len, num_kv_heads, 128] (kv_len >= 0);
+ *   d_out [num_qo_heads, 128] (q dtype); d_lse fp32 [num_qo_heads] or NULL.
+ *   q_dtype / kv_dtype as for pkd_plan; d_k_scale / d_v_scale for E4M3.
+ * Plans internally (one cudaMemcpyAsync of the schedule into d_workspace, so not
+ * capturable) and runs the batched path on it.  d_workspace must hold
+ * pkd_workspace_bytes(1, num_qo_heads, num_kv_heads, 128, num_ctas, 0) bytes.
+ */
+pkd_status pkd_single_decode(const void* d_q, const void* d_k, const void* d_v, int kv_len,
+                             int num_qo_heads, int num_kv_heads, int head_dim, int q_dtype,
+                             int kv_dtype, const float* d_k_scale, const float* d_v_scale,
+                             float sm_scale, void* d_out, float* d_lse, void* d_workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
+ * merge_state: the state over the union of two disjoint key sets
+ * (flashinfer.cascade merge_state):
+ *   s = logaddexp(s_a, s_b);  v = v_a * exp(s_a - s) + v_b * exp(s_b - s).
+ * v_a, v_b, v_out: [n, num_heads, head_dim] in v_dtype (F32, F16 or BF16);
+ * s_a, s_b, s_out: fp32 [n, num_heads], natural log.  A state with s = -inf is
+ * empty (identity); two empty states give v = 0, s = -inf.  v_out / s_out may
+ * alias v_a / s_a.  head_dim: any multiple of 8 up to 1024.
+ */
+pkd_status pkd_merge_state(const void* d_v_a, const float* d_s_a, const void* d_v_b,
+                           const float* d_s_b, void* d_v_out, float* d_s_out, int64_t n,
+                           int num_heads, int head_dim, int v_dtype, void* stream);
+
+/*
+ * merge_states: merge k states per (index, head):
+ *   d_v [n, k, num_heads, head_dim] (v_dtype), d_s fp32 [n, k, num_heads]
+ *   -> d_v_out [n, num_heads, head_dim] (v_dtype), d_s_out fp32 [n, num_heads].
+ * k = 0 gives empty states.  Same dtype and head_dim rules as pkd_merge_state.
+ */
+pkd_status pkd_merge_states(const void* d_v, const float* d_s, int64_t n, int k, int num_heads,
+                            int head_dim, int v_dtype, void* d_v_out, float* d_s_out,
+                            void* stream);
+
+/*
+ * Read and clear the plan's device error word (PKD_DEVERR_* bits), after
+ * synchronising `stream`.  Returns PKD_ERR_DEVICE_CHECK when a bit was set.
+ */
+pkd_status pkd_check_device_errors(pkd_plan_t plan, uint32_t* flags_out, void* stream);
+
+/*
+ * The split-KV rule of pkd_plan, run on the host only (no GPU), for
+ * inspection and testing.  Outputs (caller-allocated host arrays):
+ *   items           int32 [max_items * 4]: (row, chunk_begin, chunk_end, cta) per item,
+ *                   row = b * num_kv_heads + h; an item's index is its partial slot.
+ *   cta_item_begin  int32 [num_ctas + 1]: items of CTA c are [cta_item_begin[c], cta_item_begin[c+1]).
+ *   row_item_begin, row_item_count  int32 [batch * num_kv_heads].
+ *   merge_rows      int32 [batch * num_kv_heads]: rows whose item count is not 1, ascending.
+ *   counts          int32 [4]: n_items, n_merge_rows, chunk_keys, chunks per CTA (quota).
+ * Returns PKD_ERR_CAPACITY_EXCEEDED if more than max_items items result
+ * (batch * num_kv_heads + num_ctas always suffices).
+ */
+pkd_status pkd_plan_host(const int32_t* h_kv_indptr, const int32_t* h_kv_last_page_len, int batch,
+                         int num_kv_heads, int page_size, int num_ctas, int32_t* items,
+                         int max_items, int32_t* cta_item_begin, int32_t* row_item_begin,
+                         int32_t* row_item_count, int32_t* merge_rows, int32_t* counts);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKD_H */

@@ -1,0 +1,302 @@
+"""Python binding of libpkd.so: argument marshalling only.
+
+Every call here checks shapes, takes raw device addresses from torch tensors
+and calls the C ABI declared in ``include/pkd.h``; all arithmetic of the decode
+path runs in the library's sm_103a kernels.  If the library is not built the
+first call raises (there is no fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import numpy as np
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpkd.so")
+
+F16, BF16, E4M3, F32 = 0, 1, 2, 3
+_DTYPE_CODE = {torch.float16: F16, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3, torch.float32: F32}
+
+DEVERR_PAGE_INDEX = 1
+DEVERR_WAIT_TIMEOUT = 2
+
+
+class PkdError(RuntimeError):
+    """A libpkd call returned a status other than PKD_OK."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"pkd status {status}: {message}")
+        self.status = status
+
+
+_lib = None
+
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_vp = ctypes.c_void_p
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with `python -m paged_kv_decode_28_gb300._build` "
+            "or __graft_entry__.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    i, i64, f, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "pkd_version": (ctypes.c_char_p, []),
+        "pkd_status_string": (ctypes.c_char_p, [i]),
+        "pkd_last_error": (ctypes.c_char_p, []),
+        "pkd_num_ctas": (i, [i, ctypes.POINTER(ctypes.c_int)]),
+        "pkd_workspace_bytes": (sz, [i, i, i, i, i, i]),
+        "pkd_plan_create": (i, [ctypes.POINTER(_vp), i, i, i, i, i, i, _vp, sz]),
+        "pkd_plan_destroy": (i, [_vp]),
+        "pkd_plan": (i, [_vp, _i32p, _vp, _i32p, i, i, i, i, i, i, i, _vp]),
+        "pkd_run": (i, [_vp, _vp, _vp, _vp, i64, i64, _vp, _vp, f, _vp, _vp, _vp]),
+        "pkd_cascade_decode": (i, [_vp, _vp, i, i, _vp, _vp, _vp, i64, i64, _vp, _vp, f, _vp, _vp, _vp]),
+        "pkd_single_decode": (i, [_vp, _vp, _vp, i, i, i, i, i, i, _vp, _vp, f, _vp, _vp, _vp, sz, _vp]),
+        "pkd_merge_state": (i, [_vp, _vp, _vp, _vp, _vp, _vp, i64, i, i, i, _vp]),
+        "pkd_merge_states": (i, [_vp, _vp, i64, i, i, i, i, _vp, _vp, _vp]),
+        "pkd_check_device_errors": (i, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
+        "pkd_plan_host": (i, [_i32p, _i32p, i, i, i, i, _i32p, i, _i32p, _i32p, _i32p, _i32p, _i32p]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def _check(status: int):
+    if status != 0:
+        raise PkdError(status, lib().pkd_last_error().decode(errors="replace"))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _host_i32(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _as_i32p(a: np.ndarray):
+    return a.ctypes.data_as(_i32p)
+
+
+def version() -> str:
+    return lib().pkd_version().decode()
+
+
+def num_ctas(device: Optional[int] = None) -> int:
+    dev = torch.cuda.current_device() if device is None else int(device)
+    out = ctypes.c_int(0)
+    _check(lib().pkd_num_ctas(dev, ctypes.byref(out)))
+    return out.value
+
+
+def workspace_bytes(max_batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int = 128,
+                    num_ctas_: Optional[int] = None, max_prefix_splits: int = 0) -> int:
+    G = num_ctas() if num_ctas_ is None else num_ctas_
+    n = lib().pkd_workspace_bytes(max_batch, num_qo_heads, num_kv_heads, head_dim, G, max_prefix_splits)
+    if n == 0:
+        raise PkdError(1, "invalid workspace limits")
+    return int(n)
+
+
+def plan_host(kv_indptr, kv_last_page_len, num_kv_heads: int, page_size: int, num_ctas_: int) -> dict:
+    """The library's split-KV rule evaluated on the host (no GPU needed)."""
+    indptr = _host_i32(kv_indptr)
+    last = _host_i32(kv_last_page_len)
+    B = len(indptr) - 1
+    rows = max(B * num_kv_heads, 1)
+    max_items = B * num_kv_heads + num_ctas_
+    items = np.zeros(max(max_items, 1) * 4, np.int32)
+    cta = np.zeros(num_ctas_ + 1, np.int32)
+    rb = np.zeros(rows, np.int32)
+    rc = np.zeros(rows, np.int32)
+    mr = np.zeros(rows, np.int32)
+    counts = np.zeros(4, np.int32)
+    last_arg = last if len(last) else np.zeros(1, np.int32)
+    _check(lib().pkd_plan_host(_as_i32p(indptr), _as_i32p(last_arg), B, num_kv_heads, page_size, num_ctas_,
+                               _as_i32p(items), max_items, _as_i32p(cta), _as_i32p(rb), _as_i32p(rc),
+                               _as_i32p(mr), _as_i32p(counts)))
+    n, nm = int(counts[0]), int(counts[1])
+    return {
+        "items": items[: 4 * n].reshape(n, 4).copy(),
+        "cta_item_begin": cta.copy(),
+        "row_item_begin": rb[: B * num_kv_heads].copy(),
+        "row_item_count": rc[: B * num_kv_heads].copy(),
+        "merge_rows": mr[:nm].copy(),
+        "chunk_keys": int(counts[2]),
+        "quota": int(counts[3]),
+    }
+
+
+def _check_pool(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor):
+    if k_cache.dim() != 4 or v_cache.dim() != 4:
+        raise ValueError("caches must be [num_pages, page_size, num_kv_heads, head_dim]")
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must have one shape and dtype")
+    N, P, Hk, D = k_cache.shape
+    for c in (k_cache, v_cache):
+        if c.stride(3) != 1 or c.stride(2) != D or c.stride(1) != Hk * D:
+            raise ValueError("each page of the cache must be a contiguous [page_size, Hk, D] block")
+    if k_cache.stride(0) != v_cache.stride(0):
+        raise ValueError("k_cache and v_cache must share one page stride")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    return N, P, Hk, D, k_cache.stride(0)
+
+
+class Plan:
+    """A plan object with its device workspace: ``plan(...)`` then ``run(...)``.
+
+    Mirrors the batch-decode wrapper of the pages: ``plan`` takes the CSR page
+    table and the static geometry (host work, before CUDA-graph capture);
+    ``run`` takes q and the paged K/V and returns ``(out, lse)``.
+    """
+
+    def __init__(self, max_batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int = 128,
+                 max_prefix_splits: int = 0, device=None, num_ctas_: Optional[int] = None):
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        with torch.cuda.device(self.device):
+            self.num_ctas = num_ctas() if num_ctas_ is None else int(num_ctas_)
+        self.num_qo_heads, self.num_kv_heads, self.head_dim = num_qo_heads, num_kv_heads, head_dim
+        self.max_batch = max_batch
+        nbytes = workspace_bytes(max_batch, num_qo_heads, num_kv_heads, head_dim, self.num_ctas, max_prefix_splits)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        h = ctypes.c_void_p()
+        _check(lib().pkd_plan_create(ctypes.byref(h), max_batch, num_qo_heads, num_kv_heads, head_dim,
+                                     self.num_ctas, max_prefix_splits, _ptr(self.workspace), nbytes))
+        self._h = h
+        self._indices = None
+        self.batch = 0
+        self.q_dtype = self.kv_dtype = None
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _lib is not None:
+            _lib.pkd_plan_destroy(h)
+            self._h = None
+
+    def plan(self, kv_indptr, kv_page_indices: torch.Tensor, kv_last_page_len, page_size: int,
+             q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, stream=None):
+        indptr = _host_i32(kv_indptr)
+        last = _host_i32(kv_last_page_len)
+        B = len(indptr) - 1
+        if kv_page_indices.dtype != torch.int32 or kv_page_indices.device.type != "cuda":
+            raise ValueError("kv_page_indices must be an int32 CUDA tensor")
+        last_arg = last if len(last) else np.zeros(1, np.int32)
+        _check(lib().pkd_plan(self._h, _as_i32p(indptr), _ptr(kv_page_indices), _as_i32p(last_arg), B,
+                              self.num_qo_heads, self.num_kv_heads, self.head_dim, page_size,
+                              _DTYPE_CODE[q_dtype], _DTYPE_CODE[kv_dtype], _stream(stream)))
+        self._indices = kv_page_indices  # borrowed by the library until the next plan
+        self.batch, self.page_size = B, page_size
+        self.q_dtype, self.kv_dtype = q_dtype, kv_dtype
+
+    def _outputs(self, q, out, lse, B):
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, self.num_qo_heads), dtype=torch.float32, device=q.device)
+        return out, lse
+
+    def run(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, *,
+            sm_scale: Optional[float] = None, k_scale: Optional[torch.Tensor] = None,
+            v_scale: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache)
+        if self.q_dtype is not None and q.shape != (self.batch, self.num_qo_heads, self.head_dim):
+            raise ValueError(f"q must be [{self.batch}, {self.num_qo_heads}, {self.head_dim}]")
+        out, lse = self._outputs(q, out, lse, q.shape[0])
+        _check(lib().pkd_run(self._h, _ptr(q), _ptr(k_cache), _ptr(v_cache), N, stride, _ptr(k_scale),
+                             _ptr(v_scale), float(sm_scale or 0.0), _ptr(out), _ptr(lse), _stream(stream)))
+        return out, lse
+
+    def cascade_decode(self, prefix_page_indices: torch.Tensor, prefix_last_page_len: int, q: torch.Tensor,
+                       k_cache: torch.Tensor, v_cache: torch.Tensor, *, sm_scale: Optional[float] = None,
+                       k_scale=None, v_scale=None, out=None, lse=None, stream=None):
+        N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache)
+        if prefix_page_indices.dtype != torch.int32 or prefix_page_indices.device.type != "cuda":
+            raise ValueError("prefix_page_indices must be an int32 CUDA tensor")
+        out, lse = self._outputs(q, out, lse, self.batch)
+        _check(lib().pkd_cascade_decode(self._h, _ptr(prefix_page_indices), int(prefix_page_indices.numel()),
+                                        int(prefix_last_page_len), _ptr(q), _ptr(k_cache), _ptr(v_cache), N,
+                                        stride, _ptr(k_scale), _ptr(v_scale), float(sm_scale or 0.0),
+                                        _ptr(out), _ptr(lse), _stream(stream)))
+        return out, lse
+
+    def check_device_errors(self, stream=None) -> int:
+        flags = ctypes.c_uint32(0)
+        st = lib().pkd_check_device_errors(self._h, ctypes.byref(flags), _stream(stream))
+        if st not in (0, 6):
+            _check(st)
+        return int(flags.value)
+
+
+def single_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, sm_scale: Optional[float] = None,
+                  k_scale=None, v_scale=None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Quickstart call: q ``[Hq, D]``, contiguous K/V ``[kv_len, Hk, D]`` -> ``(o [Hq, D], lse [Hq])``."""
+    if q.dim() != 2 or k.dim() != 3 or k.shape != v.shape:
+        raise ValueError("q [Hq, D] and k, v [kv_len, Hk, D] expected")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    Hq, D = q.shape
+    L, Hk, _ = k.shape
+    G = num_ctas(q.device.index)
+    nbytes = workspace_bytes(1, Hq, Hk, D, G, 0)
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(q)
+    lse = torch.empty(Hq, dtype=torch.float32, device=q.device)
+    _check(lib().pkd_single_decode(_ptr(q), _ptr(k), _ptr(v), L, Hq, Hk, D, _DTYPE_CODE[q.dtype],
+                                   _DTYPE_CODE[k.dtype], _ptr(k_scale), _ptr(v_scale), float(sm_scale or 0.0),
+                                   _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out, lse
+
+
+def merge_state(v_a: torch.Tensor, s_a: torch.Tensor, v_b: torch.Tensor, s_b: torch.Tensor, *,
+                out: Optional[torch.Tensor] = None, s_out: Optional[torch.Tensor] = None, stream=None):
+    """State over the union of two disjoint key sets: v ``[n, H, D]``, s fp32 ``[n, H]`` (natural log)."""
+    if v_a.shape != v_b.shape or v_a.dim() != 3 or s_a.shape != v_a.shape[:2] or s_b.shape != s_a.shape:
+        raise ValueError("v [n, H, D] and s [n, H] expected")
+    for t in (v_a, v_b, s_a, s_b):
+        if not t.is_contiguous():
+            raise ValueError("inputs must be contiguous")
+    n, H, D = v_a.shape
+    out = torch.empty_like(v_a) if out is None else out
+    s_out = torch.empty_like(s_a) if s_out is None else s_out
+    _check(lib().pkd_merge_state(_ptr(v_a), _ptr(s_a), _ptr(v_b), _ptr(s_b), _ptr(out), _ptr(s_out), n, H, D,
+                                 _DTYPE_CODE[v_a.dtype], _stream(stream)))
+    return out, s_out
+
+
+def merge_states(v: torch.Tensor, s: torch.Tensor, *, stream=None):
+    """Merge k states: v ``[n, k, H, D]``, s fp32 ``[n, k, H]`` -> ``([n, H, D], [n, H])``."""
+    if v.dim() != 4 or s.shape != v.shape[:3]:
+        raise ValueError("v [n, k, H, D] and s [n, k, H] expected")
+    if not (v.is_contiguous() and s.is_contiguous()):
+        raise ValueError("inputs must be contiguous")
+    n, k, H, D = v.shape
+    out = torch.empty((n, H, D), dtype=v.dtype, device=v.device)
+    s_out = torch.empty((n, H), dtype=torch.float32, device=v.device)
+    _check(lib().pkd_merge_states(_ptr(v), _ptr(s), n, k, H, D, _DTYPE_CODE[v.dtype], _ptr(out), _ptr(s_out),
+                                  _stream(stream)))
+    return out, s_out

@@ -1,0 +1,491 @@
+// pkd_capi.cu -- the C ABI of libpkd.so (declared in include/pkd.h): argument
+// checking, workspace layout, TMA tensor-map encoding and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <cmath>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "pkd.h"
+#include "pkd_internal.h"
+#include "pkd_plan.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+pkd_status fail(pkd_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+pkd_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKD_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  int group = 0, max_rows = 0, max_items = 0;
+  size_t cta_begin = 0, items = 0, merge_rows = 0, row_begin = 0, row_count = 0, kv_len = 0,
+         page_begin = 0, meta_end = 0, part_o = 0, part_lse = 0, pre_o = 0, pre_lse = 0, total = 0;
+};
+
+bool make_layout(int max_batch, int hq, int hk, int d, int G, int max_splits, Layout* L) {
+  if (max_batch <= 0 || hq <= 0 || hk <= 0 || d <= 0 || G <= 0 || max_splits < 0) return false;
+  if (hq % hk != 0) return false;
+  L->group = hq / hk;
+  L->max_rows = max_batch * hk;
+  L->max_items = L->max_rows + G;
+  size_t off = sizeof(pkd::WsHeader);
+  L->cta_begin = off;
+  off += align256(4ull * (G + 1));
+  L->items = off;
+  off += align256(16ull * L->max_items);
+  L->merge_rows = off;
+  off += align256(4ull * L->max_rows);
+  L->row_begin = off;
+  off += align256(4ull * L->max_rows);
+  L->row_count = off;
+  off += align256(4ull * L->max_rows);
+  L->kv_len = off;
+  off += align256(4ull * max_batch);
+  L->page_begin = off;
+  off += align256(4ull * max_batch);
+  L->meta_end = off;
+  L->part_o = off;
+  off += align256(4ull * L->max_items * L->group * d);
+  L->part_lse = off;
+  off += align256(4ull * L->max_items * L->group);
+  L->pre_o = off;
+  off += align256(4ull * max_splits * max_batch * hq * d);
+  L->pre_lse = off;
+  off += align256(4ull * max_splits * max_batch * hq);
+  L->total = off;
+  return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int elem_bytes(int dt) { return dt == PKD_E4M3 ? 1 : (dt == PKD_F32 ? 4 : 2); }
+
+// Tensor map over a pool [num_pages, tok_extent, Hk, 128] with a page stride in
+// elements; boxes of 64 (16-bit) or 128 (fp8) head-dim elements x 1 head x
+// box_tok keys x 1 page, 128-byte swizzled.
+pkd_status encode_kv_map(CUtensorMap* m, const void* base, int kv_dtype, int hk, int64_t tok_extent,
+                         int64_t num_pages, int64_t page_stride_elems, int box_tok) {
+  auto enc = get_encode();
+  if (!enc) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int e = elem_bytes(kv_dtype);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(pkd::kHeadDim), static_cast<cuuint64_t>(hk),
+                        static_cast<cuuint64_t>(tok_extent), static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(pkd::kHeadDim) * e,
+                           static_cast<cuuint64_t>(hk) * pkd::kHeadDim * e,
+                           static_cast<cuuint64_t>(page_stride_elems) * e};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(e == 1 ? 128 : 64), 1u, static_cast<cuuint32_t>(box_tok), 1u};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUtensorMapDataType dt = kv_dtype == PKD_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                           : kv_dtype == PKD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return PKD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct pkd_plan_s {
+  int max_batch, hq, hk, d, G, max_splits;
+  uint8_t* ws;
+  size_t ws_bytes;
+  Layout lay;
+  std::vector<uint8_t> host;  // mirror of workspace bytes [0, meta_end)
+  // last plan
+  bool planned = false;
+  bool err_word_zeroed = false;  // the first plan clears the device error word
+  int batch = 0, page_size = 0, q_dtype = 0, kv_dtype = 0;
+  const int32_t* d_page_indices = nullptr;
+  pkd::PlanCounts counts{};
+};
+
+extern "C" {
+
+const char* pkd_version(void) { return "pkd 0.1.0 sm_103a"; }
+
+const char* pkd_status_string(int s) {
+  switch (s) {
+    case PKD_OK: return "ok";
+    case PKD_ERR_INVALID_ARG: return "invalid argument";
+    case PKD_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PKD_ERR_CAPACITY_EXCEEDED: return "capacity exceeded";
+    case PKD_ERR_CUDA: return "CUDA error";
+    case PKD_ERR_DEVICE_CHECK: return "device-side check failed";
+    case PKD_ERR_NO_PLAN: return "no plan";
+    default: return "unknown status";
+  }
+}
+
+const char* pkd_last_error(void) { return g_err.c_str(); }
+
+pkd_status pkd_num_ctas(int device, int* num_ctas_out) {
+  if (!num_ctas_out) return fail(PKD_ERR_INVALID_ARG, "num_ctas_out is NULL");
+  int sms = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(MultiProcessorCount)");
+  *num_ctas_out = sms * pkd::kCtasPerSm;
+  return PKD_OK;
+}
+
+size_t pkd_workspace_bytes(int max_batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                           int num_ctas, int max_prefix_splits) {
+  Layout L;
+  if (head_dim != pkd::kHeadDim) return 0;
+  if (max_prefix_splits > pkd::kMaxPrefixSplits) return 0;
+  if (!make_layout(max_batch, num_qo_heads, num_kv_heads, head_dim, num_ctas, max_prefix_splits, &L))
+    return 0;
+  return L.total;
+}
+
+pkd_status pkd_plan_create(pkd_plan_t* plan_out, int max_batch, int num_qo_heads, int num_kv_heads,
+                           int head_dim, int num_ctas, int max_prefix_splits, void* d_workspace,
+                           size_t workspace_bytes) {
+  if (!plan_out) return fail(PKD_ERR_INVALID_ARG, "plan_out is NULL");
+  *plan_out = nullptr;
+  if (head_dim != pkd::kHeadDim) return fail(PKD_ERR_UNSUPPORTED, "head_dim must be 128 (got %d)", head_dim);
+  if (num_kv_heads <= 0 || num_qo_heads <= 0 || num_qo_heads % num_kv_heads != 0)
+    return fail(PKD_ERR_INVALID_ARG, "num_qo_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                num_qo_heads, num_kv_heads);
+  if (num_qo_heads / num_kv_heads > pkd::kMaxGroup)
+    return fail(PKD_ERR_UNSUPPORTED, "group size %d above %d", num_qo_heads / num_kv_heads, pkd::kMaxGroup);
+  if (max_prefix_splits < 0 || max_prefix_splits > pkd::kMaxPrefixSplits)
+    return fail(PKD_ERR_INVALID_ARG, "max_prefix_splits must be 0..%d", pkd::kMaxPrefixSplits);
+  Layout L;
+  if (!make_layout(max_batch, num_qo_heads, num_kv_heads, head_dim, num_ctas, max_prefix_splits, &L))
+    return fail(PKD_ERR_INVALID_ARG, "invalid limits (max_batch %d, num_ctas %d)", max_batch, num_ctas);
+  if (!d_workspace) return fail(PKD_ERR_INVALID_ARG, "d_workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(d_workspace) & 255u)
+    return fail(PKD_ERR_INVALID_ARG, "d_workspace must be 256-byte aligned");
+  if (workspace_bytes < L.total)
+    return fail(PKD_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", workspace_bytes, L.total);
+  pkd_plan_s* p = new (std::nothrow) pkd_plan_s();
+  if (!p) return fail(PKD_ERR_INVALID_ARG, "out of host memory");
+  p->max_batch = max_batch;
+  p->hq = num_qo_heads;
+  p->hk = num_kv_heads;
+  p->d = head_dim;
+  p->G = num_ctas;
+  p->max_splits = max_prefix_splits;
+  p->ws = static_cast<uint8_t*>(d_workspace);
+  p->ws_bytes = workspace_bytes;
+  p->lay = L;
+  p->host.assign(L.meta_end, 0);
+  *plan_out = p;
+  return PKD_OK;
+}
+
+pkd_status pkd_plan_destroy(pkd_plan_t plan) {
+  delete plan;
+  return PKD_OK;
+}
+
+pkd_status pkd_plan_host(const int32_t* h_kv_indptr, const int32_t* h_kv_last_page_len, int batch,
+                         int num_kv_heads, int page_size, int num_ctas, int32_t* items, int max_items,
+                         int32_t* cta_item_begin, int32_t* row_item_begin, int32_t* row_item_count,
+                         int32_t* merge_rows, int32_t* counts) {
+  if (!items || !cta_item_begin || !row_item_begin || !row_item_count || !merge_rows || !counts)
+    return fail(PKD_ERR_INVALID_ARG, "NULL output array");
+  std::vector<int32_t> kv_len(batch > 0 ? batch : 1);
+  std::string err;
+  pkd::PlanCounts c{};
+  int r = pkd::compute_plan(h_kv_indptr, h_kv_last_page_len, batch, num_kv_heads, page_size, num_ctas,
+                            items, max_items, cta_item_begin, row_item_begin, row_item_count,
+                            merge_rows, kv_len.data(), &c, &err);
+  if (r != pkd::kPlanOk) return fail(static_cast<pkd_status>(r), "%s", err.c_str());
+  counts[0] = c.n_items;
+  counts[1] = c.n_merge_rows;
+  counts[2] = c.chunk_keys;
+  counts[3] = c.quota;
+  return PKD_OK;
+}
+
+pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* d_kv_page_indices,
+                    const int32_t* h_kv_last_page_len, int batch, int num_qo_heads, int num_kv_heads,
+                    int head_dim, int page_size, int q_dtype, int kv_dtype, void* stream) {
+  if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
+  plan->planned = false;
+  if (num_qo_heads != plan->hq || num_kv_heads != plan->hk || head_dim != plan->d)
+    return fail(PKD_ERR_INVALID_ARG, "heads/head_dim (%d, %d, %d) differ from the plan's (%d, %d, %d)",
+                num_qo_heads, num_kv_heads, head_dim, plan->hq, plan->hk, plan->d);
+  if (batch < 0) return fail(PKD_ERR_INVALID_ARG, "batch must be >= 0");
+  if (batch > plan->max_batch)
+    return fail(PKD_ERR_CAPACITY_EXCEEDED, "batch %d above max_batch %d", batch, plan->max_batch);
+  const bool ok_pair = (q_dtype == PKD_F16 && kv_dtype == PKD_F16) ||
+                       (q_dtype == PKD_BF16 && kv_dtype == PKD_BF16) ||
+                       (q_dtype == PKD_BF16 && kv_dtype == PKD_E4M3) ||
+                       (q_dtype == PKD_F16 && kv_dtype == PKD_E4M3);
+  if (!ok_pair) return fail(PKD_ERR_UNSUPPORTED, "dtype pair (q %d, kv %d) not supported", q_dtype, kv_dtype);
+  if (!h_kv_indptr) return fail(PKD_ERR_INVALID_ARG, "h_kv_indptr is NULL");
+  if (batch > 0 && h_kv_indptr[batch] > 0 && !d_kv_page_indices)
+    return fail(PKD_ERR_INVALID_ARG, "d_kv_page_indices is NULL");
+  const Layout& L = plan->lay;
+  uint8_t* h = plan->host.data();
+  auto* hdr = reinterpret_cast<pkd::WsHeader*>(h);
+  auto* cta_begin = reinterpret_cast<int32_t*>(h + L.cta_begin);
+  auto* items = reinterpret_cast<int32_t*>(h + L.items);
+  auto* merge_rows = reinterpret_cast<int32_t*>(h + L.merge_rows);
+  auto* row_begin = reinterpret_cast<int32_t*>(h + L.row_begin);
+  auto* row_count = reinterpret_cast<int32_t*>(h + L.row_count);
+  auto* kv_len = reinterpret_cast<int32_t*>(h + L.kv_len);
+  auto* page_begin = reinterpret_cast<int32_t*>(h + L.page_begin);
+  std::string err;
+  pkd::PlanCounts c{};
+  int r = pkd::compute_plan(h_kv_indptr, h_kv_last_page_len, batch, num_kv_heads, page_size, plan->G,
+                            items, L.max_items, cta_begin, row_begin, row_count, merge_rows, kv_len,
+                            &c, &err);
+  if (r != pkd::kPlanOk) return fail(static_cast<pkd_status>(r), "%s", err.c_str());
+  // item flags: bit 0 = row split across several items
+  for (int i = 0; i < c.n_items; ++i) {
+    const int row = items[4 * i + 0];
+    items[4 * i + 3] = row_count[row] > 1 ? pkd::kItemSplit : 0;
+  }
+  for (int b = 0; b < batch; ++b) page_begin[b] = h_kv_indptr[b];
+  hdr->n_items = c.n_items;
+  hdr->n_merge_rows = c.n_merge_rows;
+  hdr->batch = batch;
+  hdr->zero_page = 0;
+  if (!plan->err_word_zeroed) {
+    cudaError_t ez = cudaMemsetAsync(plan->ws, 0, 4, static_cast<cudaStream_t>(stream));
+    if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync(error word)");
+    plan->err_word_zeroed = true;
+  }
+  // one copy of everything after the error word (the error word stays the kernels')
+  cudaError_t e = cudaMemcpyAsync(plan->ws + 4, h + 4, L.meta_end - 4, cudaMemcpyHostToDevice,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan)");
+  plan->planned = true;
+  plan->batch = batch;
+  plan->page_size = page_size;
+  plan->q_dtype = q_dtype;
+  plan->kv_dtype = kv_dtype;
+  plan->d_page_indices = d_kv_page_indices;
+  plan->counts = c;
+  return PKD_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                      int64_t num_pages, int64_t page_stride_elems, int64_t tok_extent,
+                      const float* d_k_scale, const float* d_v_scale, float sm_scale, void* d_out,
+                      float* d_lse, void* stream, const int32_t* page_indices_override) {
+  if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
+  if (!plan->planned) return fail(PKD_ERR_NO_PLAN, "run before a successful plan");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Layout& L = plan->lay;
+  if (!d_q || !d_out) return fail(PKD_ERR_INVALID_ARG, "q/out is NULL");
+  if (!aligned16(d_q) || !aligned16(d_out)) return fail(PKD_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
+  const bool fp8 = plan->kv_dtype == PKD_E4M3;
+  if (fp8 && (!d_k_scale || !d_v_scale))
+    return fail(PKD_ERR_INVALID_ARG, "an E4M3 cache needs k_scale and v_scale");
+  if (!fp8 && (d_k_scale || d_v_scale))
+    return fail(PKD_ERR_INVALID_ARG, "k_scale/v_scale apply to an E4M3 cache only");
+  const int P = plan->page_size;
+  const int box_tok = P <= pkd::kChunkKeys ? P : pkd::kChunkKeys;
+  const float scale = (sm_scale > 0.f) ? sm_scale : 1.0f / std::sqrt(static_cast<float>(plan->d));
+  uint8_t* ws = plan->ws;
+  pkd::DecodeParams p{};
+  p.items = reinterpret_cast<const int4*>(ws + L.items);
+  p.cta_begin = reinterpret_cast<const int*>(ws + L.cta_begin);
+  p.kv_len = reinterpret_cast<const int*>(ws + L.kv_len);
+  p.page_begin = reinterpret_cast<const int*>(ws + L.page_begin);
+  p.page_indices = page_indices_override ? page_indices_override : plan->d_page_indices;
+  p.q = d_q;
+  p.out = d_out;
+  p.lse = d_lse;
+  p.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  p.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  p.k_scale = d_k_scale;
+  p.v_scale = d_v_scale;
+  p.err = reinterpret_cast<unsigned*>(ws);
+  p.num_kv_heads = plan->hk;
+  p.group = plan->hq / plan->hk;
+  p.page_size = P;
+  p.pages_per_chunk = P <= pkd::kChunkKeys ? pkd::kChunkKeys / P : 0;
+  p.chunk_keys = plan->counts.chunk_keys;
+  p.box_tok = box_tok;
+  p.num_pages = static_cast<int>(num_pages);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.force_partial = 0;
+  if (plan->counts.n_items > 0) {
+    if (!d_k_cache || !d_v_cache) return fail(PKD_ERR_INVALID_ARG, "k/v cache is NULL");
+    if (!aligned16(d_k_cache) || !aligned16(d_v_cache))
+      return fail(PKD_ERR_INVALID_ARG, "k/v cache must be 16-byte aligned");
+    if (num_pages <= 0 || num_pages > INT32_MAX) return fail(PKD_ERR_INVALID_ARG, "num_pages out of range");
+    if ((page_stride_elems * elem_bytes(plan->kv_dtype)) % 16 != 0 ||
+        page_stride_elems < static_cast<int64_t>(P) * plan->hk * plan->d)
+      return fail(PKD_ERR_INVALID_ARG, "page_stride_elems must cover a page and be a 16-byte multiple");
+    CUtensorMap tmk, tmv;
+    pkd_status s = encode_kv_map(&tmk, d_k_cache, plan->kv_dtype, plan->hk, tok_extent, num_pages,
+                                 page_stride_elems, box_tok);
+    if (s != PKD_OK) return s;
+    s = encode_kv_map(&tmv, d_v_cache, plan->kv_dtype, plan->hk, tok_extent, num_pages, page_stride_elems,
+                      box_tok);
+    if (s != PKD_OK) return s;
+    cudaError_t e = pkd::launch_decode(tmk, tmv, p, plan->q_dtype, plan->kv_dtype, plan->G, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  }
+  pkd::MergeParams m{};
+  m.merge_rows = reinterpret_cast<const int*>(ws + L.merge_rows);
+  m.header = reinterpret_cast<const pkd::WsHeader*>(ws);
+  m.row_item_begin = reinterpret_cast<const int*>(ws + L.row_begin);
+  m.row_item_count = reinterpret_cast<const int*>(ws + L.row_count);
+  m.part_o = p.part_o;
+  m.part_lse = p.part_lse;
+  m.pre_o = nullptr;
+  m.pre_lse = nullptr;
+  m.n_pre_splits = 0;
+  m.out = d_out;
+  m.lse = d_lse;
+  m.out_dtype = plan->q_dtype;
+  m.num_kv_heads = plan->hk;
+  m.group = p.group;
+  m.all_rows = 0;
+  cudaError_t e = pkd::launch_merge_rows(m, plan->G, st);
+  if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  return PKD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkd_status pkd_run(pkd_plan_t plan, const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                   int64_t num_pages, int64_t page_stride_elems, const float* d_k_scale,
+                   const float* d_v_scale, float sm_scale, void* d_out, float* d_lse, void* stream) {
+  if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
+  return run_common(plan, d_q, d_k_cache, d_v_cache, num_pages, page_stride_elems, plan->page_size,
+                    d_k_scale, d_v_scale, sm_scale, d_out, d_lse, stream, nullptr);
+}
+
+pkd_status pkd_cascade_decode(pkd_plan_t suffix_plan, const int32_t* d_prefix_page_indices,
+                              int prefix_num_pages, int prefix_last_page_len, const void* d_q,
+                              const void* d_k_cache, const void* d_v_cache, int64_t num_pages,
+                              int64_t page_stride_elems, const float* d_k_scale,
+                              const float* d_v_scale, float sm_scale, void* d_out, float* d_lse,
+                              void* stream) {
+  (void)suffix_plan; (void)d_prefix_page_indices; (void)prefix_num_pages; (void)prefix_last_page_len;
+  (void)d_q; (void)d_k_cache; (void)d_v_cache; (void)num_pages; (void)page_stride_elems;
+  (void)d_k_scale; (void)d_v_scale; (void)sm_scale; (void)d_out; (void)d_lse; (void)stream;
+  return fail(PKD_ERR_UNSUPPORTED, "cascade decode is not built yet");
+}
+
+pkd_status pkd_single_decode(const void* d_q, const void* d_k, const void* d_v, int kv_len,
+                             int num_qo_heads, int num_kv_heads, int head_dim, int q_dtype,
+                             int kv_dtype, const float* d_k_scale, const float* d_v_scale,
+                             float sm_scale, void* d_out, float* d_lse, void* d_workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (kv_len < 0) return fail(PKD_ERR_INVALID_ARG, "kv_len must be >= 0");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int G = 0;
+  pkd_status s = pkd_num_ctas(dev, &G);
+  if (s != PKD_OK) return s;
+  pkd_plan_t plan = nullptr;
+  s = pkd_plan_create(&plan, 1, num_qo_heads, num_kv_heads, head_dim, G, 0, d_workspace, workspace_bytes);
+  if (s != PKD_OK) return s;
+  // the contiguous [kv_len, Hk, D] tensor is one page; its page size is kv_len
+  // rounded up to the 64-key chunk (the TMA map's key extent stays kv_len, so
+  // keys past the end read as zeros and are masked)
+  const int P = kv_len <= pkd::kChunkKeys ? (kv_len > 0 ? kv_len : 1)
+                                          : ((kv_len + pkd::kChunkKeys - 1) / pkd::kChunkKeys) * pkd::kChunkKeys;
+  const int32_t indptr[2] = {0, kv_len > 0 ? 1 : 0};
+  const int32_t last[1] = {kv_len > 0 ? kv_len : 0};
+  const int32_t* zero_page = reinterpret_cast<const int32_t*>(
+      static_cast<uint8_t*>(d_workspace) + offsetof(pkd::WsHeader, zero_page));
+  s = pkd_plan(plan, indptr, zero_page, last, 1, num_qo_heads, num_kv_heads, head_dim, P, q_dtype,
+               kv_dtype, stream);
+  if (s == PKD_OK) {
+    // one page: its stride is never stepped, it only has to cover the page
+    const int64_t stride = static_cast<int64_t>(P) * num_kv_heads * head_dim;
+    s = run_common(plan, d_q, d_k, d_v, 1, stride, kv_len > 0 ? kv_len : 1, d_k_scale, d_v_scale, sm_scale,
+                   d_out, d_lse, stream, zero_page);
+  }
+  pkd_plan_destroy(plan);
+  return s;
+}
+
+pkd_status pkd_merge_state(const void* d_v_a, const float* d_s_a, const void* d_v_b, const float* d_s_b,
+                           void* d_v_out, float* d_s_out, int64_t n, int num_heads, int head_dim,
+                           int v_dtype, void* stream) {
+  if (n < 0 || num_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0 || head_dim > 1024)
+    return fail(PKD_ERR_INVALID_ARG, "n >= 0, num_heads > 0 and head_dim in 8..1024 (multiple of 8) required");
+  if (v_dtype != PKD_F32 && v_dtype != PKD_F16 && v_dtype != PKD_BF16)
+    return fail(PKD_ERR_UNSUPPORTED, "merge_state values must be F32, F16 or BF16");
+  if (n > 0 && (!d_v_a || !d_s_a || !d_v_b || !d_s_b || !d_v_out || !d_s_out))
+    return fail(PKD_ERR_INVALID_ARG, "NULL pointer");
+  cudaError_t e = pkd::launch_merge_state(d_v_a, d_s_a, d_v_b, d_s_b, d_v_out, d_s_out, n, num_heads, head_dim,
+                                          v_dtype, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge_state kernel launch");
+  return PKD_OK;
+}
+
+pkd_status pkd_merge_states(const void* d_v, const float* d_s, int64_t n, int k, int num_heads,
+                            int head_dim, int v_dtype, void* d_v_out, float* d_s_out, void* stream) {
+  if (n < 0 || k < 0 || num_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0 || head_dim > 1024)
+    return fail(PKD_ERR_INVALID_ARG, "n, k >= 0, num_heads > 0 and head_dim in 8..1024 (multiple of 8) required");
+  if (v_dtype != PKD_F32 && v_dtype != PKD_F16 && v_dtype != PKD_BF16)
+    return fail(PKD_ERR_UNSUPPORTED, "merge_states values must be F32, F16 or BF16");
+  if (n > 0 && (!d_v_out || !d_s_out || (k > 0 && (!d_v || !d_s))))
+    return fail(PKD_ERR_INVALID_ARG, "NULL pointer");
+  cudaError_t e = pkd::launch_merge_states(d_v, d_s, n, k, num_heads, head_dim, v_dtype, d_v_out, d_s_out,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge_states kernel launch");
+  return PKD_OK;
+}
+
+pkd_status pkd_check_device_errors(pkd_plan_t plan, uint32_t* flags_out, void* stream) {
+  if (!plan || !flags_out) return fail(PKD_ERR_INVALID_ARG, "NULL argument");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t flags = 0;
+  cudaError_t e = cudaMemcpyAsync(&flags, plan->ws, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(plan->ws, 0, 4, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  *flags_out = flags;
+  if (flags) return fail(PKD_ERR_DEVICE_CHECK, "device error bits 0x%x", flags);
+  return PKD_OK;
+}
+
+}  // extern "C"

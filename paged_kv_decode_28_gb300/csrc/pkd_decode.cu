@@ -1,0 +1,501 @@
+// pkd_decode.cu -- split-KV paged decode attention for sm_103a.
+//
+// One persistent CTA per plan slot (the plan hands CTA c the contiguous run of
+// work items cta_begin[c] .. cta_begin[c+1]).  Warp 4 is the producer: for every
+// 64-key chunk of an item it reads the chunk's physical page ids from the CSR
+// page table and issues TMA tensor loads (cp.async.bulk.tensor) of the K and V
+// rows of those pages for the item's kv head into a ring of shared-memory
+// stages, completing on an mbarrier (page-table gather of the deep dive's
+// paged pool, "The Code, Annotated", snippet one).  Warps 0..3 are consumers:
+// each owns 16 keys of every stage and keeps its own online-softmax state for
+// all g query heads of the kv head (the GQA group is the M dimension of a
+// warp-level tensor-core MMA, so every KV byte is read from HBM once).  At the
+// end of an item the four states are combined in shared memory and written
+// either as the final (out, lse) or, for a row split across CTAs, as an fp32
+// partial state that the merge pass combines (merge_state of the 2026 guide,
+// "Cascade attention for shared prefixes").
+//
+// Scores are fp32; the softmax runs in base 2 with sm_scale * log2(e) applied
+// to the fp32 dot product; partial states carry a base-2 log-sum-exp.
+#include "pkd_internal.h"
+#include "pkd_ptx.cuh"
+
+namespace pkd {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <int KVT>
+struct Cfg {
+  // bytes of one key (or value) row of one kv head
+  static constexpr int kRowBytes = (KVT == kE4M3) ? kHeadDim : 2 * kHeadDim;
+  static constexpr int kStages = (KVT == kE4M3) ? 6 : 3;
+  static constexpr bool kMmaBf16 = (KVT == kBF16);
+  // one 64-key tile of K (or V): 16-bit -> two [64][128 B] halves (d 0..63, 64..127)
+  static constexpr int kTensorBytes = kChunkKeys * kRowBytes;
+  static constexpr int kStageBytes = 2 * kTensorBytes;
+  static constexpr int kCombO = kStages * kStageBytes;                          // f32 [3][8][128]
+  static constexpr int kCombML = kCombO + 3 * kMaxGroup * kHeadDim * 4;         // f32 [3][8][2]
+  static constexpr int kBars = kCombML + 3 * kMaxGroup * 2 * 4;                 // u64 [2][stages]
+  static constexpr int kAbort = kBars + 2 * kStages * 8;                        // int
+  static constexpr int kTotal = kAbort + 16;
+  static constexpr int kAlloc = kTotal + 1024;  // slack for the 1024-byte alignment of stages
+};
+
+__device__ __forceinline__ int load_page(const DecodeParams& p, int idx) {
+  int v = __ldg(p.page_indices + idx);
+  if (static_cast<unsigned>(v) >= static_cast<unsigned>(p.num_pages)) {
+    atomicOr(p.err, kDevErrPageIndex);
+    v = 0;
+  }
+  return v;
+}
+
+// Bounded wait that also gives up at once when another warp already did.
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, unsigned* err,
+                                           volatile int* abort_flag) {
+  if (*abort_flag) return false;
+  if (ptx::mbar_wait(bar, parity, err)) return true;
+  *abort_flag = 1;
+  return false;
+}
+
+// Query fragments (A operand rows = heads of the group, padded to 16 with zeros).
+// 16-bit KV: k-step j covers d = 16j .. 16j+15 in natural order.
+// fp8 KV:   k-step j, thread t covers d = 32t + 4j + {0,1} (a0) and {2,3} (a2):
+//           the same permutation is applied to K, so the dot product is unchanged.
+template <int QT, int KVT>
+__device__ __forceinline__ void load_q(const DecodeParams& p, int b, int qo, bool hv, int t,
+                                       uint32_t (&qa0)[8], uint32_t (&qa2)[8]) {
+  const int Hq = p.num_kv_heads * p.group;
+  const uint16_t* qrow = static_cast<const uint16_t*>(p.q) + (static_cast<size_t>(b) * Hq + qo) * kHeadDim;
+  if constexpr (KVT != kE4M3) {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      qa0[j] = hv ? __ldg(q32 + (16 * j + 2 * t) / 2) : 0u;
+      qa2[j] = hv ? __ldg(q32 + (16 * j + 8 + 2 * t) / 2) : 0u;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (!hv) {
+        qa0[j] = qa2[j] = 0u;
+        continue;
+      }
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(qrow + 32 * t + 4 * j));
+      float f[4];
+      const uint32_t w[2] = {raw.x, raw.y};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint16_t bits = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+        if constexpr (QT == kBF16) {
+          f[e] = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+        } else {
+          __half_raw hr;
+          hr.x = bits;
+          f[e] = __half2float(__half(hr));
+        }
+      }
+      qa0[j] = ptx::pack2<false>(f[0], f[1]);
+      qa2[j] = ptx::pack2<false>(f[2], f[3]);
+    }
+  }
+}
+
+// Online-softmax update for one 16-key sub-tile given the raw scores.
+// x[] = (n-tile 0: keys 2t, 2t+1; n-tile 1: keys 8+2t, 9+2t) of head row gid.
+template <bool PBF16>
+__device__ __forceinline__ void softmax_step(const float (&sacc)[2][4], int t, int valid, float sl2,
+                                             float& m_run, float& l_run, float (&o)[16][4],
+                                             uint32_t& pa0, uint32_t& pa2) {
+  float x[4];
+  x[0] = (2 * t < valid) ? sacc[0][0] * sl2 : -INFINITY;
+  x[1] = (2 * t + 1 < valid) ? sacc[0][1] * sl2 : -INFINITY;
+  x[2] = (2 * t + 8 < valid) ? sacc[1][0] * sl2 : -INFINITY;
+  x[3] = (2 * t + 9 < valid) ? sacc[1][1] * sl2 : -INFINITY;
+  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  // key 0 of the sub-tile is always valid, so m_new is finite
+  const float m_new = fmaxf(m_run, mx);
+  const float alpha = ptx::ex2(m_run - m_new);
+  float pr[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) pr[i] = ptx::ex2(x[i] - m_new);
+  l_run = l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+  m_run = m_new;
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+    o[nt][0] *= alpha;
+    o[nt][1] *= alpha;
+  }
+  pa0 = ptx::pack2<PBF16>(pr[0], pr[1]);
+  pa2 = ptx::pack2<PBF16>(pr[2], pr[3]);
+}
+
+// 16 keys of a 16-bit stage: S = Q K^T (ldmatrix), softmax, O += P V (ldmatrix.trans).
+template <bool BF>
+__device__ __forceinline__ void tile16_16bit(uint32_t kb, uint32_t vb, int w, int lane, int valid,
+                                             const uint32_t (&qa0)[8], const uint32_t (&qa2)[8],
+                                             float sl2, float& m_run, float& l_run,
+                                             float (&o)[16][4]) {
+  const int t = lane & 3;
+  float sacc[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.f;
+#pragma unroll
+  for (int kp = 0; kp < 4; ++kp) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const uint32_t tok = 16 * w + 8 * nt + (lane & 7);
+      const uint32_t dch = 4 * kp + (lane >> 3);  // 16-byte chunk of the 256-byte row
+      const uint32_t addr = kb + (dch >> 3) * (kChunkKeys * 128u) + ptx::sw128(tok, dch & 7u);
+      uint32_t r0, r1, r2, r3;
+      ptx::ldsm_x4(addr, r0, r1, r2, r3);
+      ptx::mma_16816<BF>(sacc[nt], qa0[2 * kp], 0u, qa2[2 * kp], 0u, r0, r1);
+      ptx::mma_16816<BF>(sacc[nt], qa0[2 * kp + 1], 0u, qa2[2 * kp + 1], 0u, r2, r3);
+    }
+  }
+  uint32_t pa0, pa2;
+  softmax_step<BF>(sacc, t, valid, sl2, m_run, l_run, o, pa0, pa2);
+  // values of keys past the valid count are zeroed (their P is 0, but the
+  // shared-memory rows may hold stale or non-finite bits)
+  const uint32_t mlo = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
+  const uint32_t mhi = (2 * t + 8 < valid ? 0x0000ffffu : 0u) | (2 * t + 9 < valid ? 0xffff0000u : 0u);
+#pragma unroll
+  for (int dp = 0; dp < 8; ++dp) {
+    const uint32_t tok = 16 * w + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t dch = 2 * dp + (lane >> 4);
+    const uint32_t addr = vb + (dch >> 3) * (kChunkKeys * 128u) + ptx::sw128(tok, dch & 7u);
+    uint32_t r0, r1, r2, r3;
+    ptx::ldsm_x4_trans(addr, r0, r1, r2, r3);
+    r0 &= mlo;
+    r1 &= mhi;
+    r2 &= mlo;
+    r3 &= mhi;
+    ptx::mma_16816<BF>(o[2 * dp], pa0, 0u, pa2, 0u, r0, r1);
+    ptx::mma_16816<BF>(o[2 * dp + 1], pa0, 0u, pa2, 0u, r2, r3);
+  }
+}
+
+// 16 keys of an fp8 stage.  K: the thread's 32 bytes of key row gid, converted
+// e4m3x2 -> f16x2 in registers (d permuted as in load_q).  V: n-tile 4q + r,
+// column n maps to d = 32q + 4n + r, so one 32-bit load per key serves 4 n-tiles.
+__device__ __forceinline__ void tile16_e4m3(uint32_t kb, uint32_t vb, int w, int lane, int valid,
+                                            const uint32_t (&qa0)[8], const uint32_t (&qa2)[8],
+                                            float sl2, float& m_run, float& l_run,
+                                            float (&o)[16][4]) {
+  const int gid = lane >> 2, t = lane & 3;
+  float sacc[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.f;
+    const uint32_t tok = 16 * w + 8 * nt + gid;
+    const uint4 c0 = ptx::lds128(kb + ptx::sw128(tok, 2 * t));
+    const uint4 c1 = ptx::lds128(kb + ptx::sw128(tok, 2 * t + 1));
+    const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t b0 = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(wd[j] & 0xffffu));
+      const uint32_t b1 = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(wd[j] >> 16));
+      ptx::mma_16816<false>(sacc[nt], qa0[j], 0u, qa2[j], 0u, b0, b1);
+    }
+  }
+  uint32_t pa0, pa2;
+  softmax_step<false>(sacc, t, valid, sl2, m_run, l_run, o, pa0, pa2);
+  const uint32_t tA = 16 * w + 2 * t;
+  const bool vA = 2 * t < valid, vB = 2 * t + 1 < valid, vC = 2 * t + 8 < valid, vD = 2 * t + 9 < valid;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t chunk = 2 * q + (gid >> 2);
+    const uint32_t boff = 4 * (gid & 3);
+    const uint32_t wA = vA ? ptx::lds32(vb + ptx::sw128(tA, chunk) + boff) : 0u;
+    const uint32_t wB = vB ? ptx::lds32(vb + ptx::sw128(tA + 1, chunk) + boff) : 0u;
+    const uint32_t wC = vC ? ptx::lds32(vb + ptx::sw128(tA + 8, chunk) + boff) : 0u;
+    const uint32_t wD = vD ? ptx::lds32(vb + ptx::sw128(tA + 9, chunk) + boff) : 0u;
+    const uint32_t x01 = __byte_perm(wA, wB, 0x5140), x23 = __byte_perm(wA, wB, 0x7362);
+    const uint32_t y01 = __byte_perm(wC, wD, 0x5140), y23 = __byte_perm(wC, wD, 0x7362);
+    ptx::mma_16816<false>(o[4 * q + 0], pa0, 0u, pa2, 0u,
+                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(x01 & 0xffffu)),
+                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(y01 & 0xffffu)));
+    ptx::mma_16816<false>(o[4 * q + 1], pa0, 0u, pa2, 0u,
+                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(x01 >> 16)),
+                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(y01 >> 16)));
+    ptx::mma_16816<false>(o[4 * q + 2], pa0, 0u, pa2, 0u,
+                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(x23 & 0xffffu)),
+                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(y23 & 0xffffu)));
+    ptx::mma_16816<false>(o[4 * q + 3], pa0, 0u, pa2, 0u,
+                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(x23 >> 16)),
+                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(y23 >> 16)));
+  }
+}
+
+// Head dimension index of accumulator o[nt][e] held by thread t.
+template <int KVT>
+__device__ __forceinline__ int o_dim(int nt, int e, int t) {
+  if constexpr (KVT == kE4M3) {
+    return 32 * (nt >> 2) + 8 * t + 4 * e + (nt & 3);
+  } else {
+    return 8 * nt + 2 * t + e;
+  }
+}
+
+template <int QT>
+__device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
+  if constexpr (QT == kBF16) {
+    static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<__half*>(out)[idx] = __float2half_rn(v);
+  }
+}
+
+template <int QT, int KVT>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const DecodeParams p) {
+  using C = Cfg<KVT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  const uint32_t bar_full = base + C::kBars;
+  const uint32_t bar_empty = bar_full + 8 * C::kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kAbort);
+  float* comb_o = reinterpret_cast<float*>(base_ptr + C::kCombO);
+  float* comb_ml = reinterpret_cast<float*>(base_ptr + C::kCombML);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+#pragma unroll 1
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(bar_full + 8 * s, 1);
+      ptx::mbar_init(bar_empty + 8 * s, kConsumerWarps);
+    }
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int it0 = p.cta_begin[blockIdx.x];
+  const int it1 = p.cta_begin[blockIdx.x + 1];
+  const int Hk = p.num_kv_heads;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tmk);
+      ptx::prefetch_tensormap(&tmv);
+    }
+    const uint64_t policy = ptx::policy_evict_first();
+    const uint32_t box_bytes = static_cast<uint32_t>(p.box_tok) * 128u;
+    const uint32_t per_page = (C::kRowBytes == 256 ? 4u : 2u) * box_bytes;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+#pragma unroll 1
+    for (int it = it0; it < it1 && ok; ++it) {
+      const int4 item = p.items[it];
+      const int b = item.x / Hk;
+      const int h = item.x - b * Hk;
+      const int L = p.kv_len[b];
+      const int pb = p.page_begin[b];
+#pragma unroll 1
+      for (int k = item.y; k < item.z; ++k) {
+        int npg, first, tok_off;
+        if (p.pages_per_chunk > 0) {
+          first = k * p.pages_per_chunk;
+          const int row_pages = (L + p.page_size - 1) / p.page_size;
+          npg = min(p.pages_per_chunk, row_pages - first);
+          tok_off = 0;
+        } else {
+          npg = 1;
+          first = (k * kChunkKeys) / p.page_size;
+          tok_off = (k * kChunkKeys) - first * p.page_size;
+        }
+        int pid0 = 0, pid1 = 0;
+        if (lane < npg) pid0 = load_page(p, pb + first + lane);
+        if (lane + 32 < npg) pid1 = load_page(p, pb + first + lane + 32);
+        if (!stage_wait(bar_empty + 8 * s, ph ^ 1u, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = bar_full + 8 * s;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(npg) * per_page);
+        __syncwarp();
+        const uint32_t kdst = base + s * C::kStageBytes;
+        const uint32_t vdst = kdst + C::kTensorBytes;
+#pragma unroll 1
+        for (int j = lane; j < npg; j += 32) {
+          const int pid = (j < 32) ? pid0 : pid1;
+          const uint32_t off = static_cast<uint32_t>(j) * box_bytes;
+          if constexpr (C::kRowBytes == 256) {
+            constexpr uint32_t kHalf = kChunkKeys * 128u;
+            ptx::tma_load_4d_hint(kdst + off, &tmk, fb, 0, h, tok_off, pid, policy);
+            ptx::tma_load_4d_hint(kdst + kHalf + off, &tmk, fb, 64, h, tok_off, pid, policy);
+            ptx::tma_load_4d_hint(vdst + off, &tmv, fb, 0, h, tok_off, pid, policy);
+            ptx::tma_load_4d_hint(vdst + kHalf + off, &tmv, fb, 64, h, tok_off, pid, policy);
+          } else {
+            ptx::tma_load_4d_hint(kdst + off, &tmk, fb, 0, h, tok_off, pid, policy);
+            ptx::tma_load_4d_hint(vdst + off, &tmv, fb, 0, h, tok_off, pid, policy);
+          }
+        }
+        if (++s == C::kStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int w = warp;
+  const int gid = lane >> 2;
+  const int t = lane & 3;
+  const int G = p.group;
+  const int Hq = Hk * G;
+  int s = 0;
+  uint32_t ph = 0;
+#pragma unroll 1
+  for (int it = it0; it < it1; ++it) {
+    const int4 item = p.items[it];
+    const int b = item.x / Hk;
+    const int h = item.x - b * Hk;
+    const int L = p.kv_len[b];
+    const bool hv = gid < G;
+    const int qo = h * G + gid;
+    uint32_t qa0[8], qa2[8];
+    load_q<QT, KVT>(p, b, qo, hv, t, qa0, qa2);
+    const float sl2 = p.scale_log2 * (p.k_scale ? __ldg(p.k_scale + h) : 1.f);
+    float m_run = -INFINITY, l_run = 0.f;
+    float o[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[nt][i] = 0.f;
+
+#pragma unroll 1
+    for (int k = item.y; k < item.z; ++k) {
+      const int n_valid = min(p.chunk_keys, L - k * p.chunk_keys);
+      const bool ok = stage_wait(bar_full + 8 * s, ph, p.err, abort_flag);
+      const int valid = n_valid - 16 * w;
+      if (ok && valid > 0) {
+        const uint32_t kb = base + s * C::kStageBytes;
+        const uint32_t vb = kb + C::kTensorBytes;
+        if constexpr (KVT == kE4M3) {
+          tile16_e4m3(kb, vb, w, lane, valid, qa0, qa2, sl2, m_run, l_run, o);
+        } else {
+          tile16_16bit<C::kMmaBf16>(kb, vb, w, lane, valid, qa0, qa2, sl2, m_run, l_run, o);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
+      if (++s == C::kStages) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+
+    // ---- combine the four warps' states and write
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    ptx::named_bar_sync(1, kConsumerWarps * 32);
+    if (w > 0 && hv) {
+      float* dst = comb_o + ((w - 1) * kMaxGroup + gid) * kHeadDim;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        dst[o_dim<KVT>(nt, 0, t)] = o[nt][0];
+        dst[o_dim<KVT>(nt, 1, t)] = o[nt][1];
+      }
+      if (t == 0) {
+        comb_ml[((w - 1) * kMaxGroup + gid) * 2 + 0] = m_run;
+        comb_ml[((w - 1) * kMaxGroup + gid) * 2 + 1] = l_run;
+      }
+    }
+    ptx::named_bar_sync(1, kConsumerWarps * 32);
+    if (w == 0 && hv) {
+      float mw[4], lw[4];
+      mw[0] = m_run;
+      lw[0] = l_run;
+#pragma unroll
+      for (int i = 1; i < 4; ++i) {
+        mw[i] = comb_ml[((i - 1) * kMaxGroup + gid) * 2 + 0];
+        lw[i] = comb_ml[((i - 1) * kMaxGroup + gid) * 2 + 1];
+      }
+      const float M = fmaxf(fmaxf(mw[0], mw[1]), fmaxf(mw[2], mw[3]));
+      float sc[4];
+      float Ls = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sc[i] = (mw[i] == -INFINITY) ? 0.f : ptx::ex2(mw[i] - M);
+        Ls += lw[i] * sc[i];
+      }
+      const float inv = 1.f / Ls;
+      const float vsc = p.v_scale ? __ldg(p.v_scale + h) : 1.f;
+      const float lse2 = M + ptx::lg2(Ls);
+      const bool partial = (item.w & kItemSplit) || p.force_partial;
+      const float* c1 = comb_o + (0 * kMaxGroup + gid) * kHeadDim;
+      const float* c2 = comb_o + (1 * kMaxGroup + gid) * kHeadDim;
+      const float* c3 = comb_o + (2 * kMaxGroup + gid) * kHeadDim;
+      if (partial) {
+        float* po = p.part_o + (static_cast<size_t>(it) * G + gid) * kHeadDim;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int d = o_dim<KVT>(nt, e, t);
+            po[d] = (o[nt][e] * sc[0] + c1[d] * sc[1] + c2[d] * sc[2] + c3[d] * sc[3]) * inv * vsc;
+          }
+        }
+        if (t == 0) p.part_lse[static_cast<size_t>(it) * G + gid] = lse2;
+      } else {
+        const size_t orow = (static_cast<size_t>(b) * Hq + qo) * kHeadDim;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int d = o_dim<KVT>(nt, e, t);
+            const float v = (o[nt][e] * sc[0] + c1[d] * sc[1] + c2[d] * sc[2] + c3[d] * sc[3]) * inv * vsc;
+            store_out<QT>(p.out, orow + d, v);
+          }
+        }
+        if (t == 0 && p.lse) p.lse[static_cast<size_t>(b) * Hq + qo] = lse2 * kLn2;
+      }
+    }
+  }
+}
+
+template <int QT, int KVT>
+cudaError_t launch_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p, int grid,
+                     cudaStream_t stream) {
+  auto kern = decode_kernel<QT, KVT>;
+  const int smem = Cfg<KVT>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, stream>>>(tmk, tmv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_smem_bytes(int kv_dtype) {
+  return kv_dtype == kE4M3 ? Cfg<kE4M3>::kAlloc : Cfg<kBF16>::kAlloc;
+}
+
+cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
+                          int q_dtype, int kv_dtype, int grid, cudaStream_t stream) {
+  if (q_dtype == kF16 && kv_dtype == kF16) return launch_t<kF16, kF16>(tmk, tmv, p, grid, stream);
+  if (q_dtype == kBF16 && kv_dtype == kBF16) return launch_t<kBF16, kBF16>(tmk, tmv, p, grid, stream);
+  if (q_dtype == kBF16 && kv_dtype == kE4M3) return launch_t<kBF16, kE4M3>(tmk, tmv, p, grid, stream);
+  if (q_dtype == kF16 && kv_dtype == kE4M3) return launch_t<kF16, kE4M3>(tmk, tmv, p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pkd

@@ -1,0 +1,117 @@
+// pkd_internal.h -- structures shared by the host launchers and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkd {
+
+constexpr int kHeadDim = 128;
+constexpr int kChunkKeys = 64;        // keys per split-KV chunk (one pipeline stage)
+constexpr int kMaxGroup = 8;          // qo heads per kv head served by one MMA row tile
+constexpr int kMaxPrefixSplits = 16;  // cascade: pieces the shared prefix may be cut into
+constexpr int kCtasPerSm = 2;         // decode CTAs resident per SM
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // bounded pipeline waits
+
+constexpr unsigned kDevErrPageIndex = 1u;
+constexpr unsigned kDevErrWaitTimeout = 2u;
+
+enum DType : int { kF16 = 0, kBF16 = 1, kE4M3 = 2, kF32 = 3 };
+
+// Device header at the start of the workspace (int32 words).
+struct WsHeader {
+  unsigned err;       // PKD_DEVERR_* bits
+  int n_items;
+  int n_merge_rows;
+  int batch;
+  int zero_page;      // a page index of 0 for single-request decode
+  int pad[59];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// One split-KV work item: (row = b * Hk + h, first chunk, end chunk, flags).
+// flags bit 0: the row is split across items (write a partial state).
+constexpr int kItemSplit = 1;
+
+struct DecodeParams {
+  const int4* items;
+  const int* cta_begin;   // [G + 1]
+  const int* kv_len;      // [B]
+  const int* page_begin;  // [B]  (= kv_indptr[b])
+  const int* page_indices;
+  const void* q;          // [B, Hq, D]
+  void* out;              // [B, Hq, D]  (q dtype)
+  float* lse;             // [B, Hq] natural log, or nullptr
+  float* part_o;          // [slot, g, D] fp32
+  float* part_lse;        // [slot, g] base-2 log-sum-exp of the scaled scores
+  const float* k_scale;   // [Hk] or nullptr
+  const float* v_scale;
+  unsigned* err;
+  int num_kv_heads;
+  int group;
+  int page_size;          // plan page size
+  int pages_per_chunk;    // page_size <= 64: pages per chunk; else 0
+  int chunk_keys;         // keys per chunk
+  int box_tok;            // tokens per TMA box
+  int num_pages;          // pool pages (index validation)
+  float scale_log2;       // sm_scale * log2(e)
+  int force_partial;      // cascade: every item writes a partial state
+};
+
+struct MergeParams {
+  const int* merge_rows;      // rows to merge (normal mode)
+  const WsHeader* header;     // n_merge_rows, batch
+  const int* row_item_begin;  // [B * Hk]
+  const int* row_item_count;  // [B * Hk]
+  const float* part_o;        // [slot, g, D]
+  const float* part_lse;      // [slot, g] base 2
+  const float* pre_o;         // cascade: [split, B * Hq, D] or nullptr
+  const float* pre_lse;       // cascade: [split, B * Hq] base 2
+  int n_pre_splits;
+  void* out;
+  float* lse;
+  int out_dtype;
+  int num_kv_heads;
+  int group;
+  int all_rows;               // cascade: every row of the batch
+  const float* v_scale;       // unused (scales are applied before partials are written)
+};
+
+// Shared-prefix (cascade level 0) attention on the tensor cores.
+struct PrefixParams {
+  const int* prefix_pages;  // [n_prefix_pages]
+  int n_prefix_pages;
+  int prefix_len;           // keys in the prefix
+  int batch;
+  int num_kv_heads;
+  int group;
+  int num_pages;
+  int page_size;
+  int n_splits;             // key-range pieces
+  int tiles_per_split;      // 128-key tiles per piece
+  int m_tiles;              // 128-row query tiles per kv head
+  float scale_log2;
+  float* pre_o;             // [split, B * Hq, D]
+  float* pre_lse;           // [split, B * Hq] base 2
+  const float* k_scale;
+  const float* v_scale;
+  unsigned* err;
+};
+
+// Launchers (defined in the .cu files; return a cudaError_t).
+cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
+                          int q_dtype, int kv_dtype, int grid, cudaStream_t stream);
+cudaError_t launch_merge_rows(const MergeParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, const float* sb,
+                               void* vo, float* so, int64_t n, int heads, int dim, int dtype,
+                               cudaStream_t stream);
+cudaError_t launch_merge_states(const void* v, const float* s, int64_t n, int k, int heads, int dim,
+                                int dtype, void* vo, float* so, cudaStream_t stream);
+cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                          const PrefixParams& p, int kv_dtype, cudaStream_t stream);
+int decode_smem_bytes(int kv_dtype);
+int prefix_smem_bytes();
+
+}  // namespace pkd
