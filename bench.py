@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Benchmark of batched paged-KV decode attention on GB300.
+
+One step = the whole decode hot path over one batch: the host plan (split-KV
+schedule, one async upload) followed by run (the TMA-pipelined decode kernel
+and the split-KV merge kernel) on inputs resident in HBM.  The default workload
+is the batch-64 GQA decode batch (64 requests, 32 qo / 8 kv heads, head_dim
+128, bf16, lengths uniform in [512, 4096], page size 16, pages drawn from a
+20000-page pool).  Its K/V bytes (0.58 GB) exceed the 129 MB L2, so no flush
+is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+on the host cores instead (the reference arm).  Under torchrun every rank runs
+its own replica of the batch on its own GPU (weak scaling, no collective on the
+data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak) and µs/call per batch"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+KERNEL_SOURCES = ["paged_kv_decode_28_gb300/csrc/pkd_decode.cu", "paged_kv_decode_28_gb300/csrc/pkd_ptx.cuh",
+                  "paged_kv_decode_28_gb300/csrc/pkd_internal.h"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, help="standard workload index (1..5)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all-configs", action="store_true", help="also print one line per standard workload")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="shrink the workload to its first N requests (small cases for profiling)")
+    return ap.parse_args()
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(b) -> int:
+    """K/V bytes of the valid keys of every (request, kv head) row, plus q, out,
+    lse and the fp8 scales.  Split-KV partials and the schedule are excluded."""
+    e_kv = b.k_cache.element_size()
+    e_q = b.q.element_size()
+    kv = int(np.asarray(b.kv_lens, dtype=np.int64).sum()) * b.num_kv_heads * b.head_dim * 2 * e_kv
+    if b.prefix_page_indices is not None:
+        kv += b.prefix_len * b.num_kv_heads * b.head_dim * 2 * e_kv  # shared prefix counted once
+    qo = b.batch * b.num_qo_heads * b.head_dim * 2 * e_q
+    lse = 4 * b.batch * b.num_qo_heads
+    scales = 8 * b.num_kv_heads if b.k_scale is not None else 0
+    return kv + qo + lse + scales
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def cpu_sample_batch(b, n_req: int):
+    """The first n_req requests of a batch, with their pages gathered into a
+    compact host pool (input preparation for the CPU oracle)."""
+    import torch
+
+    pages, indptr, last = [], [0], []
+    for r in range(n_req):
+        own = b.kv_page_indices[b.kv_indptr[r]:b.kv_indptr[r + 1]]
+        pages.append(own)
+        indptr.append(indptr[-1] + len(own))
+        last.append(int(b.kv_last_page_len[r]))
+    allp = np.concatenate(pages).astype(np.int64)
+    sel = torch.as_tensor(allp, device=b.k_cache.device)
+    k = b.k_cache[sel].cpu().contiguous()
+    v = b.v_cache[sel].cpu().contiguous()
+    q = b.q[:n_req].cpu().contiguous()
+    idx = np.arange(len(allp), dtype=np.int32)
+    lens = b.kv_lens[:n_req]
+    return q, k, v, np.asarray(indptr, np.int32), idx, np.asarray(last, np.int32), lens
+
+
+def time_cpu_oracle(b, target_s: float, max_req=None):
+    """Run the C fp64 oracle on a bounded sample of requests (all qo heads).
+    Returns (GB/s of algorithmic bytes, seconds, requests, threads)."""
+    from oracle import c_oracle
+
+    threads = c_oracle.max_threads()
+    e_kv = b.k_cache.element_size()
+    ks = None if b.k_scale is None else b.k_scale.cpu()
+    vs = None if b.v_scale is None else b.v_scale.cpu()
+
+    def run(n):
+        q, k, v, indptr, idx, last, lens = cpu_sample_batch(b, n)
+        t0 = time.perf_counter()
+        c_oracle.paged_decode(q, k, v, indptr, idx, last, sm_scale=b.sm_scale, k_scale=ks, v_scale=vs,
+                              num_threads=threads)
+        dt = time.perf_counter() - t0
+        nbytes = (int(np.asarray(lens, np.int64).sum()) * b.num_kv_heads * b.head_dim * 2 * e_kv
+                  + n * b.num_qo_heads * b.head_dim * 2 * b.q.element_size() + 4 * n * b.num_qo_heads)
+        return nbytes, dt
+
+    nb1, dt1 = run(1)
+    n = int(max(1, min(max_req or b.batch, math.floor(target_s / max(dt1, 1e-6)))))
+    nbytes, dt = run(n)
+    reps = 1
+    if target_s > 0 and dt < 0.5 * target_s:  # whole batch is quick: repeat it to time a few seconds
+        reps = int(min(100, math.ceil(0.5 * target_s / max(dt, 1e-6))))
+        tot = 0.0
+        for _ in range(reps):
+            tot += run(n)[1]
+        dt = tot / reps
+    return nbytes / dt / 1e9, dt * reps, n, threads
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import paged_kv_decode_28_gb300 as pkd
+    from paged_kv_decode_28_gb300 import _build
+    from paged_kv_decode_28_gb300 import workloads as wl
+
+    _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    b = wl.make_config(args.config, device=dev, batch=args.batch)
+    cascade = b.prefix_page_indices is not None
+    idx = torch.from_numpy(b.kv_page_indices).to(dev)
+    pre = torch.from_numpy(b.prefix_page_indices).to(dev) if cascade else None
+    plan = pkd.Plan(b.batch, b.num_qo_heads, b.num_kv_heads, max_prefix_splits=16 if cascade else 0, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = torch.empty_like(b.q)
+    lse = torch.empty(b.batch, b.num_qo_heads, dtype=torch.float32, device=dev)
+    kw = dict(sm_scale=b.sm_scale, k_scale=b.k_scale, v_scale=b.v_scale, out=out, lse=lse)
+
+    def step():
+        plan.plan(b.kv_indptr, idx, b.kv_last_page_len, b.page_size, q_dtype=b.q.dtype, kv_dtype=b.k_cache.dtype)
+        if cascade:
+            plan.cascade_decode(pre, b.prefix_last_page_len, b.q, b.k_cache, b.v_cache, **kw)
+        else:
+            plan.run(b.q, b.k_cache, b.v_cache, **kw)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert plan.check_device_errors() == 0
+
+    # ---- device-timed steps, with the decode kernel timed alone by the library's event hook
+    K = args.steps
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, z in kev:  # torch creates the CUDA event at its first record; the library re-records it
+        a.record(stream)
+        z.record(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(K):
+            plan.set_timing_events(*kev[i])
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    plan.set_timing_events(None, None)
+    clk = clocks.summary()
+    ms_total = e0.elapsed_time(e1)
+    ms_total_max = max_over_ranks(ms_total, world, dev)
+    ms_step = ms_total_max / K
+    kern_ms = [a.elapsed_time(z) for a, z in kev]
+    kern_avg_ms = sum(kern_ms) / K
+    nbytes = algorithmic_bytes(b)
+    value = world * nbytes / (ms_step * 1e-3) / 1e9
+    assert plan.check_device_errors() == 0
+
+    # ---- end to end through the C ABI with host buffers: q and the page table in, out and lse back
+    q_h = b.q.cpu().pin_memory()
+    idx_h = torch.from_numpy(b.kv_page_indices.copy()).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d = torch.empty_like(b.q)
+    idx_d = torch.empty_like(idx)
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        idx_d.copy_(idx_h, non_blocking=True)
+        plan.plan(b.kv_indptr, idx_d, b.kv_last_page_len, b.page_size, q_dtype=b.q.dtype, kv_dtype=b.k_cache.dtype)
+        if cascade:
+            plan.cascade_decode(pre, b.prefix_last_page_len, q_d, b.k_cache, b.v_cache, **kw)
+        else:
+            plan.run(q_d, b.k_cache, b.v_cache, **kw)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e_value = world * nbytes / (e2e_s / K) / 1e9
+    h2d = q_h.numel() * q_h.element_size() + idx_h.numel() * 4 + (b.batch + 1) * 4 + b.batch * 4
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+
+    peak, peak_kind = measured_hbm_peak()
+    achieved = nbytes / (kern_avg_ms * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_hash") == kernel_hash() and tr.get("config") == args.config:
+            traffic = tr.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "us_per_call": round(ms_step * 1e3, 2),
+        "tokens_per_s": round(world * b.batch / (ms_step * 1e-3), 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {torch.bfloat16: "bf16", torch.float16: "f16"}[b.q.dtype] + (
+            "+e4m3kv" if b.k_cache.dtype == torch.float8_e4m3fn else ""),
+        "data": "synthetic (seeded N(0,1) values, seeded lengths and page placement)",
+        "config": {
+            "workload": b.name,
+            "batch": b.batch,
+            "num_qo_heads": b.num_qo_heads,
+            "num_kv_heads": b.num_kv_heads,
+            "head_dim": b.head_dim,
+            "page_size": b.page_size,
+            "kv_tokens": int(np.asarray(b.kv_lens, np.int64).sum()),
+            "algorithmic_bytes_per_step": nbytes,
+            "l2": f"inputs {nbytes / 1e9:.2f} GB > 129 MB L2; no flush between steps",
+            "parallelism": f"replicas x{world} (one batch per GPU)",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "pkd decode_kernel",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "kernel_us": round(kern_avg_ms * 1e3, 2),
+        },
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "us_per_step": round(e2e_s / K * 1e6, 2)},
+        "gpu_launches": K * (3 if cascade else 2),
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, secs, n_req, threads = time_cpu_oracle(b, target_s=10.0)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"{n_req} of {b.batch} requests, all {b.num_qo_heads} qo heads "
+                                          f"(C fp64 oracle, {secs:.1f} s)"}
+    return line
+
+
+def run_reference(args, world, rank, local):
+    """The reference arm: the fp64 CPU oracle on the host cores, on a bounded
+    sample of the same workload each step."""
+    import torch
+
+    from paged_kv_decode_28_gb300 import workloads as wl
+    from oracle import c_oracle
+
+    if rank != 0:
+        return None
+    c_oracle.build()
+    # the same seeded inputs as the GPU arm (generated by the device RNG when a GPU is present)
+    b = wl.make_config(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
+    threads = c_oracle.max_threads()
+    K, W = args.steps, max(args.warmup, 0)
+    budget = 150.0  # seconds for the whole run
+    _, dt1, _, _ = time_cpu_oracle(b, target_s=0.0, max_req=1)
+    per_step = budget / max(K + W, 1)
+    n_req = int(max(1, min(b.batch, math.floor(per_step / max(dt1, 1e-6)))))
+    q, k, v, indptr, idx, last, lens = cpu_sample_batch(b, n_req)
+    ks = None if b.k_scale is None else b.k_scale.cpu()
+    vs = None if b.v_scale is None else b.v_scale.cpu()
+
+    def step():
+        c_oracle.paged_decode(q, k, v, indptr, idx, last, sm_scale=b.sm_scale, k_scale=ks, v_scale=vs,
+                              num_threads=threads)
+
+    for _ in range(W):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        step()
+    secs = (time.perf_counter() - t0) / K
+    e_kv = b.k_cache.element_size()
+    nbytes = (int(np.asarray(lens, np.int64).sum()) * b.num_kv_heads * b.head_dim * 2 * e_kv
+              + n_req * b.num_qo_heads * b.head_dim * 2 * b.q.element_size() + 4 * n_req * b.num_qo_heads)
+    value = nbytes / secs / 1e9
+    sample = f"{n_req} of {b.batch} requests per step, all {b.num_qo_heads} qo heads (C fp64 oracle)"
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(secs * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) values, seeded lengths and page placement)",
+        "config": {"workload": b.name, "batch": b.batch, "num_qo_heads": b.num_qo_heads,
+                   "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "page_size": b.page_size,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_init(args)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank, local)
+    else:
+        line = run_ours(args, world, rank, local)
+        if args.all_configs and rank == 0 and world == 1:
+            for c in (1, 2, 3, 4, 5):
+                if c == args.config:
+                    continue
+                a2 = argparse.Namespace(**{**vars(args), "config": c, "no_cpu_baseline": True})
+                try:
+                    print(json.dumps(run_ours(a2, world, rank, local)), flush=True)
+                except Exception as exc:  # keep the headline line even if one extra workload fails
+                    print(json.dumps({"config": c, "error": str(exc)}), file=sys.stderr, flush=True)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

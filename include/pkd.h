@@ -129,10 +129,12 @@ pkd_status pkd_plan_destroy(pkd_plan_t plan);
  * order r = b * num_kv_heads + h, is divided into num_ctas equal contiguous
  * runs of ceil(total / num_ctas) chunks, one per CTA.  A row that falls to one
  * CTA is written directly; rows split across CTAs are merged by a second pass.
- * The schedule is copied into the workspace with one cudaMemcpyAsync from
- * pageable host memory on `stream`, so plan must not be called during stream
- * capture; the launch shape of run never changes, so a graph captured around
- * run stays valid across re-plans of the same plan object.
+ * The schedule is copied into the workspace with one cudaMemcpyAsync on
+ * `stream` from a pinned staging buffer owned by the plan (two slots; reusing a
+ * slot waits for the copy issued two plans earlier), so plan does not wait for
+ * the GPU.  plan must not be called during stream capture; the launch shape of
+ * run never changes, so a graph captured around run stays valid across
+ * re-plans of the same plan object.
  */
 pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* d_kv_page_indices,
                     const int32_t* h_kv_last_page_len, int batch, int num_qo_heads,
@@ -214,6 +216,15 @@ pkd_status pkd_merge_state(const void* d_v_a, const float* d_s_a, const void* d_
 pkd_status pkd_merge_states(const void* d_v, const float* d_s, int64_t n, int k, int num_heads,
                             int head_dim, int v_dtype, void* d_v_out, float* d_s_out,
                             void* stream);
+
+/*
+ * Timing hook: when both are non-NULL, pkd_run and pkd_cascade_decode record
+ * start_event just before the decode kernel and stop_event just after it, on
+ * the call's stream (cudaEvent_t handles passed as void*; the caller owns
+ * them).  NULL, NULL turns the hook off.  Lets a caller time the dominant
+ * kernel alone with CUDA events.
+ */
+pkd_status pkd_plan_set_timing_events(pkd_plan_t plan, void* start_event, void* stop_event);
 
 /*
  * Read and clear the plan's device error word (PKD_DEVERR_* bits), after

@@ -65,6 +65,7 @@ def lib() -> ctypes.CDLL:
         "pkd_merge_state": (i, [_vp, _vp, _vp, _vp, _vp, _vp, i64, i, i, i, _vp]),
         "pkd_merge_states": (i, [_vp, _vp, i64, i, i, i, i, _vp, _vp, _vp]),
         "pkd_check_device_errors": (i, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
+        "pkd_plan_set_timing_events": (i, [_vp, _vp, _vp]),
         "pkd_plan_host": (i, [_i32p, _i32p, i, i, i, i, _i32p, i, _i32p, _i32p, _i32p, _i32p, _i32p]),
     }
     for name, (res, args) in sig.items():
@@ -242,6 +243,12 @@ class Plan:
                                         stride, _ptr(k_scale), _ptr(v_scale), float(sm_scale or 0.0),
                                         _ptr(out), _ptr(lse), _stream(stream)))
         return out, lse
+
+    def set_timing_events(self, start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
+        """Record ``start``/``stop`` around the decode kernel of later run/cascade calls (None, None: off)."""
+        a = None if start is None else ctypes.c_void_p(start.cuda_event)
+        b = None if stop is None else ctypes.c_void_p(stop.cuda_event)
+        _check(lib().pkd_plan_set_timing_events(self._h, a, b))
 
     def check_device_errors(self, stream=None) -> int:
         flags = ctypes.c_uint32(0)

@@ -130,6 +130,22 @@ struct pkd_plan_s {
   // last plan
   bool planned = false;
   bool err_word_zeroed = false;  // the first plan clears the device error word
+  // pinned double buffer for the schedule upload; an event per slot guards reuse
+  bool use_pinned = true;
+  uint8_t* pinned[2] = {nullptr, nullptr};
+  cudaEvent_t pinned_done[2] = {nullptr, nullptr};
+  int next_slot = 0;
+  // optional caller events recorded around the decode kernel (timing hook)
+  cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
+  ~pkd_plan_s() {
+    for (int i = 0; i < 2; ++i) {
+      if (pinned_done[i]) {
+        cudaEventSynchronize(pinned_done[i]);
+        cudaEventDestroy(pinned_done[i]);
+      }
+      if (pinned[i]) cudaFreeHost(pinned[i]);
+    }
+  }
   int batch = 0, page_size = 0, q_dtype = 0, kv_dtype = 0;
   const int32_t* d_page_indices = nullptr;
   pkd::PlanCounts counts{};
@@ -287,9 +303,32 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
     plan->err_word_zeroed = true;
   }
   // one copy of everything after the error word (the error word stays the kernels')
-  cudaError_t e = cudaMemcpyAsync(plan->ws + 4, h + 4, L.meta_end - 4, cudaMemcpyHostToDevice,
-                                  static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint8_t* src = h;
+  int slot = -1;
+  if (plan->use_pinned) {
+    slot = plan->next_slot;
+    if (!plan->pinned[slot]) {
+      cudaError_t ea = cudaHostAlloc(reinterpret_cast<void**>(&plan->pinned[slot]), L.meta_end,
+                                     cudaHostAllocDefault);
+      if (ea != cudaSuccess) return cuda_fail(ea, "cudaHostAlloc(plan staging)");
+      ea = cudaEventCreateWithFlags(&plan->pinned_done[slot], cudaEventDisableTiming);
+      if (ea != cudaSuccess) return cuda_fail(ea, "cudaEventCreate(plan staging)");
+    } else {
+      // the copy that last used this slot was issued two plans ago
+      cudaError_t ea = cudaEventSynchronize(plan->pinned_done[slot]);
+      if (ea != cudaSuccess) return cuda_fail(ea, "cudaEventSynchronize(plan staging)");
+    }
+    memcpy(plan->pinned[slot] + 4, h + 4, L.meta_end - 4);
+    src = plan->pinned[slot];
+  }
+  cudaError_t e = cudaMemcpyAsync(plan->ws + 4, src + 4, L.meta_end - 4, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan)");
+  if (slot >= 0) {
+    e = cudaEventRecord(plan->pinned_done[slot], st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(plan staging)");
+    plan->next_slot = slot ^ 1;
+  }
   plan->planned = true;
   plan->batch = batch;
   plan->page_size = page_size;
@@ -361,8 +400,16 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
     s = encode_kv_map(&tmv, d_v_cache, plan->kv_dtype, plan->hk, tok_extent, num_pages, page_stride_elems,
                       box_tok);
     if (s != PKD_OK) return s;
+    if (plan->ev_start) {
+      cudaError_t er = cudaEventRecord(plan->ev_start, st);
+      if (er != cudaSuccess) return cuda_fail(er, "cudaEventRecord(timing start)");
+    }
     cudaError_t e = pkd::launch_decode(tmk, tmv, p, plan->q_dtype, plan->kv_dtype, plan->G, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    if (plan->ev_stop) {
+      cudaError_t er = cudaEventRecord(plan->ev_stop, st);
+      if (er != cudaSuccess) return cuda_fail(er, "cudaEventRecord(timing stop)");
+    }
   }
   pkd::MergeParams m{};
   m.merge_rows = reinterpret_cast<const int*>(ws + L.merge_rows);
@@ -433,6 +480,7 @@ pkd_status pkd_single_decode(const void* d_q, const void* d_k, const void* d_v, 
   const int32_t last[1] = {kv_len > 0 ? kv_len : 0};
   const int32_t* zero_page = reinterpret_cast<const int32_t*>(
       static_cast<uint8_t*>(d_workspace) + offsetof(pkd::WsHeader, zero_page));
+  plan->use_pinned = false;  // a one-shot plan: the pageable copy is staged before return
   s = pkd_plan(plan, indptr, zero_page, last, 1, num_qo_heads, num_kv_heads, head_dim, P, q_dtype,
                kv_dtype, stream);
   if (s == PKD_OK) {
@@ -471,6 +519,15 @@ pkd_status pkd_merge_states(const void* d_v, const float* d_s, int64_t n, int k,
   cudaError_t e = pkd::launch_merge_states(d_v, d_s, n, k, num_heads, head_dim, v_dtype, d_v_out, d_s_out,
                                            static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge_states kernel launch");
+  return PKD_OK;
+}
+
+pkd_status pkd_plan_set_timing_events(pkd_plan_t plan, void* start_event, void* stop_event) {
+  if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
+  if ((start_event == nullptr) != (stop_event == nullptr))
+    return fail(PKD_ERR_INVALID_ARG, "give both timing events or neither");
+  plan->ev_start = static_cast<cudaEvent_t>(start_event);
+  plan->ev_stop = static_cast<cudaEvent_t>(stop_event);
   return PKD_OK;
 }
 
