@@ -233,6 +233,41 @@ pkd_status pkd_plan_set_timing_events(pkd_plan_t plan, void* start_event, void* 
 pkd_status pkd_check_device_errors(pkd_plan_t plan, uint32_t* flags_out, void* stream);
 
 /*
+ * Batched paged decode that allocates nothing (the pages have no counterpart:
+ * this is a library convenience, not part of the method).
+ *
+ * For callers that may not allocate device memory when they run attention --
+ * a serving loop whose memory is carved out up front by its own pool (a
+ * cudaMalloc there can synchronise the device and fragment the pool), a plugin
+ * inside a runtime that owns every allocation, or code held to a fixed memory
+ * footprint.  It takes the arguments of pkd_plan and pkd_run together and does
+ * both, using a scratch area built into the library instead of a caller
+ * workspace: PKD_NOALLOC_SCRATCH_BYTES of device memory that every GPU loading
+ * this library holds until the process exits.  Calls that need more scratch
+ * (roughly: batch * num_kv_heads + 2 * SM count work items, each with
+ * g * 128 fp32 partial outputs) return PKD_ERR_CAPACITY_EXCEEDED with a message.
+ * No cudaMalloc, cudaFree, pinned-host or other allocating call is made.
+ *   - The first call on a device looks up that device's scratch address
+ *     (cudaGetSymbolAddress, with the device current); make that first call
+ *     before any stream capture on the device.
+ *   - All calls share the one scratch area per device and the schedule upload
+ *     is a cudaMemcpyAsync on `stream`: calls whose work can overlap on the GPU
+ *     (different streams, different threads) race and must be serialised by the
+ *     caller.  Each call resets what must start at zero.
+ *   - Device error bits (PKD_DEVERR_*) are recorded in the scratch area and are
+ *     not reported back; an out-of-range page id is read as page 0.
+ * Arguments as pkd_plan and pkd_run (h_* are host arrays, d_* device).
+ */
+#define PKD_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32_t* d_kv_page_indices,
+                              const int32_t* h_kv_last_page_len, int batch, int num_qo_heads,
+                              int num_kv_heads, int head_dim, int page_size, int q_dtype,
+                              int kv_dtype, const void* d_q, const void* d_k_cache,
+                              const void* d_v_cache, int64_t num_pages, int64_t page_stride_elems,
+                              const float* d_k_scale, const float* d_v_scale, float sm_scale,
+                              void* d_out, float* d_lse, void* stream);
+
+/*
  * The split-KV rule of pkd_plan, run on the host only (no GPU), for
  * inspection and testing.  Outputs (caller-allocated host arrays):
  *   items           int32 [max_items * 4]: (row, chunk_begin, chunk_end, cta) per item,

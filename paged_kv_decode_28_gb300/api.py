@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
         "pkd_merge_states": (i, [_vp, _vp, i64, i, i, i, i, _vp, _vp, _vp]),
         "pkd_check_device_errors": (i, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
         "pkd_plan_set_timing_events": (i, [_vp, _vp, _vp]),
+        "pkd_decode_noalloc": (i, [_i32p, _vp, _i32p, i, i, i, i, i, i, i, _vp, _vp, _vp, i64, i64, _vp, _vp, f,
+                                   _vp, _vp, _vp]),
         "pkd_plan_host": (i, [_i32p, _i32p, i, i, i, i, _i32p, i, _i32p, _i32p, _i32p, _i32p, _i32p]),
     }
     for name, (res, args) in sig.items():
@@ -307,3 +309,22 @@ def merge_states(v: torch.Tensor, s: torch.Tensor, *, stream=None):
     _check(lib().pkd_merge_states(_ptr(v), _ptr(s), n, k, H, D, _DTYPE_CODE[v.dtype], _ptr(out), _ptr(s_out),
                                   _stream(stream)))
     return out, s_out
+
+
+def decode_noalloc(kv_indptr, kv_page_indices: torch.Tensor, kv_last_page_len, page_size: int, q: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor, out: torch.Tensor, lse: torch.Tensor, *,
+                   sm_scale: Optional[float] = None, k_scale=None, v_scale=None, stream=None):
+    """Plan + run in one call that allocates nothing on the device: the library's
+    built-in scratch area replaces the workspace (see ``pkd_decode_noalloc``).
+    ``out`` and ``lse`` are caller-provided; the first call on a device must
+    come before any stream capture on it."""
+    N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache)
+    indptr = _host_i32(kv_indptr)
+    last = _host_i32(kv_last_page_len)
+    B = len(indptr) - 1
+    last_arg = last if len(last) else np.zeros(1, np.int32)
+    _check(lib().pkd_decode_noalloc(_as_i32p(indptr), _ptr(kv_page_indices), _as_i32p(last_arg), B, q.shape[1],
+                                    Hk, D, page_size, _DTYPE_CODE[q.dtype], _DTYPE_CODE[k_cache.dtype], _ptr(q),
+                                    _ptr(k_cache), _ptr(v_cache), N, stride, _ptr(k_scale), _ptr(v_scale),
+                                    float(sm_scale or 0.0), _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse

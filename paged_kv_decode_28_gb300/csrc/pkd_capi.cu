@@ -121,6 +121,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+namespace pkd {
+// Lets other translation units of the library report through pkd_last_error().
+void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace pkd
+
 struct pkd_plan_s {
   int max_batch, hq, hk, d, G, max_splits;
   uint8_t* ws;
