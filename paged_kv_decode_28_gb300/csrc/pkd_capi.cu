@@ -348,10 +348,17 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
 
 namespace {
 
+// Cascade settings for run_common: every item writes a partial state and the
+// merge pass folds n_pre_splits prefix partials into every row.
+struct CascadeMerge {
+  int n_pre_splits;
+};
+
 pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, const void* d_v_cache,
                       int64_t num_pages, int64_t page_stride_elems, int64_t tok_extent,
                       const float* d_k_scale, const float* d_v_scale, float sm_scale, void* d_out,
-                      float* d_lse, void* stream, const int32_t* page_indices_override) {
+                      float* d_lse, void* stream, const int32_t* page_indices_override,
+                      const CascadeMerge* cascade = nullptr) {
   if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
   if (!plan->planned) return fail(PKD_ERR_NO_PLAN, "run before a successful plan");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -389,7 +396,7 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
   p.box_tok = box_tok;
   p.num_pages = static_cast<int>(num_pages);
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.force_partial = 0;
+  p.force_partial = cascade ? 1 : 0;
   if (plan->counts.n_items > 0) {
     if (!d_k_cache || !d_v_cache) return fail(PKD_ERR_INVALID_ARG, "k/v cache is NULL");
     if (!aligned16(d_k_cache) || !aligned16(d_v_cache))
@@ -423,15 +430,15 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
   m.row_item_count = reinterpret_cast<const int*>(ws + L.row_count);
   m.part_o = p.part_o;
   m.part_lse = p.part_lse;
-  m.pre_o = nullptr;
-  m.pre_lse = nullptr;
-  m.n_pre_splits = 0;
+  m.pre_o = reinterpret_cast<const float*>(ws + L.pre_o);
+  m.pre_lse = reinterpret_cast<const float*>(ws + L.pre_lse);
+  m.n_pre_splits = cascade ? cascade->n_pre_splits : 0;
   m.out = d_out;
   m.lse = d_lse;
   m.out_dtype = plan->q_dtype;
   m.num_kv_heads = plan->hk;
   m.group = p.group;
-  m.all_rows = 0;
+  m.all_rows = cascade ? 1 : 0;
   cudaError_t e = pkd::launch_merge_rows(m, plan->G, st);
   if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
   return PKD_OK;
@@ -449,16 +456,95 @@ pkd_status pkd_run(pkd_plan_t plan, const void* d_q, const void* d_k_cache, cons
                     d_k_scale, d_v_scale, sm_scale, d_out, d_lse, stream, nullptr);
 }
 
-pkd_status pkd_cascade_decode(pkd_plan_t suffix_plan, const int32_t* d_prefix_page_indices,
+pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indices,
                               int prefix_num_pages, int prefix_last_page_len, const void* d_q,
                               const void* d_k_cache, const void* d_v_cache, int64_t num_pages,
                               int64_t page_stride_elems, const float* d_k_scale,
                               const float* d_v_scale, float sm_scale, void* d_out, float* d_lse,
                               void* stream) {
-  (void)suffix_plan; (void)d_prefix_page_indices; (void)prefix_num_pages; (void)prefix_last_page_len;
-  (void)d_q; (void)d_k_cache; (void)d_v_cache; (void)num_pages; (void)page_stride_elems;
-  (void)d_k_scale; (void)d_v_scale; (void)sm_scale; (void)d_out; (void)d_lse; (void)stream;
-  return fail(PKD_ERR_UNSUPPORTED, "cascade decode is not built yet");
+  if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
+  if (!plan->planned) return fail(PKD_ERR_NO_PLAN, "cascade_decode before a successful plan");
+  if (plan->max_splits < 1)
+    return fail(PKD_ERR_CAPACITY_EXCEEDED, "the plan was created with max_prefix_splits = 0");
+  if (plan->kv_dtype == PKD_E4M3)
+    return fail(PKD_ERR_UNSUPPORTED, "cascade decode is built for f16/bf16 caches only");
+  const int g = plan->hq / plan->hk;
+  if (pkd::kHeadDim % g != 0) return fail(PKD_ERR_UNSUPPORTED, "cascade decode needs a group size dividing 128");
+  const int P = plan->page_size;
+  if (P <= pkd::kChunkKeys ? (128 % P != 0) : (P % pkd::kChunkKeys != 0))
+    return fail(PKD_ERR_UNSUPPORTED, "cascade decode needs a page size dividing 128 or a multiple of 64");
+  if (prefix_num_pages < 0) return fail(PKD_ERR_INVALID_ARG, "prefix_num_pages must be >= 0");
+  if (prefix_num_pages > 0 && (prefix_last_page_len < 1 || prefix_last_page_len > P))
+    return fail(PKD_ERR_INVALID_ARG, "prefix_last_page_len %d outside 1..page_size", prefix_last_page_len);
+  if (prefix_num_pages > 0 && !d_prefix_page_indices)
+    return fail(PKD_ERR_INVALID_ARG, "d_prefix_page_indices is NULL");
+  const int64_t prefix_len64 = prefix_num_pages > 0 ? static_cast<int64_t>(prefix_num_pages - 1) * P + prefix_last_page_len : 0;
+  if (prefix_len64 > INT32_MAX) return fail(PKD_ERR_INVALID_ARG, "prefix longer than 2^31 - 1 keys");
+  const int prefix_len = static_cast<int>(prefix_len64);
+  const int B = plan->batch;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int n_pre = 0;
+  if (prefix_len > 0 && B > 0) {
+    if (!d_q || !aligned16(d_q)) return fail(PKD_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
+    if (!d_k_cache || !d_v_cache || !aligned16(d_k_cache) || !aligned16(d_v_cache))
+      return fail(PKD_ERR_INVALID_ARG, "k/v cache must be non-NULL and 16-byte aligned");
+    if (num_pages <= 0 || num_pages > INT32_MAX) return fail(PKD_ERR_INVALID_ARG, "num_pages out of range");
+    if ((page_stride_elems * elem_bytes(plan->kv_dtype)) % 16 != 0 ||
+        page_stride_elems < static_cast<int64_t>(P) * plan->hk * plan->d)
+      return fail(PKD_ERR_INVALID_ARG, "page_stride_elems must cover a page and be a 16-byte multiple");
+    const int n_tiles = (prefix_len + 127) / 128;
+    const int m_tiles = (B * g + 127) / 128;
+    const int sms = plan->G / pkd::kCtasPerSm;
+    int splits = sms / (plan->hk * m_tiles);
+    splits = splits < 1 ? 1 : splits;
+    splits = splits > plan->max_splits ? plan->max_splits : splits;
+    splits = splits > n_tiles ? n_tiles : splits;
+    const int tps = (n_tiles + splits - 1) / splits;
+    splits = (n_tiles + tps - 1) / tps;
+    // Q viewed as [B][Hk][g][128]: a box of 128 / g requests x g heads is one 128-row tile
+    auto enc = get_encode();
+    if (!enc) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    CUtensorMap tmq, tmk, tmv;
+    cuuint64_t qdims[4] = {static_cast<cuuint64_t>(pkd::kHeadDim), static_cast<cuuint64_t>(g),
+                           static_cast<cuuint64_t>(plan->hk), static_cast<cuuint64_t>(B)};
+    cuuint64_t qstr[3] = {static_cast<cuuint64_t>(pkd::kHeadDim) * 2, static_cast<cuuint64_t>(g) * pkd::kHeadDim * 2,
+                          static_cast<cuuint64_t>(plan->hq) * pkd::kHeadDim * 2};
+    cuuint32_t qbox[4] = {64u, static_cast<cuuint32_t>(g), 1u, static_cast<cuuint32_t>(128 / g)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(&tmq, plan->q_dtype == PKD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     4, const_cast<void*>(d_q), qdims, qstr, qbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed (CUresult %d)", (int)r);
+    const int box_tok = P <= pkd::kChunkKeys ? P : pkd::kChunkKeys;
+    pkd_status s = encode_kv_map(&tmk, d_k_cache, plan->kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok);
+    if (s != PKD_OK) return s;
+    s = encode_kv_map(&tmv, d_v_cache, plan->kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok);
+    if (s != PKD_OK) return s;
+    const float scale = (sm_scale > 0.f) ? sm_scale : 1.0f / std::sqrt(static_cast<float>(plan->d));
+    pkd::PrefixParams pp{};
+    pp.prefix_pages = d_prefix_page_indices;
+    pp.n_prefix_pages = prefix_num_pages;
+    pp.prefix_len = prefix_len;
+    pp.batch = B;
+    pp.num_kv_heads = plan->hk;
+    pp.group = g;
+    pp.num_pages = static_cast<int>(num_pages);
+    pp.page_size = P;
+    pp.box_tok = box_tok;
+    pp.n_splits = splits;
+    pp.tiles_per_split = tps;
+    pp.m_tiles = m_tiles;
+    pp.scale_log2 = scale * 1.4426950408889634f;
+    pp.pre_o = reinterpret_cast<float*>(plan->ws + plan->lay.pre_o);
+    pp.pre_lse = reinterpret_cast<float*>(plan->ws + plan->lay.pre_lse);
+    pp.err = reinterpret_cast<unsigned*>(plan->ws);
+    cudaError_t e = pkd::launch_prefix(tmq, tmk, tmv, pp, plan->kv_dtype, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefix kernel launch");
+    n_pre = splits;
+  }
+  CascadeMerge cm{n_pre};
+  return run_common(plan, d_q, d_k_cache, d_v_cache, num_pages, page_stride_elems, P, d_k_scale, d_v_scale,
+                    sm_scale, d_out, d_lse, stream, nullptr, &cm);
 }
 
 pkd_status pkd_single_decode(const void* d_q, const void* d_k, const void* d_v, int kv_len,

@@ -89,6 +89,7 @@ struct PrefixParams {
   int group;
   int num_pages;
   int page_size;
+  int box_tok;              // keys per TMA box (min(page_size, 64))
   int n_splits;             // key-range pieces
   int tiles_per_split;      // 128-key tiles per piece
   int m_tiles;              // 128-row query tiles per kv head

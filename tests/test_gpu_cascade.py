@@ -1,0 +1,117 @@
+"""GPU parity of cascade (shared-prefix) decode: the tcgen05 prefix kernel,
+the all-partial suffix decode and the merge pass, against the fp64 oracle's
+merge_state(attn(prefix), attn(suffix)); plus edge cases (one-key prefix,
+partial query tiles, empty suffixes, no prefix)."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_decode_28_gb300 as pkd
+from oracle import attention as orc
+from paged_kv_decode_28_gb300 import workloads as wl
+from tests.parity import assert_lse_close, assert_o_close, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_cascade(b, plan=None):
+    idx = torch.from_numpy(np.ascontiguousarray(b.kv_page_indices)).cuda()
+    pre = torch.from_numpy(np.ascontiguousarray(b.prefix_page_indices)).cuda() if b.prefix_page_indices is not None \
+        else torch.zeros(0, dtype=torch.int32, device="cuda")
+    if plan is None:
+        plan = pkd.Plan(b.batch, b.num_qo_heads, b.num_kv_heads, max_prefix_splits=16)
+    plan.plan(b.kv_indptr, idx, b.kv_last_page_len, b.page_size, q_dtype=b.q.dtype, kv_dtype=b.k_cache.dtype)
+    out, lse = plan.cascade_decode(pre, b.prefix_last_page_len, b.q, b.k_cache, b.v_cache, sm_scale=b.sm_scale)
+    torch.cuda.synchronize()
+    assert plan.check_device_errors() == 0
+    return out, lse
+
+
+def _oracle(b, rows=None):
+    pre = b.prefix_page_indices if b.prefix_page_indices is not None else np.zeros(0, np.int32)
+    return orc.cascade_decode(b.q, b.k_cache, b.v_cache, pre, b.prefix_last_page_len, b.kv_indptr,
+                              b.kv_page_indices, b.kv_last_page_len, sm_scale=b.sm_scale, rows=rows)
+
+
+@pytest.mark.parametrize("prefix_len", [1, 15, 127, 128, 129, 1000])
+@pytest.mark.parametrize("g", [1, 4, 8])
+def test_cascade_small(prefix_len, g):
+    b = wl.make_paged(seed=200 + prefix_len + g, lengths=[0, 1, 17, 300, 64, 5, 129], num_qo_heads=2 * g,
+                      num_kv_heads=2, page_size=16, prefix_len=prefix_len, device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+@pytest.mark.parametrize("P", [1, 4, 64, 128])
+def test_cascade_page_sizes(P):
+    b = wl.make_paged(seed=300 + P, lengths=[33, 0, 200, 1], num_qo_heads=16, num_kv_heads=4, page_size=P,
+                      prefix_len=3 * 128 + 7, device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+@pytest.mark.parametrize("B", [1, 31, 33, 100])
+def test_cascade_partial_query_tiles(B):
+    """B * g rows not a multiple of the 128-row tile: padded rows must not leak."""
+    rng = np.random.default_rng(B)
+    lens = rng.integers(0, 400, size=B)
+    b = wl.make_paged(seed=400 + B, lengths=lens, num_qo_heads=32, num_kv_heads=8, page_size=16,
+                      prefix_len=2048, device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+def test_cascade_f16():
+    b = wl.make_paged(seed=500, lengths=[10, 200, 0, 77], num_qo_heads=16, num_kv_heads=2, page_size=16,
+                      q_dtype="f16", kv_dtype="f16", prefix_len=777, device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+def test_cascade_without_prefix_is_plain_decode():
+    b = wl.make_paged(seed=501, lengths=[10, 200, 0, 77], num_qo_heads=16, num_kv_heads=2, page_size=16,
+                      device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = orc.paged_decode(b.q, b.k_cache, b.v_cache, b.kv_indptr, b.kv_page_indices,
+                                    b.kv_last_page_len, sm_scale=b.sm_scale)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+def test_cascade_equals_decode_over_prefix_then_suffix():
+    b = wl.make_config(4, device="cuda", batch=24)
+    out, lse = _gpu_cascade(b)
+    plain = wl.cascade_as_plain(b)
+    idx = torch.from_numpy(plain.kv_page_indices).cuda()
+    plan = pkd.Plan(plain.batch, plain.num_qo_heads, plain.num_kv_heads)
+    plan.plan(plain.kv_indptr, idx, plain.kv_last_page_len, plain.page_size)
+    o2, l2 = plan.run(plain.q, plain.k_cache, plain.v_cache, sm_scale=plain.sm_scale)
+    torch.cuda.synchronize()
+    assert_o_close(out, o2.double().cpu().numpy())
+    assert_lse_close(lse, l2.double().cpu().numpy())
+
+
+def test_cascade_workload_full_size_sampled():
+    b = wl.make_config(4, device="cuda")
+    out, lse = _gpu_cascade(b)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    rows = sample_rows(b, 40, seed=4)
+    o_ref, l_ref = _oracle(b, rows)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+def test_cascade_is_deterministic_and_replans():
+    b = wl.make_config(4, device="cuda", batch=40)
+    plan = pkd.Plan(64, b.num_qo_heads, b.num_kv_heads, max_prefix_splits=16)
+    o1, l1 = _gpu_cascade(b, plan)
+    o2, l2 = _gpu_cascade(b, plan)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
