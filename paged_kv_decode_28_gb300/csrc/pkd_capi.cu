@@ -439,7 +439,8 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
   m.num_kv_heads = plan->hk;
   m.group = p.group;
   m.all_rows = cascade ? 1 : 0;
-  cudaError_t e = pkd::launch_merge_rows(m, plan->G, st);
+  // a fixed grid (graph-static) with enough warps to keep one in flight per output row
+  cudaError_t e = pkd::launch_merge_rows(m, plan->G * 4, st);
   if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
   return PKD_OK;
 }

@@ -39,51 +39,107 @@ __device__ __forceinline__ float load_elem(const void* in, size_t idx, int dtype
   return static_cast<const float*>(in)[idx];
 }
 
-// One CTA of 128 threads per row; thread d owns head dimension d.  Partial
-// log-sum-exps are base 2 (the decode kernels' convention); the output lse is
-// natural log.
-__global__ void __launch_bounds__(kHeadDim) merge_rows_kernel(const MergeParams p) {
+// One warp per (request, qo head) output row; lane i owns head dimensions
+// 4i .. 4i+3.  The row's states are the cascade prefix pieces (if any) and
+// then its split-KV items, in slot order.  Lanes first load up to 32 state
+// log-sum-exps at once (the max and the normaliser are warp reductions), then
+// stream the states' fp32 partial outputs as float4.  Partial log-sum-exps are
+// base 2 (the decode kernels' convention); the output lse is natural log.
+constexpr int kMergeWarps = 8;
+
+__device__ __forceinline__ void store4(void* out, size_t idx, float4 v, int dtype) {
+  if (dtype == kBF16) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + idx) = u;
+  } else if (dtype == kF16) {
+    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(static_cast<__half*>(out) + idx) = u;
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = v;
+  }
+}
+
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const MergeParams p) {
   const int batch = p.header->batch;
   const int Hk = p.num_kv_heads;
   const int G = p.group;
   const int Hq = Hk * G;
   const int n_rows = p.all_rows ? batch * Hk : p.header->n_merge_rows;
-  const int d = threadIdx.x;
+  const int lane = threadIdx.x & 31;
   const size_t pre_stride = static_cast<size_t>(batch) * Hq;
+  const int n_pre = p.n_pre_splits;
+  const int64_t n_units = static_cast<int64_t>(n_rows) * G;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * kMergeWarps;
 #pragma unroll 1
-  for (int i = blockIdx.x; i < n_rows; i += gridDim.x) {
+  for (int64_t unit = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5); unit < n_units;
+       unit += warps) {
+    const int i = static_cast<int>(unit / G);
+    const int j = static_cast<int>(unit - static_cast<int64_t>(i) * G);
     const int row = p.all_rows ? i : p.merge_rows[i];
     const int b = row / Hk;
     const int h = row - b * Hk;
     const int beg = p.row_item_begin[row];
     const int cnt = p.row_item_count[row];
-#pragma unroll 1
-    for (int j = 0; j < G; ++j) {
-      const int qo = h * G + j;
-      const size_t bq = static_cast<size_t>(b) * Hq + qo;
-      float M = -INFINITY;
-      for (int s = 0; s < p.n_pre_splits; ++s) M = fmaxf(M, p.pre_lse[s * pre_stride + bq]);
-      for (int c = 0; c < cnt; ++c) M = fmaxf(M, p.part_lse[static_cast<size_t>(beg + c) * G + j]);
-      float acc = 0.f, L = 0.f;
-      if (M != -INFINITY) {
-        for (int s = 0; s < p.n_pre_splits; ++s) {
-          const float ls = p.pre_lse[s * pre_stride + bq];
-          const float w = (ls == -INFINITY) ? 0.f : ptx::ex2(ls - M);
-          L += w;
-          acc += w * p.pre_o[(s * pre_stride + bq) * kHeadDim + d];
+    const size_t bq = static_cast<size_t>(b) * Hq + h * G + j;
+    const int n_states = n_pre + cnt;
+    // state s: prefix piece s (s < n_pre) or item beg + s - n_pre
+    auto lse_of = [&](int s) -> float {
+      return s < n_pre ? p.pre_lse[s * pre_stride + bq] : p.part_lse[static_cast<size_t>(beg + s - n_pre) * G + j];
+    };
+    auto o_of = [&](int s) -> const float4* {
+      const float* base = s < n_pre ? p.pre_o + (s * pre_stride + bq) * kHeadDim
+                                    : p.part_o + (static_cast<size_t>(beg + s - n_pre) * G + j) * kHeadDim;
+      return reinterpret_cast<const float4*>(base) + lane;
+    };
+    float M = -INFINITY;
+    for (int s0 = 0; s0 < n_states; s0 += 32) {
+      const float x = (s0 + lane < n_states) ? lse_of(s0 + lane) : -INFINITY;
+      M = fmaxf(M, x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    if (M != -INFINITY) {
+      for (int s0 = 0; s0 < n_states; s0 += 32) {
+        const int ns = min(32, n_states - s0);
+        const float x = (lane < ns) ? lse_of(s0 + lane) : -INFINITY;
+        const float w = (x == -INFINITY) ? 0.f : ptx::ex2(x - M);
+        L += w;
+        int s = 0;
+        for (; s + 2 <= ns; s += 2) {
+          const float w0 = __shfl_sync(0xffffffffu, w, s), w1 = __shfl_sync(0xffffffffu, w, s + 1);
+          const float4 a = *o_of(s0 + s), c = *o_of(s0 + s + 1);
+          acc.x += w0 * a.x + w1 * c.x;
+          acc.y += w0 * a.y + w1 * c.y;
+          acc.z += w0 * a.z + w1 * c.z;
+          acc.w += w0 * a.w + w1 * c.w;
         }
-        for (int c = 0; c < cnt; ++c) {
-          const size_t slot = static_cast<size_t>(beg + c) * G + j;
-          const float ls = p.part_lse[slot];
-          const float w = (ls == -INFINITY) ? 0.f : ptx::ex2(ls - M);
-          L += w;
-          acc += w * p.part_o[slot * kHeadDim + d];
+        if (s < ns) {
+          const float w0 = __shfl_sync(0xffffffffu, w, s);
+          const float4 a = *o_of(s0 + s);
+          acc.x += w0 * a.x;
+          acc.y += w0 * a.y;
+          acc.z += w0 * a.z;
+          acc.w += w0 * a.w;
         }
       }
-      const float v = (M == -INFINITY) ? 0.f : acc / L;
-      store_elem(p.out, bq * kHeadDim + d, v, p.out_dtype);
-      if (d == 0 && p.lse) p.lse[bq] = (M == -INFINITY) ? -INFINITY : (M + ptx::lg2(L)) * kLn2;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      const float inv = 1.f / L;
+      acc.x *= inv;
+      acc.y *= inv;
+      acc.z *= inv;
+      acc.w *= inv;
     }
+    store4(p.out, bq * kHeadDim + 4 * lane, acc, p.out_dtype);
+    if (lane == 0 && p.lse) p.lse[bq] = (M == -INFINITY) ? -INFINITY : (M + ptx::lg2(L)) * kLn2;
   }
 }
 
@@ -165,7 +221,7 @@ int grid_for_rows(int64_t rows) {
 }  // namespace
 
 cudaError_t launch_merge_rows(const MergeParams& p, int grid, cudaStream_t stream) {
-  merge_rows_kernel<<<grid, kHeadDim, 0, stream>>>(p);
+  merge_rows_kernel<<<grid, kMergeWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

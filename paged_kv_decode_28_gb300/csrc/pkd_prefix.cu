@@ -12,9 +12,10 @@
 // these partials into each request's suffix states.
 //
 // Per CTA (256 threads, one CTA per SM):
-//   warp 0      TMA producer: the Q tile once, then K/V key tiles page by page
-//               into a 2-stage ring (128-byte swizzled, K-major for K, MN-major
-//               for V);
+//   warp 0      TMA producer: the Q tile once, then K and V key tiles page by
+//               page into two 3-stage rings (128-byte swizzled, K-major for K,
+//               MN-major for V); a K slot is freed as soon as its S product is
+//               done, a V slot when its P V product is done;
 //   warp 1      allocates 512 TMEM columns and issues the MMAs from one thread:
 //               S = Q K^T into one of two S buffers, then O += P V with P read
 //               from TMEM; tcgen05.commit signals the mbarriers;
@@ -37,11 +38,24 @@ constexpr float kRescaleThreshold = 8.0f;
 
 constexpr int kHalf = 16384;   // one 64-element (128-byte) column half of a 128-row tile
 constexpr int kStage = 32768;  // a K (or V) tile: two halves
+constexpr int kStages = 3;     // ring depth of K and of V
 constexpr int kQ = 0;
 constexpr int kK = kQ + kStage;
-constexpr int kV = kK + 2 * kStage;
-constexpr int kBars = kV + 2 * kStage;
-enum { B_Q = 0, B_KVF = 1, B_KVE = 3, B_SF = 5, B_SFREE = 7, B_PF = 9, B_OD = 11, B_DRAIN = 13, kNumBars = 14 };
+constexpr int kV = kK + kStages * kStage;
+constexpr int kBars = kV + kStages * kStage;
+enum {
+  B_Q = 0,
+  B_KF = 1,                  // K full  [kStages]
+  B_KE = B_KF + kStages,     // K empty [kStages]
+  B_VF = B_KE + kStages,     // V full  [kStages]
+  B_VE = B_VF + kStages,     // V empty [kStages]
+  B_SF = B_VE + kStages,     // S full  [2]
+  B_SFREE = B_SF + 2,        // S read  [2]
+  B_PF = B_SFREE + 2,        // P full  [2]
+  B_OD = B_PF + 2,           // P V done [2]
+  B_DRAIN = B_OD + 2,
+  kNumBars = B_DRAIN + 1
+};
 constexpr int kTmemSlot = kBars + kNumBars * 8;
 constexpr int kAbort = kTmemSlot + 8;
 constexpr int kTotal = kAbort + 16;
@@ -90,9 +104,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(B_Q), 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar(B_KF + s), 1);
+      ptx::mbar_init(bar(B_KE + s), 1);
+      ptx::mbar_init(bar(B_VF + s), 1);
+      ptx::mbar_init(bar(B_VE + s), 1);
+    }
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(bar(B_KVF + s), 1);
-      ptx::mbar_init(bar(B_KVE + s), 1);
       ptx::mbar_init(bar(B_SF + s), 1);
       ptx::mbar_init(bar(B_SFREE + s), kRows);
       ptx::mbar_init(bar(B_PF + s), kRows);
@@ -126,30 +144,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t policy = ptx::policy_evict_last();  // the prefix is re-read by every query tile
       const int box = p.box_tok;
       for (int i = 0; i < n; ++i) {
-        const int s = i & 1;
-        if (!warp_wait(bar(B_KVE + s), ((i >> 1) & 1) ^ 1, p.err, abort_flag)) break;
+        const int s = i % kStages;
+        const uint32_t par = ((i / kStages) & 1) ^ 1;
         const int key0 = (t0 + i) * kKeys;
         const int nv = min(kKeys, p.prefix_len - key0);
         const int boxes = (nv + box - 1) / box;
-        const uint32_t fb = bar(B_KVF + s);
-        if (lane == 0) ptx::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(boxes) * box * 128u * 4u);
-        __syncwarp();
-        for (int bx = lane; bx < boxes; bx += 32) {
-          const int key = key0 + bx * box;
-          const int pi = key / p.page_size;
-          int page = __ldg(p.prefix_pages + pi);
-          if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
-            atomicOr(p.err, kDevErrPageIndex);
-            page = 0;
+        const uint32_t tile_bytes = static_cast<uint32_t>(boxes) * box * 128u * 2u;
+        // page ids of this lane's boxes (at most 4 per lane: 128 keys / box >= 1 key)
+        int pages[4], toks[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int bx = lane + 32 * r;
+          pages[r] = 0;
+          toks[r] = 0;
+          if (bx < boxes) {
+            const int key = key0 + bx * box;
+            const int pi = key / p.page_size;
+            int page = __ldg(p.prefix_pages + pi);
+            if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
+              atomicOr(p.err, kDevErrPageIndex);
+              page = 0;
+            }
+            pages[r] = page;
+            toks[r] = key - pi * p.page_size;
           }
-          const int tok = key - pi * p.page_size;
-          const uint32_t off = static_cast<uint32_t>(bx * box) * 128u;
-          const uint32_t kd = base + kK + s * kStage + off;
-          const uint32_t vd = base + kV + s * kStage + off;
-          ptx::tma_load_4d_hint(kd, &tmk, fb, 0, h, tok, page, policy);
-          ptx::tma_load_4d_hint(kd + kHalf, &tmk, fb, 64, h, tok, page, policy);
-          ptx::tma_load_4d_hint(vd, &tmv, fb, 0, h, tok, page, policy);
-          ptx::tma_load_4d_hint(vd + kHalf, &tmv, fb, 64, h, tok, page, policy);
+        }
+        if (!warp_wait(bar(B_KE + s), par, p.err, abort_flag)) break;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(bar(B_KF + s), tile_bytes);
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int bx = lane + 32 * r;
+          if (bx < boxes) {
+            const uint32_t kd = base + kK + s * kStage + static_cast<uint32_t>(bx * box) * 128u;
+            ptx::tma_load_4d_hint(kd, &tmk, bar(B_KF + s), 0, h, toks[r], pages[r], policy);
+            ptx::tma_load_4d_hint(kd + kHalf, &tmk, bar(B_KF + s), 64, h, toks[r], pages[r], policy);
+          }
+        }
+        if (!warp_wait(bar(B_VE + s), par, p.err, abort_flag)) break;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(bar(B_VF + s), tile_bytes);
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int bx = lane + 32 * r;
+          if (bx < boxes) {
+            const uint32_t vd = base + kV + s * kStage + static_cast<uint32_t>(bx * box) * 128u;
+            ptx::tma_load_4d_hint(vd, &tmv, bar(B_VF + s), 0, h, toks[r], pages[r], policy);
+            ptx::tma_load_4d_hint(vd + kHalf, &tmv, bar(B_VF + s), 64, h, toks[r], pages[r], policy);
+          }
         }
       }
     }
@@ -161,32 +203,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = wait_or_abort(bar(B_Q), 0, p.err, abort_flag);
       auto pv = [&](int t) -> bool {
         const int u = t & 1;
+        const int sv = t % kStages;
         if (!wait_or_abort(bar(B_PF + u), (t >> 1) & 1, p.err, abort_flag)) return false;
+        if (!wait_or_abort(bar(B_VF + sv), (t / kStages) & 1, p.err, abort_flag)) return false;
         ptx::tc_fence_after();
         const uint32_t pcol = u ? kColP1 : kColP0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t bdesc = ptx::smem_desc_sw128(base + kV + u * kStage + k * 2048, kHalf, 1024);
+          const uint64_t bdesc = ptx::smem_desc_sw128(base + kV + sv * kStage + k * 2048, kHalf, 1024);
           ptx::umma_ts(tmem + kColO, tmem + pcol + 8 * k, bdesc, idesc_pv, (t > 0 || k > 0) ? 1u : 0u);
         }
         ptx::tc_commit(bar(B_OD + u));
-        ptx::tc_commit(bar(B_KVE + u));
+        ptx::tc_commit(bar(B_VE + sv));
         return true;
       };
       for (int i = 0; i < n && ok; ++i) {
-        const int s = i & 1;
-        if (!wait_or_abort(bar(B_KVF + s), (i >> 1) & 1, p.err, abort_flag)) break;
-        if (i >= 2 && !wait_or_abort(bar(B_SFREE + s), ((i - 2) >> 1) & 1, p.err, abort_flag)) break;
+        const int u = i & 1;
+        const int sk = i % kStages;
+        if (!wait_or_abort(bar(B_KF + sk), (i / kStages) & 1, p.err, abort_flag)) break;
+        if (i >= 2 && !wait_or_abort(bar(B_SFREE + u), ((i - 2) >> 1) & 1, p.err, abort_flag)) break;
         ptx::tc_fence_after();
-        const uint32_t scol = s ? kColS1 : kColS0;
+        const uint32_t scol = u ? kColS1 : kColS0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
           const uint64_t adesc = ptx::smem_desc_sw128(base + kQ + koff, 16, 1024);
-          const uint64_t bdesc = ptx::smem_desc_sw128(base + kK + s * kStage + koff, 16, 1024);
+          const uint64_t bdesc = ptx::smem_desc_sw128(base + kK + sk * kStage + koff, 16, 1024);
           ptx::umma_ss(tmem + scol, adesc, bdesc, idesc_s, k > 0 ? 1u : 0u);
         }
-        ptx::tc_commit(bar(B_SF + s));
+        ptx::tc_commit(bar(B_SF + u));
+        ptx::tc_commit(bar(B_KE + sk));
         if (i >= 1 && !pv(i - 1)) {
           ok = false;
           break;
@@ -222,13 +268,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(B_SFREE + u));
       const int nv = min(kKeys, p.prefix_len - (t0 + i) * kKeys);
-      float mx = -INFINITY;
+      // scale (and, on a ragged last tile, mask), then a tree max: 8 independent chains
+      float m8[8];
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        const float x = (c < nv) ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
-        sr[c] = __float_as_uint(x);
-        mx = fmaxf(mx, x);
+      for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
+      if (nv == kKeys) {
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c) {
+          const float x = __uint_as_float(sr[c]) * sl2;
+          sr[c] = __float_as_uint(x);
+          m8[c & 7] = fmaxf(m8[c & 7], x);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c) {
+          const float x = (c < nv) ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
+          sr[c] = __float_as_uint(x);
+          m8[c & 7] = fmaxf(m8[c & 7], x);
+        }
       }
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const bool need = (i > 0) && (mx > m_ref + kRescaleThreshold);
       if (i == 0) m_ref = mx;
       if (__any_sync(0xffffffffu, need)) {
@@ -259,7 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const uint32_t pcol = tmem + lanes + (u ? kColP1 : kColP0);
-      float rs = 0.f;
+      float rs[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rs[e] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -267,17 +329,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e) {
           const float p0 = ptx::ex2(__uint_as_float(sr[32 * c + 2 * e]) - m_ref);
           const float p1 = ptx::ex2(__uint_as_float(sr[32 * c + 2 * e + 1]) - m_ref);
-          rs += p0 + p1;
+          rs[e & 7] += p0 + p1;
           pk[e] = ptx::pack2<BF>(p0, p1);
         }
         ptx::tmem_st16(pcol + 16 * c, pk);
       }
-      l += rs;
-      if (nv < kKeys && row >= nv) {
+      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+      if (nv < kKeys) {
         // keys past the prefix end: their P is 0, and their V rows must be
-        // finite for the product, so zero them (both column halves)
+        // finite for the product, so zero them (both column halves) once the
+        // tile's V has landed
+        if (!warp_wait(bar(B_VF + i % kStages), (i / kStages) & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+      }
+      if (nv < kKeys && row >= nv) {
         uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        uint8_t* vrow = base_ptr + kV + u * kStage + row * 128;
+        uint8_t* vrow = base_ptr + kV + (i % kStages) * kStage + row * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           *reinterpret_cast<uint4*>(vrow + 16 * c) = z;
