@@ -119,6 +119,21 @@ pkd_status encode_kv_map(CUtensorMap* m, const void* base, int kv_dtype, int hk,
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Clusters of the prefix kernel that fit on the current device at once
+// (queried once per device and cluster size; 0 when unknown).
+int resident_prefix_clusters(int cluster) {
+  static std::mutex mu;
+  static int cache[64][9] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cluster < 1 || cluster > 8) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev][cluster] == 0) {
+    const int n = pkd::prefix_max_active_clusters(cluster);
+    cache[dev][cluster] = n > 0 ? n : -1;
+  }
+  return cache[dev][cluster] > 0 ? cache[dev][cluster] : 0;
+}
+
 }  // namespace
 
 namespace pkd {
@@ -495,11 +510,28 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
       return fail(PKD_ERR_INVALID_ARG, "page_stride_elems must cover a page and be a 16-byte multiple");
     const int n_tiles = (prefix_len + 127) / 128;
     const int m_tiles = (B * g + 127) / 128;
-    const int sms = plan->G / pkd::kCtasPerSm;
-    int splits = sms / (plan->hk * m_tiles);
-    splits = splits < 1 ? 1 : splits;
-    splits = splits > plan->max_splits ? plan->max_splits : splits;
-    splits = splits > n_tiles ? n_tiles : splits;
+    // clusters of C query tiles share each K/V tile (multicast)
+    // (C divides the tile count, so every CTA of a cluster owns a real tile).
+    // Key-range splits fill the clusters that fit on the GPU at once; among
+    // the sizes, take the one that keeps the most CTAs busy, then the largest.
+    int C = 1, best_ctas = -1, splits = 1;
+    for (int c = 1; c <= 8; c *= 2) {
+      if (m_tiles % c != 0) continue;
+      int resident = resident_prefix_clusters(c);
+      if (resident <= 0) resident = (plan->G / pkd::kCtasPerSm) / c;
+      int sp = resident / (plan->hk * (m_tiles / c));
+      sp = sp < 1 ? 1 : sp;
+      sp = sp > plan->max_splits ? plan->max_splits : sp;
+      sp = sp > n_tiles ? n_tiles : sp;
+      const int ctas = plan->hk * m_tiles * sp;
+      const int busy = ctas < resident * c ? ctas : resident * c;
+      if (busy >= best_ctas) {
+        best_ctas = busy;
+        C = c;
+        splits = sp;
+      }
+    }
+    const int m_groups = m_tiles / C;
     const int tps = (n_tiles + splits - 1) / splits;
     splits = (n_tiles + tps - 1) / tps;
     // Q viewed as [B][Hk][g][128]: a box of 128 / g requests x g heads is one 128-row tile
@@ -535,6 +567,8 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
     pp.n_splits = splits;
     pp.tiles_per_split = tps;
     pp.m_tiles = m_tiles;
+    pp.cluster = C;
+    pp.m_groups = m_groups;
     pp.scale_log2 = scale * 1.4426950408889634f;
     pp.pre_o = reinterpret_cast<float*>(plan->ws + plan->lay.pre_o);
     pp.pre_lse = reinterpret_cast<float*>(plan->ws + plan->lay.pre_lse);

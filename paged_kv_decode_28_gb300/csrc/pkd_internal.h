@@ -93,6 +93,8 @@ struct PrefixParams {
   int n_splits;             // key-range pieces
   int tiles_per_split;      // 128-key tiles per piece
   int m_tiles;              // 128-row query tiles per kv head
+  int cluster;              // CTAs per cluster sharing K/V tiles (1, 2, 4 or 8)
+  int m_groups;             // ceil(m_tiles / cluster)
   float scale_log2;
   float* pre_o;             // [split, B * Hq, D]
   float* pre_lse;           // [split, B * Hq] base 2
@@ -114,5 +116,6 @@ cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const 
                           const PrefixParams& p, int kv_dtype, cudaStream_t stream);
 int decode_smem_bytes(int kv_dtype);
 int prefix_smem_bytes();
+int prefix_max_active_clusters(int cluster);  // 0 if the query fails
 
 }  // namespace pkd

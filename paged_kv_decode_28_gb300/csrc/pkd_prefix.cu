@@ -11,11 +11,18 @@
 // writes an fp32 partial state (o, base-2 lse) per row; the merge pass folds
 // these partials into each request's suffix states.
 //
+// CTAs run in clusters of C (1, 2, 4 or 8): the C query tiles of one kv head
+// and key range read the same K/V tiles, so each CTA fetches 1/C of every
+// tile's TMA boxes and multicasts them to the whole cluster, and a K or V slot
+// is reused only after all C CTAs have released it (their tcgen05.commit
+// arrives on the slot's "empty" barrier in every CTA).
+//
 // Per CTA (256 threads, one CTA per SM):
-//   warp 0      TMA producer: the Q tile once, then K and V key tiles page by
-//               page into two 3-stage rings (128-byte swizzled, K-major for K,
-//               MN-major for V); a K slot is freed as soon as its S product is
-//               done, a V slot when its P V product is done;
+//   warp 0      TMA producer of Q (once) and of the K ring; warp 2 producer of
+//               the V ring: key tiles page by page into two 3-stage rings
+//               (128-byte swizzled, K-major for K, MN-major for V); a K slot is
+//               freed as soon as its S product is done, a V slot when its P V
+//               product is done, so K loads run ahead of V;
 //   warp 1      allocates 512 TMEM columns and issues the MMAs from one thread:
 //               S = Q K^T into one of two S buffers, then O += P V with P read
 //               from TMEM; tcgen05.commit signals the mbarriers;
@@ -92,11 +99,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   const int Hq = p.num_kv_heads * G;
-  const int per_head = p.m_tiles * p.n_splits;
-  const int h = blockIdx.x / per_head;
-  const int rem = blockIdx.x - h * per_head;
-  const int mt = rem / p.n_splits;
-  const int split = rem - mt * p.n_splits;
+  // blockIdx.x = ((h * n_splits + split) * m_groups + mgroup) * C + rank
+  const int C = p.cluster;
+  const int rank = static_cast<int>(ptx::cluster_ctarank());
+  const int cl = blockIdx.x / C;
+  const int mgroup = cl % p.m_groups;
+  const int hs = cl / p.m_groups;
+  const int split = hs % p.n_splits;
+  const int h = hs / p.n_splits;
+  const int mt = mgroup * C + rank;  // may pass m_tiles: such a CTA only helps load
+  const uint16_t cta_mask = static_cast<uint16_t>((1u << C) - 1u);
   const int n_tiles_all = (p.prefix_len + kKeys - 1) / kKeys;
   const int t0 = split * p.tiles_per_split;
   const int t1 = min(t0 + p.tiles_per_split, n_tiles_all);
@@ -106,9 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(B_Q), 1);
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bar(B_KF + s), 1);
-      ptx::mbar_init(bar(B_KE + s), 1);
+      ptx::mbar_init(bar(B_KE + s), C);
       ptx::mbar_init(bar(B_VF + s), 1);
-      ptx::mbar_init(bar(B_VE + s), 1);
+      ptx::mbar_init(bar(B_VE + s), C);
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(bar(B_SF + s), 1);
@@ -126,13 +138,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();  // every CTA's barriers exist before any multicast reaches them
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base_ptr + kTmemSlot);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ TMA producers (K: warp 0, V: warp 2)
+    const bool kside = warp == 0;
     if (n > 0) {
-      if (lane == 0) {
+      if (kside && lane == 0) {
         ptx::prefetch_tensormap(&tmq);
         ptx::prefetch_tensormap(&tmk);
         ptx::prefetch_tensormap(&tmv);
@@ -141,58 +155,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_4d(base + kQ, &tmq, bar(B_Q), 0, 0, h, b0);
         ptx::tma_load_4d(base + kQ + kHalf, &tmq, bar(B_Q), 64, 0, h, b0);
       }
-      const uint64_t policy = ptx::policy_evict_last();  // the prefix is re-read by every query tile
       const int box = p.box_tok;
-      for (int i = 0; i < n; ++i) {
-        const int s = i % kStages;
-        const uint32_t par = ((i / kStages) & 1) ^ 1;
-        const int key0 = (t0 + i) * kKeys;
-        const int nv = min(kKeys, p.prefix_len - key0);
-        const int boxes = (nv + box - 1) / box;
-        const uint32_t tile_bytes = static_cast<uint32_t>(boxes) * box * 128u * 2u;
-        // page ids of this lane's boxes (at most 4 per lane: 128 keys / box >= 1 key)
-        int pages[4], toks[4];
+      // this CTA's boxes of a tile are bx = rank + C * (lane + 32 * r); page ids
+      // are fetched two tiles ahead of their use
+      auto fetch = [&](int i, int (&pg)[4], int (&tk)[4]) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const int bx = lane + 32 * r;
-          pages[r] = 0;
-          toks[r] = 0;
+          pg[r] = 0;
+          tk[r] = 0;
+          if (i >= n) continue;
+          const int key0 = (t0 + i) * kKeys;
+          const int boxes = (min(kKeys, p.prefix_len - key0) + box - 1) / box;
+          const int bx = rank + C * (lane + 32 * r);
           if (bx < boxes) {
             const int key = key0 + bx * box;
             const int pi = key / p.page_size;
-            int page = __ldg(p.prefix_pages + pi);
+            pg[r] = __ldg(p.prefix_pages + pi);  // checked at use, so the load stays in flight
+            tk[r] = key - pi * p.page_size;
+          }
+        }
+      };
+      const int eb = kside ? B_KE : B_VE;
+      const int fb = kside ? B_KF : B_VF;
+      const CUtensorMap* map = kside ? &tmk : &tmv;
+      const uint32_t ring = kside ? kK : kV;
+      auto issue = [&](int i, const int (&pg)[4], const int (&tk)[4]) -> bool {
+        const int s = i % kStages;
+        const uint32_t par = ((i / kStages) & 1) ^ 1;
+        const int key0 = (t0 + i) * kKeys;
+        const int boxes = (min(kKeys, p.prefix_len - key0) + box - 1) / box;
+        const uint32_t tile_bytes = static_cast<uint32_t>(boxes) * box * 128u * 2u;  // all CTAs' boxes
+        if (!warp_wait(bar(eb + s), par, p.err, abort_flag)) return false;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(bar(fb + s), tile_bytes);
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int bx = rank + C * (lane + 32 * r);
+          if (bx < boxes) {
+            int page = pg[r];
             if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
               atomicOr(p.err, kDevErrPageIndex);
               page = 0;
             }
-            pages[r] = page;
-            toks[r] = key - pi * p.page_size;
+            const uint32_t d = base + ring + s * kStage + static_cast<uint32_t>(bx * box) * 128u;
+            ptx::tma_load_4d_mc(d, map, bar(fb + s), 0, h, tk[r], page, cta_mask);
+            ptx::tma_load_4d_mc(d + kHalf, map, bar(fb + s), 64, h, tk[r], page, cta_mask);
           }
         }
-        if (!warp_wait(bar(B_KE + s), par, p.err, abort_flag)) break;
-        if (lane == 0) ptx::mbar_arrive_expect_tx(bar(B_KF + s), tile_bytes);
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int bx = lane + 32 * r;
-          if (bx < boxes) {
-            const uint32_t kd = base + kK + s * kStage + static_cast<uint32_t>(bx * box) * 128u;
-            ptx::tma_load_4d_hint(kd, &tmk, bar(B_KF + s), 0, h, toks[r], pages[r], policy);
-            ptx::tma_load_4d_hint(kd + kHalf, &tmk, bar(B_KF + s), 64, h, toks[r], pages[r], policy);
-          }
-        }
-        if (!warp_wait(bar(B_VE + s), par, p.err, abort_flag)) break;
-        if (lane == 0) ptx::mbar_arrive_expect_tx(bar(B_VF + s), tile_bytes);
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int bx = lane + 32 * r;
-          if (bx < boxes) {
-            const uint32_t vd = base + kV + s * kStage + static_cast<uint32_t>(bx * box) * 128u;
-            ptx::tma_load_4d_hint(vd, &tmv, bar(B_VF + s), 0, h, toks[r], pages[r], policy);
-            ptx::tma_load_4d_hint(vd + kHalf, &tmv, bar(B_VF + s), 64, h, toks[r], pages[r], policy);
-          }
-        }
+        return true;
+      };
+      // three register sets in rotation, unrolled so that no set is copied
+      // while its loads are in flight: tile i's ids were requested two tiles earlier
+      int pgA[4], tkA[4], pgB[4], tkB[4], pgC[4], tkC[4];
+      fetch(0, pgA, tkA);
+      fetch(1, pgB, tkB);
+      for (int i = 0; i < n; i += 3) {
+        fetch(i + 2, pgC, tkC);
+        if (!issue(i, pgA, tkA)) break;
+        if (i + 1 >= n) break;
+        fetch(i + 3, pgA, tkA);
+        if (!issue(i + 1, pgB, tkB)) break;
+        if (i + 2 >= n) break;
+        fetch(i + 4, pgB, tkB);
+        if (!issue(i + 2, pgC, tkC)) break;
       }
     }
   } else if (warp == 1) {
@@ -214,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::umma_ts(tmem + kColO, tmem + pcol + 8 * k, bdesc, idesc_pv, (t > 0 || k > 0) ? 1u : 0u);
         }
         ptx::tc_commit(bar(B_OD + u));
-        ptx::tc_commit(bar(B_VE + sv));
+        if (t + kStages < n) ptx::tc_commit_mc(bar(B_VE + sv), cta_mask);
         return true;
       };
       for (int i = 0; i < n && ok; ++i) {
@@ -232,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::umma_ss(tmem + scol, adesc, bdesc, idesc_s, k > 0 ? 1u : 0u);
         }
         ptx::tc_commit(bar(B_SF + u));
-        ptx::tc_commit(bar(B_KE + sk));
+        if (i + kStages < n) ptx::tc_commit_mc(bar(B_KE + sk), cta_mask);
         if (i >= 1 && !pv(i - 1)) {
           ok = false;
           break;
@@ -269,26 +294,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(bar(B_SFREE + u));
       const int nv = min(kKeys, p.prefix_len - (t0 + i) * kKeys);
       // scale (and, on a ragged last tile, mask), then a tree max: 8 independent chains
+      // max of the raw scores (the scale is positive, so it commutes with max);
+      // keys past the prefix end become -inf
       float m8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
-      if (nv == kKeys) {
+      if (nv < kKeys) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          const float x = __uint_as_float(sr[c]) * sl2;
-          sr[c] = __float_as_uint(x);
-          m8[c & 7] = fmaxf(m8[c & 7], x);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          const float x = (c < nv) ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
-          sr[c] = __float_as_uint(x);
-          m8[c & 7] = fmaxf(m8[c & 7], x);
-        }
+        for (int c = 0; c < kKeys; ++c)
+          if (c >= nv) sr[c] = __float_as_uint(-INFINITY);
       }
-      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
+      const float mx = sl2 * fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const bool need = (i > 0) && (mx > m_ref + kRescaleThreshold);
       if (i == 0) m_ref = mx;
       if (__any_sync(0xffffffffu, need)) {
@@ -327,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ptx::ex2(__uint_as_float(sr[32 * c + 2 * e]) - m_ref);
-          const float p1 = ptx::ex2(__uint_as_float(sr[32 * c + 2 * e + 1]) - m_ref);
+          const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e]), sl2, -m_ref));
+          const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e + 1]), sl2, -m_ref));
           rs[e & 7] += p0 + p1;
           pk[e] = ptx::pack2<BF>(p0, p1);
         }
@@ -394,6 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // no CTA leaves while a peer may still deliver into its shared memory
+  ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
@@ -404,23 +425,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int prefix_smem_bytes() { return kAlloc; }
 
+int prefix_max_active_clusters(int cluster) {
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, PrefixParams) = prefix_kernel<true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kAlloc;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                           const PrefixParams& p, int kv_dtype, cudaStream_t stream) {
-  const int grid = p.num_kv_heads * p.m_tiles * p.n_splits;
+  const int grid = p.num_kv_heads * p.n_splits * p.m_groups * p.cluster;
   if (grid <= 0) return cudaSuccess;
-  if (kv_dtype == kBF16) {
-    auto kern = prefix_kernel<true>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kAlloc, stream>>>(tmq, tmk, tmv, p);
-  } else if (kv_dtype == kF16) {
-    auto kern = prefix_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kAlloc, stream>>>(tmq, tmk, tmv, p);
-  } else {
-    return cudaErrorInvalidValue;
-  }
+  if (kv_dtype != kBF16 && kv_dtype != kF16) return cudaErrorInvalidValue;
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, PrefixParams) =
+      kv_dtype == kBF16 ? prefix_kernel<true> : prefix_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, tmq, tmk, tmv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
