@@ -145,9 +145,9 @@ class ClockSampler:
 
 
 def dist_init(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from paged_kv_decode_28_gb300 import replicas
+
+    world, rank, local = replicas.world()
     if world > 1:
         import torch.distributed as dist
 
@@ -156,21 +156,15 @@ def dist_init(args):
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
+    from paged_kv_decode_28_gb300 import replicas
 
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return replicas.max_over_ranks(x, world, device)
 
 
 def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
+    from paged_kv_decode_28_gb300 import replicas
 
-        dist.barrier()
+    replicas.barrier(world)
 
 
 def cpu_sample_batch(b, n_req: int):
