@@ -31,12 +31,16 @@ template <int KVT>
 struct Cfg {
   // bytes of one key (or value) row of one kv head
   static constexpr int kRowBytes = (KVT == kE4M3) ? kHeadDim : 2 * kHeadDim;
-  static constexpr int kStages = (KVT == kE4M3) ? 6 : 3;
+  static constexpr int kStages = (KVT == kE4M3) ? 4 : 3;
   static constexpr bool kMmaBf16 = (KVT == kBF16);
   // one 64-key tile of K (or V): 16-bit -> two [64][128 B] halves (d 0..63, 64..127)
   static constexpr int kTensorBytes = kChunkKeys * kRowBytes;
   static constexpr int kStageBytes = 2 * kTensorBytes;
-  static constexpr int kCombO = kStages * kStageBytes;                          // f32 [3][8][128]
+  // fp8: each consumer warp's value rows of two stages converted to f16,
+  // 2 x [2 halves][16][128 B] per warp
+  static constexpr int kV16Bytes = (KVT == kE4M3) ? 4 * 8192 : 0;
+  static constexpr int kV16 = kStages * kStageBytes;
+  static constexpr int kCombO = kV16 + kV16Bytes;                               // f32 [3][8][128]
   static constexpr int kCombML = kCombO + 3 * kMaxGroup * kHeadDim * 4;         // f32 [3][8][2]
   static constexpr int kBars = kCombML + 3 * kMaxGroup * 2 * 4;                 // u64 [2][stages]
   static constexpr int kAbort = kBars + 2 * kStages * 8;                        // int
@@ -183,15 +187,46 @@ __device__ __forceinline__ void tile16_16bit(uint32_t kb, uint32_t vb, int w, in
   }
 }
 
-// 16 keys of an fp8 stage.  K: the thread's 32 bytes of key row gid, converted
-// e4m3x2 -> f16x2 in registers (d permuted as in load_q).  V: n-tile 4q + r,
-// column n maps to d = 32q + 4n + r, so one 32-bit load per key serves 4 n-tiles.
-__device__ __forceinline__ void tile16_e4m3(uint32_t kb, uint32_t vb, int w, int lane, int valid,
-                                            const uint32_t (&qa0)[8], const uint32_t (&qa2)[8],
-                                            float sl2, float& m_run, float& l_run,
-                                            float (&o)[16][4]) {
+// Four E4M3 codes (bytes 0..3 of w) -> two f16x2 (lo: bytes 0,1; hi: bytes 2,3), exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Offset of 16-byte chunk c of row r, column half hf, in a [2 halves][16][128 B]
+// f16 buffer: the chunk is XOR-swizzled by (r + 4 hf) mod 8, so both the
+// row-wise writes (two halves at once) and the 8-row ldmatrix reads are free of
+// bank conflicts.
+__device__ __forceinline__ uint32_t v16_off(uint32_t r, uint32_t hf, uint32_t c) {
+  return hf * (16 * 128u) + r * 128u + ((c ^ ((r + 4 * hf) & 7u)) << 4);
+}
+
+// The warp's 16 value rows of an fp8 stage -> f16.  Lane l converts row l / 2,
+// head-dim half l % 2.
+__device__ __forceinline__ void convert_v16(uint32_t vb, uint32_t v16, int w, int lane) {
+  const uint32_t vr = lane >> 1, hf = lane & 1;
+  const uint32_t tok = 16 * w + vr;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 raw = ptx::lds128(vb + ptx::sw128(tok, 4 * hf + c));  // codes d = 64 hf + 16 c ..
+    uint32_t f[8];
+    e4m3x4_to_f16x2x2(raw.x, f[0], f[1]);
+    e4m3x4_to_f16x2x2(raw.y, f[2], f[3]);
+    e4m3x4_to_f16x2x2(raw.z, f[4], f[5]);
+    e4m3x4_to_f16x2x2(raw.w, f[6], f[7]);
+    ptx::sts128(v16 + v16_off(vr, hf, 2 * c), f[0], f[1], f[2], f[3]);
+    ptx::sts128(v16 + v16_off(vr, hf, 2 * c + 1), f[4], f[5], f[6], f[7]);
+  }
+}
+
+// S = Q K^T for the warp's 16 keys of an fp8 stage (two n-tiles): the thread's
+// 32 bytes of key row gid, converted e4m3x2 -> f16x2 in registers (head
+// dimension permuted as in load_q).
+__device__ __forceinline__ void qk_e4m3(uint32_t kb, int w, int lane, const uint32_t (&qa0)[8],
+                                        const uint32_t (&qa2)[8], float (&sacc)[2][4]) {
   const int gid = lane >> 2, t = lane & 3;
-  float sacc[2][4];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
@@ -202,48 +237,99 @@ __device__ __forceinline__ void tile16_e4m3(uint32_t kb, uint32_t vb, int w, int
     const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint32_t b0 = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(wd[j] & 0xffffu));
-      const uint32_t b1 = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(wd[j] >> 16));
+      uint32_t b0, b1;
+      e4m3x4_to_f16x2x2(wd[j], b0, b1);
       ptx::mma_16816<false>(sacc[nt], qa0[j], 0u, qa2[j], 0u, b0, b1);
     }
   }
-  uint32_t pa0, pa2;
-  softmax_step<false>(sacc, t, valid, sl2, m_run, l_run, o, pa0, pa2);
-  const uint32_t tA = 16 * w + 2 * t;
-  const bool vA = 2 * t < valid, vB = 2 * t + 1 < valid, vC = 2 * t + 8 < valid, vD = 2 * t + 9 < valid;
+}
+
+// O += P V for 16 keys whose values are f16 in a [2][16][128 B] buffer; keys
+// past `valid` contribute zero whatever the buffer holds.
+__device__ __forceinline__ void pv_f16buf(uint32_t v16, int lane, int valid, uint32_t pa0, uint32_t pa2,
+                                          float (&o)[16][4]) {
+  const int t = lane & 3;
+  const uint32_t mlo = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
+  const uint32_t mhi = (2 * t + 8 < valid ? 0x0000ffffu : 0u) | (2 * t + 9 < valid ? 0xffff0000u : 0u);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t chunk = 2 * q + (gid >> 2);
-    const uint32_t boff = 4 * (gid & 3);
-    const uint32_t wA = vA ? ptx::lds32(vb + ptx::sw128(tA, chunk) + boff) : 0u;
-    const uint32_t wB = vB ? ptx::lds32(vb + ptx::sw128(tA + 1, chunk) + boff) : 0u;
-    const uint32_t wC = vC ? ptx::lds32(vb + ptx::sw128(tA + 8, chunk) + boff) : 0u;
-    const uint32_t wD = vD ? ptx::lds32(vb + ptx::sw128(tA + 9, chunk) + boff) : 0u;
-    const uint32_t x01 = __byte_perm(wA, wB, 0x5140), x23 = __byte_perm(wA, wB, 0x7362);
-    const uint32_t y01 = __byte_perm(wC, wD, 0x5140), y23 = __byte_perm(wC, wD, 0x7362);
-    ptx::mma_16816<false>(o[4 * q + 0], pa0, 0u, pa2, 0u,
-                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(x01 & 0xffffu)),
-                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(y01 & 0xffffu)));
-    ptx::mma_16816<false>(o[4 * q + 1], pa0, 0u, pa2, 0u,
-                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(x01 >> 16)),
-                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(y01 >> 16)));
-    ptx::mma_16816<false>(o[4 * q + 2], pa0, 0u, pa2, 0u,
-                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(x23 & 0xffffu)),
-                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(y23 & 0xffffu)));
-    ptx::mma_16816<false>(o[4 * q + 3], pa0, 0u, pa2, 0u,
-                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(x23 >> 16)),
-                          ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(y23 >> 16)));
+  for (int dp = 0; dp < 8; ++dp) {
+    const uint32_t tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t dch = 2 * dp + (lane >> 4);
+    const uint32_t addr = v16 + v16_off(tok, dch >> 3, dch & 7u);
+    uint32_t r0, r1, r2, r3;
+    ptx::ldsm_x4_trans(addr, r0, r1, r2, r3);
+    r0 &= mlo;
+    r1 &= mhi;
+    r2 &= mlo;
+    r3 &= mhi;
+    ptx::mma_16816<false>(o[2 * dp], pa0, 0u, pa2, 0u, r0, r1);
+    ptx::mma_16816<false>(o[2 * dp + 1], pa0, 0u, pa2, 0u, r2, r3);
   }
+}
+
+// 16 keys of an fp8 stage.
+__device__ __forceinline__ void tile16_e4m3(uint32_t kb, uint32_t vb, uint32_t v16, int w, int lane, int valid,
+                                            const uint32_t (&qa0)[8], const uint32_t (&qa2)[8],
+                                            float sl2, float& m_run, float& l_run,
+                                            float (&o)[16][4]) {
+  convert_v16(vb, v16, w, lane);
+  float sacc[2][4];
+  qk_e4m3(kb, w, lane, qa0, qa2, sacc);
+  uint32_t pa0, pa2;
+  softmax_step<false>(sacc, lane & 3, valid, sl2, m_run, l_run, o, pa0, pa2);
+  __syncwarp();  // the f16 value rows are written by other lanes of this warp
+  pv_f16buf(v16, lane, valid, pa0, pa2, o);
+  __syncwarp();  // the buffer is rewritten by the next tile
+}
+
+// 32 keys: the warp's 16 keys of two consecutive fp8 stages (A, B).  The two
+// halves' conversions and S products are independent work for the scheduler,
+// and the softmax state is updated once for the 32 keys.
+__device__ __forceinline__ void tile32_e4m3(uint32_t kbA, uint32_t vbA, int validA, uint32_t kbB, uint32_t vbB,
+                                            int validB, uint32_t v16, int w, int lane,
+                                            const uint32_t (&qa0)[8], const uint32_t (&qa2)[8], float sl2,
+                                            float& m_run, float& l_run, float (&o)[16][4]) {
+  const int t = lane & 3;
+  convert_v16(vbA, v16, w, lane);
+  convert_v16(vbB, v16 + 4096u, w, lane);
+  float sA[2][4], sB[2][4];
+  qk_e4m3(kbA, w, lane, qa0, qa2, sA);
+  qk_e4m3(kbB, w, lane, qa0, qa2, sB);
+  float x[8];
+  x[0] = (2 * t < validA) ? sA[0][0] * sl2 : -INFINITY;
+  x[1] = (2 * t + 1 < validA) ? sA[0][1] * sl2 : -INFINITY;
+  x[2] = (2 * t + 8 < validA) ? sA[1][0] * sl2 : -INFINITY;
+  x[3] = (2 * t + 9 < validA) ? sA[1][1] * sl2 : -INFINITY;
+  x[4] = (2 * t < validB) ? sB[0][0] * sl2 : -INFINITY;
+  x[5] = (2 * t + 1 < validB) ? sB[0][1] * sl2 : -INFINITY;
+  x[6] = (2 * t + 8 < validB) ? sB[1][0] * sl2 : -INFINITY;
+  x[7] = (2 * t + 9 < validB) ? sB[1][1] * sl2 : -INFINITY;
+  float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  // the caller guarantees a valid key in A or B, so m_new is finite
+  const float m_new = fmaxf(m_run, mx);
+  const float alpha = ptx::ex2(m_run - m_new);
+  float pr[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) pr[i] = ptx::ex2(x[i] - m_new);
+  l_run = l_run * alpha + (((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7])));
+  m_run = m_new;
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+    o[nt][0] *= alpha;
+    o[nt][1] *= alpha;
+  }
+  __syncwarp();  // the f16 value rows are written by other lanes of this warp
+  pv_f16buf(v16, lane, validA, ptx::pack2<false>(pr[0], pr[1]), ptx::pack2<false>(pr[2], pr[3]), o);
+  pv_f16buf(v16 + 4096u, lane, validB, ptx::pack2<false>(pr[4], pr[5]), ptx::pack2<false>(pr[6], pr[7]), o);
+  __syncwarp();  // the buffers are rewritten by the next step
 }
 
 // Head dimension index of accumulator o[nt][e] held by thread t.
 template <int KVT>
 __device__ __forceinline__ int o_dim(int nt, int e, int t) {
-  if constexpr (KVT == kE4M3) {
-    return 32 * (nt >> 2) + 8 * t + 4 * e + (nt & 3);
-  } else {
-    return 8 * nt + 2 * t + e;
-  }
+  return 8 * nt + 2 * t + e;
 }
 
 template <int QT>
@@ -383,6 +469,35 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 #pragma unroll 1
     for (int k = item.y; k < item.z; ++k) {
+      if constexpr (KVT == kE4M3) {
+        if (k + 1 < item.z) {
+          // two stages at once (32 keys per warp)
+          const int s2 = (s + 1 == C::kStages) ? 0 : s + 1;
+          const uint32_t ph2 = (s + 1 == C::kStages) ? (ph ^ 1u) : ph;
+          const int validA = min(p.chunk_keys, L - k * p.chunk_keys) - 16 * w;
+          const int validB = min(p.chunk_keys, L - (k + 1) * p.chunk_keys) - 16 * w;
+          const bool okA = stage_wait(bar_full + 8 * s, ph, p.err, abort_flag);
+          const bool okB = stage_wait(bar_full + 8 * s2, ph2, p.err, abort_flag);
+          if (okA && okB && (validA > 0 || validB > 0)) {
+            const uint32_t kbA = base + s * C::kStageBytes, kbB = base + s2 * C::kStageBytes;
+            tile32_e4m3(kbA, kbA + C::kTensorBytes, validA, kbB, kbB + C::kTensorBytes, validB,
+                        base + C::kV16 + w * 8192u, w, lane, qa0, qa2, sl2, m_run, l_run, o);
+          }
+          __syncwarp();
+          if (lane == 0) {
+            ptx::mbar_arrive(bar_empty + 8 * s);
+            ptx::mbar_arrive(bar_empty + 8 * s2);
+          }
+          s = s2 + 1;
+          ph = ph2;
+          if (s == C::kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+          ++k;  // the loop's increment takes the second chunk
+          continue;
+        }
+      }
       const int n_valid = min(p.chunk_keys, L - k * p.chunk_keys);
       const bool ok = stage_wait(bar_full + 8 * s, ph, p.err, abort_flag);
       const int valid = n_valid - 16 * w;
@@ -390,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const uint32_t kb = base + s * C::kStageBytes;
         const uint32_t vb = kb + C::kTensorBytes;
         if constexpr (KVT == kE4M3) {
-          tile16_e4m3(kb, vb, w, lane, valid, qa0, qa2, sl2, m_run, l_run, o);
+          tile16_e4m3(kb, vb, base + C::kV16 + w * 8192u, w, lane, valid, qa0, qa2, sl2, m_run, l_run, o);
         } else {
           tile16_16bit<C::kMmaBf16>(kb, vb, w, lane, valid, qa0, qa2, sl2, m_run, l_run, o);
         }
