@@ -3,7 +3,9 @@
 
 One step = the whole decode hot path over one batch: the host plan (split-KV
 schedule, one async upload) followed by run (the TMA-pipelined decode kernel
-and the split-KV merge kernel) on inputs resident in HBM.  The default workload
+and the split-KV merge kernel, replayed from a CUDA graph captured once) on
+inputs resident in HBM.  The end-to-end figure runs the same step eagerly
+through the public API with host buffers.  The default workload
 is the batch-64 GQA decode batch (64 requests, 32 qo / 8 kv heads, head_dim
 128, bf16, lengths uniform in [512, 4096], page size 16, pages drawn from a
 20000-page pool).  Its K/V bytes (0.58 GB) exceed the 129 MB L2, so no flush
@@ -241,36 +243,53 @@ def run_ours(args, world, rank, local):
     lse = torch.empty(b.batch, b.num_qo_heads, dtype=torch.float32, device=dev)
     kw = dict(sm_scale=b.sm_scale, k_scale=b.k_scale, v_scale=b.v_scale, out=out, lse=lse)
 
-    def step():
+    def do_plan():
         plan.plan(b.kv_indptr, idx, b.kv_last_page_len, b.page_size, q_dtype=b.q.dtype, kv_dtype=b.k_cache.dtype)
+
+    def do_run():
         if cascade:
             plan.cascade_decode(pre, b.prefix_last_page_len, b.q, b.k_cache, b.v_cache, **kw)
         else:
             plan.run(b.q, b.k_cache, b.v_cache, **kw)
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        do_plan()
+        do_run()
     torch.cuda.synchronize()
     assert plan.check_device_errors() == 0
 
-    # ---- device-timed steps, with the decode kernel timed alone by the library's event hook
+    # ---- run is captured in CUDA graphs (plan stays on the host before every
+    # replay, as in serving); one graph per timed step so that each step's
+    # decode launch is bracketed by its own events from the library's hook
     K = args.steps
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for a, z in kev:  # torch creates the CUDA event at its first record; the library re-records it
         a.record(stream)
         z.record(stream)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(K):
+        plan.set_timing_events(*kev[i])
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            do_run()
+        graphs.append(g)
+    plan.set_timing_events(None, None)
+    for i in range(max(args.warmup, 3, K)):  # every graph is uploaded before the timed steps
+        do_plan()
+        graphs[i % K].replay()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize()
         e0.record(stream)
         for i in range(K):
-            plan.set_timing_events(*kev[i])
-            step()
+            do_plan()
+            graphs[i].replay()
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-    plan.set_timing_events(None, None)
     clk = clocks.summary()
     ms_total = e0.elapsed_time(e1)
     ms_total_max = max_over_ranks(ms_total, world, dev)
@@ -289,7 +308,7 @@ def run_ours(args, world, rank, local):
     q_d = torch.empty_like(b.q)
     idx_d = torch.empty_like(idx)
 
-    def e2e_step():
+    def e2e_step():  # eager, through the public API
         q_d.copy_(q_h, non_blocking=True)
         idx_d.copy_(idx_h, non_blocking=True)
         plan.plan(b.kv_indptr, idx_d, b.kv_last_page_len, b.page_size, q_dtype=b.q.dtype, kv_dtype=b.k_cache.dtype)

@@ -222,7 +222,9 @@ pkd_status pkd_merge_states(const void* d_v, const float* d_s, int64_t n, int k,
  * start_event just before the decode kernel and stop_event just after it, on
  * the call's stream (cudaEvent_t handles passed as void*; the caller owns
  * them).  NULL, NULL turns the hook off.  Lets a caller time the dominant
- * kernel alone with CUDA events.
+ * kernel alone with CUDA events.  During stream capture the records are made
+ * with cudaEventRecordExternal, so a captured graph records them on every
+ * replay.
  */
 pkd_status pkd_plan_set_timing_events(pkd_plan_t plan, void* start_event, void* stop_event);
 

@@ -156,6 +156,7 @@ struct pkd_plan_s {
   // pinned double buffer for the schedule upload; an event per slot guards reuse
   bool use_pinned = true;
   uint8_t* pinned[2] = {nullptr, nullptr};
+  uint8_t* pinned_dev[2] = {nullptr, nullptr};  // device mapping of the staging slots
   cudaEvent_t pinned_done[2] = {nullptr, nullptr};
   int next_slot = 0;
   // optional caller events recorded around the decode kernel (timing hook)
@@ -333,8 +334,10 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
     slot = plan->next_slot;
     if (!plan->pinned[slot]) {
       cudaError_t ea = cudaHostAlloc(reinterpret_cast<void**>(&plan->pinned[slot]), L.meta_end,
-                                     cudaHostAllocDefault);
+                                     cudaHostAllocMapped);
       if (ea != cudaSuccess) return cuda_fail(ea, "cudaHostAlloc(plan staging)");
+      ea = cudaHostGetDevicePointer(reinterpret_cast<void**>(&plan->pinned_dev[slot]), plan->pinned[slot], 0);
+      if (ea != cudaSuccess) return cuda_fail(ea, "cudaHostGetDevicePointer(plan staging)");
       ea = cudaEventCreateWithFlags(&plan->pinned_done[slot], cudaEventDisableTiming);
       if (ea != cudaSuccess) return cuda_fail(ea, "cudaEventCreate(plan staging)");
     } else {
@@ -342,11 +345,18 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
       cudaError_t ea = cudaEventSynchronize(plan->pinned_done[slot]);
       if (ea != cudaSuccess) return cuda_fail(ea, "cudaEventSynchronize(plan staging)");
     }
-    memcpy(plan->pinned[slot] + 4, h + 4, L.meta_end - 4);
+    memcpy(plan->pinned[slot] + 16, h + 16, L.meta_end - 16);
     src = plan->pinned[slot];
   }
-  cudaError_t e = cudaMemcpyAsync(plan->ws + 4, src + 4, L.meta_end - 4, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan)");
+  cudaError_t e;
+  if (slot >= 0) {
+    // a copy kernel reads the staging slot through its device mapping; the
+    // first 16 bytes (the kernels' error word) are not part of the upload
+    e = pkd::launch_copy16(plan->ws + 16, plan->pinned_dev[slot] + 16, L.meta_end - 16, st);
+  } else {
+    e = cudaMemcpyAsync(plan->ws + 4, src + 4, L.meta_end - 4, cudaMemcpyHostToDevice, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "plan upload");
   if (slot >= 0) {
     e = cudaEventRecord(plan->pinned_done[slot], st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(plan staging)");
@@ -430,14 +440,19 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
     s = encode_kv_map(&tmv, d_v_cache, plan->kv_dtype, plan->hk, tok_extent, num_pages, page_stride_elems,
                       box_tok);
     if (s != PKD_OK) return s;
+    // under stream capture the records become event-record nodes that fire on every replay
+    unsigned rec_flags = cudaEventRecordDefault;
     if (plan->ev_start) {
-      cudaError_t er = cudaEventRecord(plan->ev_start, st);
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        rec_flags = cudaEventRecordExternal;
+      cudaError_t er = cudaEventRecordWithFlags(plan->ev_start, st, rec_flags);
       if (er != cudaSuccess) return cuda_fail(er, "cudaEventRecord(timing start)");
     }
     cudaError_t e = pkd::launch_decode(tmk, tmv, p, plan->q_dtype, plan->kv_dtype, plan->G, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     if (plan->ev_stop) {
-      cudaError_t er = cudaEventRecord(plan->ev_stop, st);
+      cudaError_t er = cudaEventRecordWithFlags(plan->ev_stop, st, rec_flags);
       if (er != cudaSuccess) return cuda_fail(er, "cudaEventRecord(timing stop)");
     }
   }

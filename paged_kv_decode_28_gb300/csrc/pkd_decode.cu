@@ -369,6 +369,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   __syncthreads();
 
+  // the merge pass may be scheduled now; it waits for this grid to finish
+  ptx::pdl_launch_dependents();
   const int it0 = p.cta_begin[blockIdx.x];
   const int it1 = p.cta_begin[blockIdx.x + 1];
   const int Hk = p.num_kv_heads;

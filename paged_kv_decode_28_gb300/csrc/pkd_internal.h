@@ -22,12 +22,13 @@ enum DType : int { kF16 = 0, kBF16 = 1, kE4M3 = 2, kF32 = 3 };
 
 // Device header at the start of the workspace (int32 words).
 struct WsHeader {
-  unsigned err;       // PKD_DEVERR_* bits
-  int n_items;
+  unsigned err;       // PKD_DEVERR_* bits (written by kernels, never by a plan upload)
+  int pad0[3];
+  int n_items;        // from byte 16 on, everything is the plan's upload
   int n_merge_rows;
   int batch;
   int zero_page;      // a page index of 0 for single-request decode
-  int pad[59];
+  int pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -107,6 +108,8 @@ struct PrefixParams {
 cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
                           int q_dtype, int kv_dtype, int grid, cudaStream_t stream);
 cudaError_t launch_merge_rows(const MergeParams& p, int grid, cudaStream_t stream);
+// dst, src and bytes multiples of 16; src may be mapped pinned host memory
+cudaError_t launch_copy16(void* dst, const void* src, int64_t bytes, cudaStream_t stream);
 cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, const float* sb,
                                void* vo, float* so, int64_t n, int heads, int dim, int dtype,
                                cudaStream_t stream);

@@ -66,6 +66,7 @@ __device__ __forceinline__ void store4(void* out, size_t idx, float4 v, int dtyp
 }
 
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const MergeParams p) {
+  ptx::pdl_wait_prior_grid();  // the decode grid's partials are complete and visible
   const int batch = p.header->batch;
   const int Hk = p.num_kv_heads;
   const int G = p.group;
@@ -210,6 +211,15 @@ __global__ void merge_states_kernel(const void* v, const float* s, int64_t n, in
   }
 }
 
+// Copies the plan's schedule from pinned host memory (read through its
+// device mapping) into the workspace: for a few tens of KB a kernel reaches
+// the data sooner than a DMA copy.
+__global__ void copy_words_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t n16) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[i] = src[i];
+}
+
 int grid_for_rows(int64_t rows) {
   const int64_t per_block = 8;  // warps per 256-thread block
   int64_t g = (rows + per_block - 1) / per_block;
@@ -221,7 +231,29 @@ int grid_for_rows(int64_t rows) {
 }  // namespace
 
 cudaError_t launch_merge_rows(const MergeParams& p, int grid, cudaStream_t stream) {
-  merge_rows_kernel<<<grid, kMergeWarps * 32, 0, stream>>>(p);
+  // programmatic dependent launch: scheduled while the decode grid runs, it
+  // waits in griddepcontrol.wait for that grid to complete
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, merge_rows_kernel, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy16(void* dst, const void* src, int64_t bytes, cudaStream_t stream) {
+  const int64_t n16 = bytes / 16;
+  if (n16 <= 0) return cudaSuccess;
+  int grid = static_cast<int>((n16 + 255) / 256);
+  grid = grid > 64 ? 64 : grid;
+  copy_words_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16);
   return cudaGetLastError();
 }
 

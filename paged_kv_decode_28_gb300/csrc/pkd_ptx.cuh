@@ -221,6 +221,12 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled early / wait until the previous kernel's grid has completed and its
+// memory is visible (both are no-ops without the launch attribute).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
