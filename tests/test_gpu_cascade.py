@@ -33,7 +33,7 @@ def _oracle(b, rows=None):
                               b.kv_page_indices, b.kv_last_page_len, sm_scale=b.sm_scale, rows=rows)
 
 
-@pytest.mark.parametrize("prefix_len", [1, 15, 127, 128, 129, 1000])
+@pytest.mark.parametrize("prefix_len", [1, 15, 63, 64, 65, 127, 128, 129, 191, 1000])
 @pytest.mark.parametrize("g", [1, 4, 8])
 def test_cascade_small(prefix_len, g):
     b = wl.make_paged(seed=200 + prefix_len + g, lengths=[0, 1, 17, 300, 64, 5, 129], num_qo_heads=2 * g,
@@ -54,13 +54,27 @@ def test_cascade_page_sizes(P):
     assert_lse_close(lse, l_ref)
 
 
-@pytest.mark.parametrize("B", [1, 31, 33, 100])
+@pytest.mark.parametrize("B", [1, 31, 33, 70, 100, 200])
 def test_cascade_partial_query_tiles(B):
-    """B * g rows not a multiple of the 128-row tile: padded rows must not leak."""
+    """B * g rows not a multiple of the 128-row tile (and odd tile counts, where
+    a CTA's second query tile lies past the batch): padded rows must not leak."""
     rng = np.random.default_rng(B)
     lens = rng.integers(0, 400, size=B)
     b = wl.make_paged(seed=400 + B, lengths=lens, num_qo_heads=32, num_kv_heads=8, page_size=16,
                       prefix_len=2048, device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+def test_cascade_growing_scores():
+    """Prefix keys whose norm grows along the prefix, so the running max rises
+    by more than the lazy-rescale threshold many times (O rescaled in TMEM)."""
+    b = wl.make_paged(seed=502, lengths=[3, 90, 0, 400], num_qo_heads=16, num_kv_heads=2, page_size=16,
+                      prefix_len=1000, device="cuda")
+    for pos, pid in enumerate(b.prefix_page_indices.tolist()):
+        b.k_cache[pid] *= 1.0 + 0.25 * pos
     out, lse = _gpu_cascade(b)
     o_ref, l_ref = _oracle(b)
     assert_o_close(out, o_ref)
