@@ -89,6 +89,15 @@ def algorithmic_bytes(b) -> int:
     return kv + qo + lse + scales
 
 
+def decode_kernel_bytes(b) -> int:
+    """Algorithmic bytes of the decode kernel alone: as algorithmic_bytes, but
+    without the shared prefix, which the cascade's prefix kernel reads."""
+    n = algorithmic_bytes(b)
+    if b.prefix_page_indices is not None:
+        n -= b.prefix_len * b.num_kv_heads * b.head_dim * 2 * b.k_cache.element_size()
+    return n
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
 
@@ -333,7 +342,7 @@ def run_ours(args, world, rank, local):
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
 
     peak, peak_kind = measured_hbm_peak()
-    achieved = nbytes / (kern_avg_ms * 1e-3) / 1e9
+    achieved = decode_kernel_bytes(b) / (kern_avg_ms * 1e-3) / 1e9
     traffic = None
     try:
         with open(TRAFFIC_FILE) as f:
@@ -373,7 +382,8 @@ def run_ours(args, world, rank, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "pkd decode_kernel",
+            "kernel": "pkd decode_kernel" + (" (suffix pages; the shared prefix is the prefix kernel's)" if cascade else ""),
+            "bytes_per_launch": decode_kernel_bytes(b),
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",

@@ -129,12 +129,15 @@ pkd_status pkd_plan_destroy(pkd_plan_t plan);
  * order r = b * num_kv_heads + h, is divided into num_ctas equal contiguous
  * runs of ceil(total / num_ctas) chunks, one per CTA.  A row that falls to one
  * CTA is written directly; rows split across CTAs are merged by a second pass.
- * The schedule is copied into the workspace with one cudaMemcpyAsync on
- * `stream` from a pinned staging buffer owned by the plan (two slots; reusing a
- * slot waits for the copy issued two plans earlier), so plan does not wait for
- * the GPU.  plan must not be called during stream capture; the launch shape of
- * run never changes, so a graph captured around run stays valid across
- * re-plans of the same plan object.
+ * plan writes the schedule into a pinned staging buffer owned by the plan;
+ * the next pkd_run / pkd_cascade_decode copies it into the workspace with a
+ * kernel.  Before overwriting the buffer, plan waits (host-side) for the copy
+ * that read the previous schedule, so it blocks only until the GPU has begun
+ * the previous step.  The first plan also clears the device error word with
+ * one cudaMemsetAsync on `stream`.  plan must not be called during stream
+ * capture; the launch shape of run never changes and its copy reads the
+ * staging buffer, so a graph captured around run uploads the latest plan on
+ * every replay and stays valid across re-plans of the same plan object.
  */
 pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* d_kv_page_indices,
                     const int32_t* h_kv_last_page_len, int batch, int num_qo_heads,
@@ -153,9 +156,12 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
  *   num_pages  pages in each pool; page ids must lie in [0, num_pages).
  *   d_k_scale, d_v_scale  fp32 [num_kv_heads] for an E4M3 cache, else NULL.
  *   d_out      [batch, num_qo_heads, 128] q dtype;  d_lse fp32 [batch, num_qo_heads] or NULL.
- * Enqueues two kernels on `stream` (decode, then the split-KV merge) with a
- * grid that depends only on the plan object; no allocation, no host sync:
- * capturable in a CUDA graph.
+ * Enqueues three kernels on `stream` (the schedule upload, decode, then the
+ * split-KV merge; the last two are launched programmatically so each may be
+ * scheduled before its predecessor ends, and waits for it in-kernel) with
+ * grids that depend only on the plan object, plus event records on a side
+ * stream of the plan that rejoins `stream` (created on the first call); no
+ * allocation, no host sync: capturable in a CUDA graph.
  */
 pkd_status pkd_run(pkd_plan_t plan, const void* d_q, const void* d_k_cache, const void* d_v_cache,
                    int64_t num_pages, int64_t page_stride_elems, const float* d_k_scale,
@@ -222,9 +228,13 @@ pkd_status pkd_merge_states(const void* d_v, const float* d_s, int64_t n, int k,
  * start_event just before the decode kernel and stop_event just after it, on
  * the call's stream (cudaEvent_t handles passed as void*; the caller owns
  * them).  NULL, NULL turns the hook off.  Lets a caller time the dominant
- * kernel alone with CUDA events.  During stream capture the records are made
- * with cudaEventRecordExternal, so a captured graph records them on every
- * replay.
+ * kernel alone with CUDA events.  The stop event is recorded on a side stream
+ * of the plan that waits for the decode kernel and rejoins the call's stream
+ * after the merge launch, so the merge kernel keeps its programmatic early
+ * launch.  During stream capture the records are made with
+ * cudaEventRecordExternal, so a captured graph records them on every replay.
+ * The first call that enables the hook creates the side stream and two
+ * events (PKD_ERR_CUDA if that fails); pkd_plan_destroy releases them.
  */
 pkd_status pkd_plan_set_timing_events(pkd_plan_t plan, void* start_event, void* stop_event);
 

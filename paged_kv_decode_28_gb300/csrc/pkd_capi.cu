@@ -153,22 +153,31 @@ struct pkd_plan_s {
   // last plan
   bool planned = false;
   bool err_word_zeroed = false;  // the first plan clears the device error word
-  // pinned double buffer for the schedule upload; an event per slot guards reuse
+  // pinned staging buffer of the schedule: plan writes it, every run copies it
+  // into the workspace with a kernel (so a graph captured around run uploads
+  // the latest plan on each replay); stage_done fires after each such copy and
+  // plan waits for it before overwriting the buffer
   bool use_pinned = true;
-  uint8_t* pinned[2] = {nullptr, nullptr};
-  uint8_t* pinned_dev[2] = {nullptr, nullptr};  // device mapping of the staging slots
-  cudaEvent_t pinned_done[2] = {nullptr, nullptr};
-  int next_slot = 0;
-  // optional caller events recorded around the decode kernel (timing hook)
+  uint8_t* staging = nullptr;
+  uint8_t* staging_dev = nullptr;  // device mapping of the staging buffer
+  cudaEvent_t stage_done = nullptr;
+  // optional caller events recorded around the decode kernel (timing hook);
+  // the stop record goes on a side stream forked after the decode launch
   cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
   ~pkd_plan_s() {
-    for (int i = 0; i < 2; ++i) {
-      if (pinned_done[i]) {
-        cudaEventSynchronize(pinned_done[i]);
-        cudaEventDestroy(pinned_done[i]);
-      }
-      if (pinned[i]) cudaFreeHost(pinned[i]);
+    if (side) {
+      cudaStreamSynchronize(side);
+      cudaStreamDestroy(side);
     }
+    if (fork_ev) cudaEventDestroy(fork_ev);
+    if (join_ev) cudaEventDestroy(join_ev);
+    if (stage_done) {
+      cudaEventSynchronize(stage_done);
+      cudaEventDestroy(stage_done);
+    }
+    if (staging) cudaFreeHost(staging);
   }
   int batch = 0, page_size = 0, q_dtype = 0, kv_dtype = 0;
   const int32_t* d_page_indices = nullptr;
@@ -326,41 +335,25 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
     if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync(error word)");
     plan->err_word_zeroed = true;
   }
-  // one copy of everything after the error word (the error word stays the kernels')
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const uint8_t* src = h;
-  int slot = -1;
+  // stage everything after the error word (the error word stays the kernels')
   if (plan->use_pinned) {
-    slot = plan->next_slot;
-    if (!plan->pinned[slot]) {
-      cudaError_t ea = cudaHostAlloc(reinterpret_cast<void**>(&plan->pinned[slot]), L.meta_end,
-                                     cudaHostAllocMapped);
-      if (ea != cudaSuccess) return cuda_fail(ea, "cudaHostAlloc(plan staging)");
-      ea = cudaHostGetDevicePointer(reinterpret_cast<void**>(&plan->pinned_dev[slot]), plan->pinned[slot], 0);
-      if (ea != cudaSuccess) return cuda_fail(ea, "cudaHostGetDevicePointer(plan staging)");
-      ea = cudaEventCreateWithFlags(&plan->pinned_done[slot], cudaEventDisableTiming);
-      if (ea != cudaSuccess) return cuda_fail(ea, "cudaEventCreate(plan staging)");
+    if (!plan->staging) {
+      cudaError_t ea = cudaHostAlloc(reinterpret_cast<void**>(&plan->staging), L.meta_end, cudaHostAllocMapped);
+      if (ea == cudaSuccess)
+        ea = cudaHostGetDevicePointer(reinterpret_cast<void**>(&plan->staging_dev), plan->staging, 0);
+      if (ea == cudaSuccess) ea = cudaEventCreateWithFlags(&plan->stage_done, cudaEventDisableTiming);
+      if (ea != cudaSuccess) return cuda_fail(ea, "plan staging buffer");
     } else {
-      // the copy that last used this slot was issued two plans ago
-      cudaError_t ea = cudaEventSynchronize(plan->pinned_done[slot]);
+      // the copy that read the previous schedule (issued by the last run, or by
+      // the last replay of a graph captured around run) is done with the buffer
+      cudaError_t ea = cudaEventSynchronize(plan->stage_done);
       if (ea != cudaSuccess) return cuda_fail(ea, "cudaEventSynchronize(plan staging)");
     }
-    memcpy(plan->pinned[slot] + 16, h + 16, L.meta_end - 16);
-    src = plan->pinned[slot];
-  }
-  cudaError_t e;
-  if (slot >= 0) {
-    // a copy kernel reads the staging slot through its device mapping; the
-    // first 16 bytes (the kernels' error word) are not part of the upload
-    e = pkd::launch_copy16(plan->ws + 16, plan->pinned_dev[slot] + 16, L.meta_end - 16, st);
+    memcpy(plan->staging + 16, h + 16, L.meta_end - 16);
   } else {
-    e = cudaMemcpyAsync(plan->ws + 4, src + 4, L.meta_end - 4, cudaMemcpyHostToDevice, st);
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "plan upload");
-  if (slot >= 0) {
-    e = cudaEventRecord(plan->pinned_done[slot], st);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(plan staging)");
-    plan->next_slot = slot ^ 1;
+    cudaError_t e = cudaMemcpyAsync(plan->ws + 4, h + 4, L.meta_end - 4, cudaMemcpyHostToDevice,
+                                    static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload");
   }
   plan->planned = true;
   plan->batch = batch;
@@ -375,6 +368,16 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
 }  // extern "C"
 
 namespace {
+
+// The plan's side stream and its fork/join events (created on first use).
+pkd_status ensure_side(pkd_plan_t plan) {
+  if (plan->side) return PKD_OK;
+  cudaError_t e = cudaStreamCreateWithFlags(&plan->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&plan->fork_ev, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&plan->join_ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return cuda_fail(e, "side stream/events");
+  return PKD_OK;
+}
 
 // Cascade settings for run_common: every item writes a partial state and the
 // merge pass folds n_pre_splits prefix partials into every row.
@@ -425,6 +428,30 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
   p.num_pages = static_cast<int>(num_pages);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.force_partial = cascade ? 1 : 0;
+  // under stream capture the records become event-record nodes that fire on every replay
+  unsigned rec_flags = cudaEventRecordDefault;
+  {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+      rec_flags = cudaEventRecordExternal;
+  }
+  // Upload the staged schedule with a copy kernel; the decode kernel is
+  // launched programmatically after it and waits for it in griddepcontrol.wait.
+  // The records that follow the copy (stage_done, the timing start) go on the
+  // side stream, forked here, so no node separates the two launches.
+  bool joined = true;
+  if (plan->use_pinned) {
+    pkd_status ss = ensure_side(plan);
+    if (ss != PKD_OK) return ss;
+    cudaError_t e = pkd::launch_copy16(ws + 16, plan->staging_dev + 16, L.meta_end - 16, st);
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload");
+    e = cudaEventRecord(plan->fork_ev, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->side, plan->fork_ev, 0);
+    if (e == cudaSuccess) e = cudaEventRecordWithFlags(plan->stage_done, plan->side, rec_flags);
+    if (e == cudaSuccess && plan->ev_start) e = cudaEventRecordWithFlags(plan->ev_start, plan->side, rec_flags);
+    if (e != cudaSuccess) return cuda_fail(e, "upload fork");
+    joined = false;
+  }
   if (plan->counts.n_items > 0) {
     if (!d_k_cache || !d_v_cache) return fail(PKD_ERR_INVALID_ARG, "k/v cache is NULL");
     if (!aligned16(d_k_cache) || !aligned16(d_v_cache))
@@ -440,20 +467,23 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
     s = encode_kv_map(&tmv, d_v_cache, plan->kv_dtype, plan->hk, tok_extent, num_pages, page_stride_elems,
                       box_tok);
     if (s != PKD_OK) return s;
-    // under stream capture the records become event-record nodes that fire on every replay
-    unsigned rec_flags = cudaEventRecordDefault;
-    if (plan->ev_start) {
-      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-      if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
-        rec_flags = cudaEventRecordExternal;
+    if (plan->ev_start && !plan->use_pinned) {
       cudaError_t er = cudaEventRecordWithFlags(plan->ev_start, st, rec_flags);
       if (er != cudaSuccess) return cuda_fail(er, "cudaEventRecord(timing start)");
     }
     cudaError_t e = pkd::launch_decode(tmk, tmv, p, plan->q_dtype, plan->kv_dtype, plan->G, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     if (plan->ev_stop) {
-      cudaError_t er = cudaEventRecordWithFlags(plan->ev_stop, st, rec_flags);
+      // the stop record waits for the decode kernel on the side branch, so
+      // that no node sits between the decode and merge launches: a record on
+      // the call's stream would cancel the merge's programmatic early launch
+      pkd_status ss = ensure_side(plan);
+      if (ss != PKD_OK) return ss;
+      cudaError_t er = cudaEventRecord(plan->fork_ev, st);
+      if (er == cudaSuccess) er = cudaStreamWaitEvent(plan->side, plan->fork_ev, 0);
+      if (er == cudaSuccess) er = cudaEventRecordWithFlags(plan->ev_stop, plan->side, rec_flags);
       if (er != cudaSuccess) return cuda_fail(er, "cudaEventRecord(timing stop)");
+      joined = false;
     }
   }
   pkd::MergeParams m{};
@@ -475,6 +505,11 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
   // a fixed grid (graph-static) with enough warps to keep one in flight per output row
   cudaError_t e = pkd::launch_merge_rows(m, plan->G * 4, st);
   if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  if (!joined) {  // the side branch rejoins the call's stream
+    e = cudaEventRecord(plan->join_ev, plan->side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, plan->join_ev, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "side branch join");
+  }
   return PKD_OK;
 }
 
@@ -670,6 +705,10 @@ pkd_status pkd_plan_set_timing_events(pkd_plan_t plan, void* start_event, void* 
   if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
   if ((start_event == nullptr) != (stop_event == nullptr))
     return fail(PKD_ERR_INVALID_ARG, "give both timing events or neither");
+  if (stop_event) {
+    pkd_status ss = ensure_side(plan);
+    if (ss != PKD_OK) return ss;
+  }
   plan->ev_start = static_cast<cudaEvent_t>(start_event);
   plan->ev_stop = static_cast<cudaEvent_t>(stop_event);
   return PKD_OK;

@@ -371,6 +371,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   // the merge pass may be scheduled now; it waits for this grid to finish
   ptx::pdl_launch_dependents();
+  // this grid may have been launched before the schedule upload finished
+  ptx::pdl_wait_prior_grid();
   const int it0 = p.cta_begin[blockIdx.x];
   const int it1 = p.cta_begin[blockIdx.x + 1];
   const int Hk = p.num_kv_heads;
@@ -596,7 +598,20 @@ cudaError_t launch_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const Decod
   const int smem = Cfg<KVT>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(tmk, tmv, p);
+  // programmatic dependent launch: the grid may start while the kernel before
+  // it (the schedule upload) finishes; it waits in griddepcontrol.wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, tmk, tmv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -213,8 +213,10 @@ __global__ void merge_states_kernel(const void* v, const float* s, int64_t n, in
 
 // Copies the plan's schedule from pinned host memory (read through its
 // device mapping) into the workspace: for a few tens of KB a kernel reaches
-// the data sooner than a DMA copy.
+// the data sooner than a DMA copy.  The decode grid behind it may be
+// scheduled at once; it waits for this grid in griddepcontrol.wait.
 __global__ void copy_words_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t n16) {
+  ptx::pdl_launch_dependents();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     dst[i] = src[i];
