@@ -502,8 +502,12 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
   m.num_kv_heads = plan->hk;
   m.group = p.group;
   m.all_rows = cascade ? 1 : 0;
-  // a fixed grid (graph-static) with enough warps to keep one in flight per output row
-  cudaError_t e = pkd::launch_merge_rows(m, plan->G * 4, st);
+  // a fixed grid (graph-static): one CTA per decode CTA for the split rows,
+  // two for the cascade, which merges every row.  The grid becomes resident as
+  // the decode grid drains; a larger one took longer to launch than its warps
+  // saved (batch-64 GQA: merge tail 8.6 us with 4x, 4.2 us with 1x; cascade
+  // step 128.3 us with 4x, 124.6 us with 2x, 129 us with 1x)
+  cudaError_t e = pkd::launch_merge_rows(m, cascade ? 2 * plan->G : plan->G, st);
   if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
   if (!joined) {  // the side branch rejoins the call's stream
     e = cudaEventRecord(plan->join_ev, plan->side);

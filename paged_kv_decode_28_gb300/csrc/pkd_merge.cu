@@ -214,9 +214,13 @@ __global__ void merge_states_kernel(const void* v, const float* s, int64_t n, in
 // Copies the plan's schedule from pinned host memory (read through its
 // device mapping) into the workspace: for a few tens of KB a kernel reaches
 // the data sooner than a DMA copy.  The decode grid behind it may be
-// scheduled at once; it waits for this grid in griddepcontrol.wait.
+// scheduled at once; it waits for this grid in griddepcontrol.wait.  This grid
+// is itself launched programmatically: it may become resident while the
+// previous step's merge drains, and waits for that grid before it overwrites
+// the schedule the merge reads.
 __global__ void copy_words_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t n16) {
   ptx::pdl_launch_dependents();
+  ptx::pdl_wait_prior_grid();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     dst[i] = src[i];
@@ -255,7 +259,17 @@ cudaError_t launch_copy16(void* dst, const void* src, int64_t bytes, cudaStream_
   if (n16 <= 0) return cudaSuccess;
   int grid = static_cast<int>((n16 + 255) / 256);
   grid = grid > 64 ? 64 : grid;
-  copy_words_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, copy_words_kernel, static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -50,3 +50,41 @@ def test_replan_then_replay_matches_eager():
         torch.cuda.synchronize()
         assert torch.equal(out, o2), trial
         assert torch.equal(lse, l2), trial
+
+
+def test_back_to_back_replans_without_sync():
+    """plan/run pairs of alternating batches with no host synchronization: each
+    run's upload may start while the previous step's merge drains and must not
+    overwrite the schedule that merge reads, and plan must not overwrite a
+    staged schedule before its upload has read it."""
+    B, Hq, Hk, P = 12, 32, 8, 16
+    pool = wl.make_paged(seed=31, lengths=[3000] * B, num_qo_heads=Hq, num_kv_heads=Hk, page_size=P,
+                         device="cuda")
+    rng = np.random.default_rng(1)
+    idx = torch.from_numpy(rng.permutation(pool.num_pages).astype(np.int32)).cuda()
+
+    def table(lens):
+        n = (lens + P - 1) // P
+        indptr = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+        last = np.where(n > 0, lens - (n - 1) * P, 0).astype(np.int32)
+        return indptr, last
+
+    tables = [table(rng.integers(1, 3000, size=B)), table(rng.integers(0, 600, size=B))]
+    plan = pkd.Plan(B, Hq, Hk)
+    ref = []
+    for indptr, last in tables:  # each batch alone, synchronized
+        plan.plan(indptr, idx, last, P)
+        o, l = plan.run(pool.q, pool.k_cache, pool.v_cache)
+        torch.cuda.synchronize()
+        ref.append((o.clone(), l.clone()))
+    outs = [(torch.empty_like(pool.q), torch.empty(B, Hq, device="cuda")) for _ in range(8)]
+    for i, (o, l) in enumerate(outs):
+        indptr, last = tables[i % 2]
+        plan.plan(indptr, idx, last, P)
+        plan.run(pool.q, pool.k_cache, pool.v_cache, out=o, lse=l)
+    torch.cuda.synchronize()
+    assert plan.check_device_errors() == 0
+    for i, (o, l) in enumerate(outs):
+        ro, rl = ref[i % 2]
+        assert torch.equal(o, ro), f"step {i}: output differs from the isolated run"
+        assert torch.equal(l, rl), f"step {i}: lse differs from the isolated run"
