@@ -141,3 +141,45 @@ def test_bad_arguments_raise():
     with pytest.raises(pkd.PkdError):
         big = pkd.Plan(1, 8, 2)
         big.plan([0, 1, 2], idx, [16, 16], 16)  # batch above max_batch
+
+
+@pytest.mark.parametrize("qd,kvd", [("bf16", "bf16"), ("bf16", "e4m3")])
+@pytest.mark.parametrize("g", [2, 3, 5, 6, 7])
+def test_group_sizes_not_powers_of_two(qd, kvd, g):
+    """GQA groups of 2..7 qo heads per kv head (padded to the 16 MMA rows)."""
+    b = wl.make_paged(seed=600 + g, lengths=[1, 65, 300, 0, 1500], num_qo_heads=3 * g, num_kv_heads=3,
+                      page_size=16, q_dtype=qd, kv_dtype=kvd, device="cuda")
+    out, lse, _ = gpu_paged_decode(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+def test_one_request_of_a_million_keys():
+    """One (request, kv head) row cut into one item per CTA: the merge folds
+    hundreds of partial states, more than one warp-wide batch of them."""
+    b = wl.make_paged(seed=610, lengths=[1 << 20], num_qo_heads=8, num_kv_heads=1, page_size=16, device="cuda")
+    plan = pkd.Plan(1, 8, 1)
+    sched = pkd.plan_host(b.kv_indptr, b.kv_last_page_len, 1, 16, plan.num_ctas)
+    assert sched["row_item_count"][0] > 32  # more states than one warp-wide batch
+    out, lse, plan = gpu_paged_decode(b, plan)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+def test_run_without_lse_output():
+    """d_lse = NULL is allowed: out must equal the run that also writes lse."""
+    b = wl.make_paged(seed=620, lengths=[5, 700, 2000, 64], num_qo_heads=16, num_kv_heads=4, page_size=16,
+                      device="cuda")
+    out, lse, plan = gpu_paged_decode(b)
+    out2 = torch.empty_like(out)
+    N, P, Hk, D = b.k_cache.shape
+    stride = b.k_cache.stride(0)
+    st = pkd.api.lib().pkd_run(plan._h, b.q.data_ptr(), b.k_cache.data_ptr(), b.v_cache.data_ptr(), N, stride,
+                               None, None, float(b.sm_scale), out2.data_ptr(), None,
+                               torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert plan.check_device_errors() == 0
+    assert torch.equal(out, out2)
