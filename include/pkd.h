@@ -176,7 +176,11 @@ pkd_status pkd_run(pkd_plan_t plan, const void* d_q, const void* d_k_cache, cons
  * The prefix is attended once per kv head for all requests (a dense
  * [batch * g, 128] x [128, prefix_len] product on the tensor cores), not once
  * per request.  Other arguments as pkd_run.  The plan must have been created
- * with max_prefix_splits >= 1.  Capturable like pkd_run.
+ * with max_prefix_splits >= 1.  Enqueues the schedule upload, the suffix
+ * decode (every item writes a partial state), the prefix kernel (launched
+ * programmatically, so its CTAs take the SMs the decode grid frees as it
+ * drains; it finishes only after the decode grid has) and the merge of the
+ * prefix and suffix states.  Capturable like pkd_run.
  */
 pkd_status pkd_cascade_decode(pkd_plan_t suffix_plan, const int32_t* d_prefix_page_indices,
                               int prefix_num_pages, int prefix_last_page_len, const void* d_q,

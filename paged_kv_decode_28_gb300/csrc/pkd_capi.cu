@@ -383,6 +383,10 @@ pkd_status ensure_side(pkd_plan_t plan) {
 // merge pass folds n_pre_splits prefix partials into every row.
 struct CascadeMerge {
   int n_pre_splits;
+  // the prefix kernel, launched between the decode and merge launches (when
+  // n_pre_splits > 0): its CTAs take the SMs the decode grid frees as it drains
+  CUtensorMap tmq, tmk, tmv;
+  pkd::PrefixParams pp;
 };
 
 pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, const void* d_v_cache,
@@ -486,6 +490,10 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
       joined = false;
     }
   }
+  if (cascade && cascade->n_pre_splits > 0) {
+    cudaError_t e = pkd::launch_prefix(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->kv_dtype, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefix kernel launch");
+  }
   pkd::MergeParams m{};
   m.merge_rows = reinterpret_cast<const int*>(ws + L.merge_rows);
   m.header = reinterpret_cast<const pkd::WsHeader*>(ws);
@@ -555,8 +563,8 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
   if (prefix_len64 > INT32_MAX) return fail(PKD_ERR_INVALID_ARG, "prefix longer than 2^31 - 1 keys");
   const int prefix_len = static_cast<int>(prefix_len64);
   const int B = plan->batch;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   int n_pre = 0;
+  CascadeMerge cm{};
   if (prefix_len > 0 && B > 0) {
     if (!d_q || !aligned16(d_q)) return fail(PKD_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
     if (!d_k_cache || !d_v_cache || !aligned16(d_k_cache) || !aligned16(d_v_cache))
@@ -630,11 +638,13 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
     pp.pre_o = reinterpret_cast<float*>(plan->ws + plan->lay.pre_o);
     pp.pre_lse = reinterpret_cast<float*>(plan->ws + plan->lay.pre_lse);
     pp.err = reinterpret_cast<unsigned*>(plan->ws);
-    cudaError_t e = pkd::launch_prefix(tmq, tmk, tmv, pp, plan->kv_dtype, st);
-    if (e != cudaSuccess) return cuda_fail(e, "prefix kernel launch");
+    cm.tmq = tmq;
+    cm.tmk = tmk;
+    cm.tmv = tmv;
+    cm.pp = pp;
     n_pre = splits;
   }
-  CascadeMerge cm{n_pre};
+  cm.n_pre_splits = n_pre;
   return run_common(plan, d_q, d_k_cache, d_v_cache, num_pages, page_stride_elems, P, d_k_scale, d_v_scale,
                     sm_scale, d_out, d_lse, stream, nullptr, &cm);
 }

@@ -369,10 +369,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   __syncthreads();
 
-  // the merge pass may be scheduled now; it waits for this grid to finish
-  ptx::pdl_launch_dependents();
   // this grid may have been launched before the schedule upload finished
   ptx::pdl_wait_prior_grid();
+  // the next grid (the merge, or the cascade's prefix kernel) may be scheduled
+  // now: everything enqueued before this step is complete, so it may read the
+  // step's inputs; it waits for this grid before reading this grid's output
+  ptx::pdl_launch_dependents();
   const int it0 = p.cta_begin[blockIdx.x];
   const int it1 = p.cta_begin[blockIdx.x + 1];
   const int Hk = p.num_kv_heads;

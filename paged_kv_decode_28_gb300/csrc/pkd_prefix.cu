@@ -419,6 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
+  // This grid is launched programmatically behind the decode grid and reads
+  // nothing it writes; it does not finish before that grid has, so the merge
+  // grid behind it, which waits for this one, sees the decode's partials too.
+  if (threadIdx.x == 0) ptx::pdl_wait_prior_grid();
 }
 
 }  // namespace
@@ -461,13 +465,15 @@ cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kAlloc;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = p.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, tmq, tmk, tmv, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

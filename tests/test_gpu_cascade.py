@@ -129,3 +129,25 @@ def test_cascade_is_deterministic_and_replans():
     o1, l1 = _gpu_cascade(b, plan)
     o2, l2 = _gpu_cascade(b, plan)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_cascade_back_to_back_without_sync():
+    """Cascade steps of two alternating batches with no host synchronization:
+    the prefix kernel of one step runs beside the tail of its decode grid and
+    must leave the previous step's merge inputs alone."""
+    batches = [wl.make_config(4, device="cuda", batch=24), wl.make_config(4, device="cuda", batch=40)]
+    plan = pkd.Plan(64, 32, 8, max_prefix_splits=16)
+    refs = [_gpu_cascade(b, plan) for b in batches]
+    refs = [(o.clone(), l.clone()) for o, l in refs]
+    outs = []
+    for i in range(6):
+        b = batches[i % 2]
+        idx = torch.from_numpy(np.ascontiguousarray(b.kv_page_indices)).cuda()
+        pre = torch.from_numpy(np.ascontiguousarray(b.prefix_page_indices)).cuda()
+        plan.plan(b.kv_indptr, idx, b.kv_last_page_len, b.page_size)
+        outs.append(plan.cascade_decode(pre, b.prefix_last_page_len, b.q, b.k_cache, b.v_cache, sm_scale=b.sm_scale))
+    torch.cuda.synchronize()
+    assert plan.check_device_errors() == 0
+    for i, (o, l) in enumerate(outs):
+        ro, rl = refs[i % 2]
+        assert torch.equal(o, ro) and torch.equal(l, rl), f"step {i} differs from the isolated run"
