@@ -31,14 +31,15 @@ template <int KVT>
 struct Cfg {
   // bytes of one key (or value) row of one kv head
   static constexpr int kRowBytes = (KVT == kE4M3) ? kHeadDim : 2 * kHeadDim;
-  static constexpr int kStages = (KVT == kE4M3) ? 4 : 3;
+  // fp8: consumers hold two stages per step, so the ring runs three ahead
+  static constexpr int kStages = (KVT == kE4M3) ? 5 : 3;
   static constexpr bool kMmaBf16 = (KVT == kBF16);
   // one 64-key tile of K (or V): 16-bit -> two [64][128 B] halves (d 0..63, 64..127)
   static constexpr int kTensorBytes = kChunkKeys * kRowBytes;
   static constexpr int kStageBytes = 2 * kTensorBytes;
-  // fp8: each consumer warp's value rows of two stages converted to f16,
-  // 2 x [2 halves][16][128 B] per warp
-  static constexpr int kV16Bytes = (KVT == kE4M3) ? 4 * 8192 : 0;
+  // fp8: each consumer warp's 16 value rows of a stage converted to f16,
+  // [2 halves][16][128 B] per warp
+  static constexpr int kV16Bytes = (KVT == kE4M3) ? 4 * 4096 : 0;
   static constexpr int kV16 = kStages * kStageBytes;
   static constexpr int kCombO = kV16 + kV16Bytes;                               // f32 [3][8][128]
   static constexpr int kCombML = kCombO + 3 * kMaxGroup * kHeadDim * 4;         // f32 [3][8][2]
@@ -283,15 +284,15 @@ __device__ __forceinline__ void tile16_e4m3(uint32_t kb, uint32_t vb, uint32_t v
 }
 
 // 32 keys: the warp's 16 keys of two consecutive fp8 stages (A, B).  The two
-// halves' conversions and S products are independent work for the scheduler,
-// and the softmax state is updated once for the 32 keys.
+// S products are independent work for the scheduler, and the softmax state is
+// updated once for the 32 keys; the values of A and then of B pass through
+// the warp's one f16 buffer.
 __device__ __forceinline__ void tile32_e4m3(uint32_t kbA, uint32_t vbA, int validA, uint32_t kbB, uint32_t vbB,
                                             int validB, uint32_t v16, int w, int lane,
                                             const uint32_t (&qa0)[8], const uint32_t (&qa2)[8], float sl2,
                                             float& m_run, float& l_run, float (&o)[16][4]) {
   const int t = lane & 3;
   convert_v16(vbA, v16, w, lane);
-  convert_v16(vbB, v16 + 4096u, w, lane);
   float sA[2][4], sB[2][4];
   qk_e4m3(kbA, w, lane, qa0, qa2, sA);
   qk_e4m3(kbB, w, lane, qa0, qa2, sB);
@@ -322,8 +323,11 @@ __device__ __forceinline__ void tile32_e4m3(uint32_t kbA, uint32_t vbA, int vali
   }
   __syncwarp();  // the f16 value rows are written by other lanes of this warp
   pv_f16buf(v16, lane, validA, ptx::pack2<false>(pr[0], pr[1]), ptx::pack2<false>(pr[2], pr[3]), o);
-  pv_f16buf(v16 + 4096u, lane, validB, ptx::pack2<false>(pr[4], pr[5]), ptx::pack2<false>(pr[6], pr[7]), o);
-  __syncwarp();  // the buffers are rewritten by the next step
+  __syncwarp();  // every lane has read A's rows
+  convert_v16(vbB, v16, w, lane);
+  __syncwarp();
+  pv_f16buf(v16, lane, validB, ptx::pack2<false>(pr[4], pr[5]), ptx::pack2<false>(pr[6], pr[7]), o);
+  __syncwarp();  // the buffer is rewritten by the next step
 }
 
 // Head dimension index of accumulator o[nt][e] held by thread t.
@@ -487,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           if (okA && okB && (validA > 0 || validB > 0)) {
             const uint32_t kbA = base + s * C::kStageBytes, kbB = base + s2 * C::kStageBytes;
             tile32_e4m3(kbA, kbA + C::kTensorBytes, validA, kbB, kbB + C::kTensorBytes, validB,
-                        base + C::kV16 + w * 8192u, w, lane, qa0, qa2, sl2, m_run, l_run, o);
+                        base + C::kV16 + w * 4096u, w, lane, qa0, qa2, sl2, m_run, l_run, o);
           }
           __syncwarp();
           if (lane == 0) {
@@ -511,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const uint32_t kb = base + s * C::kStageBytes;
         const uint32_t vb = kb + C::kTensorBytes;
         if constexpr (KVT == kE4M3) {
-          tile16_e4m3(kb, vb, base + C::kV16 + w * 8192u, w, lane, valid, qa0, qa2, sl2, m_run, l_run, o);
+          tile16_e4m3(kb, vb, base + C::kV16 + w * 4096u, w, lane, valid, qa0, qa2, sl2, m_run, l_run, o);
         } else {
           tile16_16bit<C::kMmaBf16>(kb, vb, w, lane, valid, qa0, qa2, sl2, m_run, l_run, o);
         }
