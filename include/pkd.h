@@ -156,12 +156,15 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
  *   num_pages  pages in each pool; page ids must lie in [0, num_pages).
  *   d_k_scale, d_v_scale  fp32 [num_kv_heads] for an E4M3 cache, else NULL.
  *   d_out      [batch, num_qo_heads, 128] q dtype;  d_lse fp32 [batch, num_qo_heads] or NULL.
- * Enqueues three kernels on `stream` (the schedule upload, decode, then the
- * split-KV merge; the last two are launched programmatically so each may be
- * scheduled before its predecessor ends, and waits for it in-kernel) with
- * grids that depend only on the plan object, plus event records on a side
- * stream of the plan that rejoins `stream` (created on the first call); no
- * allocation, no host sync: capturable in a CUDA graph.
+ * Enqueues two kernels on `stream`: the schedule upload, then decode
+ * (launched programmatically, so it may be scheduled before the upload ends,
+ * and waits for it in-kernel).  The decode kernel also merges the split rows
+ * (the CTA that finishes a row's last item folds its partial states) and
+ * writes the rows of empty requests; a plan without any work item enqueues
+ * the merge kernel instead of decode.  Grids depend only on the plan object;
+ * event records go on a side stream of the plan that rejoins `stream`
+ * (created on the first call).  No allocation, no host sync: capturable in a
+ * CUDA graph.
  */
 pkd_status pkd_run(pkd_plan_t plan, const void* d_q, const void* d_k_cache, const void* d_v_cache,
                    int64_t num_pages, int64_t page_stride_elems, const float* d_k_scale,

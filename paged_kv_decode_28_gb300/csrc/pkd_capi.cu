@@ -39,7 +39,8 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 struct Layout {
   int group = 0, max_rows = 0, max_items = 0;
   size_t cta_begin = 0, items = 0, merge_rows = 0, row_begin = 0, row_count = 0, kv_len = 0,
-         page_begin = 0, meta_end = 0, part_o = 0, part_lse = 0, pre_o = 0, pre_lse = 0, total = 0;
+         page_begin = 0, empty_rows = 0, row_done = 0, meta_end = 0, part_o = 0, part_lse = 0, pre_o = 0,
+         pre_lse = 0, total = 0;
 };
 
 bool make_layout(int max_batch, int hq, int hk, int d, int G, int max_splits, Layout* L) {
@@ -63,6 +64,10 @@ bool make_layout(int max_batch, int hq, int hk, int d, int G, int max_splits, La
   off += align256(4ull * max_batch);
   L->page_begin = off;
   off += align256(4ull * max_batch);
+  L->empty_rows = off;
+  off += align256(4ull * L->max_rows);
+  L->row_done = off;  // never written by the host: every upload resets the counters to zero
+  off += align256(4ull * L->max_rows);
   L->meta_end = off;
   L->part_o = off;
   off += align256(4ull * L->max_items * L->group * d);
@@ -326,6 +331,11 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
     items[4 * i + 3] = row_count[row] > 1 ? pkd::kItemSplit : 0;
   }
   for (int b = 0; b < batch; ++b) page_begin[b] = h_kv_indptr[b];
+  auto* empty_rows = reinterpret_cast<int32_t*>(h + L.empty_rows);
+  int n_empty = 0;
+  for (int r = 0; r < batch * num_kv_heads; ++r)
+    if (row_count[r] == 0) empty_rows[n_empty++] = r;
+  hdr->n_empty_rows = n_empty;
   hdr->n_items = c.n_items;
   hdr->n_merge_rows = c.n_merge_rows;
   hdr->batch = batch;
@@ -432,6 +442,12 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
   p.num_pages = static_cast<int>(num_pages);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.force_partial = cascade ? 1 : 0;
+  p.fused_merge = cascade ? 0 : 1;
+  p.row_done = reinterpret_cast<int*>(ws + L.row_done);
+  p.row_item_begin = reinterpret_cast<const int*>(ws + L.row_begin);
+  p.row_item_count = reinterpret_cast<const int*>(ws + L.row_count);
+  p.empty_rows = reinterpret_cast<const int*>(ws + L.empty_rows);
+  p.header = reinterpret_cast<const pkd::WsHeader*>(ws);
   // under stream capture the records become event-record nodes that fire on every replay
   unsigned rec_flags = cudaEventRecordDefault;
   {
@@ -493,6 +509,16 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
   if (cascade && cascade->n_pre_splits > 0) {
     cudaError_t e = pkd::launch_prefix(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->kv_dtype, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefix kernel launch");
+  }
+  // plain decode merges its split rows and writes its empty rows in the decode
+  // kernel; the merge kernel runs for the cascade and for a plan without items
+  if (!cascade && plan->counts.n_items > 0) {
+    if (!joined) {  // the side branch rejoins the call's stream
+      cudaError_t e = cudaEventRecord(plan->join_ev, plan->side);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, plan->join_ev, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "side branch join");
+    }
+    return PKD_OK;
   }
   pkd::MergeParams m{};
   m.merge_rows = reinterpret_cast<const int*>(ws + L.merge_rows);

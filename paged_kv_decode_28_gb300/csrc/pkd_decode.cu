@@ -345,6 +345,70 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
   }
 }
 
+template <int QT>
+__device__ __forceinline__ void store_out4(void* out, size_t idx, float4 v) {
+  uint2 u;
+  u.x = ptx::pack2<QT == kBF16>(v.x, v.y);
+  u.y = ptx::pack2<QT == kBF16>(v.z, v.w);
+  *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + idx) = u;
+}
+
+// Merge of split row `row` for qo head j of its group by one warp (lane l: dims
+// 4l..4l+3): its items' partial states (slots beg .. beg + cnt - 1) folded in
+// slot order, out in q dtype and lse in natural log.  The partials were written
+// by other CTAs; the caller has ordered them before these loads.
+template <int QT>
+__device__ __forceinline__ void merge_split_row(const DecodeParams& p, int row, int j, int lane) {
+  const int Hk = p.num_kv_heads, G = p.group, Hq = Hk * G;
+  const int b = row / Hk, h = row - b * Hk;
+  const int beg = p.row_item_begin[row], cnt = p.row_item_count[row];
+  auto lse_of = [&](int s) { return __ldcg(p.part_lse + static_cast<size_t>(beg + s) * G + j); };
+  auto o_of = [&](int s) {
+    return __ldcg(reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(beg + s) * G + j) * kHeadDim) + lane);
+  };
+  float M = -INFINITY;
+  for (int s0 = 0; s0 < cnt; s0 += 32) M = fmaxf(M, (s0 + lane < cnt) ? lse_of(s0 + lane) : -INFINITY);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int s0 = 0; s0 < cnt; s0 += 32) {
+      const int ns = min(32, cnt - s0);
+      const float x = (lane < ns) ? lse_of(s0 + lane) : -INFINITY;
+      const float wgt = (x == -INFINITY) ? 0.f : ptx::ex2(x - M);
+      L += wgt;
+      int s = 0;
+      for (; s + 2 <= ns; s += 2) {
+        const float w0 = __shfl_sync(0xffffffffu, wgt, s), w1 = __shfl_sync(0xffffffffu, wgt, s + 1);
+        const float4 a = o_of(s0 + s), c = o_of(s0 + s + 1);
+        acc.x += w0 * a.x + w1 * c.x;
+        acc.y += w0 * a.y + w1 * c.y;
+        acc.z += w0 * a.z + w1 * c.z;
+        acc.w += w0 * a.w + w1 * c.w;
+      }
+      if (s < ns) {
+        const float w0 = __shfl_sync(0xffffffffu, wgt, s);
+        const float4 a = o_of(s0 + s);
+        acc.x += w0 * a.x;
+        acc.y += w0 * a.y;
+        acc.z += w0 * a.z;
+        acc.w += w0 * a.w;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    const float inv = 1.f / L;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+  }
+  const size_t bq = static_cast<size_t>(b) * Hq + h * G + j;
+  store_out4<QT>(p.out, bq * kHeadDim + 4 * lane, acc);
+  if (lane == 0 && p.lse) p.lse[bq] = (M == -INFINITY) ? -INFINITY : (M + ptx::lg2(L)) * kLn2;
+}
+
 template <int QT, int KVT>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -457,6 +521,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int t = lane & 3;
   const int G = p.group;
   const int Hq = Hk * G;
+  volatile int* merge_flag = abort_flag + 1;
+  if (p.fused_merge) {
+    // rows without items: o = 0, lse = -inf (one warp per row, while the
+    // producer fills the first stages)
+    const int n_empty = p.header->n_empty_rows;
+    for (int i = blockIdx.x * kConsumerWarps + w; i < n_empty; i += gridDim.x * kConsumerWarps) {
+      const int row = p.empty_rows[i];
+      const int b = row / Hk, h = row - b * Hk;
+      for (int j = 0; j < G; ++j) {
+        const size_t bq = static_cast<size_t>(b) * Hq + h * G + j;
+        *(reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + bq * kHeadDim) + lane) = make_uint2(0u, 0u);
+        if (lane == 0 && p.lse) p.lse[bq] = -INFINITY;
+      }
+    }
+  }
   int s = 0;
   uint32_t ph = 0;
 #pragma unroll 1
@@ -592,6 +671,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           }
         }
         if (t == 0 && p.lse) p.lse[static_cast<size_t>(b) * Hq + qo] = lse2 * kLn2;
+      }
+    }
+    if (p.fused_merge && (item.w & kItemSplit)) {
+      // Publish this item's partial state (the fence orders its stores before
+      // the count); the item that completes the row merges it, its consumer
+      // warps taking the row's qo heads in turn.
+      if (w == 0) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) *merge_flag = (atomicAdd(p.row_done + item.x, 1) + 1 == p.row_item_count[item.x]) ? 1 : 0;
+      }
+      ptx::named_bar_sync(1, kConsumerWarps * 32);
+      if (*merge_flag) {
+        __threadfence();  // the other items' partial states are visible after the count
+        for (int j = w; j < G; j += kConsumerWarps) merge_split_row<QT>(p, item.x, j, lane);
       }
     }
   }

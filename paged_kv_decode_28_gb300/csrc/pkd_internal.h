@@ -28,7 +28,8 @@ struct WsHeader {
   int n_merge_rows;
   int batch;
   int zero_page;      // a page index of 0 for single-request decode
-  int pad[56];
+  int n_empty_rows;   // rows (request, kv head) without items
+  int pad[55];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -59,6 +60,14 @@ struct DecodeParams {
   int num_pages;          // pool pages (index validation)
   float scale_log2;       // sm_scale * log2(e)
   int force_partial;      // cascade: every item writes a partial state
+  // fused merge (plain decode): the item that completes a split row merges the
+  // row's partial states, and rows without items are written at grid start
+  int fused_merge;
+  int* row_done;              // [B * Hk] items of the row finished (zero at the start of a run)
+  const int* row_item_begin;  // [B * Hk]
+  const int* row_item_count;  // [B * Hk]
+  const int* empty_rows;      // [header->n_empty_rows]
+  const WsHeader* header;
 };
 
 struct MergeParams {
