@@ -2,9 +2,9 @@
 """Benchmark of batched paged-KV decode attention on GB300.
 
 One step = the whole decode hot path over one batch: the host plan (split-KV
-schedule, one async upload) followed by run (the TMA-pipelined decode kernel
-and the split-KV merge kernel, replayed from a CUDA graph captured once) on
-inputs resident in HBM.  The end-to-end figure runs the same step eagerly
+schedule) followed by run (the schedule upload and the TMA-pipelined decode
+kernel, which also merges its split rows, replayed from one CUDA graph per
+step) on inputs resident in HBM.  The end-to-end figure runs the same step eagerly
 through the public API with host buffers.  The default workload
 is the batch-64 GQA decode batch (64 requests, 32 qo / 8 kv heads, head_dim
 128, bf16, lengths uniform in [512, 4096], page size 16, pages drawn from a

@@ -237,8 +237,8 @@ pkd_status pkd_merge_states(const void* d_v, const float* d_s, int64_t n, int k,
  * them).  NULL, NULL turns the hook off.  Lets a caller time the dominant
  * kernel alone with CUDA events.  The stop event is recorded on a side stream
  * of the plan that waits for the decode kernel and rejoins the call's stream
- * after the merge launch, so the merge kernel keeps its programmatic early
- * launch.  During stream capture the records are made with
+ * at the end of the call, so the kernel after decode keeps its programmatic
+ * early launch.  During stream capture the records are made with
  * cudaEventRecordExternal, so a captured graph records them on every replay.
  * The first call that enables the hook creates the side stream and two
  * events (PKD_ERR_CUDA if that fails); pkd_plan_destroy releases them.
