@@ -86,7 +86,6 @@ struct MergeParams {
   int num_kv_heads;
   int group;
   int all_rows;               // cascade: every row of the batch
-  const float* v_scale;       // unused (scales are applied before partials are written)
 };
 
 // Shared-prefix (cascade level 0) attention on the tensor cores.

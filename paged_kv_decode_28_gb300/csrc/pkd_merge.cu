@@ -66,7 +66,7 @@ __device__ __forceinline__ void store4(void* out, size_t idx, float4 v, int dtyp
 }
 
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const MergeParams p) {
-  ptx::pdl_wait_prior_grid();  // the decode grid's partials are complete and visible
+  ptx::pdl_wait_prior_grid();  // the partials of the grids before this one are complete and visible
   const int batch = p.header->batch;
   const int Hk = p.num_kv_heads;
   const int G = p.group;
@@ -237,7 +237,8 @@ int grid_for_rows(int64_t rows) {
 }  // namespace
 
 cudaError_t launch_merge_rows(const MergeParams& p, int grid, cudaStream_t stream) {
-  // programmatic dependent launch: scheduled while the decode grid runs, it
+  // programmatic dependent launch: scheduled while the grid before it (the
+  // cascade's prefix kernel, or the decode grid of the no-alloc path) runs, it
   // waits in griddepcontrol.wait for that grid to complete
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
