@@ -252,6 +252,17 @@ pkd_status pkd_plan_set_timing_events(pkd_plan_t plan, void* start_event, void* 
 pkd_status pkd_check_device_errors(pkd_plan_t plan, uint32_t* flags_out, void* stream);
 
 /*
+ * Test hook for the pipeline's failure path (the pages have no counterpart).
+ * With PKD_DEBUG_STALL_PIPELINE set, the decode kernel of later pkd_run calls
+ * issues no copies, so every consumer's first pipeline wait runs out after its
+ * time limit (about 2 s): the kernel then leaves with PKD_DEVERR_WAIT_TIMEOUT
+ * in the device error word instead of hanging, and its outputs are undefined.
+ * 0 turns it off.  Host-side only; no other effect.
+ */
+#define PKD_DEBUG_STALL_PIPELINE 1
+pkd_status pkd_plan_set_debug(pkd_plan_t plan, int flags);
+
+/*
  * Batched paged decode that allocates nothing (the pages have no counterpart:
  * this is a library convenience, not part of the method).
  *

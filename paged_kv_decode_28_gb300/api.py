@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
         "pkd_merge_states": (i, [_vp, _vp, i64, i, i, i, i, _vp, _vp, _vp]),
         "pkd_check_device_errors": (i, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
         "pkd_plan_set_timing_events": (i, [_vp, _vp, _vp]),
+        "pkd_plan_set_debug": (i, [_vp, i]),
         "pkd_decode_noalloc": (i, [_i32p, _vp, _i32p, i, i, i, i, i, i, i, _vp, _vp, _vp, i64, i64, _vp, _vp, f,
                                    _vp, _vp, _vp]),
         "pkd_plan_host": (i, [_i32p, _i32p, i, i, i, i, _i32p, i, _i32p, _i32p, _i32p, _i32p, _i32p]),
@@ -251,6 +252,11 @@ class Plan:
         a = None if start is None else ctypes.c_void_p(start.cuda_event)
         b = None if stop is None else ctypes.c_void_p(stop.cuda_event)
         _check(lib().pkd_plan_set_timing_events(self._h, a, b))
+
+    def set_debug(self, flags: int):
+        """Test hook (PKD_DEBUG_STALL_PIPELINE = 1: later runs' decode pipelines stall
+        until their waits time out and flag PKD_DEVERR_WAIT_TIMEOUT); 0 turns it off."""
+        _check(lib().pkd_plan_set_debug(self._h, int(flags)))
 
     def check_device_errors(self, stream=None) -> int:
         flags = ctypes.c_uint32(0)

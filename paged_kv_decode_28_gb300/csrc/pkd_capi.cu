@@ -171,6 +171,7 @@ struct pkd_plan_s {
   cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
   cudaStream_t side = nullptr;
   cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+  int debug_flags = 0;  // PKD_DEBUG_* test hooks
   ~pkd_plan_s() {
     if (side) {
       cudaStreamSynchronize(side);
@@ -448,6 +449,7 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
   p.row_item_count = reinterpret_cast<const int*>(ws + L.row_count);
   p.empty_rows = reinterpret_cast<const int*>(ws + L.empty_rows);
   p.header = reinterpret_cast<const pkd::WsHeader*>(ws);
+  p.debug_stall = (plan->debug_flags & PKD_DEBUG_STALL_PIPELINE) ? 1 : 0;
   // under stream capture the records become event-record nodes that fire on every replay
   unsigned rec_flags = cudaEventRecordDefault;
   {
@@ -751,6 +753,13 @@ pkd_status pkd_plan_set_timing_events(pkd_plan_t plan, void* start_event, void* 
   }
   plan->ev_start = static_cast<cudaEvent_t>(start_event);
   plan->ev_stop = static_cast<cudaEvent_t>(stop_event);
+  return PKD_OK;
+}
+
+pkd_status pkd_plan_set_debug(pkd_plan_t plan, int flags) {
+  if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
+  if (flags & ~PKD_DEBUG_STALL_PIPELINE) return fail(PKD_ERR_INVALID_ARG, "unknown debug flags 0x%x", flags);
+  plan->debug_flags = flags;
   return PKD_OK;
 }
 

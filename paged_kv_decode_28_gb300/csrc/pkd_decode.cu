@@ -449,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
+    if (p.debug_stall) return;  // test hook: no copy is issued, so the consumers' waits run out
     if (lane == 0) {
       ptx::prefetch_tensormap(&tmk);
       ptx::prefetch_tensormap(&tmv);

@@ -68,6 +68,7 @@ struct DecodeParams {
   const int* row_item_count;  // [B * Hk]
   const int* empty_rows;      // [header->n_empty_rows]
   const WsHeader* header;
+  int debug_stall;            // test hook: the producer issues nothing (waits run out)
 };
 
 struct MergeParams {

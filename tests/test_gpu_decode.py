@@ -183,3 +183,28 @@ def test_run_without_lse_output():
     torch.cuda.synchronize()
     assert plan.check_device_errors() == 0
     assert torch.equal(out, out2)
+
+
+def test_stalled_pipeline_times_out_flags_and_recovers():
+    """A decode pipeline whose producer issues nothing (host-set test hook):
+    every wait runs out after its ~2 s limit, the kernel returns with
+    PKD_DEVERR_WAIT_TIMEOUT set, and the context stays usable for a normal run."""
+    import time
+    b = wl.make_paged(seed=630, lengths=[40, 300, 1000], num_qo_heads=8, num_kv_heads=2, page_size=16,
+                      device="cuda")
+    out, lse, plan = gpu_paged_decode(b)
+    plan.set_debug(1)
+    t0 = time.perf_counter()
+    plan.run(b.q, b.k_cache, b.v_cache, sm_scale=b.sm_scale)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    flags = plan.check_device_errors()
+    assert flags & pkd.api.DEVERR_WAIT_TIMEOUT, f"flags {flags:#x}"
+    assert 1.0 < waited < 30.0, f"the stalled kernel returned after {waited:.2f} s"
+    plan.set_debug(0)
+    out2, lse2 = plan.run(b.q, b.k_cache, b.v_cache, sm_scale=b.sm_scale)
+    torch.cuda.synchronize()
+    assert plan.check_device_errors() == 0
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out2, o_ref)
+    assert_lse_close(lse2, l_ref)
