@@ -41,6 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 KERNEL_SOURCES = ["paged_kv_decode_28_gb300/csrc/pkd_decode.cu", "paged_kv_decode_28_gb300/csrc/pkd_ptx.cuh",
                   "paged_kv_decode_28_gb300/csrc/pkd_internal.h"]
+APPEND_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "append_traffic.json")
+APPEND_SOURCES = ["paged_kv_decode_28_gb300/csrc/pkd_append.cu", "paged_kv_decode_28_gb300/csrc/pkd_internal.h"]
 
 
 def parse_args():
@@ -54,12 +56,17 @@ def parse_args():
     ap.add_argument("--all-configs", action="store_true", help="also print one line per standard workload")
     ap.add_argument("--batch", type=int, default=None,
                     help="shrink the workload to its first N requests (small cases for profiling)")
+    ap.add_argument("--op", choices=["decode", "append"], default="decode",
+                    help="append: time pkd_append_kv (new tokens written into the workload's pool)")
+    ap.add_argument("--append-tokens", type=int, default=0,
+                    help="--op append: new tokens per request in the bulk case (0: enough that the "
+                    "bytes moved exceed twice the 129 MB L2)")
     return ap.parse_args()
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -466,9 +473,167 @@ def run_reference(args, world, rank, local):
     }
 
 
+def run_append(args, world, rank, local):
+    """pkd_append_kv on a workload's pool geometry: a bulk append
+    (args.append_tokens new tokens per request; bandwidth-bound, reported
+    against the HBM peak) and the one-token-per-request append of a decode step
+    (latency)."""
+    import torch
+
+    import paged_kv_decode_28_gb300 as pkd
+    from paged_kv_decode_28_gb300 import _build
+    from paged_kv_decode_28_gb300 import workloads as wl
+
+    _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lens = np.asarray(wl.config_lengths(args.config, args.batch), dtype=np.int64)
+    P, _, Hk, _, kvd = wl.config_geometry(args.config)
+    row_bytes = Hk * 128 * 2 * (2 + (1 if kvd == "e4m3" else 2))  # K and V of one token, read + written
+    A = args.append_tokens or -(-int(2 * 129e6) // (len(lens) * row_bytes))
+    new_dtype = torch.float16 if kvd == "f16" else torch.bfloat16
+    # page table sized for A more tokens per request (the pages the new tokens
+    # land in), pages in a seeded random order; pool values are never read
+    rng = np.random.default_rng(900 + args.config)
+    need = int(((lens + A + P - 1) // P).sum())
+    indptr_h, idx_h, _ = wl.lengths_to_page_table(lens + A, P, rng.permutation(need))
+    pool_dtype = {"bf16": torch.bfloat16, "f16": torch.float16, "e4m3": torch.float8_e4m3fn}[kvd]
+    k_cache = torch.empty(need, P, Hk, 128, dtype=pool_dtype, device=dev)
+    v_cache = torch.empty_like(k_cache)
+    k_scale = v_scale = None
+    if kvd == "e4m3":
+        k_scale = torch.full((Hk,), 0.02, device=dev)
+        v_scale = torch.full((Hk,), 0.02, device=dev)
+    B = len(lens)
+    gen = torch.Generator(device=dev).manual_seed(1)
+    k_new = torch.randn(B * A, Hk, 128, device=dev, generator=gen).to(new_dtype)
+    v_new = torch.randn(B * A, Hk, 128, device=dev, generator=gen).to(new_dtype)
+    bi = torch.arange(B, device=dev, dtype=torch.int32).repeat_interleave(A)
+    pos = (torch.as_tensor(lens.astype(np.int32), device=dev).repeat_interleave(A) +
+           torch.arange(A, device=dev, dtype=torch.int32).repeat(B))
+    indptr = torch.as_tensor(np.asarray(indptr_h, dtype=np.int32), device=dev)
+    idx = torch.as_tensor(np.asarray(idx_h, dtype=np.int32), device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(n_tok, steps):
+        for _ in range(max(args.warmup, 3)):
+            pkd.append_kv(k_new[:n_tok], v_new[:n_tok], bi[:n_tok], pos[:n_tok], indptr, idx, k_cache, v_cache,
+                          k_scale=k_scale, v_scale=v_scale, err=err)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            pkd.append_kv(k_new[:n_tok], v_new[:n_tok], bi[:n_tok], pos[:n_tok], indptr, idx, k_cache, v_cache,
+                          k_scale=k_scale, v_scale=v_scale, err=err)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    K = args.steps
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        ms_bulk = max_over_ranks(timed(B * A, K), world, dev)
+        barrier(world)
+    clk = clocks.summary()
+    # one token per request (the first new token of every request), as in a
+    # decode step: device time per append from a captured graph of 16 appends
+    # replayed K times, and the time per append issued one call at a time
+    # from Python (host marshalling included)
+    sel = torch.arange(B, device=dev) * A
+    k1, v1, b1, p1 = k_new[sel].contiguous(), v_new[sel].contiguous(), bi[sel].contiguous(), pos[sel].contiguous()
+
+    def one():
+        pkd.append_kv(k1, v1, b1, p1, indptr, idx, k_cache, v_cache, k_scale=k_scale, v_scale=v_scale, err=err)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            one()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(16):
+            one()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us_step = e0.elapsed_time(e1) / (16 * K) * 1e3
+    e0.record(stream)
+    for _ in range(K):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us_call = e0.elapsed_time(e1) / K * 1e3
+    assert int(err.item()) == 0
+    e_new, e_kv = 2, k_cache.element_size()
+    nbytes = B * A * Hk * 128 * 2 * (e_new + e_kv) + B * A * 8  # rows read + written, plus indices
+    achieved = nbytes / (ms_bulk * 1e-3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    # DRAM bytes of one launch from an ncu capture of the same kernel source on
+    # this workload's geometry, scaled by the tokens appended (traffic grows in
+    # proportion to the tokens)
+    traffic = None
+    try:
+        with open(APPEND_TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        ent = tr.get("configs", {}).get(str(args.config))
+        if tr.get("kernel_hash") == kernel_hash(APPEND_SOURCES) and ent:
+            traffic = int(ent["dram_bytes"] * (B * A) / ent["tokens"])
+    except Exception:
+        pass
+    # the oracle on a bounded sample: 256 of the new tokens into a 512-page pool of the same geometry
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        from oracle import kv_append as ka
+
+        n_s = min(256, B * A)
+        pool = torch.zeros(512, P, Hk, 128, dtype=pool_dtype)
+        ip = torch.tensor([0, 512], dtype=torch.int32)
+        pi = torch.arange(512, dtype=torch.int32)
+        ps = torch.arange(n_s, dtype=torch.int32) % (512 * P)
+        ks = k_scale.cpu() if k_scale is not None else None
+        t0 = time.perf_counter()
+        ka.append_kv(pool, pool, k_new[:n_s].cpu(), v_new[:n_s].cpu(), torch.zeros(n_s, dtype=torch.int32), ps, ip,
+                     pi, P, ks, ks)
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(n_s * Hk * 128 * 2 * (e_new + e_kv) / dt / 1e9, 5), "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": f"{n_s} new tokens into a 512-page pool of the same geometry "
+               f"(python oracle, {dt:.2f} s)"}
+    return {
+        "metric": "kv append (pkd_append_kv): achieved HBM GB/s",
+        "value": round(world * achieved, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_bulk, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": kvd, "data": "synthetic (seeded N(0,1) rows)",
+        "config": {"workload": f"append {A} tokens to each request of {wl.CONFIG_NAMES[args.config]}",
+                   "batch": B, "num_kv_heads": Hk, "head_dim": 128, "page_size": P, "new_dtype": str(new_dtype),
+                   "bytes_per_step": int(nbytes), "parallelism": f"replicas x{world}",
+                   "l2": f"{nbytes / 1e9:.2f} GB moved per step "
+                   f"{'>' if nbytes > 129e6 else '<'} 129 MB L2; no flush between steps"},
+        "roofline": {"bound": "hbm", "kernel": "pkd append_kv_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback", "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic},
+        "decode_step_append_us": {"graph_replay": round(us_step, 2), "python_call": round(us_call, 2),
+                                  "bytes": int(B * row_bytes)},
+        "cpu_baseline": cpu, "gpu_launches": K, "clocks": clk,
+    }
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_init(args)
+    if args.op == "append":
+        line = run_append(args, world, rank, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, world, rank, local)
     else:

@@ -193,6 +193,37 @@ pkd_status pkd_cascade_decode(pkd_plan_t suffix_plan, const int32_t* d_prefix_pa
                               void* stream);
 
 /*
+ * Append new tokens' keys and values to the paged cache: the write step on
+ * either side of each decode step (README mirror, "Core Features": decode,
+ * prefill and append kernels over a paged KV cache).  Token i belongs to
+ * request d_batch_indices[i] at position d_positions[i] of that request's
+ * sequence; its rows, every kv head, go to page
+ * d_kv_page_indices[d_kv_indptr[b] + pos / page_size], slot pos % page_size.
+ * Pages must already be in the table (allocating them is the caller's); the
+ * caller then plans the next decode with the longer lengths.
+ *   d_k_new, d_v_new   device [n_tokens, num_kv_heads, 128] in new_dtype (F16 or BF16).
+ *   d_batch_indices, d_positions   device int32 [n_tokens].
+ *   d_kv_indptr        device int32 [batch + 1]; d_kv_page_indices device int32.
+ *   d_k_cache, d_v_cache, num_pages, page_stride_elems   the pools as in pkd_run, kv_dtype.
+ *   kv_dtype F16/BF16: must equal new_dtype; the values are copied.
+ *   kv_dtype E4M3: codes e4m3(x / scale[h]) with the quotient in fp32 (IEEE
+ *     division), rounded to nearest even and saturated to +-448;
+ *     d_k_scale / d_v_scale fp32 [num_kv_heads] (the scales decode reads).
+ *   d_err_word         optional device uint32: a token whose request, position
+ *     or page lies outside the table or the pool writes nothing and sets
+ *     PKD_DEVERR_PAGE_INDEX here (a plan's workspace start is such a word).
+ * Tokens must not target the same (page, slot) twice.  One kernel on `stream`,
+ * no allocation, no host sync (capturable).
+ */
+pkd_status pkd_append_kv(const void* d_k_new, const void* d_v_new, int new_dtype,
+                         const int32_t* d_batch_indices, const int32_t* d_positions, int n_tokens,
+                         const int32_t* d_kv_indptr, const int32_t* d_kv_page_indices, int batch,
+                         int num_kv_heads, int head_dim, int page_size, void* d_k_cache,
+                         void* d_v_cache, int kv_dtype, int64_t num_pages,
+                         int64_t page_stride_elems, const float* d_k_scale,
+                         const float* d_v_scale, uint32_t* d_err_word, void* stream);
+
+/*
  * Single-request decode with contiguous K/V (the quickstart call):
  *   d_q [num_qo_heads, 128]; d_k, d_v [kv_len, num_kv_heads, 128] (kv_len >= 0);
  *   d_out [num_qo_heads, 128] (q dtype); d_lse fp32 [num_qo_heads] or NULL.

@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         "pkd_check_device_errors": (i, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
         "pkd_plan_set_timing_events": (i, [_vp, _vp, _vp]),
         "pkd_plan_set_debug": (i, [_vp, i]),
+        "pkd_append_kv": (i, [_vp, _vp, i, _vp, _vp, i, _vp, _vp, i, i, i, i, _vp, _vp, i, i64, i64, _vp, _vp, _vp,
+                              _vp]),
         "pkd_decode_noalloc": (i, [_i32p, _vp, _i32p, i, i, i, i, i, i, i, _vp, _vp, _vp, i64, i64, _vp, _vp, f,
                                    _vp, _vp, _vp]),
         "pkd_plan_host": (i, [_i32p, _i32p, i, i, i, i, _i32p, i, _i32p, _i32p, _i32p, _i32p, _i32p]),
@@ -264,6 +266,35 @@ class Plan:
         if st not in (0, 6):
             _check(st)
         return int(flags.value)
+
+
+def append_kv(k_new: torch.Tensor, v_new: torch.Tensor, batch_indices: torch.Tensor, positions: torch.Tensor,
+              kv_indptr: torch.Tensor, kv_page_indices: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+              *, k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+              err: Optional[torch.Tensor] = None, stream=None):
+    """Write new tokens' rows into the paged cache (in place): k_new / v_new
+    ``[n, Hk, 128]``; token i goes to request ``batch_indices[i]`` at position
+    ``positions[i]``.  ``kv_indptr`` / ``kv_page_indices`` are int32 CUDA tensors;
+    e4m3 pools quantise with ``k_scale`` / ``v_scale``.  ``err`` (int32 CUDA
+    tensor of one element) collects PKD_DEVERR_PAGE_INDEX for skipped tokens."""
+    N, P, Hk, D, stride = _check_pool(k_new, k_cache, v_cache)
+    if k_new.dim() != 3 or k_new.shape != v_new.shape or k_new.shape[1:] != (Hk, D):
+        raise ValueError(f"k_new / v_new must be [n, {Hk}, {D}]")
+    if not (k_new.is_contiguous() and v_new.is_contiguous()):
+        raise ValueError("k_new / v_new must be contiguous")
+    for t, name in ((batch_indices, "batch_indices"), (positions, "positions"), (kv_indptr, "kv_indptr"),
+                    (kv_page_indices, "kv_page_indices")):
+        if t.dtype != torch.int32 or t.device.type != "cuda" or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    n = k_new.shape[0]
+    if batch_indices.numel() != n or positions.numel() != n:
+        raise ValueError("one batch index and one position per new token")
+    if k_new.dtype not in (torch.float16, torch.bfloat16) or k_cache.dtype not in _DTYPE_CODE:
+        raise ValueError("k_new / v_new must be f16 or bf16")
+    _check(lib().pkd_append_kv(_ptr(k_new), _ptr(v_new), _DTYPE_CODE[k_new.dtype], _ptr(batch_indices),
+                               _ptr(positions), n, _ptr(kv_indptr), _ptr(kv_page_indices), kv_indptr.numel() - 1,
+                               Hk, D, P, _ptr(k_cache), _ptr(v_cache), _DTYPE_CODE[k_cache.dtype], N, stride,
+                               _ptr(k_scale), _ptr(v_scale), _ptr(err), _stream(stream)))
 
 
 def single_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, sm_scale: Optional[float] = None,

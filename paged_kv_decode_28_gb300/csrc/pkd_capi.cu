@@ -677,6 +677,55 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
                     sm_scale, d_out, d_lse, stream, nullptr, &cm);
 }
 
+pkd_status pkd_append_kv(const void* d_k_new, const void* d_v_new, int new_dtype,
+                         const int32_t* d_batch_indices, const int32_t* d_positions, int n_tokens,
+                         const int32_t* d_kv_indptr, const int32_t* d_kv_page_indices, int batch,
+                         int num_kv_heads, int head_dim, int page_size, void* d_k_cache,
+                         void* d_v_cache, int kv_dtype, int64_t num_pages,
+                         int64_t page_stride_elems, const float* d_k_scale,
+                         const float* d_v_scale, uint32_t* d_err_word, void* stream) {
+  if (n_tokens < 0 || batch < 0 || num_kv_heads <= 0) return fail(PKD_ERR_INVALID_ARG, "bad n_tokens/batch/heads");
+  if (head_dim != pkd::kHeadDim) return fail(PKD_ERR_UNSUPPORTED, "head_dim %d (128 only)", head_dim);
+  if (page_size < 1) return fail(PKD_ERR_INVALID_ARG, "page_size must be >= 1");
+  const bool fp8 = kv_dtype == PKD_E4M3;
+  if (!fp8 && !(kv_dtype == PKD_F16 || kv_dtype == PKD_BF16))
+    return fail(PKD_ERR_UNSUPPORTED, "kv dtype %d", kv_dtype);
+  if (!(new_dtype == PKD_F16 || new_dtype == PKD_BF16)) return fail(PKD_ERR_UNSUPPORTED, "new dtype %d", new_dtype);
+  if (!fp8 && new_dtype != kv_dtype) return fail(PKD_ERR_UNSUPPORTED, "a 16-bit pool takes values of its own dtype");
+  if (fp8 && (!d_k_scale || !d_v_scale)) return fail(PKD_ERR_INVALID_ARG, "an E4M3 pool needs k_scale and v_scale");
+  if (n_tokens == 0) return PKD_OK;
+  if (!d_k_new || !d_v_new || !d_batch_indices || !d_positions || !d_kv_indptr || !d_kv_page_indices ||
+      !d_k_cache || !d_v_cache)
+    return fail(PKD_ERR_INVALID_ARG, "NULL buffer");
+  if (!aligned16(d_k_new) || !aligned16(d_v_new) || !aligned16(d_k_cache) || !aligned16(d_v_cache))
+    return fail(PKD_ERR_INVALID_ARG, "new rows and pools must be 16-byte aligned");
+  if (num_pages <= 0 || num_pages > INT32_MAX) return fail(PKD_ERR_INVALID_ARG, "num_pages out of range");
+  if ((page_stride_elems * elem_bytes(kv_dtype)) % 16 != 0 ||
+      page_stride_elems < static_cast<int64_t>(page_size) * num_kv_heads * head_dim)
+    return fail(PKD_ERR_INVALID_ARG, "page_stride_elems must cover a page and be a 16-byte multiple");
+  pkd::AppendParams p{};
+  p.k_new = d_k_new;
+  p.v_new = d_v_new;
+  p.batch_indices = d_batch_indices;
+  p.positions = d_positions;
+  p.kv_indptr = d_kv_indptr;
+  p.page_indices = d_kv_page_indices;
+  p.k_cache = d_k_cache;
+  p.v_cache = d_v_cache;
+  p.k_scale = d_k_scale;
+  p.v_scale = d_v_scale;
+  p.err = d_err_word;
+  p.page_stride = page_stride_elems;
+  p.n_tokens = n_tokens;
+  p.batch = batch;
+  p.num_kv_heads = num_kv_heads;
+  p.page_size = page_size;
+  p.num_pages = static_cast<int>(num_pages);
+  cudaError_t e = pkd::launch_append_kv(p, new_dtype, kv_dtype, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
+  return PKD_OK;
+}
+
 pkd_status pkd_single_decode(const void* d_q, const void* d_k, const void* d_v, int kv_len,
                              int num_qo_heads, int num_kv_heads, int head_dim, int q_dtype,
                              int kv_dtype, const float* d_k_scale, const float* d_v_scale,

@@ -113,10 +113,32 @@ struct PrefixParams {
   unsigned* err;
 };
 
+// Writing new tokens' K/V rows into the paged cache (pkd_append.cu).
+struct AppendParams {
+  const void* k_new;          // [n_tokens, Hk, D] in the new dtype (f16 / bf16)
+  const void* v_new;
+  const int* batch_indices;   // [n_tokens]
+  const int* positions;       // [n_tokens]
+  const int* kv_indptr;       // [batch + 1] (device)
+  const int* page_indices;    // [kv_indptr[batch]]
+  void* k_cache;              // pool [num_pages, P, Hk, D] with a page stride
+  void* v_cache;
+  const float* k_scale;       // e4m3 pools: [Hk]
+  const float* v_scale;
+  unsigned* err;              // optional device error word
+  int64_t page_stride;        // elements
+  int n_tokens;
+  int batch;
+  int num_kv_heads;
+  int page_size;
+  int num_pages;
+};
+
 // Launchers (defined in the .cu files; return a cudaError_t).
 cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
                           int q_dtype, int kv_dtype, int grid, cudaStream_t stream);
 cudaError_t launch_merge_rows(const MergeParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_append_kv(const AppendParams& p, int new_dtype, int kv_dtype, cudaStream_t stream);
 // dst, src and bytes multiples of 16; src may be mapped pinned host memory
 cudaError_t launch_copy16(void* dst, const void* src, int64_t bytes, cudaStream_t stream);
 cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, const float* sb,

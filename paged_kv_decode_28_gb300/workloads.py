@@ -270,6 +270,12 @@ def config_lengths(idx: int, batch: Optional[int] = None) -> np.ndarray:
     raise ValueError(idx)
 
 
+def config_geometry(idx: int):
+    """(page_size, num_qo_heads, num_kv_heads, q dtype, kv dtype) of a standard workload."""
+    return {1: (16, 32, 32, "f16", "f16"), 2: (16, 32, 8, "bf16", "bf16"), 3: (16, 64, 8, "bf16", "bf16"),
+            4: (16, 32, 8, "bf16", "bf16"), 5: (64, 64, 8, "bf16", "e4m3")}[idx]
+
+
 def make_config(idx: int, device="cpu", batch: Optional[int] = None) -> PagedBatch:
     """The five standard workloads.  ``batch`` shrinks the request count (for
     tests that keep a config's structure at a size the oracle finishes fast)."""
