@@ -24,7 +24,11 @@ What it computes is the plain definition of decode attention over a paged
   state over their union.
 * Cascade decode (same section; deep dive, "Why This Design Works": the shared
   prefix is read once but counted as if each request owns it): the prefix state
-  merged with each request's own state.
+  merged with each request's own state; over a prefix tree, one state per
+  level merged with the request's own.
+* Prefill / append attention (README mirror, "Core Features"): several query
+  tokens per request, each at the end of its sequence, attending the keys up to
+  its own position (causal) or all keys.
 
 Readings where the pages are silent (each is also listed in the design notes):
 natural-log LSE; ``sm_scale`` defaults to ``1/sqrt(head_dim)``; an empty key
@@ -53,6 +57,8 @@ __all__ = [
     "merge_state",
     "merge_states",
     "cascade_decode",
+    "multilevel_cascade_decode",
+    "paged_prefill",
 ]
 
 
@@ -258,3 +264,114 @@ def cascade_decode(
     o_s, s_s = paged_decode(q, k_cache, v_cache, kv_indptr, kv_page_indices, kv_last_page_len,
                             sm_scale=sm_scale, k_scale=k_scale, v_scale=v_scale, rows=rows)
     return merge_state(o_p, s_p, o_s, s_s)
+
+
+def _expand_level(req_indptr, kv_indptr, kv_page_indices, kv_last_page_len, batch: int):
+    """Per-request page table of one shared level: request b in node n (the
+    nodes' request ranges ``req_indptr[n] .. req_indptr[n+1]-1`` partition the
+    batch) owns node n's pages."""
+    req_indptr = np.asarray(req_indptr, dtype=np.int64)
+    kv_indptr = np.asarray(kv_indptr, dtype=np.int64)
+    idx = np.asarray(kv_page_indices, dtype=np.int64)
+    last = np.asarray(kv_last_page_len, dtype=np.int64)
+    if req_indptr[0] != 0 or req_indptr[-1] != batch or np.any(np.diff(req_indptr) < 0):
+        raise ValueError("the nodes' request ranges must partition the batch")
+    out_indptr = [0]
+    out_idx = []
+    out_last = np.zeros(batch, dtype=np.int64)
+    for n in range(len(req_indptr) - 1):
+        pages = idx[kv_indptr[n]:kv_indptr[n + 1]]
+        for b in range(req_indptr[n], req_indptr[n + 1]):
+            out_idx.extend(pages.tolist())
+            out_indptr.append(out_indptr[-1] + len(pages))
+            out_last[b] = last[n] if len(pages) else 0
+    return np.asarray(out_indptr, np.int64), np.asarray(out_idx, np.int64), out_last
+
+
+def multilevel_cascade_decode(q, k_cache, v_cache, levels, kv_indptr, kv_page_indices, kv_last_page_len, *,
+                              sm_scale: Optional[float] = None, k_scale=None, v_scale=None, rows=None):
+    """Cascade decode over a prefix tree (2026 guide, "Cascade attention for
+    shared prefixes"; README mirror, "Core Features": cascade attention as a
+    hierarchical KV cache for shared prefixes).
+
+    ``levels`` lists the shared levels, outermost first, each as
+    ``(req_indptr, kv_indptr, kv_page_indices, kv_last_page_len)``: node n of
+    the level serves requests ``req_indptr[n] .. req_indptr[n+1]-1`` (the
+    nodes partition the batch) and owns pages ``kv_page_indices[kv_indptr[n]
+    .. kv_indptr[n+1]-1`` (all full but the last).  The last three arguments
+    are each request's own pages, as for ``paged_decode``.  Each request's
+    state over every level's keys and its own is the merge of the per-level
+    states (merge_state over disjoint key sets)."""
+    B = to_f64(q).shape[0]
+    acc_o = acc_s = None
+    for req_indptr, ip, idx, last in levels:
+        e_ip, e_idx, e_last = _expand_level(req_indptr, ip, idx, last, B)
+        o_l, s_l = paged_decode(q, k_cache, v_cache, e_ip, e_idx, e_last, sm_scale=sm_scale, k_scale=k_scale,
+                                v_scale=v_scale, rows=rows)
+        acc_o, acc_s = (o_l, s_l) if acc_o is None else merge_state(acc_o, acc_s, o_l, s_l)
+    o_s, s_s = paged_decode(q, k_cache, v_cache, kv_indptr, kv_page_indices, kv_last_page_len,
+                            sm_scale=sm_scale, k_scale=k_scale, v_scale=v_scale, rows=rows)
+    if acc_o is None:
+        return o_s, s_s
+    return merge_state(acc_o, acc_s, o_s, s_s)
+
+
+def paged_prefill(q, qo_indptr, k_cache, v_cache, kv_indptr, kv_page_indices, kv_last_page_len, *,
+                  causal: bool = True, sm_scale: Optional[float] = None, k_scale=None, v_scale=None,
+                  rows: Optional[Iterable[Tuple[int, int]]] = None):
+    """Prefill / append attention over a paged KV cache (README mirror, "Core
+    Features": decode, prefill and append kernels over a paged KV cache).
+
+    q ``[T, Hq, D]``: request r's query tokens are ``q[qo_indptr[r] ..
+    qo_indptr[r+1]-1]``; its keys are all of its pages (``kv_len_r`` keys),
+    the query tokens' own keys included, so token i of the request sits at
+    sequence position ``kv_len_r - q_len_r + i`` and, when ``causal``, attends
+    keys ``0 .. kv_len_r - q_len_r + i``; otherwise all ``kv_len_r`` keys.
+    Returns ``(o [T, Hq, D], lse [T, Hq])`` in float64; with ``rows`` (pairs
+    ``(token, qo head)``) only those, the rest NaN."""
+    qf = to_f64(q)
+    T, Hq, D = qf.shape
+    P, Hk = int(k_cache.shape[1]), int(k_cache.shape[2])
+    g = Hq // Hk
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    ks = None if k_scale is None else to_f64(k_scale)
+    vs = None if v_scale is None else to_f64(v_scale)
+    qo = np.asarray(qo_indptr, dtype=np.int64)
+    want = None
+    if rows is not None:
+        want = {}
+        for t, h in rows:
+            want.setdefault(int(t), set()).add(int(h))
+    o = np.full((T, Hq, D), np.nan)
+    lse = np.full((T, Hq), np.nan)
+    for r in range(len(qo) - 1):
+        q0, q1 = int(qo[r]), int(qo[r + 1])
+        if q1 == q0 or (want is not None and not any(t in want for t in range(q0, q1))):
+            continue
+        toks = request_tokens(kv_indptr, kv_page_indices, kv_last_page_len, P, r)
+        L = len(toks)
+        if L < q1 - q0:
+            raise ValueError(f"request {r}: {q1 - q0} query tokens but only {L} keys")
+        if toks:
+            pages = sorted({p for p, _ in toks})
+            remap = {p: i for i, p in enumerate(pages)}
+            kp = to_f64(_take_pages(k_cache, pages))
+            vp = to_f64(_take_pages(v_cache, pages))
+            local = [(remap[p], t) for p, t in toks]
+            kb, vb = gather_kv(kp, local), gather_kv(vp, local)
+        else:
+            kb = vb = np.zeros((0, Hk, D))
+        if ks is not None:
+            kb = kb * ks[None, :, None]
+        if vs is not None:
+            vb = vb * vs[None, :, None]
+        for t in range(q0, q1):
+            if want is not None and t not in want:
+                continue
+            n_keys = (L - (q1 - q0) + (t - q0) + 1) if causal else L
+            heads = range(Hq) if want is None else sorted(want[t])
+            for h in heads:
+                kvh = h // g
+                o[t, h], lse[t, h] = attend(qf[t, h], kb[:n_keys, kvh, :], vb[:n_keys, kvh, :], sm_scale)
+    return o, lse

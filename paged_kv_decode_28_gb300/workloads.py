@@ -25,7 +25,7 @@ from __future__ import annotations
 
 import math
 from dataclasses import dataclass, field
-from typing import Optional, Sequence
+from typing import Optional, Sequence, Tuple
 
 import numpy as np
 import torch
@@ -83,6 +83,11 @@ class PagedBatch:
     # cascade: one shared prefix page list, attended by every request
     prefix_page_indices: Optional[np.ndarray] = None
     prefix_last_page_len: int = 0
+    # prefix tree: shared levels, outermost first, each
+    # (req_indptr, kv_indptr, kv_page_indices, kv_last_page_len) over its nodes
+    levels: Optional[list] = None
+    # prefill: request r's query tokens are q[qo_indptr[r] .. qo_indptr[r+1]-1]
+    qo_indptr: Optional[np.ndarray] = None
 
     @property
     def batch(self) -> int:
@@ -249,6 +254,64 @@ def make_paged(
         prefix_page_indices=prefix_idx,
         prefix_last_page_len=int(prefix_last),
     )
+
+
+def make_tree(*, seed: int, levels: Sequence[Tuple[Sequence[int], Sequence[int]]], lengths: Sequence[int],
+              num_qo_heads: int, num_kv_heads: int, head_dim: int = 128, page_size: int = 16,
+              q_dtype: str = "bf16", kv_dtype: str = "bf16", device="cpu", name: str = "tree") -> PagedBatch:
+    """A decode batch over a prefix tree: ``levels`` lists the shared levels,
+    outermost first, as (requests per node, tokens per node); each level's
+    request counts sum to the batch (``len(lengths)``), node n serving the
+    next ``count[n]`` requests in order.  ``lengths`` are the requests' own
+    (suffix) token counts.  All pages of all levels and of the suffixes are
+    placed by one seeded permutation of the pool."""
+    B = len(lengths)
+    P = page_size
+    need = sum(int(((np.asarray(toks, np.int64) + P - 1) // P).sum()) for _, toks in levels)
+    base = make_paged(seed=seed, lengths=lengths, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+                      head_dim=head_dim, page_size=P, q_dtype=q_dtype, kv_dtype=kv_dtype, device=device,
+                      name=name, pool_pages=int(((np.asarray(lengths, np.int64) + P - 1) // P).sum()) + need)
+    # the suffix tables use the first pages of make_paged's permutation; the
+    # levels take the pages it left over, in a second seeded order
+    used = set(np.asarray(base.kv_page_indices, np.int64).tolist())
+    free = np.asarray([p for p in range(base.num_pages) if p not in used], np.int64)
+    free = np.random.default_rng(seed + 1).permutation(free)
+    out_levels = []
+    off = 0
+    for counts, toks in levels:
+        counts = np.asarray(counts, np.int64)
+        if counts.sum() != B or np.any(counts < 0):
+            raise ValueError("each level's request counts must sum to the batch")
+        req_indptr = np.zeros(len(counts) + 1, np.int32)
+        req_indptr[1:] = np.cumsum(counts)
+        ip, idx, last = lengths_to_page_table(toks, P, free[off:])
+        off += int(ip[-1])
+        out_levels.append((req_indptr, ip, idx, last))
+    base.levels = out_levels
+    return base
+
+
+def make_prefill(*, seed: int, q_lens: Sequence[int], kv_lens: Sequence[int], num_qo_heads: int,
+                 num_kv_heads: int, head_dim: int = 128, page_size: int = 16, q_dtype: str = "bf16",
+                 kv_dtype: str = "bf16", device="cpu", name: str = "prefill") -> PagedBatch:
+    """A prefill / append batch: request r has ``kv_lens[r]`` keys in its pages
+    (its new tokens' keys included) and ``q_lens[r] <= kv_lens[r]`` query
+    tokens, stacked into q ``[sum(q_lens), Hq, D]``."""
+    q_lens = np.asarray(q_lens, np.int64)
+    kv_lens = np.asarray(kv_lens, np.int64)
+    if np.any(q_lens > kv_lens) or np.any(q_lens < 0):
+        raise ValueError("0 <= q_len <= kv_len per request")
+    b = make_paged(seed=seed, lengths=kv_lens, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+                   head_dim=head_dim, page_size=page_size, q_dtype=q_dtype, kv_dtype=kv_dtype, device=device,
+                   name=name)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 7)
+    T = int(q_lens.sum())
+    b.q = _randn((max(T, 0), num_qo_heads, head_dim), gen, device, _TORCH_DTYPES[q_dtype])
+    qo = np.zeros(len(q_lens) + 1, np.int32)
+    qo[1:] = np.cumsum(q_lens)
+    b.qo_indptr = qo
+    return b
 
 
 def config_lengths(idx: int, batch: Optional[int] = None) -> np.ndarray:
