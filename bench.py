@@ -56,8 +56,11 @@ def parse_args():
     ap.add_argument("--all-configs", action="store_true", help="also print one line per standard workload")
     ap.add_argument("--batch", type=int, default=None,
                     help="shrink the workload to its first N requests (small cases for profiling)")
-    ap.add_argument("--op", choices=["decode", "append"], default="decode",
-                    help="append: time pkd_append_kv (new tokens written into the workload's pool)")
+    ap.add_argument("--op", choices=["decode", "append", "tree", "prefill"], default="decode",
+                    help="append: pkd_append_kv (new tokens written into the workload's pool); tree: "
+                    "prefix-tree decode on the 3-level tree workload; prefill: append-prefill attention")
+    ap.add_argument("--kv-layout", choices=["NHD", "HND"], default="NHD",
+                    help="page layout of the K/V pools: NHD [P, Hk, D] pages or HND [Hk, P, D] pages")
     ap.add_argument("--append-tokens", type=int, default=0,
                     help="--op append: new tokens per request in the bulk case (0: enough that the "
                     "bytes moved exceed twice the 129 MB L2)")
@@ -250,10 +253,16 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     b = wl.make_config(args.config, device=dev, batch=args.batch)
+    if args.kv_layout == "HND":  # the same pages re-laid as [Hk, P, D] blocks
+        for name in ("k_cache", "v_cache"):
+            c = getattr(b, name)
+            setattr(b, name, c.view(torch.uint8).permute(0, 2, 1, 3).contiguous().view(c.dtype))
+            del c
     cascade = b.prefix_page_indices is not None
     idx = torch.from_numpy(b.kv_page_indices).to(dev)
     pre = torch.from_numpy(b.prefix_page_indices).to(dev) if cascade else None
-    plan = pkd.Plan(b.batch, b.num_qo_heads, b.num_kv_heads, max_prefix_splits=16 if cascade else 0, device=dev)
+    plan = pkd.Plan(b.batch, b.num_qo_heads, b.num_kv_heads, max_prefix_splits=16 if cascade else 0, device=dev,
+                    kv_layout=args.kv_layout)
     stream = torch.cuda.current_stream(dev)
     out = torch.empty_like(b.q)
     lse = torch.empty(b.batch, b.num_qo_heads, dtype=torch.float32, device=dev)
@@ -354,7 +363,7 @@ def run_ours(args, world, rank, local):
     try:
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
-        if tr.get("kernel_hash") == kernel_hash() and tr.get("config") == args.config:
+        if tr.get("kernel_hash") == kernel_hash() and tr.get("config") == args.config and args.kv_layout == "NHD":
             traffic = tr.get("dram_bytes_per_launch")
     except Exception:
         pass
@@ -382,6 +391,7 @@ def run_ours(args, world, rank, local):
             "num_kv_heads": b.num_kv_heads,
             "head_dim": b.head_dim,
             "page_size": b.page_size,
+            "kv_layout": args.kv_layout,
             "kv_tokens": int(np.asarray(b.kv_lens, np.int64).sum()),
             "algorithmic_bytes_per_step": nbytes,
             "l2": f"inputs {nbytes / 1e9:.2f} GB > 129 MB L2; no flush between steps",
@@ -498,7 +508,8 @@ def run_append(args, world, rank, local):
     need = int(((lens + A + P - 1) // P).sum())
     indptr_h, idx_h, _ = wl.lengths_to_page_table(lens + A, P, rng.permutation(need))
     pool_dtype = {"bf16": torch.bfloat16, "f16": torch.float16, "e4m3": torch.float8_e4m3fn}[kvd]
-    k_cache = torch.empty(need, P, Hk, 128, dtype=pool_dtype, device=dev)
+    shape = (need, Hk, P, 128) if args.kv_layout == "HND" else (need, P, Hk, 128)
+    k_cache = torch.empty(shape, dtype=pool_dtype, device=dev)
     v_cache = torch.empty_like(k_cache)
     k_scale = v_scale = None
     if kvd == "e4m3":
@@ -519,13 +530,13 @@ def run_append(args, world, rank, local):
     def timed(n_tok, steps):
         for _ in range(max(args.warmup, 3)):
             pkd.append_kv(k_new[:n_tok], v_new[:n_tok], bi[:n_tok], pos[:n_tok], indptr, idx, k_cache, v_cache,
-                          k_scale=k_scale, v_scale=v_scale, err=err)
+                          k_scale=k_scale, v_scale=v_scale, err=err, kv_layout=args.kv_layout)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(steps):
             pkd.append_kv(k_new[:n_tok], v_new[:n_tok], bi[:n_tok], pos[:n_tok], indptr, idx, k_cache, v_cache,
-                          k_scale=k_scale, v_scale=v_scale, err=err)
+                          k_scale=k_scale, v_scale=v_scale, err=err, kv_layout=args.kv_layout)
         e1.record(stream)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / steps
@@ -544,7 +555,8 @@ def run_append(args, world, rank, local):
     k1, v1, b1, p1 = k_new[sel].contiguous(), v_new[sel].contiguous(), bi[sel].contiguous(), pos[sel].contiguous()
 
     def one():
-        pkd.append_kv(k1, v1, b1, p1, indptr, idx, k_cache, v_cache, k_scale=k_scale, v_scale=v_scale, err=err)
+        pkd.append_kv(k1, v1, b1, p1, indptr, idx, k_cache, v_cache, k_scale=k_scale, v_scale=v_scale, err=err,
+                      kv_layout=args.kv_layout)
 
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
@@ -585,7 +597,7 @@ def run_append(args, world, rank, local):
         with open(APPEND_TRAFFIC_FILE) as f:
             tr = json.load(f)
         ent = tr.get("configs", {}).get(str(args.config))
-        if tr.get("kernel_hash") == kernel_hash(APPEND_SOURCES) and ent:
+        if tr.get("kernel_hash") == kernel_hash(APPEND_SOURCES) and ent and args.kv_layout == "NHD":
             traffic = int(ent["dram_bytes"] * (B * A) / ent["tokens"])
     except Exception:
         pass
@@ -613,7 +625,8 @@ def run_append(args, world, rank, local):
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_bulk, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": kvd, "data": "synthetic (seeded N(0,1) rows)",
         "config": {"workload": f"append {A} tokens to each request of {wl.CONFIG_NAMES[args.config]}",
-                   "batch": B, "num_kv_heads": Hk, "head_dim": 128, "page_size": P, "new_dtype": str(new_dtype),
+                   "batch": B, "num_kv_heads": Hk, "head_dim": 128, "page_size": P, "kv_layout": args.kv_layout,
+                   "new_dtype": str(new_dtype),
                    "bytes_per_step": int(nbytes), "parallelism": f"replicas x{world}",
                    "l2": f"{nbytes / 1e9:.2f} GB moved per step "
                    f"{'>' if nbytes > 129e6 else '<'} 129 MB L2; no flush between steps"},
@@ -626,11 +639,213 @@ def run_append(args, world, rank, local):
     }
 
 
+def tree_bytes(b) -> int:
+    """K/V bytes of every shared node (once) and of every request's own keys,
+    plus q, out and lse."""
+    e = b.k_cache.element_size()
+    row = b.num_kv_heads * b.head_dim * 2 * e  # K and V of one key, all kv heads
+    kv = int(np.asarray(b.kv_lens, dtype=np.int64).sum()) * row
+    for _, ip, _, last in b.levels:
+        for n in range(len(ip) - 1):
+            pages = int(ip[n + 1] - ip[n])
+            kv += ((pages - 1) * b.page_size + int(last[n])) * row if pages else 0
+    return kv + b.batch * b.num_qo_heads * (b.head_dim * 2 * b.q.element_size() + 4)
+
+
+def prefill_flops(b) -> int:
+    """Multiply-adds of S = q K^T and O = P V, two flops each, over the keys
+    each query token sees (causal: up to its own position)."""
+    n = 0
+    for r in range(len(b.qo_indptr) - 1):
+        q_len = int(b.qo_indptr[r + 1] - b.qo_indptr[r])
+        kv = int(b.kv_lens[r])
+        # token i sees kv - q_len + i + 1 keys
+        n += q_len * (kv - q_len) + q_len * (q_len + 1) // 2
+    return 4 * n * b.num_qo_heads * b.head_dim
+
+
+def measured_tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_tree(args, world, rank, local):
+    """Prefix-tree decode (pkd_plan_tree / pkd_tree_decode) on the 3-level
+    tree workload: run captured in CUDA graphs, both plans on the host before
+    every replay."""
+    import torch
+
+    import paged_kv_decode_28_gb300 as pkd
+    from paged_kv_decode_28_gb300 import _build
+    from paged_kv_decode_28_gb300 import workloads as wl
+
+    _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    b = wl.make_config_tree(device=dev, batch=args.batch)
+    idx = torch.from_numpy(b.kv_page_indices).to(dev)
+    lv = [(ri, ki, torch.from_numpy(np.asarray(ix)).to(dev), last) for ri, ki, ix, last in b.levels]
+    plan = pkd.Plan(b.batch, b.num_qo_heads, b.num_kv_heads, max_prefix_splits=16, device=dev)
+    out = torch.empty_like(b.q)
+    lse = torch.empty(b.batch, b.num_qo_heads, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def do_plan():
+        plan.plan(b.kv_indptr, idx, b.kv_last_page_len, b.page_size)
+        plan.plan_tree(lv)
+
+    def do_run():
+        plan.tree_decode(b.q, b.k_cache, b.v_cache, sm_scale=b.sm_scale, out=out, lse=lse)
+
+    for _ in range(max(args.warmup, 3)):
+        do_plan()
+        do_run()
+    torch.cuda.synchronize()
+    assert plan.check_device_errors() == 0
+    K = args.steps
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        do_run()
+    for _ in range(3):
+        do_plan()
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        e0.record(stream)
+        for _ in range(K):
+            do_plan()
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    clk = clocks.summary()
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+    assert plan.check_device_errors() == 0
+    nbytes = tree_bytes(b)
+    achieved = nbytes / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        from oracle import attention as orc
+
+        rows = [(r, h) for r in range(0, b.batch, max(1, b.batch // 8)) for h in (0, b.num_qo_heads - 1)]
+        bc = b.to("cpu")
+        t0 = time.perf_counter()
+        orc.multilevel_cascade_decode(bc.q, bc.k_cache, bc.v_cache, bc.levels, bc.kv_indptr, bc.kv_page_indices,
+                                      bc.kv_last_page_len, sm_scale=b.sm_scale, rows=rows)
+        dt = time.perf_counter() - t0
+        frac = len(rows) / (b.batch * b.num_qo_heads)
+        cpu = {"value": round(nbytes * frac / dt / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{len(rows)} of {b.batch * b.num_qo_heads} (request, qo head) rows, bytes scaled by "
+               f"that fraction (python fp64 oracle, {dt:.2f} s)"}
+    return {
+        "metric": "prefix-tree decode (pkd_tree_decode): achieved HBM GB/s per step", "value": round(world * achieved, 1),
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
+        "us_per_call": round(ms_step * 1e3, 2), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) values, seeded lengths and page placement)",
+        "config": {"workload": b.name, "batch": b.batch, "num_qo_heads": b.num_qo_heads,
+                   "num_kv_heads": b.num_kv_heads, "page_size": b.page_size, "bytes_per_step": nbytes,
+                   "l2": f"inputs {nbytes / 1e9:.2f} GB > 129 MB L2; no flush between steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "whole step (schedule upload, own-page decode, tree kernel, merge)",
+                     "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback", "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None},
+        "cpu_baseline": cpu, "gpu_launches": 4 * K, "clocks": clk,
+    }
+
+
+def run_prefill(args, world, rank, local):
+    """Paged append-prefill (pkd_plan_prefill / pkd_prefill_run) on the
+    prefill workload: K back-to-back launches timed with CUDA events."""
+    import torch
+
+    import paged_kv_decode_28_gb300 as pkd
+    from paged_kv_decode_28_gb300 import _build
+    from paged_kv_decode_28_gb300 import workloads as wl
+
+    _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    b = wl.make_config_prefill(device=dev, batch=args.batch)
+    idx = torch.from_numpy(b.kv_page_indices).to(dev)
+    plan = pkd.Plan(b.batch, b.num_qo_heads, b.num_kv_heads, device=dev)
+    plan.plan_prefill(b.qo_indptr, b.kv_indptr, idx, b.kv_last_page_len, b.page_size, causal=True)
+    out = torch.empty_like(b.q)
+    lse = torch.empty(b.q.shape[0], b.num_qo_heads, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        plan.prefill(b.q, b.k_cache, b.v_cache, sm_scale=b.sm_scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert plan.check_device_errors() == 0
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        e0.record(stream)
+        for _ in range(K):
+            plan.prefill(b.q, b.k_cache, b.v_cache, sm_scale=b.sm_scale, out=out, lse=lse)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    clk = clocks.summary()
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+    assert plan.check_device_errors() == 0
+    flops = prefill_flops(b)
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    peak, peak_kind = measured_tensor_peak()
+    e = b.k_cache.element_size()
+    nbytes = (int(np.asarray(b.kv_lens, np.int64).sum()) * b.num_kv_heads * b.head_dim * 2 * e
+              + 2 * b.q.numel() * b.q.element_size() + lse.numel() * 4)
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        from oracle import attention as orc
+
+        T = b.q.shape[0]
+        rows = [(t, h) for t in range(0, T, max(1, T // 16)) for h in (0, b.num_qo_heads - 1)]
+        bc = b.to("cpu")
+        t0 = time.perf_counter()
+        orc.paged_prefill(bc.q, bc.qo_indptr, bc.k_cache, bc.v_cache, bc.kv_indptr, bc.kv_page_indices,
+                          bc.kv_last_page_len, causal=True, sm_scale=b.sm_scale, rows=rows)
+        dt = time.perf_counter() - t0
+        frac = len(rows) / (T * b.num_qo_heads)
+        cpu = {"value": round(flops * frac / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{len(rows)} of {T * b.num_qo_heads} (token, qo head) rows, flops scaled by that "
+               f"fraction (python fp64 oracle, {dt:.2f} s)"}
+    return {
+        "metric": "paged append-prefill attention (pkd_prefill_run): achieved TFLOP/s",
+        "value": round(world * achieved, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) values, seeded lengths and page placement)",
+        "config": {"workload": b.name, "batch": b.batch, "query_tokens": int(b.q.shape[0]),
+                   "num_qo_heads": b.num_qo_heads, "num_kv_heads": b.num_kv_heads, "page_size": b.page_size,
+                   "causal": True, "flops_per_step": flops, "bytes_per_step": nbytes,
+                   "l2": f"inputs {nbytes / 1e9:.2f} GB > 129 MB L2; no flush between steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "pkd prefix_kernel (work-list mode)", "achieved": round(achieved, 2),
+                     "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, burst)"
+                     if peak_kind == "measured" else "fallback", "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "hbm_gbs": round(nbytes / (ms_step * 1e-3) / 1e9, 1)},
+        "cpu_baseline": cpu, "gpu_launches": K, "clocks": clk,
+    }
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_init(args)
-    if args.op == "append":
-        line = run_append(args, world, rank, local)
+    if args.op in ("append", "tree", "prefill"):
+        line = {"append": run_append, "tree": run_tree, "prefill": run_prefill}[args.op](args, world, rank, local)
         if rank == 0:
             print(json.dumps(line), flush=True)
         return

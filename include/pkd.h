@@ -68,6 +68,20 @@ typedef enum pkd_dtype {
   PKD_F32 = 3   /* merge_state / merge_states values only */
 } pkd_dtype;
 
+/*
+ * Page layout of a K or V pool (the batch-decode wrapper of the 2026 Guide,
+ * "When to use it", defaults to NHD; the deep dive, "The Code, Annotated",
+ * passes kv_layout="NHD").  Element (page p, slot t, kv head h, dim d) is at
+ *   NHD: p * page_stride_elems + (t * num_kv_heads + h) * 128 + d
+ *   HND: p * page_stride_elems + (h * page_size + t) * 128 + d
+ * HND keeps one head's keys of a page contiguous (page_size * 256 bytes for
+ * 16-bit values).
+ */
+typedef enum pkd_kv_layout {
+  PKD_LAYOUT_NHD = 0,
+  PKD_LAYOUT_HND = 1
+} pkd_kv_layout;
+
 /* Device error bits recorded by the kernels (pkd_check_device_errors). */
 #define PKD_DEVERR_PAGE_INDEX 1u    /* a page index outside [0, num_pages): page 0 was read instead */
 #define PKD_DEVERR_WAIT_TIMEOUT 2u  /* a pipeline wait gave up after ~2 s; outputs are invalid */
@@ -121,6 +135,9 @@ pkd_status pkd_plan_destroy(pkd_plan_t plan);
  *   d_kv_page_indices  device int32 [kv_indptr[batch]]: physical page ids.
  *                      Borrowed: it must hold the same contents at every
  *                      pkd_run / pkd_cascade_decode until the next pkd_plan.
+ *                      Launches read it through this pointer, and a captured
+ *                      graph keeps the pointer of the plan it was captured
+ *                      with: re-plans for such a graph pass the same buffer.
  *   h_kv_last_page_len host int32 [batch]: valid tokens in each request's last
  *                      page, 1..page_size (ignored for a request with no page).
  *   page_size          tokens per page: 1..64, or a multiple of 64.
@@ -149,9 +166,11 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
  * and qo head.
  *   d_q        [batch, num_qo_heads, 128] in the planned q dtype.
  *   d_k_cache, d_v_cache  the K and V pools: page p, slot t, kv head h, dim d at
- *              element p * page_stride_elems + (t * num_kv_heads + h) * 128 + d.
+ *              element p * page_stride_elems + (t * num_kv_heads + h) * 128 + d
+ *              (NHD, the default), or + (h * page_size + t) * 128 + d when the
+ *              plan's layout is PKD_LAYOUT_HND (pkd_plan_set_kv_layout).
  *              page_stride_elems = page_size * num_kv_heads * 128 for separate
- *              pools, 2 * that for one interleaved [pages, 2, P, Hk, D] pool
+ *              pools, 2 * that for one interleaved [pages, 2, page] pool
  *              (then d_v_cache = d_k_cache + page_size * num_kv_heads * 128).
  *   num_pages  pages in each pool; page ids must lie in [0, num_pages).
  *   d_k_scale, d_v_scale  fp32 [num_kv_heads] for an E4M3 cache, else NULL.
@@ -193,6 +212,78 @@ pkd_status pkd_cascade_decode(pkd_plan_t suffix_plan, const int32_t* d_prefix_pa
                               void* stream);
 
 /*
+ * Prefix-tree (multi-level cascade) decode: every request attends the keys of
+ * one node per shared level and then its own pages, the states of all parts
+ * merged per (request, qo head) (2026 Guide, "Cascade attention for shared
+ * prefixes"; README mirror, "Core Features": cascade attention as a
+ * hierarchical KV cache).  Each node's keys are read once per kv head for all
+ * of its requests (a dense [requests * g, 128] x [128, keys] product on the
+ * tensor cores).
+ *
+ * pkd_plan_tree (host, after pkd_plan, which gives the requests' own pages;
+ * not during stream capture) takes num_levels (1..4) shared levels, outermost
+ * first.  For level l with h_num_nodes[l] nodes:
+ *   h_req_indptr[l]        host int32 [nodes + 1]: node n serves requests
+ *                          req_indptr[n] .. req_indptr[n+1]-1; the nodes
+ *                          cover the batch in order (req_indptr[nodes] = batch).
+ *   h_kv_indptr[l]         host int32 [nodes + 1] into the level's page list.
+ *   d_kv_page_indices[l]   device int32 page ids (borrowed until the next plan;
+ *                          a captured graph keeps these pointers, as for pkd_plan).
+ *   h_kv_last_page_len[l]  host int32 [nodes]: 1..page_size (ignored for a
+ *                          node without pages).
+ * It cuts each level into key-range pieces (at most max_prefix_splits over all
+ * levels; a level needs one), writes the work units into the workspace with
+ * one cudaMemcpyAsync on `stream` (waiting first for the previous such upload
+ * of this plan) and fails with PKD_ERR_CAPACITY_EXCEEDED above the workspace's
+ * unit capacity (8 * (max_batch + num_ctas), at least 4096).  f16/bf16 only
+ * (q and K/V of one type), group sizes dividing 128, page sizes dividing 128
+ * or multiples of 64.
+ *
+ * pkd_tree_decode enqueues the schedule upload, the requests' own decode
+ * (every item writes a partial state), the tree kernel (one launch for all
+ * levels) and the merge; arguments as pkd_run.  It fails with PKD_ERR_NO_PLAN
+ * unless pkd_plan_tree followed the last pkd_plan.  The launch shapes follow
+ * the tree's node and tile counts: a graph captured around it stays valid for
+ * re-plans whose trees keep those counts.
+ */
+pkd_status pkd_plan_tree(pkd_plan_t plan, int num_levels, const int32_t* const* h_req_indptr,
+                         const int32_t* const* h_kv_indptr, const int32_t* const* d_kv_page_indices,
+                         const int32_t* const* h_kv_last_page_len, const int32_t* h_num_nodes, void* stream);
+pkd_status pkd_tree_decode(pkd_plan_t plan, const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                           int64_t num_pages, int64_t page_stride_elems, float sm_scale, void* d_out,
+                           float* d_lse, void* stream);
+
+/*
+ * Paged prefill / append attention (README mirror, "Core Features": prefill
+ * and append kernels over a paged KV cache): several query tokens per request.
+ * Request r's query tokens are rows h_qo_indptr[r] .. h_qo_indptr[r+1]-1 of
+ * d_q [T, num_qo_heads, 128]; its keys are all of its pages (kv_len_r keys,
+ * the query tokens' own keys already appended), so its token i sits at
+ * position kv_len_r - q_len_r + i and, with `causal`, attends keys 0 .. that
+ * position (otherwise all keys); q_len_r <= kv_len_r.
+ *
+ * pkd_plan_prefill (host; not during stream capture): page table as for
+ * pkd_plan (h_kv_indptr, d_kv_page_indices borrowed until the next plan,
+ * h_kv_last_page_len), head counts equal to the plan's, f16/bf16 q and K/V of
+ * one type, group sizes dividing 128, page sizes dividing 128 or multiples of
+ * 64.  One unit per 128-row query tile (128 / g tokens x g heads of a kv
+ * head) and kv head; uploads the units like pkd_plan_tree
+ * (PKD_ERR_CAPACITY_EXCEEDED above the unit capacity).
+ *
+ * pkd_prefill_run: d_out [T, num_qo_heads, 128] in q's dtype, d_lse fp32
+ * [T, num_qo_heads] (natural log) or NULL; pools as pkd_run (the plan's
+ * layout).  One kernel on `stream` (ordered after everything before it),
+ * no allocation, no host sync.
+ */
+pkd_status pkd_plan_prefill(pkd_plan_t plan, const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
+                            const int32_t* d_kv_page_indices, const int32_t* h_kv_last_page_len, int batch,
+                            int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int q_dtype,
+                            int kv_dtype, int causal, void* stream);
+pkd_status pkd_prefill_run(pkd_plan_t plan, const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                           int64_t num_pages, int64_t page_stride_elems, float sm_scale, void* d_out,
+                           float* d_lse, void* stream);
+
+/*
  * Append new tokens' keys and values to the paged cache: the write step on
  * either side of each decode step (README mirror, "Core Features": decode,
  * prefill and append kernels over a paged KV cache).  Token i belongs to
@@ -204,7 +295,8 @@ pkd_status pkd_cascade_decode(pkd_plan_t suffix_plan, const int32_t* d_prefix_pa
  *   d_k_new, d_v_new   device [n_tokens, num_kv_heads, 128] in new_dtype (F16 or BF16).
  *   d_batch_indices, d_positions   device int32 [n_tokens].
  *   d_kv_indptr        device int32 [batch + 1]; d_kv_page_indices device int32.
- *   d_k_cache, d_v_cache, num_pages, page_stride_elems   the pools as in pkd_run, kv_dtype.
+ *   d_k_cache, d_v_cache, num_pages, page_stride_elems   the pools as in pkd_run, kv_dtype;
+ *   kv_layout          PKD_LAYOUT_NHD or PKD_LAYOUT_HND (the pools' page layout).
  *   kv_dtype F16/BF16: must equal new_dtype; the values are copied.
  *   kv_dtype E4M3: codes e4m3(x / scale[h]) with the quotient in fp32 (IEEE
  *     division), rounded to nearest even and saturated to +-448;
@@ -219,7 +311,7 @@ pkd_status pkd_append_kv(const void* d_k_new, const void* d_v_new, int new_dtype
                          const int32_t* d_batch_indices, const int32_t* d_positions, int n_tokens,
                          const int32_t* d_kv_indptr, const int32_t* d_kv_page_indices, int batch,
                          int num_kv_heads, int head_dim, int page_size, void* d_k_cache,
-                         void* d_v_cache, int kv_dtype, int64_t num_pages,
+                         void* d_v_cache, int kv_dtype, int kv_layout, int64_t num_pages,
                          int64_t page_stride_elems, const float* d_k_scale,
                          const float* d_v_scale, uint32_t* d_err_word, void* stream);
 
@@ -283,6 +375,14 @@ pkd_status pkd_plan_set_timing_events(pkd_plan_t plan, void* start_event, void* 
 pkd_status pkd_check_device_errors(pkd_plan_t plan, uint32_t* flags_out, void* stream);
 
 /*
+ * Page layout (pkd_kv_layout) of the pools later pkd_run / pkd_cascade_decode
+ * calls of this plan read; PKD_LAYOUT_NHD until set.  PKD_ERR_INVALID_ARG for
+ * another value.  Host-side only; a graph captured around run keeps the
+ * layout it was captured with.
+ */
+pkd_status pkd_plan_set_kv_layout(pkd_plan_t plan, int kv_layout);
+
+/*
  * Test hook for the pipeline's failure path (the pages have no counterpart).
  * With PKD_DEBUG_STALL_PIPELINE set, the decode kernel of later pkd_run calls
  * issues no copies, so every consumer's first pipeline wait runs out after its
@@ -317,13 +417,14 @@ pkd_status pkd_plan_set_debug(pkd_plan_t plan, int flags);
  *     caller.  Each call resets what must start at zero.
  *   - Device error bits (PKD_DEVERR_*) are recorded in the scratch area and are
  *     not reported back; an out-of-range page id is read as page 0.
- * Arguments as pkd_plan and pkd_run (h_* are host arrays, d_* device).
+ * Arguments as pkd_plan and pkd_run (h_* are host arrays, d_* device);
+ * kv_layout is the pools' page layout (pkd_kv_layout).
  */
 #define PKD_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32_t* d_kv_page_indices,
                               const int32_t* h_kv_last_page_len, int batch, int num_qo_heads,
                               int num_kv_heads, int head_dim, int page_size, int q_dtype,
-                              int kv_dtype, const void* d_q, const void* d_k_cache,
+                              int kv_dtype, int kv_layout, const void* d_q, const void* d_k_cache,
                               const void* d_v_cache, int64_t num_pages, int64_t page_stride_elems,
                               const float* d_k_scale, const float* d_v_scale, float sm_scale,
                               void* d_out, float* d_lse, void* stream);

@@ -67,9 +67,14 @@ def lib() -> ctypes.CDLL:
         "pkd_check_device_errors": (i, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
         "pkd_plan_set_timing_events": (i, [_vp, _vp, _vp]),
         "pkd_plan_set_debug": (i, [_vp, i]),
-        "pkd_append_kv": (i, [_vp, _vp, i, _vp, _vp, i, _vp, _vp, i, i, i, i, _vp, _vp, i, i64, i64, _vp, _vp, _vp,
-                              _vp]),
-        "pkd_decode_noalloc": (i, [_i32p, _vp, _i32p, i, i, i, i, i, i, i, _vp, _vp, _vp, i64, i64, _vp, _vp, f,
+        "pkd_plan_set_kv_layout": (i, [_vp, i]),
+        "pkd_plan_tree": (i, [_vp, i, _vp, _vp, _vp, _vp, _i32p, _vp]),
+        "pkd_tree_decode": (i, [_vp, _vp, _vp, _vp, i64, i64, f, _vp, _vp, _vp]),
+        "pkd_plan_prefill": (i, [_vp, _i32p, _i32p, _vp, _i32p, i, i, i, i, i, i, i, i, _vp]),
+        "pkd_prefill_run": (i, [_vp, _vp, _vp, _vp, i64, i64, f, _vp, _vp, _vp]),
+        "pkd_append_kv": (i, [_vp, _vp, i, _vp, _vp, i, _vp, _vp, i, i, i, i, _vp, _vp, i, i, i64, i64, _vp, _vp,
+                              _vp, _vp]),
+        "pkd_decode_noalloc": (i, [_i32p, _vp, _i32p, i, i, i, i, i, i, i, i, _vp, _vp, _vp, i64, i64, _vp, _vp, f,
                                    _vp, _vp, _vp]),
         "pkd_plan_host": (i, [_i32p, _i32p, i, i, i, i, _i32p, i, _i32p, _i32p, _i32p, _i32p, _i32p]),
     }
@@ -155,20 +160,37 @@ def plan_host(kv_indptr, kv_last_page_len, num_kv_heads: int, page_size: int, nu
     }
 
 
-def _check_pool(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor):
+# page layouts of a pool: NHD pages [page_size, Hk, D], HND pages [Hk, page_size, D]
+_LAYOUT_CODE = {"NHD": 0, "HND": 1}
+
+
+def _check_pool(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, kv_layout: str = "NHD"):
+    """Pool geometry (N, P, Hk, D, page stride): NHD pools are
+    ``[num_pages, page_size, Hk, D]``, HND pools ``[num_pages, Hk, page_size, D]``,
+    each page one contiguous block."""
+    if kv_layout not in _LAYOUT_CODE:
+        raise ValueError("kv_layout must be 'NHD' or 'HND'")
+    hnd = kv_layout == "HND"
     if k_cache.dim() != 4 or v_cache.dim() != 4:
-        raise ValueError("caches must be [num_pages, page_size, num_kv_heads, head_dim]")
+        raise ValueError("caches must be [num_pages, num_kv_heads, page_size, head_dim]" if hnd else
+                         "caches must be [num_pages, page_size, num_kv_heads, head_dim]")
     if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
         raise ValueError("k_cache and v_cache must have one shape and dtype")
-    N, P, Hk, D = k_cache.shape
+    if hnd:
+        N, Hk, P, D = k_cache.shape
+    else:
+        N, P, Hk, D = k_cache.shape
+    inner = P if hnd else Hk
     for c in (k_cache, v_cache):
-        if c.stride(3) != 1 or c.stride(2) != D or c.stride(1) != Hk * D:
-            raise ValueError("each page of the cache must be a contiguous [page_size, Hk, D] block")
-    if k_cache.stride(0) != v_cache.stride(0):
+        # the stride of a dimension of extent 1 is never stepped (torch leaves it arbitrary)
+        want = ((3, 1), (2, D), (1, inner * D))
+        if any(c.shape[d] > 1 and c.stride(d) != s for d, s in want):
+            raise ValueError(f"each page of the cache must be a contiguous {kv_layout} block")
+    if N > 1 and k_cache.stride(0) != v_cache.stride(0):
         raise ValueError("k_cache and v_cache must share one page stride")
     if not q.is_contiguous():
         raise ValueError("q must be contiguous")
-    return N, P, Hk, D, k_cache.stride(0)
+    return N, P, Hk, D, (k_cache.stride(0) if N > 1 else P * Hk * D)
 
 
 class Plan:
@@ -180,7 +202,8 @@ class Plan:
     """
 
     def __init__(self, max_batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int = 128,
-                 max_prefix_splits: int = 0, device=None, num_ctas_: Optional[int] = None):
+                 max_prefix_splits: int = 0, device=None, num_ctas_: Optional[int] = None,
+                 kv_layout: str = "NHD"):
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         with torch.cuda.device(self.device):
             self.num_ctas = num_ctas() if num_ctas_ is None else int(num_ctas_)
@@ -192,6 +215,10 @@ class Plan:
         _check(lib().pkd_plan_create(ctypes.byref(h), max_batch, num_qo_heads, num_kv_heads, head_dim,
                                      self.num_ctas, max_prefix_splits, _ptr(self.workspace), nbytes))
         self._h = h
+        if kv_layout not in _LAYOUT_CODE:
+            raise ValueError("kv_layout must be 'NHD' or 'HND'")
+        self.kv_layout = kv_layout
+        _check(lib().pkd_plan_set_kv_layout(h, _LAYOUT_CODE[kv_layout]))
         self._indices = None
         self.batch = 0
         self.q_dtype = self.kv_dtype = None
@@ -217,6 +244,11 @@ class Plan:
         self.batch, self.page_size = B, page_size
         self.q_dtype, self.kv_dtype = q_dtype, kv_dtype
 
+    def _check_geometry(self, P, Hk, D):
+        if Hk != self.num_kv_heads or D != self.head_dim or (self.q_dtype is not None and P != self.page_size):
+            raise ValueError(f"pool geometry (page_size {P}, kv heads {Hk}, head_dim {D}) does not match the plan "
+                             f"({self.kv_layout} pages)")
+
     def _outputs(self, q, out, lse, B):
         if out is None:
             out = torch.empty_like(q)
@@ -228,7 +260,8 @@ class Plan:
             sm_scale: Optional[float] = None, k_scale: Optional[torch.Tensor] = None,
             v_scale: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-        N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache)
+        N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache, self.kv_layout)
+        self._check_geometry(P, Hk, D)
         if self.q_dtype is not None and q.shape != (self.batch, self.num_qo_heads, self.head_dim):
             raise ValueError(f"q must be [{self.batch}, {self.num_qo_heads}, {self.head_dim}]")
         out, lse = self._outputs(q, out, lse, q.shape[0])
@@ -239,7 +272,8 @@ class Plan:
     def cascade_decode(self, prefix_page_indices: torch.Tensor, prefix_last_page_len: int, q: torch.Tensor,
                        k_cache: torch.Tensor, v_cache: torch.Tensor, *, sm_scale: Optional[float] = None,
                        k_scale=None, v_scale=None, out=None, lse=None, stream=None):
-        N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache)
+        N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache, self.kv_layout)
+        self._check_geometry(P, Hk, D)
         if prefix_page_indices.dtype != torch.int32 or prefix_page_indices.device.type != "cuda":
             raise ValueError("prefix_page_indices must be an int32 CUDA tensor")
         out, lse = self._outputs(q, out, lse, self.batch)
@@ -247,6 +281,84 @@ class Plan:
                                         int(prefix_last_page_len), _ptr(q), _ptr(k_cache), _ptr(v_cache), N,
                                         stride, _ptr(k_scale), _ptr(v_scale), float(sm_scale or 0.0),
                                         _ptr(out), _ptr(lse), _stream(stream)))
+        return out, lse
+
+    def plan_tree(self, levels, stream=None):
+        """Shared levels of a prefix tree, outermost first, after ``plan`` (which
+        gave each request's own pages).  Each level is ``(req_indptr, kv_indptr,
+        kv_page_indices, kv_last_page_len)`` over its nodes: node n serves
+        requests ``req_indptr[n] .. req_indptr[n+1]-1`` (the nodes cover the
+        batch in order) and owns pages ``kv_page_indices[kv_indptr[n] ..]``
+        (an int32 CUDA tensor; the others are host arrays)."""
+        L = len(levels)
+        if not 1 <= L <= 4:
+            raise ValueError("1 to 4 shared levels")
+        keep = []
+        ri, ki, pi, lp = (ctypes.c_void_p * L)(), (ctypes.c_void_p * L)(), (ctypes.c_void_p * L)(), \
+            (ctypes.c_void_p * L)()
+        nn = np.zeros(L, np.int32)
+        for l, (req_indptr, kv_indptr, idx, last) in enumerate(levels):
+            r = _host_i32(req_indptr)
+            k = _host_i32(kv_indptr)
+            la = _host_i32(last)
+            if len(la) == 0:
+                la = np.zeros(1, np.int32)
+            if idx.dtype != torch.int32 or idx.device.type != "cuda" or not idx.is_contiguous():
+                raise ValueError("each level's kv_page_indices must be a contiguous int32 CUDA tensor")
+            nn[l] = len(r) - 1
+            keep += [r, k, la, idx]
+            ri[l] = r.ctypes.data
+            ki[l] = k.ctypes.data
+            lp[l] = la.ctypes.data
+            pi[l] = idx.data_ptr() if idx.numel() else None
+        _check(lib().pkd_plan_tree(self._h, L, ri, ki, pi, lp, _as_i32p(nn), _stream(stream)))
+        self._tree = keep  # the page-index tensors are borrowed until the next plan
+
+    def tree_decode(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, *,
+                    sm_scale: Optional[float] = None, out=None, lse=None, stream=None):
+        """Decode over the prefix tree of ``plan_tree`` and the requests' own pages."""
+        N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache, self.kv_layout)
+        self._check_geometry(P, Hk, D)
+        out, lse = self._outputs(q, out, lse, self.batch)
+        _check(lib().pkd_tree_decode(self._h, _ptr(q), _ptr(k_cache), _ptr(v_cache), N, stride,
+                                     float(sm_scale or 0.0), _ptr(out), _ptr(lse), _stream(stream)))
+        return out, lse
+
+    def plan_prefill(self, qo_indptr, kv_indptr, kv_page_indices: torch.Tensor, kv_last_page_len, page_size: int,
+                     *, causal: bool = True, q_dtype=torch.bfloat16, kv_dtype=None, stream=None):
+        """Prefill / append: request r's query tokens are rows ``qo_indptr[r] ..
+        qo_indptr[r+1]-1`` of q; its keys are all of its pages (its new tokens'
+        keys included); ``causal`` aligns the mask to the end of the sequence."""
+        qo = _host_i32(qo_indptr)
+        ip = _host_i32(kv_indptr)
+        last = _host_i32(kv_last_page_len)
+        B = len(ip) - 1
+        if len(qo) != B + 1:
+            raise ValueError("qo_indptr and kv_indptr must describe the same requests")
+        if kv_page_indices.dtype != torch.int32 or kv_page_indices.device.type != "cuda":
+            raise ValueError("kv_page_indices must be an int32 CUDA tensor")
+        kv_dtype = q_dtype if kv_dtype is None else kv_dtype
+        last_arg = last if len(last) else np.zeros(1, np.int32)
+        _check(lib().pkd_plan_prefill(self._h, _as_i32p(qo), _as_i32p(ip), _ptr(kv_page_indices),
+                                      _as_i32p(last_arg), B, self.num_qo_heads, self.num_kv_heads, self.head_dim,
+                                      page_size, _DTYPE_CODE[q_dtype], _DTYPE_CODE[kv_dtype], int(bool(causal)),
+                                      _stream(stream)))
+        self._pf_indices = kv_page_indices
+        self.pf_tokens, self.pf_page_size = int(qo[-1]), page_size
+
+    def prefill(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, *,
+                sm_scale: Optional[float] = None, out=None, lse=None, stream=None):
+        """q ``[T, Hq, 128]`` -> ``(out [T, Hq, 128], lse [T, Hq])`` for the last ``plan_prefill``."""
+        N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache, self.kv_layout)
+        if Hk != self.num_kv_heads or D != self.head_dim or P != getattr(self, "pf_page_size", P):
+            raise ValueError("pool geometry does not match the prefill plan")
+        if q.shape != (getattr(self, "pf_tokens", q.shape[0]), self.num_qo_heads, self.head_dim):
+            raise ValueError("q must be [T, num_qo_heads, head_dim] for the planned T")
+        out = torch.empty_like(q) if out is None else out
+        lse = torch.empty((q.shape[0], self.num_qo_heads), dtype=torch.float32, device=q.device) if lse is None \
+            else lse
+        _check(lib().pkd_prefill_run(self._h, _ptr(q), _ptr(k_cache), _ptr(v_cache), N, stride,
+                                     float(sm_scale or 0.0), _ptr(out), _ptr(lse), _stream(stream)))
         return out, lse
 
     def set_timing_events(self, start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
@@ -271,13 +383,14 @@ class Plan:
 def append_kv(k_new: torch.Tensor, v_new: torch.Tensor, batch_indices: torch.Tensor, positions: torch.Tensor,
               kv_indptr: torch.Tensor, kv_page_indices: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
               *, k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
-              err: Optional[torch.Tensor] = None, stream=None):
+              err: Optional[torch.Tensor] = None, kv_layout: str = "NHD", stream=None):
     """Write new tokens' rows into the paged cache (in place): k_new / v_new
     ``[n, Hk, 128]``; token i goes to request ``batch_indices[i]`` at position
     ``positions[i]``.  ``kv_indptr`` / ``kv_page_indices`` are int32 CUDA tensors;
     e4m3 pools quantise with ``k_scale`` / ``v_scale``.  ``err`` (int32 CUDA
-    tensor of one element) collects PKD_DEVERR_PAGE_INDEX for skipped tokens."""
-    N, P, Hk, D, stride = _check_pool(k_new, k_cache, v_cache)
+    tensor of one element) collects PKD_DEVERR_PAGE_INDEX for skipped tokens.
+    ``kv_layout`` is the pools' page layout ('NHD' or 'HND')."""
+    N, P, Hk, D, stride = _check_pool(k_new, k_cache, v_cache, kv_layout)
     if k_new.dim() != 3 or k_new.shape != v_new.shape or k_new.shape[1:] != (Hk, D):
         raise ValueError(f"k_new / v_new must be [n, {Hk}, {D}]")
     if not (k_new.is_contiguous() and v_new.is_contiguous()):
@@ -293,7 +406,8 @@ def append_kv(k_new: torch.Tensor, v_new: torch.Tensor, batch_indices: torch.Ten
         raise ValueError("k_new / v_new must be f16 or bf16")
     _check(lib().pkd_append_kv(_ptr(k_new), _ptr(v_new), _DTYPE_CODE[k_new.dtype], _ptr(batch_indices),
                                _ptr(positions), n, _ptr(kv_indptr), _ptr(kv_page_indices), kv_indptr.numel() - 1,
-                               Hk, D, P, _ptr(k_cache), _ptr(v_cache), _DTYPE_CODE[k_cache.dtype], N, stride,
+                               Hk, D, P, _ptr(k_cache), _ptr(v_cache), _DTYPE_CODE[k_cache.dtype],
+                               _LAYOUT_CODE[kv_layout], N, stride,
                                _ptr(k_scale), _ptr(v_scale), _ptr(err), _stream(stream)))
 
 
@@ -350,18 +464,20 @@ def merge_states(v: torch.Tensor, s: torch.Tensor, *, stream=None):
 
 def decode_noalloc(kv_indptr, kv_page_indices: torch.Tensor, kv_last_page_len, page_size: int, q: torch.Tensor,
                    k_cache: torch.Tensor, v_cache: torch.Tensor, out: torch.Tensor, lse: torch.Tensor, *,
-                   sm_scale: Optional[float] = None, k_scale=None, v_scale=None, stream=None):
+                   sm_scale: Optional[float] = None, k_scale=None, v_scale=None, kv_layout: str = "NHD",
+                   stream=None):
     """Plan + run in one call that allocates nothing on the device: the library's
     built-in scratch area replaces the workspace (see ``pkd_decode_noalloc``).
     ``out`` and ``lse`` are caller-provided; the first call on a device must
-    come before any stream capture on it."""
-    N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache)
+    come before any stream capture on it.  ``kv_layout``: 'NHD' or 'HND' pools."""
+    N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache, kv_layout)
     indptr = _host_i32(kv_indptr)
     last = _host_i32(kv_last_page_len)
     B = len(indptr) - 1
     last_arg = last if len(last) else np.zeros(1, np.int32)
     _check(lib().pkd_decode_noalloc(_as_i32p(indptr), _ptr(kv_page_indices), _as_i32p(last_arg), B, q.shape[1],
-                                    Hk, D, page_size, _DTYPE_CODE[q.dtype], _DTYPE_CODE[k_cache.dtype], _ptr(q),
+                                    Hk, D, page_size, _DTYPE_CODE[q.dtype], _DTYPE_CODE[k_cache.dtype],
+                                    _LAYOUT_CODE[kv_layout], _ptr(q),
                                     _ptr(k_cache), _ptr(v_cache), N, stride, _ptr(k_scale), _ptr(v_scale),
                                     float(sm_scale or 0.0), _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse

@@ -10,10 +10,11 @@
 // e4m3(x / scale[h]), the quotient in fp32 (IEEE division), rounded to nearest
 // even and saturated to +-448.
 //
-// One warp per token: the token's rows of all kv heads are contiguous both in
-// the new-token tensor ([Hk, 128]) and in its page slot ((slot * Hk + h) * 128),
-// so after one page lookup the warp moves Hk * 256 bytes of K and of V with
-// independent 16-byte loads and stores (8-byte stores of codes for e4m3).  A
+// One warp per token: after one page lookup the warp moves the token's Hk * 256
+// bytes of K and of V with independent 16-byte loads and stores (8-byte stores
+// of codes for e4m3).  The token's rows are contiguous in the new-token tensor
+// ([Hk, 128]); in an NHD page they are contiguous too ((slot * Hk + h) * 128),
+// in an HND page ([Hk, P, 128]) head h's row sits at (h * P + slot) * 128.  A
 // decode step's append is a few hundred KB, bound by launch latency; a bulk
 // append is bound by HBM.
 #include <cuda_bf16.h>
@@ -26,6 +27,7 @@ namespace pkd {
 namespace {
 
 constexpr int kAppendWarps = 8;
+static_assert(kHeadDim == 128, "a head row is sixteen 16-byte chunks of 16-bit source");
 
 // Two fp32 -> two E4M3 codes (round to nearest even, saturating): the low
 // byte holds `lo`.
@@ -61,7 +63,7 @@ __device__ __forceinline__ uint2 quantise8(const float (&f)[8], float scale) {
 }
 
 template <int NT, int KVT>
-__global__ void __launch_bounds__(kAppendWarps * 32) append_kv_kernel(const AppendParams p) {
+__global__ void __launch_bounds__(kAppendWarps * 32, KVT == kE4M3 ? 4 : 6) append_kv_kernel(const AppendParams p) {
   const int lane = threadIdx.x & 31;
   const int Hk = p.num_kv_heads;
   const int chunks = Hk * (kHeadDim / 8);  // 16-byte chunks of 16-bit source per token
@@ -84,32 +86,40 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kv_kernel(const Appe
       continue;
     }
     const int slot = pos - (pos / p.page_size) * p.page_size;
-    // element offsets of the token's first row (head 0)
+    // element offsets of the token's first row (head 0) and of 16-byte chunk c
+    // of its 16-bit source (eight elements, never straddling two heads)
     const size_t src = static_cast<size_t>(i) * Hk * kHeadDim;
-    const size_t dst = static_cast<size_t>(page) * p.page_stride + static_cast<size_t>(slot) * Hk * kHeadDim;
+    const size_t dst = static_cast<size_t>(page) * p.page_stride +
+                       static_cast<size_t>(slot) * (p.kv_hnd ? kHeadDim : Hk * kHeadDim);
+    // within the page: head h's row starts h * P * 128 (HND) or h * 128 (NHD)
+    // elements after head 0's (a page holds under 2^31 elements)
+    const uint32_t head_step = p.kv_hnd ? static_cast<uint32_t>(p.page_size) * kHeadDim : kHeadDim;
+    auto chunk_off = [&](int c) -> uint32_t { return (c >> 4) * head_step + (c & 15) * 8; };
     const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_new) + src);
     const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v_new) + src);
     if constexpr (KVT == kE4M3) {
-      uint2* kd = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.k_cache) + dst);
-      uint2* vd = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.v_cache) + dst);
+      uint8_t* kd = static_cast<uint8_t*>(p.k_cache) + dst;
+      uint8_t* vd = static_cast<uint8_t*>(p.v_cache) + dst;
 #pragma unroll 4
       for (int c = lane; c < chunks; c += 32) {
-        const int h = c / (kHeadDim / 8);  // eight elements never straddle two heads
+        const int h = c >> 4;
         const uint4 ku = __ldg(ks + c), vu = __ldg(vs + c);
         float kf[8], vf[8];
         unpack8<NT>(ku, kf);
         unpack8<NT>(vu, vf);
-        kd[c] = quantise8(kf, __ldg(p.k_scale + h));
-        vd[c] = quantise8(vf, __ldg(p.v_scale + h));
+        const uint32_t o = chunk_off(c);
+        *reinterpret_cast<uint2*>(kd + o) = quantise8(kf, __ldg(p.k_scale + h));
+        *reinterpret_cast<uint2*>(vd + o) = quantise8(vf, __ldg(p.v_scale + h));
       }
     } else {
-      uint4* kd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.k_cache) + dst);
-      uint4* vd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.v_cache) + dst);
+      uint16_t* kd = static_cast<uint16_t*>(p.k_cache) + dst;
+      uint16_t* vd = static_cast<uint16_t*>(p.v_cache) + dst;
 #pragma unroll 4
       for (int c = lane; c < chunks; c += 32) {
         const uint4 ku = __ldg(ks + c), vu = __ldg(vs + c);
-        kd[c] = ku;
-        vd[c] = vu;
+        const uint32_t o = chunk_off(c);
+        *reinterpret_cast<uint4*>(kd + o) = ku;
+        *reinterpret_cast<uint4*>(vd + o) = vu;
       }
     }
   }

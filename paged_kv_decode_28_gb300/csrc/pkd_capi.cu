@@ -37,10 +37,10 @@ pkd_status cuda_fail(cudaError_t e, const char* what) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-  int group = 0, max_rows = 0, max_items = 0;
+  int group = 0, max_rows = 0, max_items = 0, max_work = 0;
   size_t cta_begin = 0, items = 0, merge_rows = 0, row_begin = 0, row_count = 0, kv_len = 0,
          page_begin = 0, empty_rows = 0, row_done = 0, meta_end = 0, part_o = 0, part_lse = 0, pre_o = 0,
-         pre_lse = 0, total = 0;
+         pre_lse = 0, work = 0, total = 0;
 };
 
 bool make_layout(int max_batch, int hq, int hk, int d, int G, int max_splits, Layout* L) {
@@ -77,6 +77,11 @@ bool make_layout(int max_batch, int hq, int hk, int d, int G, int max_splits, La
   off += align256(4ull * max_splits * max_batch * hq * d);
   L->pre_lse = off;
   off += align256(4ull * max_splits * max_batch * hq);
+  // units of the tile-attention kernel's work-list mode (prefix-tree levels,
+  // prefill), uploaded by pkd_plan_tree / pkd_plan_prefill
+  L->max_work = 8 * (max_batch + G) > 4096 ? 8 * (max_batch + G) : 4096;
+  L->work = off;
+  off += align256(sizeof(pkd::TileWork) * static_cast<size_t>(L->max_work));
   L->total = off;
   return true;
 }
@@ -97,20 +102,23 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 int elem_bytes(int dt) { return dt == PKD_E4M3 ? 1 : (dt == PKD_F32 ? 4 : 2); }
 
-// Tensor map over a pool [num_pages, tok_extent, Hk, 128] with a page stride in
-// elements; boxes of 64 (16-bit) or 128 (fp8) head-dim elements x 1 head x
-// box_tok keys x 1 page, 128-byte swizzled.
+// Tensor map over a pool of NHD pages [num_pages, tok_extent, Hk, 128] (dims
+// dim, head, key, page) or HND pages [num_pages, Hk, tok_extent, 128] (dims
+// dim, key, head, page), with a page stride in elements; boxes of 64 (16-bit)
+// or 128 (fp8) head-dim elements x box_tok keys of one head of one page,
+// 128-byte swizzled.  Either way a box lands in shared memory as box_tok rows.
 pkd_status encode_kv_map(CUtensorMap* m, const void* base, int kv_dtype, int hk, int64_t tok_extent,
-                         int64_t num_pages, int64_t page_stride_elems, int box_tok) {
+                         int64_t num_pages, int64_t page_stride_elems, int box_tok, bool hnd) {
   auto enc = get_encode();
   if (!enc) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const int e = elem_bytes(kv_dtype);
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(pkd::kHeadDim), static_cast<cuuint64_t>(hk),
-                        static_cast<cuuint64_t>(tok_extent), static_cast<cuuint64_t>(num_pages)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(pkd::kHeadDim) * e,
-                           static_cast<cuuint64_t>(hk) * pkd::kHeadDim * e,
-                           static_cast<cuuint64_t>(page_stride_elems) * e};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(e == 1 ? 128 : 64), 1u, static_cast<cuuint32_t>(box_tok), 1u};
+  const cuuint64_t row = static_cast<cuuint64_t>(pkd::kHeadDim) * e;
+  const cuuint64_t n1 = hnd ? static_cast<cuuint64_t>(tok_extent) : static_cast<cuuint64_t>(hk);
+  const cuuint64_t n2 = hnd ? static_cast<cuuint64_t>(hk) : static_cast<cuuint64_t>(tok_extent);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(pkd::kHeadDim), n1, n2, static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {row, n1 * row, static_cast<cuuint64_t>(page_stride_elems) * e};
+  const cuuint32_t bx = static_cast<cuuint32_t>(e == 1 ? 128 : 64), bt = static_cast<cuuint32_t>(box_tok);
+  cuuint32_t box[4] = {bx, hnd ? bt : 1u, hnd ? 1u : bt, 1u};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUtensorMapDataType dt = kv_dtype == PKD_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                            : kv_dtype == PKD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -172,7 +180,23 @@ struct pkd_plan_s {
   cudaStream_t side = nullptr;
   cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
   int debug_flags = 0;  // PKD_DEBUG_* test hooks
+  int kv_layout = PKD_LAYOUT_NHD;  // page layout of the pools given to run / cascade_decode
+  int plan_gen = 0;                // successful pkd_plan calls
+  // work-list units of the last pkd_plan_tree (kind 1) or pkd_plan_prefill
+  // (kind 2), uploaded into the workspace's work region from a pinned buffer;
+  // work_done fires after each upload and the next one waits for it
+  int work_kind = 0, n_work = 0, work_gen = 0;
+  pkd::TileWork* work_staging = nullptr;
+  cudaEvent_t work_done = nullptr;
+  const int32_t* level_pages[pkd::kMaxTreeLevels] = {};
+  int tree_pieces = 0;
+  int pf_tokens = 0, pf_page_size = 0, pf_dtype = 0;
   ~pkd_plan_s() {
+    if (work_done) {
+      cudaEventSynchronize(work_done);
+      cudaEventDestroy(work_done);
+    }
+    if (work_staging) cudaFreeHost(work_staging);
     if (side) {
       cudaStreamSynchronize(side);
       cudaStreamDestroy(side);
@@ -367,6 +391,7 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
     if (e != cudaSuccess) return cuda_fail(e, "plan upload");
   }
   plan->planned = true;
+  ++plan->plan_gen;
   plan->batch = batch;
   plan->page_size = page_size;
   plan->q_dtype = q_dtype;
@@ -450,6 +475,7 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
   p.empty_rows = reinterpret_cast<const int*>(ws + L.empty_rows);
   p.header = reinterpret_cast<const pkd::WsHeader*>(ws);
   p.debug_stall = (plan->debug_flags & PKD_DEBUG_STALL_PIPELINE) ? 1 : 0;
+  p.kv_hnd = plan->kv_layout == PKD_LAYOUT_HND ? 1 : 0;
   // under stream capture the records become event-record nodes that fire on every replay
   unsigned rec_flags = cudaEventRecordDefault;
   {
@@ -484,10 +510,10 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
       return fail(PKD_ERR_INVALID_ARG, "page_stride_elems must cover a page and be a 16-byte multiple");
     CUtensorMap tmk, tmv;
     pkd_status s = encode_kv_map(&tmk, d_k_cache, plan->kv_dtype, plan->hk, tok_extent, num_pages,
-                                 page_stride_elems, box_tok);
+                                 page_stride_elems, box_tok, p.kv_hnd != 0);
     if (s != PKD_OK) return s;
     s = encode_kv_map(&tmv, d_v_cache, plan->kv_dtype, plan->hk, tok_extent, num_pages, page_stride_elems,
-                      box_tok);
+                      box_tok, p.kv_hnd != 0);
     if (s != PKD_OK) return s;
     if (plan->ev_start && !plan->use_pinned) {
       cudaError_t er = cudaEventRecordWithFlags(plan->ev_start, st, rec_flags);
@@ -509,7 +535,8 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
     }
   }
   if (cascade && cascade->n_pre_splits > 0) {
-    cudaError_t e = pkd::launch_prefix(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->kv_dtype, st);
+    cudaError_t e = pkd::launch_prefix(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->kv_dtype, st,
+                                       true);
     if (e != cudaSuccess) return cuda_fail(e, "prefix kernel launch");
   }
   // plain decode merges its split rows and writes its empty rows in the decode
@@ -551,6 +578,100 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
     if (e != cudaSuccess) return cuda_fail(e, "side branch join");
   }
   return PKD_OK;
+}
+
+// Upload work-list units into the workspace's work region: copied into the
+// plan's pinned buffer (after the previous upload from it has finished), then
+// one cudaMemcpyAsync on `st`.
+pkd_status upload_work(pkd_plan_t plan, const std::vector<pkd::TileWork>& w, cudaStream_t st) {
+  if (static_cast<int64_t>(w.size()) > plan->lay.max_work)
+    return fail(PKD_ERR_CAPACITY_EXCEEDED, "%zu work units above the workspace's %d", w.size(), plan->lay.max_work);
+  cudaError_t e = cudaSuccess;
+  if (!plan->work_staging) {
+    e = cudaHostAlloc(reinterpret_cast<void**>(&plan->work_staging),
+                      sizeof(pkd::TileWork) * static_cast<size_t>(plan->lay.max_work), cudaHostAllocDefault);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&plan->work_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "work staging buffer");
+  } else {
+    e = cudaEventSynchronize(plan->work_done);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize(work staging)");
+  }
+  if (!w.empty()) {
+    memcpy(plan->work_staging, w.data(), sizeof(pkd::TileWork) * w.size());
+    e = cudaMemcpyAsync(plan->ws + plan->lay.work, plan->work_staging, sizeof(pkd::TileWork) * w.size(),
+                        cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "work upload");
+  }
+  e = cudaEventRecord(plan->work_done, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(work upload)");
+  plan->n_work = static_cast<int>(w.size());
+  return PKD_OK;
+}
+
+// Tensor map over query rows viewed as [rows][Hk][g][128] (rows = requests or
+// tokens): a box of 128 / g rows x g heads of one kv head is one 128-row tile.
+pkd_status encode_q_tile_map(CUtensorMap* m, const void* q, int q_dtype, int g, int hk, int64_t rows) {
+  auto enc = get_encode();
+  if (!enc) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t qdims[4] = {static_cast<cuuint64_t>(pkd::kHeadDim), static_cast<cuuint64_t>(g),
+                         static_cast<cuuint64_t>(hk), static_cast<cuuint64_t>(rows)};
+  cuuint64_t qstr[3] = {static_cast<cuuint64_t>(pkd::kHeadDim) * 2, static_cast<cuuint64_t>(g) * pkd::kHeadDim * 2,
+                        static_cast<cuuint64_t>(hk) * g * pkd::kHeadDim * 2};
+  cuuint32_t qbox[4] = {64u, static_cast<cuuint32_t>(g), 1u, static_cast<cuuint32_t>(128 / g)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, q_dtype == PKD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                   const_cast<void*>(q), qdims, qstr, qbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed (CUresult %d)", (int)r);
+  return PKD_OK;
+}
+
+// Checks shared by the tile-attention entry points: 16-bit K/V of q's type, a
+// group size dividing 128, a page size the kernel's boxes cover.
+pkd_status check_tile_geometry(int q_dtype, int kv_dtype, int g, int P, const char* what) {
+  if (kv_dtype == PKD_E4M3 || !(kv_dtype == PKD_F16 || kv_dtype == PKD_BF16) || q_dtype != kv_dtype)
+    return fail(PKD_ERR_UNSUPPORTED, "%s is built for f16/bf16 q and K/V of one type", what);
+  if (pkd::kHeadDim % g != 0) return fail(PKD_ERR_UNSUPPORTED, "%s needs a group size dividing 128", what);
+  if (P <= pkd::kChunkKeys ? (128 % P != 0) : (P % pkd::kChunkKeys != 0))
+    return fail(PKD_ERR_UNSUPPORTED, "%s needs a page size dividing 128 or a multiple of 64", what);
+  return PKD_OK;
+}
+
+// Validate a pool and encode its K/V maps for the tile-attention kernel.
+pkd_status tile_kv_maps(pkd_plan_t plan, int kv_dtype, int P, const void* d_k, const void* d_v, int64_t num_pages,
+                        int64_t page_stride_elems, CUtensorMap* tmk, CUtensorMap* tmv) {
+  if (!d_k || !d_v || !aligned16(d_k) || !aligned16(d_v))
+    return fail(PKD_ERR_INVALID_ARG, "k/v cache must be non-NULL and 16-byte aligned");
+  if (num_pages <= 0 || num_pages > INT32_MAX) return fail(PKD_ERR_INVALID_ARG, "num_pages out of range");
+  if ((page_stride_elems * elem_bytes(kv_dtype)) % 16 != 0 ||
+      page_stride_elems < static_cast<int64_t>(P) * plan->hk * plan->d)
+    return fail(PKD_ERR_INVALID_ARG, "page_stride_elems must cover a page and be a 16-byte multiple");
+  const int box_tok = P <= pkd::kChunkKeys ? P : pkd::kChunkKeys;
+  const bool hnd = plan->kv_layout == PKD_LAYOUT_HND;
+  pkd_status s = encode_kv_map(tmk, d_k, kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok, hnd);
+  if (s != PKD_OK) return s;
+  return encode_kv_map(tmv, d_v, kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok, hnd);
+}
+
+// Parameters common to the work-list launches.
+pkd::PrefixParams tile_params(pkd_plan_t plan, int P, int64_t num_pages, float sm_scale) {
+  pkd::PrefixParams pp{};
+  const float scale = (sm_scale > 0.f) ? sm_scale : 1.0f / std::sqrt(static_cast<float>(plan->d));
+  pp.num_kv_heads = plan->hk;
+  pp.group = plan->hq / plan->hk;
+  pp.num_pages = static_cast<int>(num_pages);
+  pp.page_size = P;
+  pp.box_tok = P <= pkd::kChunkKeys ? P : pkd::kChunkKeys;
+  pp.cluster = 1;
+  pp.n_splits = 1;
+  pp.m_groups = 1;
+  pp.scale_log2 = scale * 1.4426950408889634f;
+  pp.err = reinterpret_cast<unsigned*>(plan->ws);
+  pp.kv_hnd = plan->kv_layout == PKD_LAYOUT_HND ? 1 : 0;
+  pp.work = reinterpret_cast<const pkd::TileWork*>(plan->ws + plan->lay.work);
+  pp.n_work = plan->n_work;
+  for (int l = 0; l < pkd::kMaxTreeLevels; ++l) pp.level_pages[l] = plan->level_pages[l];
+  return pp;
 }
 
 }  // namespace
@@ -642,9 +763,11 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed (CUresult %d)", (int)r);
     const int box_tok = P <= pkd::kChunkKeys ? P : pkd::kChunkKeys;
-    pkd_status s = encode_kv_map(&tmk, d_k_cache, plan->kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok);
+    const bool hnd = plan->kv_layout == PKD_LAYOUT_HND;
+    pkd_status s = encode_kv_map(&tmk, d_k_cache, plan->kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok,
+                                 hnd);
     if (s != PKD_OK) return s;
-    s = encode_kv_map(&tmv, d_v_cache, plan->kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok);
+    s = encode_kv_map(&tmv, d_v_cache, plan->kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok, hnd);
     if (s != PKD_OK) return s;
     const float scale = (sm_scale > 0.f) ? sm_scale : 1.0f / std::sqrt(static_cast<float>(plan->d));
     pkd::PrefixParams pp{};
@@ -666,6 +789,8 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
     pp.pre_o = reinterpret_cast<float*>(plan->ws + plan->lay.pre_o);
     pp.pre_lse = reinterpret_cast<float*>(plan->ws + plan->lay.pre_lse);
     pp.err = reinterpret_cast<unsigned*>(plan->ws);
+    pp.kv_hnd = hnd ? 1 : 0;
+    pp.rows_per_piece = B * plan->hq;
     cm.tmq = tmq;
     cm.tmk = tmk;
     cm.tmv = tmv;
@@ -677,14 +802,230 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
                     sm_scale, d_out, d_lse, stream, nullptr, &cm);
 }
 
+pkd_status pkd_plan_tree(pkd_plan_t plan, int num_levels, const int32_t* const* h_req_indptr,
+                         const int32_t* const* h_kv_indptr, const int32_t* const* d_kv_page_indices,
+                         const int32_t* const* h_kv_last_page_len, const int32_t* h_num_nodes, void* stream) {
+  if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
+  if (!plan->planned) return fail(PKD_ERR_NO_PLAN, "pkd_plan_tree needs the requests' own pages planned first");
+  if (num_levels < 1 || num_levels > pkd::kMaxTreeLevels)
+    return fail(PKD_ERR_UNSUPPORTED, "num_levels %d outside 1..%d", num_levels, pkd::kMaxTreeLevels);
+  if (!h_req_indptr || !h_kv_indptr || !d_kv_page_indices || !h_kv_last_page_len || !h_num_nodes)
+    return fail(PKD_ERR_INVALID_ARG, "NULL level array");
+  if (plan->max_splits < num_levels)
+    return fail(PKD_ERR_CAPACITY_EXCEEDED, "the plan was created with max_prefix_splits %d < %d levels",
+                plan->max_splits, num_levels);
+  const int g = plan->hq / plan->hk;
+  const int P = plan->page_size;
+  pkd_status s = check_tile_geometry(plan->q_dtype, plan->kv_dtype, g, P, "prefix-tree decode");
+  if (s != PKD_OK) return s;
+  const int B = plan->batch;
+  const int per_tile = 128 / g;  // requests per 128-row query tile
+  // validate the levels and count each level's query tiles and key tiles
+  std::vector<int64_t> level_mtiles(num_levels, 0);
+  std::vector<int> level_max_tiles(num_levels, 0);
+  for (int l = 0; l < num_levels; ++l) {
+    const int nn = h_num_nodes[l];
+    const int32_t* ri = h_req_indptr[l];
+    const int32_t* ki = h_kv_indptr[l];
+    const int32_t* lp = h_kv_last_page_len[l];
+    if (nn < 1 || !ri || !ki || (!lp && nn > 0)) return fail(PKD_ERR_INVALID_ARG, "level %d: bad node arrays", l);
+    if (ri[0] != 0 || ri[nn] != B) return fail(PKD_ERR_INVALID_ARG, "level %d: nodes must cover requests 0..%d", l, B);
+    if (ki[0] != 0) return fail(PKD_ERR_INVALID_ARG, "level %d: kv_indptr[0] must be 0", l);
+    if (ki[nn] > 0 && !d_kv_page_indices[l]) return fail(PKD_ERR_INVALID_ARG, "level %d: page indices NULL", l);
+    for (int n = 0; n < nn; ++n) {
+      if (ri[n + 1] < ri[n] || ki[n + 1] < ki[n])
+        return fail(PKD_ERR_INVALID_ARG, "level %d node %d: decreasing indptr", l, n);
+      const int pages = ki[n + 1] - ki[n];
+      if (pages > 0 && (lp[n] < 1 || lp[n] > P))
+        return fail(PKD_ERR_INVALID_ARG, "level %d node %d: last_page_len %d outside 1..%d", l, n, lp[n], P);
+      const int64_t len = pages > 0 ? static_cast<int64_t>(pages - 1) * P + lp[n] : 0;
+      if (len > INT32_MAX - 128) return fail(PKD_ERR_INVALID_ARG, "level %d node %d: too many keys", l, n);
+      level_mtiles[l] += (ri[n + 1] - ri[n] + per_tile - 1) / per_tile;
+      const int tiles = static_cast<int>((len + 127) / 128);
+      level_max_tiles[l] = tiles > level_max_tiles[l] ? tiles : level_max_tiles[l];
+    }
+  }
+  // key-range pieces per level: enough CTAs (kv heads x query tiles x pieces)
+  // to cover the SMs, within the plan's piece budget (each level keeps one)
+  const int sms = plan->G / pkd::kCtasPerSm;
+  std::vector<int> S(num_levels, 1);
+  int budget = plan->max_splits;
+  for (int l = 0; l < num_levels; ++l) {
+    const int64_t ctas1 = static_cast<int64_t>(plan->hk) * (level_mtiles[l] > 0 ? level_mtiles[l] : 1);
+    int want = static_cast<int>((sms + ctas1 - 1) / ctas1);
+    want = want < 1 ? 1 : want;
+    want = want > level_max_tiles[l] ? (level_max_tiles[l] > 0 ? level_max_tiles[l] : 1) : want;
+    const int cap = budget - (num_levels - 1 - l);
+    S[l] = want > cap ? cap : want;
+    budget -= S[l];
+  }
+  std::vector<pkd::TileWork> w;
+  int piece = 0;
+  for (int l = 0; l < num_levels; ++l) {
+    const int32_t* ri = h_req_indptr[l];
+    const int32_t* ki = h_kv_indptr[l];
+    const int32_t* lp = h_kv_last_page_len[l];
+    for (int n = 0; n < h_num_nodes[l]; ++n) {
+      const int pages = ki[n + 1] - ki[n];
+      const int len = pages > 0 ? (pages - 1) * P + lp[n] : 0;
+      const int tiles = (len + 127) / 128;
+      const int tps = tiles > 0 ? (tiles + S[l] - 1) / S[l] : 0;
+      for (int r0 = ri[n]; r0 < ri[n + 1]; r0 += per_tile) {
+        for (int sp = 0; sp < S[l]; ++sp) {
+          pkd::TileWork t{};
+          t.q0 = r0;
+          t.q_end = ri[n + 1];
+          t.page_begin = ki[n];
+          t.kv_len = len;
+          t.t0 = sp * tps < tiles ? sp * tps : tiles;
+          t.t1 = (sp + 1) * tps < tiles ? (sp + 1) * tps : tiles;
+          t.piece = piece + sp;  // every piece of every request is written (empty ranges as empty states)
+          t.level = l;
+          t.diag = pkd::kNoCausal;
+          w.push_back(t);
+        }
+      }
+    }
+    piece += S[l];
+  }
+  s = upload_work(plan, w, static_cast<cudaStream_t>(stream));
+  if (s != PKD_OK) return s;
+  for (int l = 0; l < pkd::kMaxTreeLevels; ++l) plan->level_pages[l] = l < num_levels ? d_kv_page_indices[l] : nullptr;
+  plan->tree_pieces = piece;
+  plan->work_kind = 1;
+  plan->work_gen = plan->plan_gen;
+  return PKD_OK;
+}
+
+pkd_status pkd_tree_decode(pkd_plan_t plan, const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                           int64_t num_pages, int64_t page_stride_elems, float sm_scale, void* d_out,
+                           float* d_lse, void* stream) {
+  if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
+  if (!plan->planned || plan->work_kind != 1 || plan->work_gen != plan->plan_gen)
+    return fail(PKD_ERR_NO_PLAN, "tree_decode needs pkd_plan_tree after the last pkd_plan");
+  const int B = plan->batch;
+  const int P = plan->page_size;
+  const int g = plan->hq / plan->hk;
+  CascadeMerge cm{};
+  if (B > 0 && plan->n_work > 0) {
+    if (!d_q || !aligned16(d_q)) return fail(PKD_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
+    pkd_status s = encode_q_tile_map(&cm.tmq, d_q, plan->q_dtype, g, plan->hk, B);
+    if (s != PKD_OK) return s;
+    s = tile_kv_maps(plan, plan->kv_dtype, P, d_k_cache, d_v_cache, num_pages, page_stride_elems, &cm.tmk, &cm.tmv);
+    if (s != PKD_OK) return s;
+    cm.pp = tile_params(plan, P, num_pages, sm_scale);
+    cm.pp.batch = B;
+    cm.pp.rows_per_piece = B * plan->hq;
+    cm.pp.pre_o = reinterpret_cast<float*>(plan->ws + plan->lay.pre_o);
+    cm.pp.pre_lse = reinterpret_cast<float*>(plan->ws + plan->lay.pre_lse);
+    cm.n_pre_splits = plan->tree_pieces;
+  }
+  return run_common(plan, d_q, d_k_cache, d_v_cache, num_pages, page_stride_elems, P, nullptr, nullptr, sm_scale,
+                    d_out, d_lse, stream, nullptr, &cm);
+}
+
+pkd_status pkd_plan_prefill(pkd_plan_t plan, const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
+                            const int32_t* d_kv_page_indices, const int32_t* h_kv_last_page_len, int batch,
+                            int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int q_dtype,
+                            int kv_dtype, int causal, void* stream) {
+  if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
+  if (num_qo_heads != plan->hq || num_kv_heads != plan->hk || head_dim != plan->d)
+    return fail(PKD_ERR_INVALID_ARG, "head counts / head_dim differ from the plan's");
+  if (batch < 0) return fail(PKD_ERR_INVALID_ARG, "batch must be >= 0");
+  if (page_size < 1) return fail(PKD_ERR_INVALID_ARG, "page_size must be >= 1");
+  const int g = plan->hq / plan->hk;
+  pkd_status s = check_tile_geometry(q_dtype, kv_dtype, g, page_size, "prefill");
+  if (s != PKD_OK) return s;
+  if (!h_qo_indptr || !h_kv_indptr || (batch > 0 && !h_kv_last_page_len))
+    return fail(PKD_ERR_INVALID_ARG, "NULL host array");
+  if (h_qo_indptr[0] != 0 || h_kv_indptr[0] != 0) return fail(PKD_ERR_INVALID_ARG, "indptr[0] must be 0");
+  if (h_kv_indptr[batch] > 0 && !d_kv_page_indices) return fail(PKD_ERR_INVALID_ARG, "d_kv_page_indices is NULL");
+  const int per_tile = 128 / g;  // query tokens per 128-row tile
+  std::vector<pkd::TileWork> w;
+  for (int r = 0; r < batch; ++r) {
+    const int q_len = h_qo_indptr[r + 1] - h_qo_indptr[r];
+    const int pages = h_kv_indptr[r + 1] - h_kv_indptr[r];
+    if (q_len < 0 || pages < 0) return fail(PKD_ERR_INVALID_ARG, "request %d: decreasing indptr", r);
+    if (pages > 0 && (h_kv_last_page_len[r] < 1 || h_kv_last_page_len[r] > page_size))
+      return fail(PKD_ERR_INVALID_ARG, "request %d: last_page_len %d outside 1..%d", r, h_kv_last_page_len[r],
+                  page_size);
+    const int64_t len64 = pages > 0 ? static_cast<int64_t>(pages - 1) * page_size + h_kv_last_page_len[r] : 0;
+    if (len64 > INT32_MAX - 128) return fail(PKD_ERR_INVALID_ARG, "request %d: too many keys", r);
+    const int kv_len = static_cast<int>(len64);
+    if (q_len > kv_len)
+      return fail(PKD_ERR_INVALID_ARG, "request %d: %d query tokens but %d keys (the new tokens' keys are in "
+                  "the cache)", r, q_len, kv_len);
+    const int q0 = h_qo_indptr[r], q_end = h_qo_indptr[r + 1];
+    const int diag = kv_len - q_len - q0;  // token q sits at position q + diag
+    for (int a = q0; a < q_end; a += per_tile) {
+      const int last_tok = (a + per_tile < q_end ? a + per_tile : q_end) - 1;
+      const int keys = causal ? last_tok + diag + 1 : kv_len;  // keys the tile's last row sees
+      pkd::TileWork t{};
+      t.q0 = a;
+      t.q_end = q_end;
+      t.page_begin = h_kv_indptr[r];
+      t.kv_len = kv_len;
+      t.t0 = 0;
+      t.t1 = (keys + 127) / 128;
+      t.piece = -1;
+      t.level = 0;
+      t.diag = causal ? diag : pkd::kNoCausal;
+      w.push_back(t);
+    }
+  }
+  if (!plan->err_word_zeroed) {  // a plan used for prefill only: the first plan clears the error word
+    cudaError_t ez = cudaMemsetAsync(plan->ws, 0, 4, static_cast<cudaStream_t>(stream));
+    if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync(error word)");
+    plan->err_word_zeroed = true;
+  }
+  s = upload_work(plan, w, static_cast<cudaStream_t>(stream));
+  if (s != PKD_OK) return s;
+  plan->level_pages[0] = d_kv_page_indices;
+  for (int l = 1; l < pkd::kMaxTreeLevels; ++l) plan->level_pages[l] = nullptr;
+  plan->pf_tokens = h_qo_indptr[batch];
+  plan->pf_page_size = page_size;
+  plan->pf_dtype = kv_dtype;
+  plan->work_kind = 2;
+  return PKD_OK;
+}
+
+pkd_status pkd_prefill_run(pkd_plan_t plan, const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                           int64_t num_pages, int64_t page_stride_elems, float sm_scale, void* d_out,
+                           float* d_lse, void* stream) {
+  if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->work_kind != 2) return fail(PKD_ERR_NO_PLAN, "prefill_run before a successful pkd_plan_prefill");
+  if (plan->n_work == 0) return PKD_OK;
+  if (!d_q || !d_out || !aligned16(d_q) || !aligned16(d_out))
+    return fail(PKD_ERR_INVALID_ARG, "q/out must be non-NULL and 16-byte aligned");
+  const int P = plan->pf_page_size;
+  const int g = plan->hq / plan->hk;
+  CUtensorMap tmq, tmk, tmv;
+  pkd_status s = encode_q_tile_map(&tmq, d_q, plan->pf_dtype, g, plan->hk, plan->pf_tokens);
+  if (s != PKD_OK) return s;
+  s = tile_kv_maps(plan, plan->pf_dtype, P, d_k_cache, d_v_cache, num_pages, page_stride_elems, &tmk, &tmv);
+  if (s != PKD_OK) return s;
+  pkd::PrefixParams pp = tile_params(plan, P, num_pages, sm_scale);
+  pp.batch = plan->pf_tokens;
+  pp.out = d_out;
+  pp.lse = d_lse;
+  pp.out_dtype = plan->pf_dtype;
+  // not programmatic: the kernel reads K/V that the previous launch on the
+  // stream (an append) may have written
+  cudaError_t e = pkd::launch_prefix(tmq, tmk, tmv, pp, plan->pf_dtype, static_cast<cudaStream_t>(stream), false);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
+  return PKD_OK;
+}
+
 pkd_status pkd_append_kv(const void* d_k_new, const void* d_v_new, int new_dtype,
                          const int32_t* d_batch_indices, const int32_t* d_positions, int n_tokens,
                          const int32_t* d_kv_indptr, const int32_t* d_kv_page_indices, int batch,
                          int num_kv_heads, int head_dim, int page_size, void* d_k_cache,
-                         void* d_v_cache, int kv_dtype, int64_t num_pages,
+                         void* d_v_cache, int kv_dtype, int kv_layout, int64_t num_pages,
                          int64_t page_stride_elems, const float* d_k_scale,
                          const float* d_v_scale, uint32_t* d_err_word, void* stream) {
   if (n_tokens < 0 || batch < 0 || num_kv_heads <= 0) return fail(PKD_ERR_INVALID_ARG, "bad n_tokens/batch/heads");
+  if (kv_layout != PKD_LAYOUT_NHD && kv_layout != PKD_LAYOUT_HND)
+    return fail(PKD_ERR_INVALID_ARG, "kv_layout %d (PKD_LAYOUT_NHD or PKD_LAYOUT_HND)", kv_layout);
   if (head_dim != pkd::kHeadDim) return fail(PKD_ERR_UNSUPPORTED, "head_dim %d (128 only)", head_dim);
   if (page_size < 1) return fail(PKD_ERR_INVALID_ARG, "page_size must be >= 1");
   const bool fp8 = kv_dtype == PKD_E4M3;
@@ -721,6 +1062,7 @@ pkd_status pkd_append_kv(const void* d_k_new, const void* d_v_new, int new_dtype
   p.num_kv_heads = num_kv_heads;
   p.page_size = page_size;
   p.num_pages = static_cast<int>(num_pages);
+  p.kv_hnd = kv_layout == PKD_LAYOUT_HND ? 1 : 0;
   cudaError_t e = pkd::launch_append_kv(p, new_dtype, kv_dtype, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
   return PKD_OK;
@@ -802,6 +1144,14 @@ pkd_status pkd_plan_set_timing_events(pkd_plan_t plan, void* start_event, void* 
   }
   plan->ev_start = static_cast<cudaEvent_t>(start_event);
   plan->ev_stop = static_cast<cudaEvent_t>(stop_event);
+  return PKD_OK;
+}
+
+pkd_status pkd_plan_set_kv_layout(pkd_plan_t plan, int kv_layout) {
+  if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
+  if (kv_layout != PKD_LAYOUT_NHD && kv_layout != PKD_LAYOUT_HND)
+    return fail(PKD_ERR_INVALID_ARG, "kv_layout %d (PKD_LAYOUT_NHD or PKD_LAYOUT_HND)", kv_layout);
+  plan->kv_layout = kv_layout;
   return PKD_OK;
 }
 

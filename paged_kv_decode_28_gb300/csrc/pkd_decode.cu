@@ -110,12 +110,27 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, int b, int qo, boo
   }
 }
 
+// Scale the output accumulators (both the hi rows 0..7 and the lo rows 8..15)
+// by the row's rescale factor; skipped when no row of the warp changed its max.
+__device__ __forceinline__ void rescale_o(float (&o)[16][4], float alpha) {
+  if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[nt][i] *= alpha;
+    }
+  }
+}
+
 // Online-softmax update for one 16-key sub-tile given the raw scores.
 // x[] = (n-tile 0: keys 2t, 2t+1; n-tile 1: keys 8+2t, 9+2t) of head row gid.
+// P leaves as hi/lo 16-bit pairs: the P V product puts hi in A rows 0..7
+// (the group's heads) and lo in the otherwise empty rows 8..15, so the
+// accumulator rows gid and gid + 8 sum to P V with P carried to ~2^-17.
 template <bool PBF16>
 __device__ __forceinline__ void softmax_step(const float (&sacc)[2][4], int t, int valid, float sl2,
                                              float& m_run, float& l_run, float (&o)[16][4],
-                                             uint32_t& pa0, uint32_t& pa2) {
+                                             uint32_t& pa0, uint32_t& pa2, uint32_t& pl0, uint32_t& pl2) {
   float x[4];
   x[0] = (2 * t < valid) ? sacc[0][0] * sl2 : -INFINITY;
   x[1] = (2 * t + 1 < valid) ? sacc[0][1] * sl2 : -INFINITY;
@@ -132,13 +147,9 @@ __device__ __forceinline__ void softmax_step(const float (&sacc)[2][4], int t, i
   for (int i = 0; i < 4; ++i) pr[i] = ptx::ex2(x[i] - m_new);
   l_run = l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
   m_run = m_new;
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    o[nt][0] *= alpha;
-    o[nt][1] *= alpha;
-  }
-  pa0 = ptx::pack2<PBF16>(pr[0], pr[1]);
-  pa2 = ptx::pack2<PBF16>(pr[2], pr[3]);
+  rescale_o(o, alpha);
+  ptx::split2<PBF16>(pr[0], pr[1], pa0, pl0);
+  ptx::split2<PBF16>(pr[2], pr[3], pa2, pl2);
 }
 
 // 16 keys of a 16-bit stage: S = Q K^T (ldmatrix), softmax, O += P V (ldmatrix.trans).
@@ -166,8 +177,8 @@ __device__ __forceinline__ void tile16_16bit(uint32_t kb, uint32_t vb, int w, in
       ptx::mma_16816<BF>(sacc[nt], qa0[2 * kp + 1], 0u, qa2[2 * kp + 1], 0u, r2, r3);
     }
   }
-  uint32_t pa0, pa2;
-  softmax_step<BF>(sacc, t, valid, sl2, m_run, l_run, o, pa0, pa2);
+  uint32_t pa0, pa2, pl0, pl2;
+  softmax_step<BF>(sacc, t, valid, sl2, m_run, l_run, o, pa0, pa2, pl0, pl2);
   // values of keys past the valid count are zeroed (their P is 0, but the
   // shared-memory rows may hold stale or non-finite bits)
   const uint32_t mlo = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
@@ -183,8 +194,8 @@ __device__ __forceinline__ void tile16_16bit(uint32_t kb, uint32_t vb, int w, in
     r1 &= mhi;
     r2 &= mlo;
     r3 &= mhi;
-    ptx::mma_16816<BF>(o[2 * dp], pa0, 0u, pa2, 0u, r0, r1);
-    ptx::mma_16816<BF>(o[2 * dp + 1], pa0, 0u, pa2, 0u, r2, r3);
+    ptx::mma_16816<BF>(o[2 * dp], pa0, pl0, pa2, pl2, r0, r1);
+    ptx::mma_16816<BF>(o[2 * dp + 1], pa0, pl0, pa2, pl2, r2, r3);
   }
 }
 
@@ -246,9 +257,10 @@ __device__ __forceinline__ void qk_e4m3(uint32_t kb, int w, int lane, const uint
 }
 
 // O += P V for 16 keys whose values are f16 in a [2][16][128 B] buffer; keys
-// past `valid` contribute zero whatever the buffer holds.
+// past `valid` contribute zero whatever the buffer holds.  P as hi/lo pairs
+// (A rows 0..7 and 8..15).
 __device__ __forceinline__ void pv_f16buf(uint32_t v16, int lane, int valid, uint32_t pa0, uint32_t pa2,
-                                          float (&o)[16][4]) {
+                                          uint32_t pl0, uint32_t pl2, float (&o)[16][4]) {
   const int t = lane & 3;
   const uint32_t mlo = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
   const uint32_t mhi = (2 * t + 8 < valid ? 0x0000ffffu : 0u) | (2 * t + 9 < valid ? 0xffff0000u : 0u);
@@ -263,8 +275,8 @@ __device__ __forceinline__ void pv_f16buf(uint32_t v16, int lane, int valid, uin
     r1 &= mhi;
     r2 &= mlo;
     r3 &= mhi;
-    ptx::mma_16816<false>(o[2 * dp], pa0, 0u, pa2, 0u, r0, r1);
-    ptx::mma_16816<false>(o[2 * dp + 1], pa0, 0u, pa2, 0u, r2, r3);
+    ptx::mma_16816<false>(o[2 * dp], pa0, pl0, pa2, pl2, r0, r1);
+    ptx::mma_16816<false>(o[2 * dp + 1], pa0, pl0, pa2, pl2, r2, r3);
   }
 }
 
@@ -276,10 +288,10 @@ __device__ __forceinline__ void tile16_e4m3(uint32_t kb, uint32_t vb, uint32_t v
   convert_v16(vb, v16, w, lane);
   float sacc[2][4];
   qk_e4m3(kb, w, lane, qa0, qa2, sacc);
-  uint32_t pa0, pa2;
-  softmax_step<false>(sacc, lane & 3, valid, sl2, m_run, l_run, o, pa0, pa2);
+  uint32_t pa0, pa2, pl0, pl2;
+  softmax_step<false>(sacc, lane & 3, valid, sl2, m_run, l_run, o, pa0, pa2, pl0, pl2);
   __syncwarp();  // the f16 value rows are written by other lanes of this warp
-  pv_f16buf(v16, lane, valid, pa0, pa2, o);
+  pv_f16buf(v16, lane, valid, pa0, pa2, pl0, pl2, o);
   __syncwarp();  // the buffer is rewritten by the next tile
 }
 
@@ -316,17 +328,23 @@ __device__ __forceinline__ void tile32_e4m3(uint32_t kbA, uint32_t vbA, int vali
   for (int i = 0; i < 8; ++i) pr[i] = ptx::ex2(x[i] - m_new);
   l_run = l_run * alpha + (((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7])));
   m_run = m_new;
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    o[nt][0] *= alpha;
-    o[nt][1] *= alpha;
+  rescale_o(o, alpha);
+  {
+    uint32_t h0, h1, l0, l1;
+    ptx::split2<false>(pr[0], pr[1], h0, l0);
+    ptx::split2<false>(pr[2], pr[3], h1, l1);
+    __syncwarp();  // the f16 value rows are written by other lanes of this warp
+    pv_f16buf(v16, lane, validA, h0, h1, l0, l1, o);
   }
-  __syncwarp();  // the f16 value rows are written by other lanes of this warp
-  pv_f16buf(v16, lane, validA, ptx::pack2<false>(pr[0], pr[1]), ptx::pack2<false>(pr[2], pr[3]), o);
   __syncwarp();  // every lane has read A's rows
   convert_v16(vbB, v16, w, lane);
-  __syncwarp();
-  pv_f16buf(v16, lane, validB, ptx::pack2<false>(pr[4], pr[5]), ptx::pack2<false>(pr[6], pr[7]), o);
+  {
+    uint32_t h0, h1, l0, l1;
+    ptx::split2<false>(pr[4], pr[5], h0, l0);
+    ptx::split2<false>(pr[6], pr[7], h1, l1);
+    __syncwarp();
+    pv_f16buf(v16, lane, validB, h0, h1, l0, l1, o);
+  }
   __syncwarp();  // the buffer is rewritten by the next step
 }
 
@@ -492,19 +510,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         __syncwarp();
         const uint32_t kdst = base + s * C::kStageBytes;
         const uint32_t vdst = kdst + C::kTensorBytes;
+        // tensor-map coordinates (dim, head, key, page) for NHD pages, (dim, key, head, page) for HND
+        const int c1 = p.kv_hnd ? tok_off : h, c2 = p.kv_hnd ? h : tok_off;
 #pragma unroll 1
         for (int j = lane; j < npg; j += 32) {
           const int pid = (j < 32) ? pid0 : pid1;
           const uint32_t off = static_cast<uint32_t>(j) * box_bytes;
           if constexpr (C::kRowBytes == 256) {
             constexpr uint32_t kHalf = kChunkKeys * 128u;
-            ptx::tma_load_4d_hint(kdst + off, &tmk, fb, 0, h, tok_off, pid, policy);
-            ptx::tma_load_4d_hint(kdst + kHalf + off, &tmk, fb, 64, h, tok_off, pid, policy);
-            ptx::tma_load_4d_hint(vdst + off, &tmv, fb, 0, h, tok_off, pid, policy);
-            ptx::tma_load_4d_hint(vdst + kHalf + off, &tmv, fb, 64, h, tok_off, pid, policy);
+            ptx::tma_load_4d_hint(kdst + off, &tmk, fb, 0, c1, c2, pid, policy);
+            ptx::tma_load_4d_hint(kdst + kHalf + off, &tmk, fb, 64, c1, c2, pid, policy);
+            ptx::tma_load_4d_hint(vdst + off, &tmv, fb, 0, c1, c2, pid, policy);
+            ptx::tma_load_4d_hint(vdst + kHalf + off, &tmv, fb, 64, c1, c2, pid, policy);
           } else {
-            ptx::tma_load_4d_hint(kdst + off, &tmk, fb, 0, h, tok_off, pid, policy);
-            ptx::tma_load_4d_hint(vdst + off, &tmv, fb, 0, h, tok_off, pid, policy);
+            ptx::tma_load_4d_hint(kdst + off, &tmk, fb, 0, c1, c2, pid, policy);
+            ptx::tma_load_4d_hint(vdst + off, &tmv, fb, 0, c1, c2, pid, policy);
           }
         }
         if (++s == C::kStages) {
@@ -609,6 +629,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 
     // ---- combine the four warps' states and write
+    // the lo rows (P's low parts) join the hi rows
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      o[nt][0] += o[nt][2];
+      o[nt][1] += o[nt][3];
+    }
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     ptx::named_bar_sync(1, kConsumerWarps * 32);

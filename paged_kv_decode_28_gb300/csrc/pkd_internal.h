@@ -69,6 +69,7 @@ struct DecodeParams {
   const int* empty_rows;      // [header->n_empty_rows]
   const WsHeader* header;
   int debug_stall;            // test hook: the producer issues nothing (waits run out)
+  int kv_hnd;                 // pages are [Hk, P, D] (HND) instead of [P, Hk, D] (NHD)
 };
 
 struct MergeParams {
@@ -88,6 +89,26 @@ struct MergeParams {
   int group;
   int all_rows;               // cascade: every row of the batch
 };
+
+constexpr int kMaxTreeLevels = 4;  // shared levels of a prefix tree
+constexpr int kNoCausal = 0x7fffffff;
+
+// One unit of the tile-attention kernel's work-list mode (prefix-tree levels,
+// prefill): the 128-row query tile of one kv head whose first row-token is q0
+// (rows r = (q - q0) * g + j for query token / request q and group head j),
+// against 128-key tiles [t0, t1) of one page list.
+struct TileWork {
+  int q0;          // first query token (prefill) or request (tree) of the tile
+  int q_end;       // tokens / requests at or past q_end are not this unit's
+  int page_begin;  // the list is pages[level][page_begin ..]
+  int kv_len;      // keys in the list
+  int t0, t1;      // key tiles of this unit
+  int piece;       // output piece (fp32 partial state), or -1: final out / lse
+  int level;       // page array
+  int diag;        // causal: token q sees keys 0 .. q + diag; kNoCausal: all keys
+  int pad[3];
+};
+static_assert(sizeof(TileWork) == 48, "three 16-byte loads");
 
 // Shared-prefix (cascade level 0) attention on the tensor cores.
 struct PrefixParams {
@@ -111,6 +132,16 @@ struct PrefixParams {
   const float* k_scale;
   const float* v_scale;
   unsigned* err;
+  int kv_hnd;               // pages are [Hk, P, D] (HND) instead of [P, Hk, D] (NHD)
+  // work-list mode (cluster 1): CTA x takes kv head x / n_work of unit
+  // work[x % n_work]; pieces are pre_o[piece][row][D] with rows_per_piece rows
+  const TileWork* work;
+  int n_work;
+  int rows_per_piece;       // query rows (tokens or requests times Hq) per piece
+  const int* level_pages[kMaxTreeLevels];
+  void* out;                // final-output units: [rows, Hq, D] in out_dtype
+  float* lse;               //   and lse [rows, Hq] (natural log) or nullptr
+  int out_dtype;
 };
 
 // Writing new tokens' K/V rows into the paged cache (pkd_append.cu).
@@ -121,7 +152,7 @@ struct AppendParams {
   const int* positions;       // [n_tokens]
   const int* kv_indptr;       // [batch + 1] (device)
   const int* page_indices;    // [kv_indptr[batch]]
-  void* k_cache;              // pool [num_pages, P, Hk, D] with a page stride
+  void* k_cache;              // pool [num_pages, P, Hk, D] (NHD) or [num_pages, Hk, P, D] (HND), page stride
   void* v_cache;
   const float* k_scale;       // e4m3 pools: [Hk]
   const float* v_scale;
@@ -132,6 +163,7 @@ struct AppendParams {
   int num_kv_heads;
   int page_size;
   int num_pages;
+  int kv_hnd;                 // HND pages
 };
 
 // Launchers (defined in the .cu files; return a cudaError_t).
@@ -147,7 +179,7 @@ cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, 
 cudaError_t launch_merge_states(const void* v, const float* s, int64_t n, int k, int heads, int dim,
                                 int dtype, void* vo, float* so, cudaStream_t stream);
 cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                          const PrefixParams& p, int kv_dtype, cudaStream_t stream);
+                          const PrefixParams& p, int kv_dtype, cudaStream_t stream, bool pdl);
 int decode_smem_bytes(int kv_dtype);
 int prefix_smem_bytes();
 int prefix_max_active_clusters(int cluster);  // 0 if the query fails

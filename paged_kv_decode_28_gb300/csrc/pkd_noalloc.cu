@@ -136,17 +136,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// dims (dim, head, key, page) for NHD pages, (dim, key, head, page) for HND;
+// a box is box_tok rows of one head of one page either way
 pkd_status kv_map(CUtensorMap* m, const void* base, int kv_dtype, int hk, int64_t tok_extent,
-                  int64_t num_pages, int64_t page_stride_elems, int box_tok) {
+                  int64_t num_pages, int64_t page_stride_elems, int box_tok, bool hnd) {
   auto enc = encode_fn();
   if (!enc) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const int e = kv_dtype == PKD_E4M3 ? 1 : 2;
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(pkd::kHeadDim), static_cast<cuuint64_t>(hk),
-                        static_cast<cuuint64_t>(tok_extent), static_cast<cuuint64_t>(num_pages)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(pkd::kHeadDim) * e,
-                           static_cast<cuuint64_t>(hk) * pkd::kHeadDim * e,
-                           static_cast<cuuint64_t>(page_stride_elems) * e};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(e == 1 ? 128 : 64), 1u, static_cast<cuuint32_t>(box_tok), 1u};
+  const cuuint64_t row = static_cast<cuuint64_t>(pkd::kHeadDim) * e;
+  const cuuint64_t n1 = hnd ? static_cast<cuuint64_t>(tok_extent) : static_cast<cuuint64_t>(hk);
+  const cuuint64_t n2 = hnd ? static_cast<cuuint64_t>(hk) : static_cast<cuuint64_t>(tok_extent);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(pkd::kHeadDim), n1, n2, static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {row, n1 * row, static_cast<cuuint64_t>(page_stride_elems) * e};
+  const cuuint32_t bx = static_cast<cuuint32_t>(e == 1 ? 128 : 64), bt = static_cast<cuuint32_t>(box_tok);
+  cuuint32_t box[4] = {bx, hnd ? bt : 1u, hnd ? 1u : bt, 1u};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUtensorMapDataType dt = kv_dtype == PKD_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                            : kv_dtype == PKD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -166,7 +169,7 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 extern "C" pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32_t* d_kv_page_indices,
                                          const int32_t* h_kv_last_page_len, int batch, int num_qo_heads,
                                          int num_kv_heads, int head_dim, int page_size, int q_dtype,
-                                         int kv_dtype, const void* d_q, const void* d_k_cache,
+                                         int kv_dtype, int kv_layout, const void* d_q, const void* d_k_cache,
                                          const void* d_v_cache, int64_t num_pages, int64_t page_stride_elems,
                                          const float* d_k_scale, const float* d_v_scale, float sm_scale,
                                          void* d_out, float* d_lse, void* stream) {
@@ -192,6 +195,8 @@ extern "C" pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32
     return fail(PKD_ERR_INVALID_ARG, "k_scale/v_scale apply to an E4M3 cache only");
   if (pkd::chunk_keys_for(page_size) < 0)
     return fail(PKD_ERR_UNSUPPORTED, "page_size must be 1..64 or a multiple of 64 (got %d)", page_size);
+  if (kv_layout != PKD_LAYOUT_NHD && kv_layout != PKD_LAYOUT_HND)
+    return fail(PKD_ERR_INVALID_ARG, "kv_layout %d (PKD_LAYOUT_NHD or PKD_LAYOUT_HND)", kv_layout);
 
   // ---- sizes against the fixed scratch
   int dev = 0;
@@ -264,6 +269,7 @@ extern "C" pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32
   p.kv_len = reinterpret_cast<const int*>(ws + L.kv_len);
   p.page_begin = reinterpret_cast<const int*>(ws + L.page_begin);
   p.page_indices = d_kv_page_indices;
+  p.kv_hnd = kv_layout == PKD_LAYOUT_HND ? 1 : 0;
   p.q = d_q;
   p.out = d_out;
   p.lse = d_lse;
@@ -289,9 +295,11 @@ extern "C" pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32
         page_stride_elems < static_cast<int64_t>(page_size) * num_kv_heads * head_dim)
       return fail(PKD_ERR_INVALID_ARG, "page_stride_elems must cover a page and be a 16-byte multiple");
     CUtensorMap tmk, tmv;
-    s = kv_map(&tmk, d_k_cache, kv_dtype, num_kv_heads, page_size, num_pages, page_stride_elems, box_tok);
+    s = kv_map(&tmk, d_k_cache, kv_dtype, num_kv_heads, page_size, num_pages, page_stride_elems, box_tok,
+               kv_layout == PKD_LAYOUT_HND);
     if (s != PKD_OK) return s;
-    s = kv_map(&tmv, d_v_cache, kv_dtype, num_kv_heads, page_size, num_pages, page_stride_elems, box_tok);
+    s = kv_map(&tmv, d_v_cache, kv_dtype, num_kv_heads, page_size, num_pages, page_stride_elems, box_tok,
+               kv_layout == PKD_LAYOUT_HND);
     if (s != PKD_OK) return s;
     e = pkd::launch_decode(tmk, tmv, p, q_dtype, kv_dtype, G, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");

@@ -24,14 +24,20 @@
 //               freed as soon as its S product is done, a V slot when its P V
 //               product is done, so K loads run ahead of V;
 //   warp 1      allocates 512 TMEM columns and issues the MMAs from one thread:
-//               S = Q K^T into one of two S buffers, then O += P V with P read
-//               from TMEM; tcgen05.commit signals the mbarriers;
+//               S = Q K^T into one of three S buffers (two tiles ahead of the
+//               P V product), then O += P_hi V + P_lo V with both parts of P
+//               read from TMEM; tcgen05.commit signals the mbarriers;
 //   warps 4..7  softmax: thread r owns query row r (TMEM lane r), loads its 128
 //               scores, keeps a running reference max (rescaling O in TMEM only
 //               when the tile max exceeds it by more than 8 in log2 units, which
-//               leaves the result exact), writes P as bf16/f16 into TMEM and
-//               accumulates its row sum in a register.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), P0 [384,448), P1 [448,512).
+//               leaves the result exact), writes P as two bf16/f16 parts
+//               (P_hi = round(P), P_lo = round(P - P_hi), so P reaches the
+//               product to ~2^-17 instead of the 16-bit type's 2^-9 / 2^-11)
+//               into TMEM and accumulates its row sum in a register.
+// TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512).  Tile
+// i uses S (i mod 3): once its scores are in registers, P_hi overwrites its
+// columns [0,64) and P_lo [64,128), so S u is rewritten (for tile i + 3) only
+// after the P V product of tile i is done.
 #include "pkd_internal.h"
 #include "pkd_ptx.cuh"
 
@@ -56,11 +62,10 @@ enum {
   B_KE = B_KF + kStages,     // K empty [kStages]
   B_VF = B_KE + kStages,     // V full  [kStages]
   B_VE = B_VF + kStages,     // V empty [kStages]
-  B_SF = B_VE + kStages,     // S full  [2]
-  B_SFREE = B_SF + 2,        // S read  [2]
-  B_PF = B_SFREE + 2,        // P full  [2]
-  B_OD = B_PF + 2,           // P V done [2]
-  B_DRAIN = B_OD + 2,
+  B_SF = B_VE + kStages,     // S full  [3]
+  B_PF = B_SF + 3,           // P full  [3]
+  B_OD = B_PF + 3,           // P V done [3]
+  B_DRAIN = B_OD + 3,
   kNumBars = B_DRAIN + 1
 };
 constexpr int kTmemSlot = kBars + kNumBars * 8;
@@ -68,7 +73,8 @@ constexpr int kAbort = kTmemSlot + 8;
 constexpr int kTotal = kAbort + 16;
 constexpr int kAlloc = kTotal + 1024;
 
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448, kTmemCols = 512;
+constexpr uint32_t kColO = 384, kTmemCols = 512;
+__device__ __forceinline__ uint32_t col_s(int u) { return static_cast<uint32_t>(u) * 128u; }  // S buffer u
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, unsigned* err, volatile int* abort_flag) {
   if (*abort_flag) return false;
@@ -99,20 +105,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   const int Hq = p.num_kv_heads * G;
-  // blockIdx.x = ((h * n_splits + split) * m_groups + mgroup) * C + rank
   const int C = p.cluster;
   const int rank = static_cast<int>(ptx::cluster_ctarank());
-  const int cl = blockIdx.x / C;
-  const int mgroup = cl % p.m_groups;
-  const int hs = cl / p.m_groups;
-  const int split = hs % p.n_splits;
-  const int h = hs / p.n_splits;
-  const int mt = mgroup * C + rank;  // may pass m_tiles: such a CTA only helps load
   const uint16_t cta_mask = static_cast<uint16_t>((1u << C) - 1u);
-  const int n_tiles_all = (p.prefix_len + kKeys - 1) / kKeys;
-  const int t0 = split * p.tiles_per_split;
-  const int t1 = min(t0 + p.tiles_per_split, n_tiles_all);
-  const int n = max(t1 - t0, 0);
+  // this CTA's unit: kv head h, query row-tokens from b0 (rows past row_end
+  // are not written), keys of `pages` (kv_len of them) in tiles t0 .. t0+n-1,
+  // output piece (or -1: final output), causal offset
+  int h, b0, row_end, kv_len, t0, n, piece, diag;
+  const int* pages;
+  if (p.work != nullptr) {
+    const int wi = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_work));
+    h = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_work));
+    const int4* wp = reinterpret_cast<const int4*>(p.work + wi);
+    const int4 wa = __ldg(wp), wb = __ldg(wp + 1), wc = __ldg(wp + 2);
+    b0 = wa.x;
+    row_end = wa.y;
+    kv_len = wa.w;
+    const int lv = wb.w;
+    pages = (lv == 0 ? p.level_pages[0] : lv == 1 ? p.level_pages[1] : lv == 2 ? p.level_pages[2]
+                                                                                : p.level_pages[3]) + wa.z;
+    t0 = wb.x;
+    n = max(min(wb.y, (kv_len + kKeys - 1) / kKeys) - t0, 0);
+    piece = wb.z;
+    diag = wc.x;
+  } else {
+    // blockIdx.x = ((h * n_splits + split) * m_groups + mgroup) * C + rank
+    const int cl = blockIdx.x / C;
+    const int mgroup = cl % p.m_groups;
+    const int hs = cl / p.m_groups;
+    const int split = hs % p.n_splits;
+    h = hs / p.n_splits;
+    const int mt = mgroup * C + rank;  // may pass m_tiles: such a CTA only helps load
+    b0 = mt * (kRows / G);
+    row_end = p.batch;
+    kv_len = p.prefix_len;
+    pages = p.prefix_pages;
+    const int n_tiles_all = (kv_len + kKeys - 1) / kKeys;
+    t0 = split * p.tiles_per_split;
+    n = max(min(t0 + p.tiles_per_split, n_tiles_all) - t0, 0);
+    piece = split;
+    diag = kNoCausal;
+  }
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(B_Q), 1);
@@ -122,9 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(B_VF + s), 1);
       ptx::mbar_init(bar(B_VE + s), C);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       ptx::mbar_init(bar(B_SF + s), 1);
-      ptx::mbar_init(bar(B_SFREE + s), kRows);
       ptx::mbar_init(bar(B_PF + s), kRows);
       ptx::mbar_init(bar(B_OD + s), 1);
     }
@@ -151,7 +183,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmk);
         ptx::prefetch_tensormap(&tmv);
         ptx::mbar_arrive_expect_tx(bar(B_Q), 2u * kHalf);
-        const int b0 = mt * (kRows / G);
         ptx::tma_load_4d(base + kQ, &tmq, bar(B_Q), 0, 0, h, b0);
         ptx::tma_load_4d(base + kQ + kHalf, &tmq, bar(B_Q), 64, 0, h, b0);
       }
@@ -165,12 +196,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tk[r] = 0;
           if (i >= n) continue;
           const int key0 = (t0 + i) * kKeys;
-          const int boxes = (min(kKeys, p.prefix_len - key0) + box - 1) / box;
+          const int boxes = (min(kKeys, kv_len - key0) + box - 1) / box;
           const int bx = rank + C * (lane + 32 * r);
           if (bx < boxes) {
             const int key = key0 + bx * box;
             const int pi = key / p.page_size;
-            pg[r] = __ldg(p.prefix_pages + pi);  // checked at use, so the load stays in flight
+            pg[r] = __ldg(pages + pi);  // checked at use, so the load stays in flight
             tk[r] = key - pi * p.page_size;
           }
         }
@@ -183,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = i % kStages;
         const uint32_t par = ((i / kStages) & 1) ^ 1;
         const int key0 = (t0 + i) * kKeys;
-        const int boxes = (min(kKeys, p.prefix_len - key0) + box - 1) / box;
+        const int boxes = (min(kKeys, kv_len - key0) + box - 1) / box;
         const uint32_t tile_bytes = static_cast<uint32_t>(boxes) * box * 128u * 2u;  // all CTAs' boxes
         if (!warp_wait(bar(eb + s), par, p.err, abort_flag)) return false;
         if (lane == 0) ptx::mbar_arrive_expect_tx(bar(fb + s), tile_bytes);
@@ -198,8 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               page = 0;
             }
             const uint32_t d = base + ring + s * kStage + static_cast<uint32_t>(bx * box) * 128u;
-            ptx::tma_load_4d_mc(d, map, bar(fb + s), 0, h, tk[r], page, cta_mask);
-            ptx::tma_load_4d_mc(d + kHalf, map, bar(fb + s), 64, h, tk[r], page, cta_mask);
+            // map coordinates (dim, head, key, page) for NHD pages, (dim, key, head, page) for HND
+            const int c1 = p.kv_hnd ? tk[r] : h, c2 = p.kv_hnd ? h : tk[r];
+            ptx::tma_load_4d_mc(d, map, bar(fb + s), 0, c1, c2, page, cta_mask);
+            ptx::tma_load_4d_mc(d + kHalf, map, bar(fb + s), 64, c1, c2, page, cta_mask);
           }
         }
         return true;
@@ -227,28 +260,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = ptx::idesc_f16(BF, true, kRows, kHeadDim);
       bool ok = wait_or_abort(bar(B_Q), 0, p.err, abort_flag);
       auto pv = [&](int t) -> bool {
-        const int u = t & 1;
+        const int u = t % 3;
         const int sv = t % kStages;
-        if (!wait_or_abort(bar(B_PF + u), (t >> 1) & 1, p.err, abort_flag)) return false;
+        if (!wait_or_abort(bar(B_PF + u), (t / 3) & 1, p.err, abort_flag)) return false;
         if (!wait_or_abort(bar(B_VF + sv), (t / kStages) & 1, p.err, abort_flag)) return false;
         ptx::tc_fence_after();
-        const uint32_t pcol = u ? kColP1 : kColP0;
+        const uint32_t pcol = col_s(u);       // P_hi
+        const uint32_t lcol = col_s(u) + 64;  // P_lo
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint64_t bdesc = ptx::smem_desc_sw128(base + kV + sv * kStage + k * 2048, kHalf, 1024);
           ptx::umma_ts(tmem + kColO, tmem + pcol + 8 * k, bdesc, idesc_pv, (t > 0 || k > 0) ? 1u : 0u);
+          ptx::umma_ts(tmem + kColO, tmem + lcol + 8 * k, bdesc, idesc_pv, 1u);
         }
         ptx::tc_commit(bar(B_OD + u));
         if (t + kStages < n) ptx::tc_commit_mc(bar(B_VE + sv), cta_mask);
         return true;
       };
       for (int i = 0; i < n && ok; ++i) {
-        const int u = i & 1;
+        const int u = i % 3;
         const int sk = i % kStages;
         if (!wait_or_abort(bar(B_KF + sk), (i / kStages) & 1, p.err, abort_flag)) break;
-        if (i >= 2 && !wait_or_abort(bar(B_SFREE + u), ((i - 2) >> 1) & 1, p.err, abort_flag)) break;
+        // S u holds P of tile i - 3 until that tile's P V product is done
+        // (issued by this thread in the previous iteration)
+        if (i >= 3 && !wait_or_abort(bar(B_OD + u), ((i - 3) / 3) & 1, p.err, abort_flag)) break;
         ptx::tc_fence_after();
-        const uint32_t scol = u ? kColS1 : kColS0;
+        const uint32_t scol = col_s(u);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
@@ -258,11 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_commit(bar(B_SF + u));
         if (i + kStages < n) ptx::tc_commit_mc(bar(B_KE + sk), cta_mask);
-        if (i >= 1 && !pv(i - 1)) {
+        // the P V product runs two tiles behind S
+        if (i >= 2 && !pv(i - 2)) {
           ok = false;
           break;
         }
       }
+      if (ok && !*abort_flag && n >= 2) ok = pv(n - 2);
       if (ok && !*abort_flag) pv(n - 1);
       // drain: every MMA issued above has finished before TMEM is released
       ptx::tc_commit(bar(B_DRAIN));
@@ -276,33 +315,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    // this thread's query row: token (or request) tok, qo head h * G + jj
+    const int tok = b0 + row / G;
+    const int jj = row - (row / G) * G;
     for (int i = 0; i < n; ++i) {
-      const int u = i & 1;
-      if (!warp_wait(bar(B_SF + u), (i >> 1) & 1, p.err, abort_flag)) {
+      const int u = i % 3;
+      if (!warp_wait(bar(B_SF + u), (i / 3) & 1, p.err, abort_flag)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t scol = tmem + lanes + (u ? kColS1 : kColS0);
+      const uint32_t scol = tmem + lanes + col_s(u);
       uint32_t sr[128];
       ptx::tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       ptx::tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       ptx::tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
       ptx::tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
       ptx::tmem_ld_wait();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(B_SFREE + u));
-      const int nv = min(kKeys, p.prefix_len - (t0 + i) * kKeys);
-      // scale (and, on a ragged last tile, mask), then a tree max: 8 independent chains
-      // max of the raw scores (the scale is positive, so it commutes with max);
-      // keys past the prefix end become -inf
+      const int key0 = (t0 + i) * kKeys;
+      const int nv = min(kKeys, kv_len - key0);
+      // keys this row sees: those before the list's end and, for a causal
+      // unit, at or before the row's position tok + diag (units that mask
+      // start at key 0, so every row of theirs sees key 0 in its first tile)
+      const int vr = diag == kNoCausal ? nv : max(0, min(nv, tok + diag + 1 - key0));
+      // mask, then a tree max of the raw scores (the scale is positive, so it
+      // commutes with max): 8 independent chains
       float m8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
-      if (nv < kKeys) {
+      if (vr < kKeys) {
 #pragma unroll
         for (int c = 0; c < kKeys; ++c)
-          if (c >= nv) sr[c] = __float_as_uint(-INFINITY);
+          if (c >= vr) sr[c] = __float_as_uint(-INFINITY);
       }
 #pragma unroll
       for (int c = 0; c < kKeys; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
@@ -311,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool need = (i > 0) && (mx > m_ref + kRescaleThreshold);
       if (i == 0) m_ref = mx;
       if (__any_sync(0xffffffffu, need)) {
-        if (!warp_wait(bar(B_OD + ((i - 1) & 1)), ((i - 1) >> 1) & 1, p.err, abort_flag)) {
+        if (!warp_wait(bar(B_OD + (i - 1) % 3), ((i - 1) / 3) & 1, p.err, abort_flag)) {
           ok = false;
           break;
         }
@@ -332,26 +376,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mx;
         }
       }
-      // P buffer u was last read by the P V product of tile i - 2
-      if (i >= 2 && !warp_wait(bar(B_OD + u), ((i - 2) >> 1) & 1, p.err, abort_flag)) {
-        ok = false;
-        break;
-      }
-      const uint32_t pcol = tmem + lanes + (u ? kColP1 : kColP0);
+      // P goes into S u itself (this thread's lane, whose scores are in
+      // registers): P_hi in columns [0,64), P_lo in [64,128)
+      const uint32_t pcol = scol;
+      const uint32_t lcol = scol + 64;
       float rs[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) rs[e] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
+        uint32_t pk[16], pl[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e]), sl2, -m_ref));
           const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e + 1]), sl2, -m_ref));
           rs[e & 7] += p0 + p1;
-          pk[e] = ptx::pack2<BF>(p0, p1);
+          ptx::split2<BF>(p0, p1, pk[e], pl[e]);
         }
         ptx::tmem_st16(pcol + 16 * c, pk);
+        ptx::tmem_st16(lcol + 16 * c, pl);
       }
       l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       if (nv < kKeys) {
@@ -377,18 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(B_PF + u));
     }
-    // ---- epilogue: o = O / l, lse2 = m_ref + log2(l)
-    const int grow = mt * kRows + row;
-    const bool row_valid = grow < p.batch * G;
-    float* dst = nullptr;
-    size_t sidx = 0;
-    if (row_valid) {
-      const int b = grow / G;
-      const int jj = grow - b * G;
-      sidx = static_cast<size_t>(split) * p.batch * Hq + static_cast<size_t>(b) * Hq + h * G + jj;
-      dst = p.pre_o + sidx * kHeadDim;
-    }
-    if (n > 0 && ok && warp_wait(bar(B_OD + ((n - 1) & 1)), ((n - 1) >> 1) & 1, p.err, abort_flag)) {
+    // ---- epilogue: o = O / l, lse2 = m_ref + log2(l); into piece `piece`
+    // as an fp32 partial state, or (piece < 0) as the final out / lse
+    const bool row_valid = tok < row_end;
+    const size_t orow = static_cast<size_t>(tok) * Hq + h * G + jj;
+    const size_t sidx = static_cast<size_t>(piece < 0 ? 0 : piece) * p.rows_per_piece + orow;
+    float* dst = p.pre_o + sidx * kHeadDim;
+    uint16_t* fdst = static_cast<uint16_t*>(p.out) + orow * kHeadDim;
+    if (n > 0 && ok && warp_wait(bar(B_OD + (n - 1) % 3), ((n - 1) / 3) & 1, p.err, abort_flag)) {
       ptx::tc_fence_after();
       const float inv = 1.f / l;
 #pragma unroll
@@ -396,19 +435,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t o[32];
         ptx::tmem_ld32(tmem + lanes + kColO + 32 * c, o);
         ptx::tmem_ld_wait();
-        if (row_valid) {
+        if (row_valid && piece >= 0) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             float4 v = make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
                                    __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
             *reinterpret_cast<float4*>(dst + 32 * c + e) = v;
           }
+        } else if (row_valid) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 v;
+            v.x = ptx::pack2<BF>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+            v.y = ptx::pack2<BF>(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            v.z = ptx::pack2<BF>(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+            v.w = ptx::pack2<BF>(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+            *reinterpret_cast<uint4*>(fdst + 32 * c + e) = v;
+          }
         }
       }
-      if (row_valid) p.pre_lse[sidx] = m_ref + ptx::lg2(l);
-    } else if (row_valid) {
+      if (row_valid && piece >= 0) p.pre_lse[sidx] = m_ref + ptx::lg2(l);
+      if (row_valid && piece < 0 && p.lse) p.lse[orow] = (m_ref + ptx::lg2(l)) * 0.6931471805599453f;
+    } else if (row_valid && piece >= 0) {
       for (int d = 0; d < kHeadDim; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
       p.pre_lse[sidx] = -INFINITY;
+    } else if (row_valid) {
+      for (int d = 0; d < kHeadDim; d += 8) *reinterpret_cast<uint4*>(fdst + d) = make_uint4(0u, 0u, 0u, 0u);
+      if (p.lse) p.lse[orow] = -INFINITY;
     }
   }
   ptx::tc_fence_before();
@@ -452,8 +505,8 @@ int prefix_max_active_clusters(int cluster) {
 }
 
 cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                          const PrefixParams& p, int kv_dtype, cudaStream_t stream) {
-  const int grid = p.num_kv_heads * p.n_splits * p.m_groups * p.cluster;
+                          const PrefixParams& p, int kv_dtype, cudaStream_t stream, bool pdl) {
+  const int grid = p.work != nullptr ? p.num_kv_heads * p.n_work : p.num_kv_heads * p.n_splits * p.m_groups * p.cluster;
   if (grid <= 0) return cudaSuccess;
   if (kv_dtype != kBF16 && kv_dtype != kF16) return cudaErrorInvalidValue;
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, PrefixParams) =
@@ -473,7 +526,7 @@ cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const 
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = pdl ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kern, tmq, tmk, tmv, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

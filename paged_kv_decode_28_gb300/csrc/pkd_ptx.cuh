@@ -203,6 +203,26 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return r;
 }
 
+// Two floats as a sum of two packed 16-bit pairs: hi = round(x), lo =
+// round(x - hi).  hi + lo carries about twice the 16-bit significand, so a
+// product with hi and lo as two operands (or two rows of one MMA) loses only
+// ~2^-17 of each x instead of 2^-9 (bf16) or 2^-11 (f16).
+template <bool BF16>
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack2<BF16>(a, b);
+  float ha, hb;
+  if constexpr (BF16) {
+    ha = __uint_as_float(hi << 16);
+    hb = __uint_as_float(hi & 0xffff0000u);
+  } else {
+    const __half2 h = *reinterpret_cast<const __half2*>(&hi);
+    const float2 f = __half22float2(h);
+    ha = f.x;
+    hb = f.y;
+  }
+  lo = pack2<BF16>(a - ha, b - hb);
+}
+
 // Two E4M3 codes (lo byte = first element) -> f16x2, exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);

@@ -314,6 +314,33 @@ def make_prefill(*, seed: int, q_lens: Sequence[int], kv_lens: Sequence[int], nu
     return b
 
 
+TREE_WORKLOAD = "tree3_b256_root4096_16x1024_suffix64to512_gqa4_bf16_p16"
+PREFILL_WORKLOAD = "prefill_b16_q512_kv1024to4096_gqa4_bf16_p16"
+
+
+def make_config_tree(device="cpu", batch: Optional[int] = None) -> PagedBatch:
+    """Prefix-tree decode workload: 256 requests (or ``batch``, a multiple of
+    16) under one 4096-key root, 16 branches of 1024 keys (16 requests each)
+    and their own 64-512 keys; GQA 32/8, bf16, page 16 (the cascade
+    workload's shapes, with one more shared level)."""
+    B = batch or 256
+    rng = np.random.default_rng(2001)
+    lengths = rng.integers(64, 512, size=B, endpoint=True)
+    return make_tree(seed=2001, levels=[([B], [4096]), ([B // 16] * 16, [1024] * 16)], lengths=lengths,
+                     num_qo_heads=32, num_kv_heads=8, page_size=16, device=device, name=TREE_WORKLOAD)
+
+
+def make_config_prefill(device="cpu", batch: Optional[int] = None) -> PagedBatch:
+    """Append-prefill workload: 16 requests (or ``batch``), 512 new tokens
+    each on top of 512-3584 cached ones (1024-4096 keys in all, the new
+    tokens' included); GQA 32/8, bf16, page 16."""
+    B = batch or 16
+    rng = np.random.default_rng(2002)
+    kv = rng.integers(1024, 4096, size=B, endpoint=True)
+    return make_prefill(seed=2002, q_lens=[512] * B, kv_lens=kv, num_qo_heads=32, num_kv_heads=8, page_size=16,
+                        device=device, name=PREFILL_WORKLOAD)
+
+
 def config_lengths(idx: int, batch: Optional[int] = None) -> np.ndarray:
     """Per-request token counts of the five standard workloads (seeded)."""
     rng = np.random.default_rng(1000 + idx)

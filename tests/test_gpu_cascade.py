@@ -44,6 +44,21 @@ def test_cascade_small(prefix_len, g):
     assert_lse_close(lse, l_ref)
 
 
+@pytest.mark.parametrize("prefix_len", [1, 2, 3])
+def test_cascade_few_prefix_keys_many_requests(prefix_len):
+    """A prefix of 1-3 keys and suffixes of 0-2 keys for many requests: the
+    prefix state is a sum of 1-3 value rows, so the weights' precision in the
+    tensor-core P V product shows at full size."""
+    rng = np.random.default_rng(62 + prefix_len)
+    lengths = rng.integers(0, 3, size=300).tolist()
+    b = wl.make_paged(seed=620 + prefix_len, lengths=lengths, num_qo_heads=16, num_kv_heads=2, page_size=16,
+                      prefix_len=prefix_len, device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
 @pytest.mark.parametrize("P", [1, 4, 64, 128])
 def test_cascade_page_sizes(P):
     b = wl.make_paged(seed=300 + P, lengths=[33, 0, 200, 1], num_qo_heads=16, num_kv_heads=4, page_size=P,

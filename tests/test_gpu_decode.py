@@ -35,6 +35,23 @@ def test_small_batches_edge_lengths(qd, kvd, P, g):
     assert_lse_close(lse, l_ref)
 
 
+@pytest.mark.parametrize("qd,kvd", DTYPES)
+def test_few_keys_many_requests(qd, kvd):
+    """Requests of 1-3 keys: with so few keys the output is a sum of 1-3 value
+    rows whose weights are not averaged out, so an error in the weights passed
+    to the P V product (e.g. rounding P to the 16-bit type) shows at full size,
+    and cancellations make |o| small against the absolute tolerance."""
+    rng = np.random.default_rng(61)
+    lengths = rng.integers(1, 4, size=400).tolist()
+    for P, g in ((1, 8), (16, 4), (64, 1)):
+        b = wl.make_paged(seed=610 + P + g, lengths=lengths, num_qo_heads=2 * g, num_kv_heads=2, page_size=P,
+                          q_dtype=qd, kv_dtype=kvd, device="cuda")
+        out, lse, _ = gpu_paged_decode(b)
+        o_ref, l_ref = _oracle(b)
+        assert_o_close(out, o_ref)
+        assert_lse_close(lse, l_ref)
+
+
 def test_batch_of_one_and_all_empty():
     b = wl.make_paged(seed=7, lengths=[37], num_qo_heads=8, num_kv_heads=1, page_size=16, device="cuda")
     out, lse, _ = gpu_paged_decode(b)
