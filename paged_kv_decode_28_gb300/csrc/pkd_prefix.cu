@@ -17,7 +17,7 @@
 // is reused only after all C CTAs have released it (their tcgen05.commit
 // arrives on the slot's "empty" barrier in every CTA).
 //
-// Per CTA (256 threads, one CTA per SM):
+// Per CTA (384 threads, one CTA per SM):
 //   warp 0      TMA producer of Q (once) and of the K ring; warp 2 producer of
 //               the V ring: key tiles page by page into two 3-stage rings
 //               (128-byte swizzled, K-major for K, MN-major for V); a K slot is
@@ -27,13 +27,17 @@
 //               S = Q K^T into one of three S buffers (two tiles ahead of the
 //               P V product), then O += P_hi V + P_lo V with both parts of P
 //               read from TMEM; tcgen05.commit signals the mbarriers;
-//   warps 4..7  softmax: thread r owns query row r (TMEM lane r), loads its 128
-//               scores, keeps a running reference max (rescaling O in TMEM only
-//               when the tile max exceeds it by more than 8 in log2 units, which
-//               leaves the result exact), writes P as two bf16/f16 parts
-//               (P_hi = round(P), P_lo = round(P - P_hi), so P reaches the
-//               product to ~2^-17 instead of the 16-bit type's 2^-9 / 2^-11)
-//               into TMEM and accumulates its row sum in a register.
+//   warps 4..11 softmax, two threads per query row: warps 4 + q and 8 + q
+//               share TMEM lanes 32q .. 32q+31 (query rows), the first taking
+//               keys 0..63 of each tile and the second keys 64..127.  The two
+//               halves of a row swap their partial maxima through shared
+//               memory, keep one running reference max (rescaling O in TMEM,
+//               each its 64 columns, only when the tile max exceeds it by more
+//               than 8 in log2 units, which leaves the result exact), write P
+//               as two bf16/f16 parts (P_hi = round(P), P_lo = round(P - P_hi),
+//               so P reaches the product to ~2^-17 instead of the 16-bit type's
+//               2^-9 / 2^-11) into TMEM and keep partial row sums, added at the
+//               end.
 // TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512).  Tile
 // i uses S (i mod 3): once its scores are in registers, P_hi overwrites its
 // columns [0,64) and P_lo [64,128), so S u is rewritten (for tile i + 3) only
@@ -46,7 +50,8 @@ namespace {
 
 constexpr int kRows = 128;  // query rows per CTA
 constexpr int kKeys = 128;  // keys per tile
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kSoftmaxWarps = 8;
 constexpr float kRescaleThreshold = 8.0f;
 
 constexpr int kHalf = 16384;   // one 64-element (128-byte) column half of a 128-row tile
@@ -70,8 +75,10 @@ enum {
 };
 constexpr int kTmemSlot = kBars + kNumBars * 8;
 constexpr int kAbort = kTmemSlot + 8;
-constexpr int kTotal = kAbort + 16;
+constexpr int kXchg = kAbort + 16;  // fp32 [2 halves][128 rows]: the softmax halves' partial maxima / sums
+constexpr int kTotal = kXchg + 4 * 2 * kRows;
 constexpr int kAlloc = kTotal + 1024;
+static_assert(kAlloc <= 227 * 1024, "dynamic shared memory above the 227 KB a CTA may use");
 
 constexpr uint32_t kColO = 384, kTmemCols = 512;
 __device__ __forceinline__ uint32_t col_s(int u) { return static_cast<uint32_t>(u) * 128u; }  // S buffer u
@@ -157,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 3; ++s) {
       ptx::mbar_init(bar(B_SF + s), 1);
-      ptx::mbar_init(bar(B_PF + s), kRows);
+      ptx::mbar_init(bar(B_PF + s), kSoftmaxWarps * 32);
       ptx::mbar_init(bar(B_OD + s), 1);
     }
     ptx::mbar_init(bar(B_DRAIN), 1);
@@ -310,65 +317,80 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int wq = warp & 3;
+    const int hf = (warp - 4) >> 2;  // keys [64 hf, 64 hf + 64) of each tile
     const int row = wq * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
+    float* xchg = reinterpret_cast<float*>(base_ptr + kXchg);  // [half][row]
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     // this thread's query row: token (or request) tok, qo head h * G + jj
     const int tok = b0 + row / G;
     const int jj = row - (row / G) * G;
+    // Each iteration passes the pair's named barrier exactly twice, also after
+    // a failed wait (ok false: the rest of the work is skipped, and every later
+    // wait returns at once on the abort flag), so the two halves never wait at
+    // barriers the other does not reach.
     for (int i = 0; i < n; ++i) {
       const int u = i % 3;
-      if (!warp_wait(bar(B_SF + u), (i / 3) & 1, p.err, abort_flag)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
+      ok = ok && warp_wait(bar(B_SF + u), (i / 3) & 1, p.err, abort_flag);
       const uint32_t scol = tmem + lanes + col_s(u);
-      uint32_t sr[128];
-      ptx::tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      ptx::tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      ptx::tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-      ptx::tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-      ptx::tmem_ld_wait();
+      uint32_t sr[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) sr[c] = __float_as_uint(-INFINITY);
+      if (ok) {
+        ptx::tc_fence_after();
+        ptx::tmem_ld32(scol + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        ptx::tmem_ld32(scol + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        ptx::tmem_ld_wait();
+      }
       const int key0 = (t0 + i) * kKeys;
       const int nv = min(kKeys, kv_len - key0);
       // keys this row sees: those before the list's end and, for a causal
       // unit, at or before the row's position tok + diag (units that mask
-      // start at key 0, so every row of theirs sees key 0 in its first tile)
-      const int vr = diag == kNoCausal ? nv : max(0, min(nv, tok + diag + 1 - key0));
+      // start at key 0, so every row of theirs sees key 0 in its first tile);
+      // vr counts them within this thread's half
+      const int vrow = diag == kNoCausal ? nv : max(0, min(nv, tok + diag + 1 - key0));
+      const int vr = min(max(vrow - 64 * hf, 0), 64);
       // mask, then a tree max of the raw scores (the scale is positive, so it
-      // commutes with max): 8 independent chains
+      // commutes with max): 8 independent chains, then the other half's
       float m8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
-      if (vr < kKeys) {
+      if (vr < 64) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c >= vr) sr[c] = __float_as_uint(-INFINITY);
       }
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
-      const float mx = sl2 * fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      for (int c = 0; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
+      const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      xchg[hf * kRows + row] = mh;
+      // both halves' scores are in registers past this barrier, so P may
+      // overwrite any column of S u
+      ptx::named_bar_sync(1 + wq, 64);
+      const float mo = xchg[(hf ^ 1) * kRows + row];
+      ptx::named_bar_sync(1 + wq, 64);  // both have read before the next tile writes
+      if (!ok) continue;
+      const float mx = sl2 * fmaxf(mh, mo);
       const bool need = (i > 0) && (mx > m_ref + kRescaleThreshold);
       if (i == 0) m_ref = mx;
       if (__any_sync(0xffffffffu, need)) {
         if (!warp_wait(bar(B_OD + (i - 1) % 3), ((i - 1) / 3) & 1, p.err, abort_flag)) {
           ok = false;
-          break;
+          continue;
         }
         ptx::tc_fence_after();
         const float alpha = need ? ptx::ex2(m_ref - mx) : 1.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          ptx::tmem_ld32(tmem + lanes + kColO + 32 * c, o);
+          ptx::tmem_ld32(tmem + lanes + kColO + 64 * hf + 32 * c, o);
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          ptx::tmem_st32(tmem + lanes + kColO + 32 * c, o);
+          ptx::tmem_st32(tmem + lanes + kColO + 64 * hf + 32 * c, o);
         }
         ptx::tmem_st_wait();
         if (need) {
@@ -376,15 +398,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mx;
         }
       }
-      // P goes into S u itself (this thread's lane, whose scores are in
-      // registers): P_hi in columns [0,64), P_lo in [64,128)
-      const uint32_t pcol = scol;
-      const uint32_t lcol = scol + 64;
+      // P goes into S u itself: P_hi of keys 2c, 2c + 1 in column c, P_lo in
+      // column 64 + c (this half: columns 32 hf .. 32 hf + 31 of each)
+      const uint32_t pcol = scol + 32 * hf;
+      const uint32_t lcol = scol + 64 + 32 * hf;
       float rs[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) rs[e] = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t pk[16], pl[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -398,22 +420,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       if (nv < kKeys) {
-        // keys past the prefix end: their P is 0, and their V rows must be
-        // finite for the product, so zero them (both column halves) once the
-        // tile's V has landed
+        // keys past the list's end: their P is 0, and their V rows must be
+        // finite for the product, so zero them (each half one column half)
+        // once the tile's V has landed
         if (!warp_wait(bar(B_VF + i % kStages), (i / kStages) & 1, p.err, abort_flag)) {
           ok = false;
-          break;
+          continue;
         }
       }
       if (nv < kKeys && row >= nv) {
         uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        uint8_t* vrow = base_ptr + kV + (i % kStages) * kStage + row * 128;
+        uint8_t* vrow = base_ptr + kV + (i % kStages) * kStage + hf * kHalf + row * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          *reinterpret_cast<uint4*>(vrow + 16 * c) = z;
-          *reinterpret_cast<uint4*>(vrow + kHalf + 16 * c) = z;
-        }
+        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + 16 * c) = z;
         ptx::fence_proxy_async_smem();
       }
       ptx::tmem_st_wait();
@@ -421,19 +440,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(bar(B_PF + u));
     }
     // ---- epilogue: o = O / l, lse2 = m_ref + log2(l); into piece `piece`
-    // as an fp32 partial state, or (piece < 0) as the final out / lse
+    // as an fp32 partial state, or (piece < 0) as the final out / lse; each
+    // half writes its 64 columns, the first half the lse
     const bool row_valid = tok < row_end;
     const size_t orow = static_cast<size_t>(tok) * Hq + h * G + jj;
     const size_t sidx = static_cast<size_t>(piece < 0 ? 0 : piece) * p.rows_per_piece + orow;
-    float* dst = p.pre_o + sidx * kHeadDim;
-    uint16_t* fdst = static_cast<uint16_t*>(p.out) + orow * kHeadDim;
+    float* dst = p.pre_o + sidx * kHeadDim + 64 * hf;
+    uint16_t* fdst = static_cast<uint16_t*>(p.out) + orow * kHeadDim + 64 * hf;
+    // the row sum is the two halves' partial sums (every thread arrives here,
+    // also after a failed wait, so the barrier is always complete)
+    xchg[hf * kRows + row] = l;
+    ptx::named_bar_sync(1 + wq, 64);
+    l += xchg[(hf ^ 1) * kRows + row];
     if (n > 0 && ok && warp_wait(bar(B_OD + (n - 1) % 3), ((n - 1) / 3) & 1, p.err, abort_flag)) {
       ptx::tc_fence_after();
       const float inv = 1.f / l;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        ptx::tmem_ld32(tmem + lanes + kColO + 32 * c, o);
+        ptx::tmem_ld32(tmem + lanes + kColO + 64 * hf + 32 * c, o);
         ptx::tmem_ld_wait();
         if (row_valid && piece >= 0) {
 #pragma unroll
@@ -454,14 +479,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (row_valid && piece >= 0) p.pre_lse[sidx] = m_ref + ptx::lg2(l);
-      if (row_valid && piece < 0 && p.lse) p.lse[orow] = (m_ref + ptx::lg2(l)) * 0.6931471805599453f;
+      if (hf == 0 && row_valid && piece >= 0) p.pre_lse[sidx] = m_ref + ptx::lg2(l);
+      if (hf == 0 && row_valid && piece < 0 && p.lse) p.lse[orow] = (m_ref + ptx::lg2(l)) * 0.6931471805599453f;
     } else if (row_valid && piece >= 0) {
-      for (int d = 0; d < kHeadDim; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-      p.pre_lse[sidx] = -INFINITY;
+      for (int d = 0; d < 64; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (hf == 0) p.pre_lse[sidx] = -INFINITY;
     } else if (row_valid) {
-      for (int d = 0; d < kHeadDim; d += 8) *reinterpret_cast<uint4*>(fdst + d) = make_uint4(0u, 0u, 0u, 0u);
-      if (p.lse) p.lse[orow] = -INFINITY;
+      for (int d = 0; d < 64; d += 8) *reinterpret_cast<uint4*>(fdst + d) = make_uint4(0u, 0u, 0u, 0u);
+      if (hf == 0 && p.lse) p.lse[orow] = -INFINITY;
     }
   }
   ptx::tc_fence_before();
