@@ -341,6 +341,72 @@ def make_config_prefill(device="cpu", batch: Optional[int] = None) -> PagedBatch
                         device=device, name=PREFILL_WORKLOAD)
 
 
+@dataclass
+class MlaBatch:
+    """One MLA decode batch: latent cache ckv ``[N, P, 512]`` and rotary key
+    cache kpe ``[N, P, 64]`` (one latent "kv head" shared by all query heads),
+    queries q_nope ``[B, H, 512]`` (already in the latent space) and q_pe
+    ``[B, H, 64]``, and a CSR page table as for ``PagedBatch``."""
+
+    name: str
+    q_nope: torch.Tensor
+    q_pe: torch.Tensor
+    ckv_cache: torch.Tensor
+    kpe_cache: torch.Tensor
+    kv_indptr: np.ndarray
+    kv_page_indices: np.ndarray
+    kv_last_page_len: np.ndarray
+    page_size: int
+    num_heads: int
+    sm_scale: float
+    kv_lens: np.ndarray
+
+    @property
+    def batch(self) -> int:
+        return int(self.kv_indptr.shape[0] - 1)
+
+
+MLA_WORKLOAD = "mla_b64_h128_l3072to8192_latent512_rope64_bf16_p16"
+
+
+def make_mla(*, seed: int, lengths: Sequence[int], num_heads: int = 128, page_size: int = 16,
+             pool_pages: Optional[int] = None, device="cpu", name: str = "mla",
+             sm_scale: Optional[float] = None) -> MlaBatch:
+    """Seeded MLA decode batch (bf16, N(0,1) values).  ``sm_scale`` defaults to
+    1/sqrt(128 + 64), the query-key width of the decompressed heads (128
+    no-RoPE + 64 RoPE dimensions)."""
+    rng = np.random.default_rng(seed)
+    lengths = np.asarray(lengths, dtype=np.int64)
+    P = page_size
+    need = int(((lengths + P - 1) // P).sum())
+    pool_pages = max(need, 1) if pool_pages is None else pool_pages
+    order = rng.permutation(pool_pages)
+    indptr, indices, last = lengths_to_page_table(lengths, P, order)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    B = len(lengths)
+    bf = torch.bfloat16
+    return MlaBatch(
+        name=name,
+        q_nope=_randn((B, num_heads, 512), gen, device, bf),
+        q_pe=_randn((B, num_heads, 64), gen, device, bf),
+        ckv_cache=_randn((pool_pages, P, 512), gen, device, bf),
+        kpe_cache=_randn((pool_pages, P, 64), gen, device, bf),
+        kv_indptr=indptr, kv_page_indices=indices, kv_last_page_len=last, page_size=P, num_heads=num_heads,
+        sm_scale=(1.0 / math.sqrt(192.0)) if sm_scale is None else float(sm_scale),
+        kv_lens=lengths.astype(np.int32))
+
+
+def make_config_mla(device="cpu", batch: Optional[int] = None) -> MlaBatch:
+    """The deep dive's DeepSeek-V3 serving step: 64 concurrent decode requests
+    (or ``batch``) of 3072-8192 cached tokens, 128 query heads, latent 512 +
+    RoPE 64, bf16, page 16."""
+    B = batch or 64
+    rng = np.random.default_rng(3003)
+    lengths = rng.integers(3072, 8192, size=B, endpoint=True)
+    return make_mla(seed=3003, lengths=lengths, num_heads=128, page_size=16, device=device, name=MLA_WORKLOAD)
+
+
 def config_lengths(idx: int, batch: Optional[int] = None) -> np.ndarray:
     """Per-request token counts of the five standard workloads (seeded)."""
     rng = np.random.default_rng(1000 + idx)
