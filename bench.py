@@ -56,9 +56,9 @@ def parse_args():
     ap.add_argument("--all-configs", action="store_true", help="also print one line per standard workload")
     ap.add_argument("--batch", type=int, default=None,
                     help="shrink the workload to its first N requests (small cases for profiling)")
-    ap.add_argument("--op", choices=["decode", "append", "tree", "prefill"], default="decode",
+    ap.add_argument("--op", choices=["decode", "append", "tree", "prefill", "mla"], default="decode",
                     help="append: pkd_append_kv (new tokens written into the workload's pool); tree: "
-                    "prefix-tree decode on the 3-level tree workload; prefill: append-prefill attention")
+                    "prefix-tree decode on the 3-level tree workload; prefill: append-prefill attention; mla: MLA decode")
     ap.add_argument("--kv-layout", choices=["NHD", "HND"], default="NHD",
                     help="page layout of the K/V pools: NHD [P, Hk, D] pages or HND [Hk, P, D] pages")
     ap.add_argument("--append-tokens", type=int, default=0,
@@ -841,11 +841,96 @@ def run_prefill(args, world, rank, local):
     }
 
 
+def mla_bytes(b) -> int:
+    """Each request's latent and rotary rows once (1152 bytes per key), plus q,
+    out and lse."""
+    kv = int(np.asarray(b.kv_lens, np.int64).sum()) * (512 + 64) * 2
+    B, H = b.batch, b.num_heads
+    return kv + B * H * (576 * 2 + 512 * 2 + 4)
+
+
+def run_mla(args, world, rank, local):
+    """MLA decode (pkd_mla_decode) on the 64-request DeepSeek-V3 workload: K
+    back-to-back calls (host planning and the unit upload included) timed with
+    CUDA events."""
+    import torch
+
+    import paged_kv_decode_28_gb300 as pkd
+    from paged_kv_decode_28_gb300 import _build
+    from paged_kv_decode_28_gb300 import workloads as wl
+
+    _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    b = wl.make_config_mla(device=dev, batch=args.batch)
+    idx = torch.from_numpy(np.asarray(b.kv_page_indices, np.int32)).to(dev)
+    out = torch.empty((b.batch, b.num_heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((b.batch, b.num_heads), dtype=torch.float32, device=dev)
+    ws = None
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        nonlocal ws
+        _, _, ws = pkd.mla_decode(b.q_nope, b.q_pe, b.ckv_cache, b.kpe_cache, b.kv_indptr, idx, b.kv_last_page_len,
+                                  sm_scale=b.sm_scale, out=out, lse=lse, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        e0.record(stream)
+        for _ in range(K):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    clk = clocks.summary()
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+    nbytes = mla_bytes(b)
+    achieved = nbytes / (ms_step * 1e-3) / 1e9
+    flops = int(np.asarray(b.kv_lens, np.int64).sum()) * b.num_heads * (576 + 512) * 2
+    peak, peak_kind = measured_hbm_peak()
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        from oracle import mla as orc
+
+        rows = [(r, h) for r in range(0, b.batch, max(1, b.batch // 8)) for h in (0, b.num_heads - 1)]
+        t0 = time.perf_counter()
+        orc.mla_decode(b.q_nope.cpu(), b.q_pe.cpu(), b.ckv_cache.cpu(), b.kpe_cache.cpu(), b.kv_indptr,
+                       b.kv_page_indices, b.kv_last_page_len, sm_scale=b.sm_scale, rows=rows)
+        dt = time.perf_counter() - t0
+        frac = len(rows) / (b.batch * b.num_heads)
+        cpu = {"value": round(nbytes * frac / dt / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{len(rows)} of {b.batch * b.num_heads} (request, head) rows, bytes scaled by that "
+               f"fraction (python fp64 oracle, {dt:.2f} s, pool copied to the host first)"}
+    return {
+        "metric": "MLA decode (pkd_mla_decode): achieved HBM GB/s per call", "value": round(world * achieved, 1),
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
+        "us_per_call": round(ms_step * 1e3, 2), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) values, seeded lengths and page placement)",
+        "config": {"workload": b.name, "batch": b.batch, "num_heads": b.num_heads, "page_size": b.page_size,
+                   "kv_tokens": int(np.asarray(b.kv_lens, np.int64).sum()), "bytes_per_step": nbytes,
+                   "flops_per_step": flops, "tflops": round(flops / (ms_step * 1e-3) / 1e12, 1),
+                   "l2": f"inputs {nbytes / 1e9:.2f} GB > 129 MB L2; no flush between steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "pkd mla_kernel + mla_merge_kernel (whole call)",
+                     "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback", "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None},
+        "cpu_baseline": cpu, "gpu_launches": 2 * K, "clocks": clk,
+    }
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_init(args)
-    if args.op in ("append", "tree", "prefill"):
-        line = {"append": run_append, "tree": run_tree, "prefill": run_prefill}[args.op](args, world, rank, local)
+    if args.op in ("append", "tree", "prefill", "mla"):
+        line = {"append": run_append, "tree": run_tree, "prefill": run_prefill, "mla": run_mla}[args.op](
+            args, world, rank, local)
         if rank == 0:
             print(json.dumps(line), flush=True)
         return

@@ -284,6 +284,41 @@ pkd_status pkd_prefill_run(pkd_plan_t plan, const void* d_q, const void* d_k_cac
                            float* d_lse, void* stream);
 
 /*
+ * Multi-latent attention (MLA) decode over a paged latent cache (deep dive,
+ * "Technical Moats": DeepSeek-V2/V3's compressed KV attended without expanding
+ * it; "The Code, Annotated": kv_lora_rank 512, q_rope_dim 64).  Every query
+ * head of a request attends the request's cached rows, each a latent row ckv
+ * (512) and a rotary key kpe (64) shared by all heads:
+ *   s_j = sm_scale * (<q_nope[h], ckv_j> + <q_pe[h], kpe_j>),
+ *   out[b, h] = sum_j softmax(s)_j ckv_j (512, in the latent space),
+ *   lse[b, h] = ln sum_j exp(s_j).
+ * q_nope is the no-RoPE query with the key up-projection already applied
+ * (512), q_pe the rotary query (64); the value up-projection is the caller's.
+ *   d_q_nope   bf16 [batch, num_heads, 512];  d_q_pe bf16 [batch, num_heads, 64].
+ *   d_ckv_cache  bf16 pool: page p, slot t, dim d at p * ckv_page_stride_elems + t * 512 + d.
+ *   d_kpe_cache  bf16 pool: p * kpe_page_stride_elems + t * 64 + d.
+ *   h_kv_indptr, d_kv_page_indices, h_kv_last_page_len: the page table as for pkd_plan.
+ *   num_heads 1..128; page_size a divisor of 32 or a multiple of 32.
+ *   sm_scale <= 0 selects 1/sqrt(192) (128 no-RoPE + 64 RoPE query-key dims).
+ *   d_out bf16 [batch, num_heads, 512]; d_lse fp32 [batch, num_heads] or NULL.
+ *   d_workspace  pkd_mla_workspace_bytes(batch, num_heads, num_sms) bytes, 16-byte
+ *                aligned; num_sms the device's SM count (work is cut for it).
+ * Plans on the host (requests cut into key ranges that fill the SMs about
+ * twice; two CTAs per range, one per half of the 512 output dims, each forming
+ * the full S on the tensor cores), uploads the units with cudaMemcpyAsync into
+ * the workspace (so not capturable), then enqueues the kernel and, when a
+ * request was cut, a merge kernel.  Page ids outside [0, num_pages) are read
+ * as page 0 and flagged in the workspace's first word (PKD_DEVERR_* bits).
+ */
+size_t pkd_mla_workspace_bytes(int max_batch, int num_heads, int num_sms);
+pkd_status pkd_mla_decode(const void* d_q_nope, const void* d_q_pe, const void* d_ckv_cache,
+                          const void* d_kpe_cache, const int32_t* h_kv_indptr, const int32_t* d_kv_page_indices,
+                          const int32_t* h_kv_last_page_len, int batch, int num_heads, int page_size,
+                          int64_t num_pages, int64_t ckv_page_stride_elems, int64_t kpe_page_stride_elems,
+                          float sm_scale, void* d_out, float* d_lse, void* d_workspace, size_t workspace_bytes,
+                          int num_sms, void* stream);
+
+/*
  * Append new tokens' keys and values to the paged cache: the write step on
  * either side of each decode step (README mirror, "Core Features": decode,
  * prefill and append kernels over a paged KV cache).  Token i belongs to

@@ -5,7 +5,7 @@ C ABI in ``include/pkd.h``); ``api`` is its Python binding.  ``workloads``
 builds seeded synthetic inputs.
 """
 from .api import (  # noqa: F401
-    BF16, E4M3, F16, F32, Plan, PkdError, append_kv, decode_noalloc, lib, merge_state, merge_states, num_ctas,
+    BF16, E4M3, F16, F32, Plan, PkdError, append_kv, decode_noalloc, lib, mla_decode, merge_state, merge_states, num_ctas,
     plan_host,
     single_decode, version, workspace_bytes,
 )

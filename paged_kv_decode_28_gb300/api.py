@@ -68,6 +68,9 @@ def lib() -> ctypes.CDLL:
         "pkd_plan_set_timing_events": (i, [_vp, _vp, _vp]),
         "pkd_plan_set_debug": (i, [_vp, i]),
         "pkd_plan_set_kv_layout": (i, [_vp, i]),
+        "pkd_mla_workspace_bytes": (sz, [i, i, i]),
+        "pkd_mla_decode": (i, [_vp, _vp, _vp, _vp, _i32p, _vp, _i32p, i, i, i, i64, i64, i64, f, _vp, _vp, _vp, sz,
+                               i, _vp]),
         "pkd_plan_tree": (i, [_vp, i, _vp, _vp, _vp, _vp, _i32p, _vp]),
         "pkd_tree_decode": (i, [_vp, _vp, _vp, _vp, i64, i64, f, _vp, _vp, _vp]),
         "pkd_plan_prefill": (i, [_vp, _i32p, _i32p, _vp, _i32p, i, i, i, i, i, i, i, i, _vp]),
@@ -409,6 +412,50 @@ def append_kv(k_new: torch.Tensor, v_new: torch.Tensor, batch_indices: torch.Ten
                                Hk, D, P, _ptr(k_cache), _ptr(v_cache), _DTYPE_CODE[k_cache.dtype],
                                _LAYOUT_CODE[kv_layout], N, stride,
                                _ptr(k_scale), _ptr(v_scale), _ptr(err), _stream(stream)))
+
+
+def mla_decode(q_nope: torch.Tensor, q_pe: torch.Tensor, ckv_cache: torch.Tensor, kpe_cache: torch.Tensor,
+               kv_indptr, kv_page_indices: torch.Tensor, kv_last_page_len, *, sm_scale: Optional[float] = None,
+               out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None, stream=None):
+    """Multi-latent attention decode: q_nope ``[B, H, 512]`` (key up-projection
+    folded in), q_pe ``[B, H, 64]``, latent pool ckv ``[N, P, 512]`` and rotary
+    pool kpe ``[N, P, 64]`` (bf16) -> ``(out [B, H, 512] bf16, lse [B, H])``."""
+    if q_nope.dim() != 3 or q_nope.shape[2] != 512 or q_pe.shape != q_nope.shape[:2] + (64,):
+        raise ValueError("q_nope [B, H, 512] and q_pe [B, H, 64] expected")
+    if ckv_cache.dim() != 3 or ckv_cache.shape[2] != 512 or kpe_cache.shape[:2] != ckv_cache.shape[:2] \
+            or kpe_cache.shape[2] != 64:
+        raise ValueError("ckv_cache [N, P, 512] and kpe_cache [N, P, 64] expected")
+    for t in (q_nope, q_pe, ckv_cache, kpe_cache):
+        if t.dtype != torch.bfloat16:
+            raise ValueError("MLA decode takes bf16 tensors")
+    if not (q_nope.is_contiguous() and q_pe.is_contiguous()):
+        raise ValueError("q_nope / q_pe must be contiguous")
+    for c, w in ((ckv_cache, 512), (kpe_cache, 64)):
+        if c.stride(2) != 1 or (c.shape[1] > 1 and c.stride(1) != w):
+            raise ValueError("each page of a pool must be contiguous")
+    if kv_page_indices.dtype != torch.int32 or kv_page_indices.device.type != "cuda":
+        raise ValueError("kv_page_indices must be an int32 CUDA tensor")
+    B, H, _ = q_nope.shape
+    N, P, _ = ckv_cache.shape
+    indptr = _host_i32(kv_indptr)
+    last = _host_i32(kv_last_page_len)
+    if len(indptr) != B + 1:
+        raise ValueError("kv_indptr must have batch + 1 entries")
+    sms = torch.cuda.get_device_properties(q_nope.device).multi_processor_count
+    nbytes = lib().pkd_mla_workspace_bytes(max(B, 1), H, sms)
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q_nope.device)
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q_nope.device) if out is None else out
+    lse = torch.empty((B, H), dtype=torch.float32, device=q_nope.device) if lse is None else lse
+    last_arg = last if len(last) else np.zeros(1, np.int32)
+    ckv_stride = ckv_cache.stride(0) if N > 1 else P * 512
+    kpe_stride = kpe_cache.stride(0) if N > 1 else P * 64
+    _check(lib().pkd_mla_decode(_ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache), _as_i32p(indptr),
+                                _ptr(kv_page_indices), _as_i32p(last_arg), B, H, P, N, ckv_stride, kpe_stride,
+                                float(sm_scale or 0.0), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                sms, _stream(stream)))
+    return out, lse, workspace
 
 
 def single_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, sm_scale: Optional[float] = None,

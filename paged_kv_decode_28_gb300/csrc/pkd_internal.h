@@ -166,10 +166,35 @@ struct AppendParams {
   int kv_hnd;                 // HND pages
 };
 
+// Multi-latent attention decode (pkd_mla.cu): one CTA per unit (request,
+// output half, key range) given as TileWork {q0 = request, -, page_begin,
+// kv_len, t0, t1 (32-key tiles), piece (-1: final output), level = half}.
+struct MlaParams {
+  const TileWork* work;
+  int n_work;
+  const int* page_indices;      // CSR page ids (device)
+  int num_pages;
+  int page_size;
+  int box_tok;                  // keys per TMA box: min(page_size, 32)
+  int num_heads;                // <= 128
+  int batch;
+  float scale_log2;             // sm_scale * log2(e)
+  float* part_o;                // [piece][H][512] fp32
+  float* part_lse;              // [piece][H] base-2
+  const int* req_piece_begin;   // [batch + 1]
+  int any_split;                // some request has more than one piece
+  void* out;                    // [batch][H][512] bf16
+  float* lse;                   // [batch][H] natural log, or nullptr
+  unsigned* err;
+};
+
 // Launchers (defined in the .cu files; return a cudaError_t).
 cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
                           int q_dtype, int kv_dtype, int grid, cudaStream_t stream);
 cudaError_t launch_merge_rows(const MergeParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_mla(const CUtensorMap& tq_nope, const CUtensorMap& tq_pe, const CUtensorMap& tckv,
+                       const CUtensorMap& tkpe, const MlaParams& p, cudaStream_t stream);
+int mla_smem_bytes();
 cudaError_t launch_append_kv(const AppendParams& p, int new_dtype, int kv_dtype, cudaStream_t stream);
 // dst, src and bytes multiples of 16; src may be mapped pinned host memory
 cudaError_t launch_copy16(void* dst, const void* src, int64_t bytes, cudaStream_t stream);
