@@ -1071,21 +1071,24 @@ pkd_status pkd_mla_decode(const void* d_q_nope, const void* d_q_pe, const void* 
         (kpe_page_stride_elems * 2) % 16 || kpe_page_stride_elems < static_cast<int64_t>(P) * 64)
       return fail(PKD_ERR_INVALID_ARG, "page strides must cover a page and be 16-byte multiples");
   }
-  // key ranges: requests cut into pieces of at most `chunk` keys (a multiple
-  // of 32) so that the units (two output halves per piece) fill the SMs about
-  // twice; a request with one piece is written directly, the others merged
-  int64_t chunk = (total + num_sms - 1) / num_sms;
-  chunk = ((chunk + 31) / 32) * 32;
-  if (chunk < 256) chunk = 256;
+  // key ranges: each request cut into about L * num_sms / total pieces of
+  // whole 32-key tiles (at least 512 keys each), so that the units (two output
+  // halves per piece) fill the SMs about twice with equal work; a request with
+  // one piece is written directly, the others merged
+  constexpr int kTileKeys = 32;
   std::vector<pkd::TileWork> w;
   std::vector<int32_t> rpb(batch + 1, 0);
   int piece = 0;
   bool any_split = false;
   for (int b = 0; b < batch; ++b) {
     const int L = lens[b];
-    const int np = L > chunk ? static_cast<int>((L + chunk - 1) / chunk) : 1;
+    const int tiles = (L + kTileKeys - 1) / kTileKeys;
+    int64_t want = total > 0 ? (static_cast<int64_t>(L) * num_sms + total / 2) / total : 1;
+    want = want < 1 ? 1 : want;
+    const int64_t by_min = (L + 511) / 512;  // no piece under 512 keys
+    want = want > by_min ? (by_min < 1 ? 1 : by_min) : want;
+    const int np = static_cast<int>(want > tiles ? (tiles > 0 ? tiles : 1) : want);
     if (np > 1) any_split = true;
-    const int tiles = (L + 31) / 32;
     const int tpp = (tiles + np - 1) / np;
     for (int s = 0; s < np; ++s) {
       for (int hv = 0; hv < 2; ++hv) {
@@ -1172,6 +1175,8 @@ pkd_status pkd_mla_decode(const void* d_q_nope, const void* d_q_pe, const void* 
   p.out = d_out;
   p.lse = d_lse;
   p.err = reinterpret_cast<unsigned*>(ws);
+  p.q_nope = d_q_nope;
+  p.q_pe = d_q_pe;
   e = pkd::launch_mla(tqn, tqp, tckv, tkpe, p, st);
   if (e != cudaSuccess) return cuda_fail(e, "MLA kernel launch");
   return PKD_OK;

@@ -186,6 +186,8 @@ struct MlaParams {
   void* out;                    // [batch][H][512] bf16
   float* lse;                   // [batch][H] natural log, or nullptr
   unsigned* err;
+  const void* q_nope;           // [batch][H][512] bf16 (chunks 4..7 are read directly)
+  const void* q_pe;             // [batch][H][64] bf16
 };
 
 // Launchers (defined in the .cu files; return a cudaError_t).

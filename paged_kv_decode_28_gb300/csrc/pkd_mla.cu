@@ -18,18 +18,26 @@
 // the whole S (the dot products need all 576 dimensions) and each accumulate
 // P V for their 256 dimensions.
 //
+// Q is 144 KB for 128 heads; the first four 64-dim chunks stay in shared
+// memory and the other five (latent dims 256..511 and the rotary part) go to
+// TMEM, so that shared memory holds a 4-stage ring of key tiles and the loads
+// run ahead of the MMAs.
+//
 // Per CTA (256 threads, one CTA per SM):
-//   warp 0      TMA producer: Q once (9 boxes of 64 dims x H heads), then key
-//               tiles of 32 keys (9 boxes of 64 dims x 32 keys, 36 KB) into a
-//               2-stage ring, page by page;
+//   warp 0      TMA producer: Q chunks 0..3 once (64 dims x H heads each), then
+//               key tiles of 32 keys (9 boxes of 64 dims x 32 keys, 36 KB) into
+//               a 4-stage ring, page by page;
 //   warp 1      allocates 512 TMEM columns and issues the MMAs from one thread:
-//               S = Q K^T (36 MMAs of N = 32 per tile) into one of three S
+//               S = Q K^T (36 MMAs of N = 32 per tile, A from shared memory for
+//               chunks 0..3 and from TMEM for 4..8) into one of three S
 //               buffers, and one tile behind, O += P_hi V + P_lo V (N = 256);
-//   warps 4..7  softmax, thread r = head row r (TMEM lane r): a running
+//   warps 4..7  first write Q chunks 4..8 of their head row into TMEM, then the
+//               softmax, thread r = head row r (TMEM lane r): a running
 //               reference max with lazy rescaling of O, P written over its S
 //               buffer as two 16-bit parts (P_hi = round(p), P_lo =
 //               round(p - P_hi)), the row sum in a register.
-// TMEM columns: O [0,256), S u [256 + 32u, 288 + 32u) for u = 0..2.
+// TMEM columns: O [0,256), S u [256 + 32u, 288 + 32u) for u = 0..2, Q chunks
+// 4..8 [352, 512) (two bf16 per column, K order).
 #include "pkd_internal.h"
 #include "pkd_ptx.cuh"
 
@@ -43,9 +51,10 @@ constexpr int kChunks = 9;         // 64-dim chunks of a 576-dim row (8 latent +
 constexpr int kQBox = 16384;       // one chunk of Q: 128 rows x 128 bytes
 constexpr int kKBox = 4096;        // one chunk of a key tile: 32 rows x 128 bytes
 constexpr int kTile = kChunks * kKBox;
-constexpr int kMlaStages = 2;
+constexpr int kMlaStages = 4;
+constexpr int kQSmem = 4;          // Q chunks in shared memory (the rest in TMEM)
 constexpr int kMQ = 0;
-constexpr int kMK = kMQ + kChunks * kQBox;
+constexpr int kMK = kMQ + kQSmem * kQBox;
 constexpr int kMBars = kMK + kMlaStages * kTile;
 enum {
   MB_Q = 0,
@@ -54,7 +63,8 @@ enum {
   MB_SF = MB_E + kMlaStages,    // S full [3]
   MB_PF = MB_SF + 3,            // P full [3]
   MB_OD = MB_PF + 3,            // P V done [3]
-  MB_DRAIN = MB_OD + 3,
+  MB_QT = MB_OD + 3,           // Q chunks in TMEM written
+  MB_DRAIN = MB_QT + 1,
   kMNumBars = MB_DRAIN + 1
 };
 constexpr int kMTmemSlot = kMBars + kMNumBars * 8;
@@ -62,7 +72,7 @@ constexpr int kMAbort = kMTmemSlot + 8;
 constexpr int kMTotal = kMAbort + 16;
 constexpr int kMAlloc = kMTotal + 1024;
 static_assert(kMAlloc <= 227 * 1024, "dynamic shared memory above the 227 KB a CTA may use");
-constexpr uint32_t kMColO = 0, kMTmemCols = 512;
+constexpr uint32_t kMColO = 0, kMColQ = 352, kMTmemCols = 512;
 constexpr float kMRescale = 8.0f;
 __device__ __forceinline__ uint32_t mcol_s(int u) { return 256u + 32u * static_cast<uint32_t>(u); }
 
@@ -114,6 +124,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       ptx::mbar_init(bar(MB_PF + s), kMlaRows);
       ptx::mbar_init(bar(MB_OD + s), 1);
     }
+    ptx::mbar_init(bar(MB_QT), kMlaRows);
     ptx::mbar_init(bar(MB_DRAIN), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
@@ -135,9 +146,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         ptx::prefetch_tensormap(&tq_pe);
         ptx::prefetch_tensormap(&tckv);
         ptx::prefetch_tensormap(&tkpe);
-        ptx::mbar_arrive_expect_tx(bar(MB_Q), static_cast<uint32_t>(kChunks) * H * 128u);
-        for (int c = 0; c < 8; ++c) ptx::tma_load_4d(base + kMQ + c * kQBox, &tq_nope, bar(MB_Q), 0, c, 0, b);
-        ptx::tma_load_4d(base + kMQ + 8 * kQBox, &tq_pe, bar(MB_Q), 0, 0, b, 0);
+        ptx::mbar_arrive_expect_tx(bar(MB_Q), static_cast<uint32_t>(kQSmem) * H * 128u);
+        for (int c = 0; c < kQSmem; ++c) ptx::tma_load_4d(base + kMQ + c * kQBox, &tq_nope, bar(MB_Q), 0, c, 0, b);
       }
       const int P = p.page_size;
       const int box = p.box_tok;  // keys per box: min(P, 32)
@@ -170,7 +180,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     if (lane == 0 && n > 0) {
       constexpr uint32_t idesc_s = ptx::idesc_f16(true, false, kMlaRows, kMlaKeys);
       constexpr uint32_t idesc_pv = ptx::idesc_f16(true, true, kMlaRows, 256);
-      bool ok = mwait(bar(MB_Q), 0, p.err, abort_flag);
+      bool ok = mwait(bar(MB_Q), 0, p.err, abort_flag) && mwait(bar(MB_QT), 0, p.err, abort_flag);
       auto pv = [&](int t) -> bool {
         const int u = t % 3;
         const int s = t % kMlaStages;
@@ -195,12 +205,21 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         // S u holds P of tile i - 3 until that tile's P V product is done
         if (i >= 3 && !mwait(bar(MB_OD + u), ((i - 3) / 3) & 1, p.err, abort_flag)) break;
         ptx::tc_fence_after();
-#pragma unroll 4
-        for (int k = 0; k < kChunks * 4; ++k) {
+        // descriptors of the first chunk; a byte offset adds offset / 16 to
+        // the start-address field (addresses stay below 256 KB)
+        const uint64_t a0 = ptx::smem_desc_sw128(base + kMQ, 16, 1024);
+        const uint64_t b0 = ptx::smem_desc_sw128(base + kMK + s * kTile, 16, 1024);
+        const uint32_t dcol = tmem + mcol_s(u);
+#pragma unroll
+        for (int k = 0; k < kQSmem * 4; ++k) {
           const uint32_t c = static_cast<uint32_t>(k >> 2), sub = static_cast<uint32_t>(k & 3) * 32u;
-          const uint64_t adesc = ptx::smem_desc_sw128(base + kMQ + c * kQBox + sub, 16, 1024);
-          const uint64_t bdesc = ptx::smem_desc_sw128(base + kMK + s * kTile + c * kKBox + sub, 16, 1024);
-          ptx::umma_ss(tmem + mcol_s(u), adesc, bdesc, idesc_s, k > 0 ? 1u : 0u);
+          ptx::umma_ss(dcol, a0 + ((c * kQBox + sub) >> 4), b0 + ((c * kKBox + sub) >> 4), idesc_s, k > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = kQSmem * 4; k < kChunks * 4; ++k) {
+          const uint32_t c = static_cast<uint32_t>(k >> 2), sub = static_cast<uint32_t>(k & 3);
+          ptx::umma_ts(dcol, tmem + kMColQ + 32u * (c - kQSmem) + 8u * sub, b0 + ((c * kKBox + sub * 32u) >> 4),
+                       idesc_s, 1u);
         }
         ptx::tc_commit(bar(MB_SF + u));
         if (i >= 1 && !pv(i - 1)) {
@@ -220,6 +239,30 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    if (n > 0) {
+      // Q chunks 4..8 of this head row into TMEM (zeros for rows past H)
+      const uint4* qn = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_nope) +
+                                                       (static_cast<size_t>(b) * H + row) * 512 + 64 * kQSmem);
+      const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_pe) +
+                                                       (static_cast<size_t>(b) * H + row) * 64);
+#pragma unroll 1
+      for (int c = 0; c < kChunks - kQSmem; ++c) {
+        uint32_t v[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint4 x = make_uint4(0u, 0u, 0u, 0u);
+          if (row < H) x = __ldg(c < kChunks - kQSmem - 1 ? qn + 8 * c + q : qp + q);
+          v[4 * q] = x.x;
+          v[4 * q + 1] = x.y;
+          v[4 * q + 2] = x.z;
+          v[4 * q + 3] = x.w;
+        }
+        ptx::tmem_st32(tmem + lanes + kMColQ + 32 * c, v);
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(MB_QT));
+    }
     for (int i = 0; i < n; ++i) {
       const int u = i % 3;
       if (!mwarp_wait(bar(MB_SF + u), (i / 3) & 1, p.err, abort_flag)) {

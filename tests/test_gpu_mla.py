@@ -30,7 +30,7 @@ def _oracle(b, rows=None):
                           b.kv_last_page_len, sm_scale=b.sm_scale, rows=rows)
 
 
-@pytest.mark.parametrize("P", [1, 16, 32, 64])
+@pytest.mark.parametrize("P", [1, 16, 32, 64, 128])
 @pytest.mark.parametrize("H", [8, 16, 128])
 def test_mla_matches_oracle(P, H):
     lengths = [1, 31, 32, 33, 100, 0, 777, 2100]
