@@ -29,6 +29,35 @@ def test_library_exports_every_declared_symbol():
     assert pkd.version().startswith("pkd ")
 
 
+def test_binding_signatures_match_the_header():
+    """Every entry point the binding declares has the header's argument count
+    and 64-bit integers where the header has int64_t / size_t (a mismatch
+    would pass wrong values through ctypes without any error)."""
+    import ctypes
+
+    header = open(os.path.join(ROOT, "include", "pkd.h")).read()
+    protos = {}
+    for m in re.finditer(r"\b(?:pkd_status|size_t|const char\*)\s+(pkd_[a-z_]+)\s*\(([^;]*?)\);", header, re.S):
+        args = [a.strip() for a in m.group(2).split(",")] if m.group(2).strip() not in ("", "void") else []
+        protos[m.group(1)] = args
+    L = pkd.lib()
+    checked = 0
+    for name, args in protos.items():
+        fn = getattr(L, name)
+        if fn.argtypes is None:
+            continue
+        assert len(fn.argtypes) == len(args), (name, len(fn.argtypes), len(args))
+        for decl, ct in zip(args, fn.argtypes):
+            if re.match(r"(int64_t|size_t)\s+\w+$", decl):
+                assert ct in (ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint64), (name, decl, ct)
+            elif re.match(r"int\s+\w+$", decl):
+                assert ct is ctypes.c_int, (name, decl, ct)
+            elif re.match(r"float\s+\w+$", decl):
+                assert ct is ctypes.c_float, (name, decl, ct)
+        checked += 1
+    assert checked >= 20
+
+
 def _random_table(rng, B, P, max_len, empty_frac=0.1):
     lens = rng.integers(1, max_len + 1, size=B)
     lens[rng.random(B) < empty_frac] = 0
