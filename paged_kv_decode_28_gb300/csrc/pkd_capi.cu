@@ -7,6 +7,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 #include <string>
@@ -1071,23 +1072,37 @@ pkd_status pkd_mla_decode(const void* d_q_nope, const void* d_q_pe, const void* 
         (kpe_page_stride_elems * 2) % 16 || kpe_page_stride_elems < static_cast<int64_t>(P) * 64)
       return fail(PKD_ERR_INVALID_ARG, "page strides must cover a page and be 16-byte multiples");
   }
-  // key ranges: each request cut into about L * num_sms / total pieces of
-  // whole 32-key tiles (at least 512 keys each), so that the units (two output
-  // halves per piece) fill the SMs about twice with equal work; a request with
-  // one piece is written directly, the others merged
+  // key ranges: the smallest piece size C (in 32-key tiles, at least 16 =
+  // 512 keys) for which cutting every request into pieces of at most C tiles
+  // gives at most num_sms pieces, so the units (two output halves per piece)
+  // make at most two full waves and the longest unit is as short as possible;
+  // a request with one piece is written directly, the others merged
   constexpr int kTileKeys = 32;
+  std::vector<int> tiles_of(batch);
+  int max_tiles = 1;
+  for (int b = 0; b < batch; ++b) {
+    tiles_of[b] = (lens[b] + kTileKeys - 1) / kTileKeys;
+    max_tiles = tiles_of[b] > max_tiles ? tiles_of[b] : max_tiles;
+  }
+  auto pieces_for = [&](int C) {
+    int64_t cnt = 0;
+    for (int b = 0; b < batch; ++b) cnt += tiles_of[b] > C ? (tiles_of[b] + C - 1) / C : 1;
+    return cnt;
+  };
+  int lo = 1, hi = max_tiles;
+  while (lo < hi) {
+    const int mid = lo + (hi - lo) / 2;
+    if (pieces_for(mid) <= num_sms) hi = mid; else lo = mid + 1;
+  }
+  const int C = lo < 16 ? 16 : lo;
   std::vector<pkd::TileWork> w;
   std::vector<int32_t> rpb(batch + 1, 0);
   int piece = 0;
   bool any_split = false;
   for (int b = 0; b < batch; ++b) {
     const int L = lens[b];
-    const int tiles = (L + kTileKeys - 1) / kTileKeys;
-    int64_t want = total > 0 ? (static_cast<int64_t>(L) * num_sms + total / 2) / total : 1;
-    want = want < 1 ? 1 : want;
-    const int64_t by_min = (L + 511) / 512;  // no piece under 512 keys
-    want = want > by_min ? (by_min < 1 ? 1 : by_min) : want;
-    const int np = static_cast<int>(want > tiles ? (tiles > 0 ? tiles : 1) : want);
+    const int tiles = tiles_of[b];
+    const int np = tiles > C ? (tiles + C - 1) / C : 1;
     if (np > 1) any_split = true;
     const int tpp = (tiles + np - 1) / np;
     for (int s = 0; s < np; ++s) {
@@ -1108,6 +1123,11 @@ pkd_status pkd_mla_decode(const void* d_q_nope, const void* d_q_pe, const void* 
     rpb[b + 1] = np > 1 ? piece : rpb[b];
   }
   if (piece > batch + num_sms) return fail(PKD_ERR_CAPACITY_EXCEEDED, "%d pieces above capacity", piece);
+  // longest units first: CTAs are dispatched in grid order, so the short
+  // units fill in behind the long ones
+  std::stable_sort(w.begin(), w.end(), [](const pkd::TileWork& x, const pkd::TileWork& y) {
+    return (x.t1 - x.t0) > (y.t1 - y.t0);
+  });
   // workspace: error word | units | request piece ranges | partial o | partial lse
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
   const size_t pieces_cap = static_cast<size_t>(batch) + num_sms;
