@@ -18,26 +18,30 @@
 // the whole S (the dot products need all 576 dimensions) and each accumulate
 // P V for their 256 dimensions.
 //
-// Q is 144 KB for 128 heads; the first four 64-dim chunks stay in shared
-// memory and the other five (latent dims 256..511 and the rotary part) go to
+// Q is 144 KB for 128 heads; its first five 64-dim chunks stay in shared
+// memory and the other four (latent dims 320..511 and the rotary part) go to
 // TMEM, so that shared memory holds a 4-stage ring of key tiles and the loads
-// run ahead of the MMAs.
+// run ahead of the MMAs.  S takes 36 single-thread MMA issues per tile, so it
+// is issued by two threads into two accumulators that the softmax adds.
 //
 // Per CTA (256 threads, one CTA per SM):
-//   warp 0      TMA producer: Q chunks 0..3 once (64 dims x H heads each), then
+//   warp 0      TMA producer: Q chunks 0..4 once (64 dims x H heads each), then
 //               key tiles of 32 keys (9 boxes of 64 dims x 32 keys, 36 KB) into
 //               a 4-stage ring, page by page;
-//   warp 1      allocates 512 TMEM columns and issues the MMAs from one thread:
-//               S = Q K^T (36 MMAs of N = 32 per tile, A from shared memory for
-//               chunks 0..3 and from TMEM for 4..8) into one of three S
-//               buffers, and one tile behind, O += P_hi V + P_lo V (N = 256);
-//   warps 4..7  first write Q chunks 4..8 of their head row into TMEM, then the
-//               softmax, thread r = head row r (TMEM lane r): a running
-//               reference max with lazy rescaling of O, P written over its S
-//               buffer as two 16-bit parts (P_hi = round(p), P_lo =
+//   warp 1      allocates 512 TMEM columns; one thread issues S_a = Q K^T over
+//               chunks 0..4 (20 MMAs of N = 32, A from shared memory) into one
+//               of two buffers and, one tile behind, O += P_hi V + P_lo V
+//               (N = 256);
+//   warp 3      one thread issues S_b over chunks 5..8 (16 MMAs, A = Q from
+//               TMEM) into its own two buffers;
+//   warps 4..7  first write Q chunks 5..8 of their head row into TMEM, then the
+//               softmax, thread r = head row r (TMEM lane r): S = S_a + S_b, a
+//               running reference max with lazy rescaling of O, P written over
+//               S_a's buffer as two 16-bit parts (P_hi = round(p), P_lo =
 //               round(p - P_hi)), the row sum in a register.
-// TMEM columns: O [0,256), S u [256 + 32u, 288 + 32u) for u = 0..2, Q chunks
-// 4..8 [352, 512) (two bf16 per column, K order).
+// TMEM columns: O [0,256), S_a u [256 + 32u, 288 + 32u), S_b u [320 + 32u,
+// 352 + 32u) for u = 0, 1, Q chunks 5..8 [384, 512) (two bf16 per column, K
+// order).
 #include "pkd_internal.h"
 #include "pkd_ptx.cuh"
 
@@ -52,7 +56,7 @@ constexpr int kQBox = 16384;       // one chunk of Q: 128 rows x 128 bytes
 constexpr int kKBox = 4096;        // one chunk of a key tile: 32 rows x 128 bytes
 constexpr int kTile = kChunks * kKBox;
 constexpr int kMlaStages = 4;
-constexpr int kQSmem = 4;          // Q chunks in shared memory (the rest in TMEM)
+constexpr int kQSmem = 5;          // Q chunks in shared memory (the rest in TMEM)
 constexpr int kMQ = 0;
 constexpr int kMK = kMQ + kQSmem * kQBox;
 constexpr int kMBars = kMK + kMlaStages * kTile;
@@ -60,21 +64,24 @@ enum {
   MB_Q = 0,
   MB_F = 1,                    // tile full  [kMlaStages]
   MB_E = MB_F + kMlaStages,     // tile empty [kMlaStages]
-  MB_SF = MB_E + kMlaStages,    // S full [3]
-  MB_PF = MB_SF + 3,            // P full [3]
-  MB_OD = MB_PF + 3,            // P V done [3]
-  MB_QT = MB_OD + 3,           // Q chunks in TMEM written
+  MB_SF = MB_E + kMlaStages,    // S_a full [2]
+  MB_SB = MB_SF + 2,            // S_b full [2]
+  MB_PF = MB_SB + 2,            // P full (S_a and S_b read) [2]
+  MB_OD = MB_PF + 2,            // P V done [2]
+  MB_QT = MB_OD + 2,            // Q chunks in TMEM written
   MB_DRAIN = MB_QT + 1,
-  kMNumBars = MB_DRAIN + 1
+  MB_DRAINB = MB_DRAIN + 1,
+  kMNumBars = MB_DRAINB + 1
 };
 constexpr int kMTmemSlot = kMBars + kMNumBars * 8;
 constexpr int kMAbort = kMTmemSlot + 8;
 constexpr int kMTotal = kMAbort + 16;
 constexpr int kMAlloc = kMTotal + 1024;
 static_assert(kMAlloc <= 227 * 1024, "dynamic shared memory above the 227 KB a CTA may use");
-constexpr uint32_t kMColO = 0, kMColQ = 352, kMTmemCols = 512;
+constexpr uint32_t kMColO = 0, kMColQ = 384, kMTmemCols = 512;
 constexpr float kMRescale = 8.0f;
-__device__ __forceinline__ uint32_t mcol_s(int u) { return 256u + 32u * static_cast<uint32_t>(u); }
+__device__ __forceinline__ uint32_t mcol_s(int u) { return 256u + 32u * static_cast<uint32_t>(u); }   // S_a u
+__device__ __forceinline__ uint32_t mcol_sb(int u) { return 320u + 32u * static_cast<uint32_t>(u); }  // S_b u
 
 __device__ __forceinline__ bool mwait(uint32_t bar, uint32_t parity, unsigned* err, volatile int* abort_flag) {
   if (*abort_flag) return false;
@@ -119,13 +126,15 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       ptx::mbar_init(bar(MB_F + s), 1);
       ptx::mbar_init(bar(MB_E + s), 1);
     }
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(bar(MB_SF + s), 1);
+      ptx::mbar_init(bar(MB_SB + s), 1);
       ptx::mbar_init(bar(MB_PF + s), kMlaRows);
       ptx::mbar_init(bar(MB_OD + s), 1);
     }
     ptx::mbar_init(bar(MB_QT), kMlaRows);
     ptx::mbar_init(bar(MB_DRAIN), 1);
+    ptx::mbar_init(bar(MB_DRAINB), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -180,11 +189,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     if (lane == 0 && n > 0) {
       constexpr uint32_t idesc_s = ptx::idesc_f16(true, false, kMlaRows, kMlaKeys);
       constexpr uint32_t idesc_pv = ptx::idesc_f16(true, true, kMlaRows, 256);
-      bool ok = mwait(bar(MB_Q), 0, p.err, abort_flag) && mwait(bar(MB_QT), 0, p.err, abort_flag);
+      bool ok = mwait(bar(MB_Q), 0, p.err, abort_flag);
       auto pv = [&](int t) -> bool {
-        const int u = t % 3;
+        const int u = t & 1;
         const int s = t % kMlaStages;
-        if (!mwait(bar(MB_PF + u), (t / 3) & 1, p.err, abort_flag)) return false;
+        if (!mwait(bar(MB_PF + u), (t >> 1) & 1, p.err, abort_flag)) return false;
         ptx::tc_fence_after();
         const uint32_t scol = mcol_s(u);
 #pragma unroll
@@ -199,11 +208,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         return true;
       };
       for (int i = 0; i < n && ok; ++i) {
-        const int u = i % 3;
+        const int u = i & 1;
         const int s = i % kMlaStages;
         if (!mwait(bar(MB_F + s), (i / kMlaStages) & 1, p.err, abort_flag)) break;
-        // S u holds P of tile i - 3 until that tile's P V product is done
-        if (i >= 3 && !mwait(bar(MB_OD + u), ((i - 3) / 3) & 1, p.err, abort_flag)) break;
+        // S_a u holds P of tile i - 2 until that tile's P V product is done
+        // (issued by this thread in the previous iteration)
+        if (i >= 2 && !mwait(bar(MB_OD + u), ((i - 2) >> 1) & 1, p.err, abort_flag)) break;
         ptx::tc_fence_after();
         // descriptors of the first chunk; a byte offset adds offset / 16 to
         // the start-address field (addresses stay below 256 KB)
@@ -215,12 +225,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           const uint32_t c = static_cast<uint32_t>(k >> 2), sub = static_cast<uint32_t>(k & 3) * 32u;
           ptx::umma_ss(dcol, a0 + ((c * kQBox + sub) >> 4), b0 + ((c * kKBox + sub) >> 4), idesc_s, k > 0 ? 1u : 0u);
         }
-#pragma unroll
-        for (int k = kQSmem * 4; k < kChunks * 4; ++k) {
-          const uint32_t c = static_cast<uint32_t>(k >> 2), sub = static_cast<uint32_t>(k & 3);
-          ptx::umma_ts(dcol, tmem + kMColQ + 32u * (c - kQSmem) + 8u * sub, b0 + ((c * kKBox + sub * 32u) >> 4),
-                       idesc_s, 1u);
-        }
         ptx::tc_commit(bar(MB_SF + u));
         if (i >= 1 && !pv(i - 1)) {
           ok = false;
@@ -230,6 +234,32 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       if (ok && !*abort_flag) pv(n - 1);
       ptx::tc_commit(bar(MB_DRAIN));
       ptx::mbar_wait(bar(MB_DRAIN), 0, p.err);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ second S issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idesc_s = ptx::idesc_f16(true, false, kMlaRows, kMlaKeys);
+      bool ok = mwait(bar(MB_QT), 0, p.err, abort_flag);
+      for (int i = 0; i < n && ok; ++i) {
+        const int u = i & 1;
+        const int s = i % kMlaStages;
+        if (!mwait(bar(MB_F + s), (i / kMlaStages) & 1, p.err, abort_flag)) break;
+        // S_b u was read by the softmax of tile i - 2 (before its P arrived)
+        if (i >= 2 && !mwait(bar(MB_PF + u), ((i - 2) >> 1) & 1, p.err, abort_flag)) break;
+        ptx::tc_fence_after();
+        const uint64_t b0 = ptx::smem_desc_sw128(base + kMK + s * kTile, 16, 1024);
+        const uint32_t dcol = tmem + mcol_sb(u);
+#pragma unroll
+        for (int k = kQSmem * 4; k < kChunks * 4; ++k) {
+          const uint32_t c = static_cast<uint32_t>(k >> 2), sub = static_cast<uint32_t>(k & 3);
+          ptx::umma_ts(dcol, tmem + kMColQ + 32u * (c - kQSmem) + 8u * sub, b0 + ((c * kKBox + sub * 32u) >> 4),
+                       idesc_s, k > kQSmem * 4 ? 1u : 0u);
+        }
+        ptx::tc_commit(bar(MB_SB + u));
+      }
+      // every MMA this thread issued has finished before TMEM is released
+      ptx::tc_commit(bar(MB_DRAINB));
+      ptx::mbar_wait(bar(MB_DRAINB), 0, p.err);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
@@ -264,16 +294,20 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       ptx::mbar_arrive(bar(MB_QT));
     }
     for (int i = 0; i < n; ++i) {
-      const int u = i % 3;
-      if (!mwarp_wait(bar(MB_SF + u), (i / 3) & 1, p.err, abort_flag)) {
+      const int u = i & 1;
+      if (!mwarp_wait(bar(MB_SF + u), (i >> 1) & 1, p.err, abort_flag) ||
+          !mwarp_wait(bar(MB_SB + u), (i >> 1) & 1, p.err, abort_flag)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
       const uint32_t scol = tmem + lanes + mcol_s(u);
-      uint32_t sr[32];
+      uint32_t sr[32], sb[32];
       ptx::tmem_ld32(scol, sr);
+      ptx::tmem_ld32(tmem + lanes + mcol_sb(u), sb);
       ptx::tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) + __uint_as_float(sb[c]));
       const int key0 = (t0 + i) * kMlaKeys;
       const int nv = min(kMlaKeys, kv_len - key0);
       if (nv < kMlaKeys) {
@@ -289,7 +323,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       if (i == 0) m_ref = mx;
       if (__any_sync(0xffffffffu, need)) {
         // O holds the products of tiles up to i - 1
-        if (!mwarp_wait(bar(MB_OD + (i - 1) % 3), ((i - 1) / 3) & 1, p.err, abort_flag)) {
+        if (!mwarp_wait(bar(MB_OD + ((i - 1) & 1)), ((i - 1) >> 1) & 1, p.err, abort_flag)) {
           ok = false;
           break;
         }
@@ -341,7 +375,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     // ---- epilogue: this CTA's 256 dims of o = O / l and lse, for heads < H
     const bool row_valid = row < H;
     const size_t orow = static_cast<size_t>(b) * H + row;
-    if (n > 0 && ok && mwarp_wait(bar(MB_OD + (n - 1) % 3), ((n - 1) / 3) & 1, p.err, abort_flag)) {
+    if (n > 0 && ok && mwarp_wait(bar(MB_OD + ((n - 1) & 1)), ((n - 1) >> 1) & 1, p.err, abort_flag)) {
       ptx::tc_fence_after();
       const float inv = 1.f / l;
       const float lse2 = m_ref + ptx::lg2(l);
