@@ -29,11 +29,12 @@
 //               key tiles of 32 keys (9 boxes of 64 dims x 32 keys, 36 KB) into
 //               a 4-stage ring, page by page;
 //   warp 1      allocates 512 TMEM columns; one thread issues S_a = Q K^T over
-//               chunks 0..4 (20 MMAs of N = 32, A from shared memory) into one
+//               chunks 0..2 (12 MMAs of N = 32, A from shared memory) into one
 //               of two buffers and, one tile behind, O += P_hi V + P_lo V
-//               (N = 256);
-//   warp 3      one thread issues S_b over chunks 5..8 (16 MMAs, A = Q from
-//               TMEM) into its own two buffers;
+//               (4 MMAs of N = 256);
+//   warp 3      one thread issues S_b over chunks 3..8 (24 MMAs, A = Q from
+//               shared memory for 3..4 and from TMEM for 5..8) into its own two
+//               buffers, so the two threads issue about equal work;
 //   warps 4..7  first write Q chunks 5..8 of their head row into TMEM, then the
 //               softmax, thread r = head row r (TMEM lane r): S = S_a + S_b, a
 //               running reference max with lazy rescaling of O, P written over
@@ -55,6 +56,7 @@ constexpr int kChunks = 9;         // 64-dim chunks of a 576-dim row (8 latent +
 constexpr int kQBox = 16384;       // one chunk of Q: 128 rows x 128 bytes
 constexpr int kKBox = 4096;        // one chunk of a key tile: 32 rows x 128 bytes
 constexpr int kTile = kChunks * kKBox;
+constexpr int kSplitA = 3;         // S chunks of the first issuer (it also issues P V); the rest are the second's
 constexpr int kMlaStages = 4;
 constexpr int kQSmem = 5;          // Q chunks in shared memory (the rest in TMEM)
 constexpr int kMQ = 0;
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         const uint64_t b0 = ptx::smem_desc_sw128(base + kMK + s * kTile, 16, 1024);
         const uint32_t dcol = tmem + mcol_s(u);
 #pragma unroll
-        for (int k = 0; k < kQSmem * 4; ++k) {
+        for (int k = 0; k < kSplitA * 4; ++k) {
           const uint32_t c = static_cast<uint32_t>(k >> 2), sub = static_cast<uint32_t>(k & 3) * 32u;
           ptx::umma_ss(dcol, a0 + ((c * kQBox + sub) >> 4), b0 + ((c * kKBox + sub) >> 4), idesc_s, k > 0 ? 1u : 0u);
         }
@@ -239,7 +241,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     // ------------------------------------------------------------ second S issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t idesc_s = ptx::idesc_f16(true, false, kMlaRows, kMlaKeys);
-      bool ok = mwait(bar(MB_QT), 0, p.err, abort_flag);
+      bool ok = mwait(bar(MB_Q), 0, p.err, abort_flag) && mwait(bar(MB_QT), 0, p.err, abort_flag);
       for (int i = 0; i < n && ok; ++i) {
         const int u = i & 1;
         const int s = i % kMlaStages;
@@ -247,13 +249,20 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         // S_b u was read by the softmax of tile i - 2 (before its P arrived)
         if (i >= 2 && !mwait(bar(MB_PF + u), ((i - 2) >> 1) & 1, p.err, abort_flag)) break;
         ptx::tc_fence_after();
+        const uint64_t a0 = ptx::smem_desc_sw128(base + kMQ, 16, 1024);
         const uint64_t b0 = ptx::smem_desc_sw128(base + kMK + s * kTile, 16, 1024);
         const uint32_t dcol = tmem + mcol_sb(u);
 #pragma unroll
-        for (int k = kQSmem * 4; k < kChunks * 4; ++k) {
+        for (int k = kSplitA * 4; k < kQSmem * 4; ++k) {  // A = Q from shared memory
+          const uint32_t c = static_cast<uint32_t>(k >> 2), sub = static_cast<uint32_t>(k & 3) * 32u;
+          ptx::umma_ss(dcol, a0 + ((c * kQBox + sub) >> 4), b0 + ((c * kKBox + sub) >> 4), idesc_s,
+                       k > kSplitA * 4 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = kQSmem * 4; k < kChunks * 4; ++k) {  // A = Q from TMEM
           const uint32_t c = static_cast<uint32_t>(k >> 2), sub = static_cast<uint32_t>(k & 3);
           ptx::umma_ts(dcol, tmem + kMColQ + 32u * (c - kQSmem) + 8u * sub, b0 + ((c * kKBox + sub * 32u) >> 4),
-                       idesc_s, k > kQSmem * 4 ? 1u : 0u);
+                       idesc_s, 1u);
         }
         ptx::tc_commit(bar(MB_SB + u));
       }
