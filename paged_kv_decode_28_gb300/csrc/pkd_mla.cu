@@ -24,10 +24,16 @@
 // run ahead of the MMAs.  S takes 36 single-thread MMA issues per tile, so it
 // is issued by two threads into two accumulators that the softmax adds.
 //
+// The two CTAs of a key range form a cluster: each issues half of every
+// tile's TMA boxes with multicast to both, and a stage is refilled once both
+// have finished its P V product (their commits arrive on both CTAs' "empty"
+// barriers).
+//
 // Per CTA (256 threads, one CTA per SM):
 //   warp 0      TMA producer: Q chunks 0..4 once (64 dims x H heads each), then
-//               key tiles of 32 keys (9 boxes of 64 dims x 32 keys, 36 KB) into
-//               a 4-stage ring, page by page;
+//               its half of the boxes of key tiles of 32 keys (9 boxes of 64
+//               dims x 32 keys per page, 36 KB a tile) into a 4-stage ring,
+//               multicast to the pair;
 //   warp 1      allocates 512 TMEM columns; one thread issues S_a = Q K^T over
 //               chunks 0..2 (12 MMAs of N = 32, A from shared memory) into one
 //               of two buffers and, one tile behind, O += P_hi V + P_lo V
@@ -120,13 +126,15 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   const int t0 = wb.x;
   const int n = max(min(wb.y, (kv_len + kMlaKeys - 1) / kMlaKeys) - t0, 0);
   const int piece = wb.z;
-  const int hv = wb.w;
+  const int hv = wb.w;  // equals the cluster rank: the pair's units are adjacent, first half first
+  const uint32_t rank = ptx::cluster_ctarank();
+  constexpr uint16_t kPair = 0x3;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(MB_Q), 1);
     for (int s = 0; s < kMlaStages; ++s) {
       ptx::mbar_init(bar(MB_F + s), 1);
-      ptx::mbar_init(bar(MB_E + s), 1);
+      ptx::mbar_init(bar(MB_E + s), 2);  // both CTAs' P V products of the tile
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(bar(MB_SF + s), 1);
@@ -146,6 +154,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers exist before any multicast reaches them
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base_ptr + kMTmemSlot);
 
@@ -181,8 +190,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           }
           const int tok = key - pi * P;
           const uint32_t d = base + kMK + s * kTile + static_cast<uint32_t>(j * box) * 128u;
-          for (int c = 0; c < 8; ++c) ptx::tma_load_4d(d + c * kKBox, &tckv, bar(MB_F + s), 0, c, tok, page);
-          ptx::tma_load_4d(d + 8 * kKBox, &tkpe, bar(MB_F + s), 0, tok, page, 0);
+          // this CTA's half of the page's nine boxes, delivered to both CTAs
+          for (int c = 0; c < 8; ++c)
+            if (((c + j) & 1) == static_cast<int>(rank))
+              ptx::tma_load_4d_mc(d + c * kKBox, &tckv, bar(MB_F + s), 0, c, tok, page, kPair);
+          if (((8 + j) & 1) == static_cast<int>(rank))
+            ptx::tma_load_4d_mc(d + 8 * kKBox, &tkpe, bar(MB_F + s), 0, tok, page, 0, kPair);
         }
       }
     }
@@ -206,7 +219,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           ptx::umma_ts(tmem + kMColO, tmem + scol + 16 + 8 * k, bdesc, idesc_pv, 1u);
         }
         ptx::tc_commit(bar(MB_OD + u));
-        ptx::tc_commit(bar(MB_E + s));  // the tile is free once its P V product is done
+        ptx::tc_commit_mc(bar(MB_E + s), kPair);  // both CTAs' stage s: this CTA is done with the tile
         return true;
       };
       for (int i = 0; i < n && ok; ++i) {
@@ -438,6 +451,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // no CTA leaves while its peer may still deliver into its shared memory or
+  // arrive on its barriers
+  ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kMTmemCols);
@@ -500,8 +516,20 @@ cudaError_t launch_mla(const CUtensorMap& tq_nope, const CUtensorMap& tq_pe, con
   if (p.n_work <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMAlloc);
   if (e != cudaSuccess) return e;
-  mla_kernel<<<p.n_work, kMlaThreads, kMAlloc, stream>>>(tq_nope, tq_pe, tckv, tkpe, p);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_work);
+  cfg.blockDim = dim3(kMlaThreads);
+  cfg.dynamicSmemBytes = kMAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;  // the two output halves of a key range
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mla_kernel, tq_nope, tq_pe, tckv, tkpe, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || !p.any_split) return e;
   const int warps = p.batch * p.num_heads;
   mla_merge_kernel<<<(warps + 7) / 8, 256, 0, stream>>>(p);
