@@ -267,7 +267,9 @@ pkd_status pkd_tree_decode(pkd_plan_t plan, const void* d_q, const void* d_k_cac
  * h_kv_last_page_len), head counts equal to the plan's, f16/bf16 q and K/V of
  * one type, group sizes dividing 128, page sizes dividing 128 or multiples of
  * 64.  One unit per 128-row query tile (128 / g tokens x g heads of a kv
- * head) and kv head; uploads the units like pkd_plan_tree
+ * head) and kv head, in pairs of consecutive tiles of a request that run as a
+ * two-CTA cluster sharing each key tile (a request's odd last tile gets an
+ * idle partner); uploads the units like pkd_plan_tree
  * (PKD_ERR_CAPACITY_EXCEEDED above the unit capacity).
  *
  * pkd_prefill_run: d_out [T, num_qo_heads, 128] in q's dtype, d_lse fp32

@@ -958,20 +958,25 @@ pkd_status pkd_plan_prefill(pkd_plan_t plan, const int32_t* h_qo_indptr, const i
                   "the cache)", r, q_len, kv_len);
     const int q0 = h_qo_indptr[r], q_end = h_qo_indptr[r + 1];
     const int diag = kv_len - q_len - q0;  // token q sits at position q + diag
-    for (int a = q0; a < q_end; a += per_tile) {
-      const int last_tok = (a + per_tile < q_end ? a + per_tile : q_end) - 1;
-      const int keys = causal ? last_tok + diag + 1 : kv_len;  // keys the tile's last row sees
-      pkd::TileWork t{};
-      t.q0 = a;
-      t.q_end = q_end;
-      t.page_begin = h_kv_indptr[r];
-      t.kv_len = kv_len;
-      t.t0 = 0;
-      t.t1 = (keys + 127) / 128;
-      t.piece = -1;
-      t.level = 0;
-      t.diag = causal ? diag : pkd::kNoCausal;
-      w.push_back(t);
+    // query tiles in pairs (a cluster of two CTAs sharing every key tile by
+    // multicast): both take the key tiles the later tile's last row sees; a
+    // lone last tile is paired with a helper whose rows are all past the end
+    for (int a = q0; a < q_end; a += 2 * per_tile) {
+      const int last_tok = (a + 2 * per_tile < q_end ? a + 2 * per_tile : q_end) - 1;
+      const int keys = causal ? last_tok + diag + 1 : kv_len;  // keys the pair's last row sees
+      for (int k = 0; k < 2; ++k) {
+        pkd::TileWork t{};
+        t.q0 = a + k * per_tile < q_end ? a + k * per_tile : q_end;
+        t.q_end = q_end;
+        t.page_begin = h_kv_indptr[r];
+        t.kv_len = kv_len;
+        t.t0 = 0;
+        t.t1 = (keys + 127) / 128;
+        t.piece = -1;
+        t.level = 0;
+        t.diag = causal ? diag : pkd::kNoCausal;
+        w.push_back(t);
+      }
     }
   }
   if (!plan->err_word_zeroed) {  // a plan used for prefill only: the first plan clears the error word
@@ -1006,6 +1011,7 @@ pkd_status pkd_prefill_run(pkd_plan_t plan, const void* d_q, const void* d_k_cac
   s = tile_kv_maps(plan, plan->pf_dtype, P, d_k_cache, d_v_cache, num_pages, page_stride_elems, &tmk, &tmv);
   if (s != PKD_OK) return s;
   pkd::PrefixParams pp = tile_params(plan, P, num_pages, sm_scale);
+  pp.cluster = 2;  // the units come in pairs of query tiles that share their key tiles
   pp.batch = plan->pf_tokens;
   pp.out = d_out;
   pp.lse = d_lse;
