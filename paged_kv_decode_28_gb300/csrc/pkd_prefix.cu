@@ -1,5 +1,6 @@
-// pkd_prefix.cu -- shared-prefix attention (cascade level 0) on the sm_103a
-// tensor cores (tcgen05 + TMEM).
+// pkd_prefix.cu -- tile attention on the sm_103a tensor cores (tcgen05 +
+// TMEM): a 128-row query tile of one kv head against a range of 128-key tiles
+// of one page list.  It serves three paths.
 //
 // Cascade decode attends one shared prefix for every request and merges that
 // state with each request's own (2026 guide, "Cascade attention for shared
@@ -10,6 +11,12 @@
 // 128-row query tile and a contiguous range of 128-key tiles of the prefix and
 // writes an fp32 partial state (o, base-2 lse) per row; the merge pass folds
 // these partials into each request's suffix states.
+//
+// In work-list mode (params.work) each CTA's unit comes from a host-built list
+// (TileWork): the nodes of a prefix tree's shared levels (each node's request
+// range against its page list, partial states per key-range piece), or the
+// query tiles of paged prefill (a request's new tokens against its pages, the
+// causal mask aligned to the end of the sequence, output written directly).
 //
 // CTAs run in clusters of C (1, 2, 4 or 8): the C query tiles of one kv head
 // and key range read the same K/V tiles, so each CTA fetches 1/C of every
