@@ -144,3 +144,60 @@ def test_plan_create_validates_without_a_gpu():
     st = L.pkd_plan_create(ctypes.byref(h), 4, 32, 8, 128, 8, 0, ctypes.c_void_p(256), 1 << 30)
     assert st == 0
     assert L.pkd_plan_destroy(h) == 0
+
+
+def test_next_row_entry_points_validate_without_a_gpu():
+    """Argument checks of the append, layout, tree, prefill and MLA entry points
+    run on the host before any CUDA call (status codes as in pkd.h)."""
+    import ctypes
+    L = pkd.lib()
+    OK, INVALID, UNSUPPORTED, SMALL, NO_PLAN = 0, 1, 2, 3, 7
+    p16 = ctypes.c_void_p(1 << 20)  # a 16-byte aligned stand-in address, never dereferenced
+    one = np.array([0, 1], np.int32)
+    last = np.array([1], np.int32)
+    i32 = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+    # KV append: no tokens is a no-op; head_dim, dtype pairing, scales, layout and alignment are checked
+    args = lambda **kw: dict(dict(k=p16, v=p16, nd=1, bi=p16, pos=p16, n=4, ip=p16, idx=p16, B=1, Hk=2, D=128, P=16,
+                                  kc=p16, vc=p16, kd=1, lay=0, N=8, stride=16 * 2 * 128, ks=None, vs=None), **kw)
+    call = lambda a: L.pkd_append_kv(a["k"], a["v"], a["nd"], a["bi"], a["pos"], a["n"], a["ip"], a["idx"], a["B"],
+                                     a["Hk"], a["D"], a["P"], a["kc"], a["vc"], a["kd"], a["lay"], a["N"], a["stride"],
+                                     a["ks"], a["vs"], None, None)
+    assert call(args(n=0)) == OK
+    assert call(args(D=64)) == UNSUPPORTED
+    assert call(args(nd=0)) == UNSUPPORTED                 # f16 values into a bf16 pool
+    assert call(args(kd=2, stride=16 * 2 * 128)) == INVALID  # an e4m3 pool needs scales
+    assert call(args(lay=2)) == INVALID
+    assert call(args(kc=ctypes.c_void_p((1 << 20) + 8))) == INVALID
+    assert call(args(stride=100)) == INVALID
+
+    # the page layout of a plan
+    h = ctypes.c_void_p()
+    assert L.pkd_plan_create(ctypes.byref(h), 4, 32, 8, 128, 8, 2, ctypes.c_void_p(256), 1 << 30) == OK
+    assert L.pkd_plan_set_kv_layout(h, 2) == INVALID
+    assert L.pkd_plan_set_kv_layout(h, 1) == OK
+    # prefix tree and its decode before a plan of the requests' own pages
+    lv = (ctypes.c_void_p * 1)(one.ctypes.data)
+    pg = (ctypes.c_void_p * 1)(p16.value)
+    nn = np.array([1], np.int32)
+    assert L.pkd_plan_tree(h, 1, lv, lv, pg, (ctypes.c_void_p * 1)(last.ctypes.data), i32(nn), None) == NO_PLAN
+    assert L.pkd_tree_decode(h, p16, p16, p16, 8, 16 * 8 * 128, 0.0, p16, None, None) == NO_PLAN
+    # prefill: head counts must be the plan's, K/V 16-bit of q's type, q_len <= kv_len
+    qo = np.array([0, 5], np.int32)
+    assert L.pkd_plan_prefill(h, i32(qo), i32(one), p16, i32(last), 1, 16, 8, 128, 16, 1, 1, 1, None) == INVALID
+    assert L.pkd_plan_prefill(h, i32(qo), i32(one), p16, i32(last), 1, 32, 8, 128, 16, 1, 2, 1, None) == UNSUPPORTED
+    assert L.pkd_plan_prefill(h, i32(qo), i32(one), p16, i32(last), 1, 32, 8, 128, 16, 1, 1, 1, None) == INVALID
+    assert L.pkd_prefill_run(h, p16, p16, p16, 8, 16 * 8 * 128, 0.0, p16, None, None) == NO_PLAN
+    assert L.pkd_plan_destroy(h) == OK
+
+    # MLA: workspace rule and argument checks
+    assert L.pkd_mla_workspace_bytes(64, 128, 148) > L.pkd_mla_workspace_bytes(64, 16, 148) > 0
+    assert L.pkd_mla_workspace_bytes(64, 129, 148) == 0
+    assert L.pkd_mla_workspace_bytes(64, 128, 0) == 0
+    need = L.pkd_mla_workspace_bytes(1, 16, 148)
+    mla = lambda P=16, H=16, ws=need, B=1: L.pkd_mla_decode(p16, p16, p16, p16, i32(one), p16, i32(last), B, H, P, 8,
+                                                           P * 512, P * 64, 0.0, p16, None, p16, ws, 148, None)
+    assert mla(P=24) == UNSUPPORTED
+    assert mla(H=200) == UNSUPPORTED
+    assert mla(ws=need - 256) == SMALL
+    assert mla(B=0) == OK
