@@ -846,16 +846,29 @@ pkd_status pkd_plan_tree(pkd_plan_t plan, int num_levels, const int32_t* const* 
       level_max_tiles[l] = tiles > level_max_tiles[l] ? tiles : level_max_tiles[l];
     }
   }
-  // key-range pieces per level: enough CTAs (kv heads x query tiles x pieces)
-  // to cover the SMs, within the plan's piece budget (each level keeps one)
+  // key-range pieces per level: one target unit length (in 128-key tiles) for
+  // the whole launch, the work of all levels over about two waves of CTAs,
+  // and each level cut into the pieces its longest node needs for it, within
+  // the plan's piece budget (each level keeps one)
   const int sms = plan->G / pkd::kCtasPerSm;
+  int64_t work = 0;  // CTA-tiles with one piece per level
+  for (int l = 0; l < num_levels; ++l) {
+    const int32_t* ri = h_req_indptr[l];
+    const int32_t* ki = h_kv_indptr[l];
+    const int32_t* lp = h_kv_last_page_len[l];
+    for (int n = 0; n < h_num_nodes[l]; ++n) {
+      const int pages = ki[n + 1] - ki[n];
+      const int64_t len = pages > 0 ? static_cast<int64_t>(pages - 1) * P + lp[n] : 0;
+      work += static_cast<int64_t>((ri[n + 1] - ri[n] + per_tile - 1) / per_tile) * ((len + 127) / 128);
+    }
+  }
+  work *= plan->hk;
+  const int64_t target = (work + 2 * sms - 1) / (2 * sms) > 2 ? (work + 2 * sms - 1) / (2 * sms) : 2;
   std::vector<int> S(num_levels, 1);
   int budget = plan->max_splits;
   for (int l = 0; l < num_levels; ++l) {
-    const int64_t ctas1 = static_cast<int64_t>(plan->hk) * (level_mtiles[l] > 0 ? level_mtiles[l] : 1);
-    int want = static_cast<int>((sms + ctas1 - 1) / ctas1);
+    int want = static_cast<int>((level_max_tiles[l] + target - 1) / target);
     want = want < 1 ? 1 : want;
-    want = want > level_max_tiles[l] ? (level_max_tiles[l] > 0 ? level_max_tiles[l] : 1) : want;
     const int cap = budget - (num_levels - 1 - l);
     S[l] = want > cap ? cap : want;
     budget -= S[l];

@@ -31,7 +31,7 @@ def _oracle(b, rows=None):
 
 
 @pytest.mark.parametrize("P", [1, 16, 32, 64, 128])
-@pytest.mark.parametrize("H", [8, 16, 128])
+@pytest.mark.parametrize("H", [1, 8, 16, 128])
 def test_mla_matches_oracle(P, H):
     lengths = [1, 31, 32, 33, 100, 0, 777, 2100]
     b = wl.make_mla(seed=1300 + P + H, lengths=lengths, num_heads=H, page_size=P, device="cuda")
