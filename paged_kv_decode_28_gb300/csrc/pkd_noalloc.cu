@@ -31,13 +31,9 @@
 #include <string>
 
 #include "pkd.h"
+#include "pkd_host.h"
 #include "pkd_internal.h"
 #include "pkd_plan.h"
-
-namespace pkd {
-// Defined in pkd_capi.cu: sets the thread's message returned by pkd_last_error().
-void set_last_error(const char* msg);
-}  // namespace pkd
 
 namespace {
 
@@ -52,22 +48,11 @@ std::mutex g_host_mutex;
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
-pkd_status fail(pkd_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
-pkd_status fail(pkd_status st, const char* fmt, ...) {
-  char buf[512];
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(buf, sizeof(buf), fmt, ap);
-  va_end(ap);
-  pkd::set_last_error(buf);
-  return st;
-}
-
-pkd_status cuda_fail(cudaError_t e, const char* what) {
-  return fail(PKD_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
-}
-
-size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+using pkd::host::aligned16;
+using pkd::host::align256;
+using pkd::host::cuda_fail;
+using pkd::host::fail;
+using pkd::host::get_encode;
 
 // Scratch layout for one call: the same regions as a plan workspace, sized
 // exactly for this batch.
@@ -83,24 +68,24 @@ NaLayout na_layout(int batch, int hk, int group, int G) {
   L.max_items = rows + G;
   size_t off = sizeof(pkd::WsHeader);
   L.cta_begin = off;
-  off += up256(4ull * (G + 1));
+  off += align256(4ull * (G + 1));
   L.items = off;
-  off += up256(16ull * L.max_items);
+  off += align256(16ull * L.max_items);
   L.merge_rows = off;
-  off += up256(4ull * (rows > 0 ? rows : 1));
+  off += align256(4ull * (rows > 0 ? rows : 1));
   L.row_begin = off;
-  off += up256(4ull * (rows > 0 ? rows : 1));
+  off += align256(4ull * (rows > 0 ? rows : 1));
   L.row_count = off;
-  off += up256(4ull * (rows > 0 ? rows : 1));
+  off += align256(4ull * (rows > 0 ? rows : 1));
   L.kv_len = off;
-  off += up256(4ull * (batch > 0 ? batch : 1));
+  off += align256(4ull * (batch > 0 ? batch : 1));
   L.page_begin = off;
-  off += up256(4ull * (batch > 0 ? batch : 1));
+  off += align256(4ull * (batch > 0 ? batch : 1));
   L.meta_end = off;
   L.part_o = off;
-  off += up256(4ull * L.max_items * group * pkd::kHeadDim);
+  off += align256(4ull * L.max_items * group * pkd::kHeadDim);
   L.part_lse = off;
-  off += up256(4ull * L.max_items * group);
+  off += align256(4ull * L.max_items * group);
   L.total = off;
   return L;
 }
@@ -122,25 +107,11 @@ pkd_status scratch_for_current_device(uint8_t** out) {
   return PKD_OK;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // dims (dim, head, key, page) for NHD pages, (dim, key, head, page) for HND;
 // a box is box_tok rows of one head of one page either way
 pkd_status kv_map(CUtensorMap* m, const void* base, int kv_dtype, int hk, int64_t tok_extent,
                   int64_t num_pages, int64_t page_stride_elems, int box_tok, bool hnd) {
-  auto enc = encode_fn();
+  auto enc = get_encode();
   if (!enc) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const int e = kv_dtype == PKD_E4M3 ? 1 : 2;
   const cuuint64_t row = static_cast<cuuint64_t>(pkd::kHeadDim) * e;
@@ -161,8 +132,6 @@ pkd_status kv_map(CUtensorMap* m, const void* base, int kv_dtype, int hk, int64_
   if (r != CUDA_SUCCESS) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
   return PKD_OK;
 }
-
-bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
@@ -187,7 +156,7 @@ extern "C" pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32
   if (!h_kv_indptr || (batch > 0 && !h_kv_last_page_len))
     return fail(PKD_ERR_INVALID_ARG, "h_kv_indptr / h_kv_last_page_len is NULL");
   if (batch > 0 && (!d_q || !d_out)) return fail(PKD_ERR_INVALID_ARG, "q/out is NULL");
-  if ((d_q && !al16(d_q)) || (d_out && !al16(d_out)))
+  if ((d_q && !aligned16(d_q)) || (d_out && !aligned16(d_out)))
     return fail(PKD_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
   const bool fp8 = kv_dtype == PKD_E4M3;
   if (fp8 && (!d_k_scale || !d_v_scale)) return fail(PKD_ERR_INVALID_ARG, "an E4M3 cache needs k_scale and v_scale");
@@ -288,7 +257,7 @@ extern "C" pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32
   p.scale_log2 = scale * 1.4426950408889634f;
   p.force_partial = 0;
   if (counts.n_items > 0) {
-    if (!d_k_cache || !d_v_cache || !al16(d_k_cache) || !al16(d_v_cache))
+    if (!d_k_cache || !d_v_cache || !aligned16(d_k_cache) || !aligned16(d_v_cache))
       return fail(PKD_ERR_INVALID_ARG, "k/v cache must be non-NULL and 16-byte aligned");
     if (num_pages <= 0 || num_pages > INT32_MAX) return fail(PKD_ERR_INVALID_ARG, "num_pages out of range");
     if ((page_stride_elems * (fp8 ? 1 : 2)) % 16 != 0 ||
