@@ -52,6 +52,39 @@ def test_append_matches_oracle_bit_for_bit(kvd, newd, P):
     assert torch.equal(view(b.k_cache.cpu()), view(kr)) and torch.equal(view(b.v_cache.cpu()), view(vr))
 
 
+@pytest.mark.parametrize("newd", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("scale", [1.7, 3.0, 0.37, 0.0123, 1e-3])
+def test_e4m3_codes_of_every_16_bit_value(newd, scale):
+    """Every finite bf16 / f16 value through the e4m3 path: the codes must be
+    those of the fp32 quotient x / scale.  Scales such as 3 put quotients
+    exactly on rounding midpoints (x = 3 * midpoint), where the quotient's
+    tie-to-even decides and a reciprocal multiply alone lands on the wrong side
+    for some of them (1.7); tiny scales overflow the quotient."""
+    allv = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(newd)
+    vals = allv[torch.isfinite(allv)]
+    Hk, P = 2, 16
+    per = Hk * 128
+    n = (vals.numel() + per - 1) // per
+    flat = torch.zeros(n * per, dtype=newd)
+    flat[:vals.numel()] = vals
+    k_new = flat.view(n, Hk, 128).cuda()
+    v_new = (-flat).view(n, Hk, 128).cuda()  # the negative half again, in the other table
+    pages = (n + P - 1) // P
+    b = wl.make_paged(seed=840, lengths=[n], num_qo_heads=4, num_kv_heads=Hk, page_size=P, kv_dtype="e4m3",
+                      pool_pages=pages, device="cuda")
+    k_scale = torch.tensor([scale, scale * 1.25], dtype=torch.float32, device="cuda")
+    v_scale = torch.tensor([scale * 0.75, scale], dtype=torch.float32, device="cuda")
+    pos = np.arange(n)
+    kr, vr, skipped = ka.append_kv(b.k_cache, b.v_cache, k_new, v_new, np.zeros(n, np.int64), pos, b.kv_indptr,
+                                   b.kv_page_indices, P, k_scale, v_scale)
+    assert skipped == 0
+    pkd.append_kv(k_new, v_new, _cuda_i32(np.zeros(n, np.int64)), _cuda_i32(pos), _cuda_i32(b.kv_indptr),
+                  _cuda_i32(b.kv_page_indices), b.k_cache, b.v_cache, k_scale=k_scale, v_scale=v_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(b.k_cache.cpu().view(torch.uint8), kr.view(torch.uint8))
+    assert torch.equal(b.v_cache.cpu().view(torch.uint8), vr.view(torch.uint8))
+
+
 def test_append_then_decode_equals_oracle():
     lens = np.array([1, 17, 300, 64, 1000])
     for kvd in ("bf16", "e4m3"):
