@@ -832,7 +832,7 @@ def run_prefill(args, world, rank, local):
                    "causal": True, "flops_per_step": flops, "bytes_per_step": nbytes,
                    "l2": f"inputs {nbytes / 1e9:.2f} GB > 129 MB L2; no flush between steps",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "kernel": "pkd prefix_kernel (work-list mode)", "achieved": round(achieved, 2),
+        "roofline": {"bound": "tensor", "kernel": "pkd tile2_kernel (paired query tiles)", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, burst)"
                      if peak_kind == "measured" else "fallback", "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None,

@@ -232,7 +232,9 @@ pkd_status pkd_cascade_decode(pkd_plan_t suffix_plan, const int32_t* d_prefix_pa
  *   h_kv_last_page_len[l]  host int32 [nodes]: 1..page_size (ignored for a
  *                          node without pages).
  * It cuts each level into key-range pieces (at most max_prefix_splits over all
- * levels; a level needs one), writes the work units into the workspace with
+ * levels; a level needs one), pairs each node's 128-row query tiles (one CTA
+ * per pair, piece and kv head; a node's odd last tile is paired with an empty
+ * one), writes the work units into the workspace with
  * one cudaMemcpyAsync on `stream` (waiting first for the previous such upload
  * of this plan) and fails with PKD_ERR_CAPACITY_EXCEEDED above the workspace's
  * unit capacity (8 * (max_batch + num_ctas), at least 4096).  f16/bf16 only
@@ -267,10 +269,11 @@ pkd_status pkd_tree_decode(pkd_plan_t plan, const void* d_q, const void* d_k_cac
  * h_kv_last_page_len), head counts equal to the plan's, f16/bf16 q and K/V of
  * one type, group sizes dividing 128, page sizes dividing 128 or multiples of
  * 64.  One unit per 128-row query tile (128 / g tokens x g heads of a kv
- * head) and kv head, in pairs of consecutive tiles of a request that run as a
- * two-CTA cluster sharing each key tile (a request's odd last tile gets an
- * idle partner); uploads the units like pkd_plan_tree
- * (PKD_ERR_CAPACITY_EXCEEDED above the unit capacity).
+ * head), in pairs of consecutive tiles of a request that one CTA per kv head
+ * runs together, each key tile read once for both (a request's odd last tile
+ * is paired with an empty one); the pairs are listed longest first and
+ * uploaded like pkd_plan_tree's units (PKD_ERR_CAPACITY_EXCEEDED above the
+ * unit capacity).
  *
  * pkd_prefill_run: d_out [T, num_qo_heads, 128] in q's dtype, d_lse fp32
  * [T, num_qo_heads] (natural log) or NULL; pools as pkd_run (the plan's

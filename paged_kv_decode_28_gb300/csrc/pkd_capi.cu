@@ -544,8 +544,13 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
     }
   }
   if (cascade && cascade->n_pre_splits > 0) {
-    cudaError_t e = pkd::launch_prefix(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->kv_dtype, st,
-                                       true);
+    // a prefix tree's levels are work-list pairs; a single shared prefix is
+    // the tile kernel's cluster mode
+    cudaError_t e = cascade->pp.work
+                        ? pkd::launch_tile2(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->kv_dtype, st,
+                                            true)
+                        : pkd::launch_prefix(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->kv_dtype,
+                                             st, true);
     if (e != cudaSuccess) return cuda_fail(e, "prefix kernel launch");
   }
   // plain decode merges its split rows and writes its empty rows in the decode
@@ -587,6 +592,25 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
     if (e != cudaSuccess) return cuda_fail(e, "side branch join");
   }
   return PKD_OK;
+}
+
+// Two work-list units with the same keys: one CTA of the paired-tile kernel.
+struct UnitPair {
+  pkd::TileWork a, b;
+};
+
+// The pairs as the kernel's list, longest key range first: the grid takes
+// them in list order, so the long ones do not start last.
+std::vector<pkd::TileWork> longest_first(std::vector<UnitPair>& pairs) {
+  std::stable_sort(pairs.begin(), pairs.end(),
+                   [](const UnitPair& x, const UnitPair& y) { return x.a.t1 - x.a.t0 > y.a.t1 - y.a.t0; });
+  std::vector<pkd::TileWork> w;
+  w.reserve(2 * pairs.size());
+  for (const UnitPair& q : pairs) {
+    w.push_back(q.a);
+    w.push_back(q.b);
+  }
+  return w;
 }
 
 // Upload work-list units into the workspace's work region: copied into the
@@ -855,7 +879,8 @@ pkd_status pkd_plan_tree(pkd_plan_t plan, int num_levels, const int32_t* const* 
     }
   }
   // key-range pieces per level: one target unit length (in 128-key tiles) for
-  // the whole launch, the work of all levels over about two waves of CTAs,
+  // the whole launch, the work of all levels (CTA-tiles, a CTA per pair of
+  // query tiles) over about one wave of CTAs,
   // and each level cut into the pieces its longest node needs for it, within
   // the plan's piece budget (each level keeps one)
   const int sms = plan->G / pkd::kCtasPerSm;
@@ -867,11 +892,11 @@ pkd_status pkd_plan_tree(pkd_plan_t plan, int num_levels, const int32_t* const* 
     for (int n = 0; n < h_num_nodes[l]; ++n) {
       const int pages = ki[n + 1] - ki[n];
       const int64_t len = pages > 0 ? static_cast<int64_t>(pages - 1) * P + lp[n] : 0;
-      work += static_cast<int64_t>((ri[n + 1] - ri[n] + per_tile - 1) / per_tile) * ((len + 127) / 128);
+      work += static_cast<int64_t>((ri[n + 1] - ri[n] + 2 * per_tile - 1) / (2 * per_tile)) * ((len + 127) / 128);
     }
   }
   work *= plan->hk;
-  const int64_t target = (work + 2 * sms - 1) / (2 * sms) > 2 ? (work + 2 * sms - 1) / (2 * sms) : 2;
+  const int64_t target = (work + sms - 1) / sms > 2 ? (work + sms - 1) / sms : 2;
   std::vector<int> S(num_levels, 1);
   int budget = plan->max_splits;
   for (int l = 0; l < num_levels; ++l) {
@@ -881,7 +906,10 @@ pkd_status pkd_plan_tree(pkd_plan_t plan, int num_levels, const int32_t* const* 
     S[l] = want > cap ? cap : want;
     budget -= S[l];
   }
-  std::vector<pkd::TileWork> w;
+  // units in pairs (two query tiles of one node with the same keys: one CTA
+  // per pair and kv head); a node's lone last tile is paired with a tile
+  // without rows, which the kernel skips
+  std::vector<UnitPair> pairs;
   int piece = 0;
   for (int l = 0; l < num_levels; ++l) {
     const int32_t* ri = h_req_indptr[l];
@@ -892,7 +920,7 @@ pkd_status pkd_plan_tree(pkd_plan_t plan, int num_levels, const int32_t* const* 
       const int len = pages > 0 ? (pages - 1) * P + lp[n] : 0;
       const int tiles = (len + 127) / 128;
       const int tps = tiles > 0 ? (tiles + S[l] - 1) / S[l] : 0;
-      for (int r0 = ri[n]; r0 < ri[n + 1]; r0 += per_tile) {
+      for (int r0 = ri[n]; r0 < ri[n + 1]; r0 += 2 * per_tile) {
         for (int sp = 0; sp < S[l]; ++sp) {
           pkd::TileWork t{};
           t.q0 = r0;
@@ -904,12 +932,15 @@ pkd_status pkd_plan_tree(pkd_plan_t plan, int num_levels, const int32_t* const* 
           t.piece = piece + sp;  // every piece of every request is written (empty ranges as empty states)
           t.level = l;
           t.diag = pkd::kNoCausal;
-          w.push_back(t);
+          pkd::TileWork u = t;
+          u.q0 = r0 + per_tile < ri[n + 1] ? r0 + per_tile : ri[n + 1];
+          pairs.push_back({t, u});
         }
       }
     }
     piece += S[l];
   }
+  std::vector<pkd::TileWork> w = longest_first(pairs);
   s = upload_work(plan, w, static_cast<cudaStream_t>(stream));
   if (s != PKD_OK) return s;
   for (int l = 0; l < pkd::kMaxTreeLevels; ++l) plan->level_pages[l] = l < num_levels ? d_kv_page_indices[l] : nullptr;
@@ -963,7 +994,7 @@ pkd_status pkd_plan_prefill(pkd_plan_t plan, const int32_t* h_qo_indptr, const i
   if (h_qo_indptr[0] != 0 || h_kv_indptr[0] != 0) return fail(PKD_ERR_INVALID_ARG, "indptr[0] must be 0");
   if (h_kv_indptr[batch] > 0 && !d_kv_page_indices) return fail(PKD_ERR_INVALID_ARG, "d_kv_page_indices is NULL");
   const int per_tile = 128 / g;  // query tokens per 128-row tile
-  std::vector<pkd::TileWork> w;
+  std::vector<UnitPair> pairs;
   for (int r = 0; r < batch; ++r) {
     const int q_len = h_qo_indptr[r + 1] - h_qo_indptr[r];
     const int pages = h_kv_indptr[r + 1] - h_kv_indptr[r];
@@ -979,27 +1010,28 @@ pkd_status pkd_plan_prefill(pkd_plan_t plan, const int32_t* h_qo_indptr, const i
                   "the cache)", r, q_len, kv_len);
     const int q0 = h_qo_indptr[r], q_end = h_qo_indptr[r + 1];
     const int diag = kv_len - q_len - q0;  // token q sits at position q + diag
-    // query tiles in pairs (a cluster of two CTAs sharing every key tile by
-    // multicast): both take the key tiles the later tile's last row sees; a
-    // lone last tile is paired with a helper whose rows are all past the end
+    // query tiles in pairs (one CTA for both, every key tile read once for
+    // 256 rows): both take the key tiles the later tile's last row sees; a
+    // lone last tile is paired with a tile without rows, which the kernel skips
     for (int a = q0; a < q_end; a += 2 * per_tile) {
       const int last_tok = (a + 2 * per_tile < q_end ? a + 2 * per_tile : q_end) - 1;
       const int keys = causal ? last_tok + diag + 1 : kv_len;  // keys the pair's last row sees
-      for (int k = 0; k < 2; ++k) {
-        pkd::TileWork t{};
-        t.q0 = a + k * per_tile < q_end ? a + k * per_tile : q_end;
-        t.q_end = q_end;
-        t.page_begin = h_kv_indptr[r];
-        t.kv_len = kv_len;
-        t.t0 = 0;
-        t.t1 = (keys + 127) / 128;
-        t.piece = -1;
-        t.level = 0;
-        t.diag = causal ? diag : pkd::kNoCausal;
-        w.push_back(t);
-      }
+      pkd::TileWork t{};
+      t.q0 = a;
+      t.q_end = q_end;
+      t.page_begin = h_kv_indptr[r];
+      t.kv_len = kv_len;
+      t.t0 = 0;
+      t.t1 = (keys + 127) / 128;
+      t.piece = -1;
+      t.level = 0;
+      t.diag = causal ? diag : pkd::kNoCausal;
+      pkd::TileWork u = t;
+      u.q0 = a + per_tile < q_end ? a + per_tile : q_end;
+      pairs.push_back({t, u});
     }
   }
+  std::vector<pkd::TileWork> w = longest_first(pairs);
   if (!plan->err_word_zeroed) {  // a plan used for prefill only: the first plan clears the error word
     cudaError_t ez = cudaMemsetAsync(plan->ws, 0, 4, static_cast<cudaStream_t>(stream));
     if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync(error word)");
@@ -1032,14 +1064,13 @@ pkd_status pkd_prefill_run(pkd_plan_t plan, const void* d_q, const void* d_k_cac
   s = tile_kv_maps(plan, plan->pf_dtype, P, d_k_cache, d_v_cache, num_pages, page_stride_elems, &tmk, &tmv);
   if (s != PKD_OK) return s;
   pkd::PrefixParams pp = tile_params(plan, P, num_pages, sm_scale);
-  pp.cluster = 2;  // the units come in pairs of query tiles that share their key tiles
   pp.batch = plan->pf_tokens;
   pp.out = d_out;
   pp.lse = d_lse;
   pp.out_dtype = plan->pf_dtype;
   // not programmatic: the kernel reads K/V that the previous launch on the
   // stream (an append) may have written
-  cudaError_t e = pkd::launch_prefix(tmq, tmk, tmv, pp, plan->pf_dtype, static_cast<cudaStream_t>(stream), false);
+  cudaError_t e = pkd::launch_tile2(tmq, tmk, tmv, pp, plan->pf_dtype, static_cast<cudaStream_t>(stream), false);
   if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
   return PKD_OK;
 }

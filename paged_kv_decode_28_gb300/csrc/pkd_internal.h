@@ -133,8 +133,9 @@ struct PrefixParams {
   const float* v_scale;
   unsigned* err;
   int kv_hnd;               // pages are [Hk, P, D] (HND) instead of [P, Hk, D] (NHD)
-  // work-list mode (cluster 1): CTA x takes kv head x / n_work of unit
-  // work[x % n_work]; pieces are pre_o[piece][row][D] with rows_per_piece rows
+  // work-list mode (pkd_tile2.cu): the units come in pairs with the same keys;
+  // CTA x takes kv head x % Hk of units work[2 (x / Hk)] and work[2 (x / Hk) + 1];
+  // pieces are pre_o[piece][row][D] with rows_per_piece rows
   const TileWork* work;
   int n_work;
   int rows_per_piece;       // query rows (tokens or requests times Hq) per piece
@@ -207,8 +208,12 @@ cudaError_t launch_merge_states(const void* v, const float* s, int64_t n, int k,
                                 int dtype, void* vo, float* so, cudaStream_t stream);
 cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                           const PrefixParams& p, int kv_dtype, cudaStream_t stream, bool pdl);
+// work-list units in pairs (p.work, p.n_work even): one CTA per pair and kv head
+cudaError_t launch_tile2(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                         const PrefixParams& p, int kv_dtype, cudaStream_t stream, bool pdl);
 int decode_smem_bytes(int kv_dtype);
 int prefix_smem_bytes();
+int tile2_smem_bytes();
 int prefix_max_active_clusters(int cluster);  // 0 if the query fails
 
 }  // namespace pkd

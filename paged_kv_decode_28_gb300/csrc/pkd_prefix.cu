@@ -1,6 +1,6 @@
 // pkd_prefix.cu -- tile attention on the sm_103a tensor cores (tcgen05 +
 // TMEM): a 128-row query tile of one kv head against a range of 128-key tiles
-// of one page list.  It serves three paths.
+// of the shared prefix's page list.
 //
 // Cascade decode attends one shared prefix for every request and merges that
 // state with each request's own (2026 guide, "Cascade attention for shared
@@ -12,11 +12,8 @@
 // writes an fp32 partial state (o, base-2 lse) per row; the merge pass folds
 // these partials into each request's suffix states.
 //
-// In work-list mode (params.work) each CTA's unit comes from a host-built list
-// (TileWork): the nodes of a prefix tree's shared levels (each node's request
-// range against its page list, partial states per key-range piece), or the
-// query tiles of paged prefill (a request's new tokens against its pages, the
-// causal mask aligned to the end of the sequence, output written directly).
+// (The prefix tree's levels and paged prefill are work lists of query tiles in
+// pairs, run by the paired-tile kernel of pkd_tile2.cu.)
 //
 // CTAs run in clusters of C (1, 2, 4 or 8): the C query tiles of one kv head
 // and key range read the same K/V tiles, so each CTA fetches 1/C of every
@@ -122,44 +119,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int C = p.cluster;
   const int rank = static_cast<int>(ptx::cluster_ctarank());
   const uint16_t cta_mask = static_cast<uint16_t>((1u << C) - 1u);
-  // this CTA's unit: kv head h, query row-tokens from b0 (rows past row_end
-  // are not written), keys of `pages` (kv_len of them) in tiles t0 .. t0+n-1,
-  // output piece (or -1: final output), causal offset
-  int h, b0, row_end, kv_len, t0, n, piece, diag;
-  const int* pages;
-  if (p.work != nullptr) {
-    const int wi = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_work));
-    h = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_work));
-    const int4* wp = reinterpret_cast<const int4*>(p.work + wi);
-    const int4 wa = __ldg(wp), wb = __ldg(wp + 1), wc = __ldg(wp + 2);
-    b0 = wa.x;
-    row_end = wa.y;
-    kv_len = wa.w;
-    const int lv = wb.w;
-    pages = (lv == 0 ? p.level_pages[0] : lv == 1 ? p.level_pages[1] : lv == 2 ? p.level_pages[2]
-                                                                                : p.level_pages[3]) + wa.z;
-    t0 = wb.x;
-    n = max(min(wb.y, (kv_len + kKeys - 1) / kKeys) - t0, 0);
-    piece = wb.z;
-    diag = wc.x;
-  } else {
-    // blockIdx.x = ((h * n_splits + split) * m_groups + mgroup) * C + rank
-    const int cl = blockIdx.x / C;
-    const int mgroup = cl % p.m_groups;
-    const int hs = cl / p.m_groups;
-    const int split = hs % p.n_splits;
-    h = hs / p.n_splits;
-    const int mt = mgroup * C + rank;  // may pass m_tiles: such a CTA only helps load
-    b0 = mt * (kRows / G);
-    row_end = p.batch;
-    kv_len = p.prefix_len;
-    pages = p.prefix_pages;
-    const int n_tiles_all = (kv_len + kKeys - 1) / kKeys;
-    t0 = split * p.tiles_per_split;
-    n = max(min(t0 + p.tiles_per_split, n_tiles_all) - t0, 0);
-    piece = split;
-    diag = kNoCausal;
-  }
+  // this CTA's unit: kv head h, query rows from request b0 (requests past
+  // the batch are not written), prefix keys in tiles t0 .. t0+n-1, piece
+  // `split`; blockIdx.x = ((h * n_splits + split) * m_groups + mgroup) * C + rank
+  const int cl = blockIdx.x / C;
+  const int mgroup = cl % p.m_groups;
+  const int hs = cl / p.m_groups;
+  const int split = hs % p.n_splits;
+  const int h = hs / p.n_splits;
+  const int mt = mgroup * C + rank;  // may pass m_tiles: such a CTA only helps load
+  const int b0 = mt * (kRows / G);
+  const int row_end = p.batch;
+  const int kv_len = p.prefix_len;
+  const int* pages = p.prefix_pages;
+  const int n_tiles_all = (kv_len + kKeys - 1) / kKeys;
+  const int t0 = split * p.tiles_per_split;
+  const int n = max(min(t0 + p.tiles_per_split, n_tiles_all) - t0, 0);
+  const int piece = split;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(B_Q), 1);
@@ -331,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    // this thread's query row: token (or request) tok, qo head h * G + jj
+    // this thread's query row: request tok, qo head h * G + jj
     const int tok = b0 + row / G;
     const int jj = row - (row / G) * G;
     // Each iteration passes the pair's named barrier exactly twice, also after
@@ -353,12 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int key0 = (t0 + i) * kKeys;
       const int nv = min(kKeys, kv_len - key0);
-      // keys this row sees: those before the list's end and, for a causal
-      // unit, at or before the row's position tok + diag (units that mask
-      // start at key 0, so every row of theirs sees key 0 in its first tile);
-      // vr counts them within this thread's half
-      const int vrow = diag == kNoCausal ? nv : max(0, min(nv, tok + diag + 1 - key0));
-      const int vr = min(max(vrow - 64 * hf, 0), 64);
+      // the tile's keys before the prefix's end, counted within this thread's half
+      const int vr = min(max(nv - 64 * hf, 0), 64);
       // mask, then a tree max of the raw scores (the scale is positive, so it
       // commutes with max): 8 independent chains, then the other half's
       float m8[8];
@@ -427,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       if (nv < kKeys) {
-        // keys past the list's end: their P is 0, and their V rows must be
+        // keys past the prefix's end: their P is 0, and their V rows must be
         // finite for the product, so zero them (each half one column half)
         // once the tile's V has landed
         if (!warp_wait(bar(B_VF + i % kStages), (i / kStages) & 1, p.err, abort_flag)) {
@@ -446,14 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(B_PF + u));
     }
-    // ---- epilogue: o = O / l, lse2 = m_ref + log2(l); into piece `piece`
-    // as an fp32 partial state, or (piece < 0) as the final out / lse; each
-    // half writes its 64 columns, the first half the lse
+    // ---- epilogue: o = O / l, lse2 = m_ref + log2(l) into piece `piece` as
+    // an fp32 partial state; each half writes its 64 columns, the first half
+    // the lse
     const bool row_valid = tok < row_end;
     const size_t orow = static_cast<size_t>(tok) * Hq + h * G + jj;
-    const size_t sidx = static_cast<size_t>(piece < 0 ? 0 : piece) * p.rows_per_piece + orow;
+    const size_t sidx = static_cast<size_t>(piece) * p.rows_per_piece + orow;
     float* dst = p.pre_o + sidx * kHeadDim + 64 * hf;
-    uint16_t* fdst = static_cast<uint16_t*>(p.out) + orow * kHeadDim + 64 * hf;
     // the row sum is the two halves' partial sums (every thread arrives here,
     // also after a failed wait, so the barrier is always complete)
     xchg[hf * kRows + row] = l;
@@ -467,33 +438,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t o[32];
         ptx::tmem_ld32(tmem + lanes + kColO + 64 * hf + 32 * c, o);
         ptx::tmem_ld_wait();
-        if (row_valid && piece >= 0) {
+        if (row_valid) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             float4 v = make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
                                    __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
             *reinterpret_cast<float4*>(dst + 32 * c + e) = v;
           }
-        } else if (row_valid) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 v;
-            v.x = ptx::pack2<BF>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-            v.y = ptx::pack2<BF>(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-            v.z = ptx::pack2<BF>(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-            v.w = ptx::pack2<BF>(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-            *reinterpret_cast<uint4*>(fdst + 32 * c + e) = v;
-          }
         }
       }
-      if (hf == 0 && row_valid && piece >= 0) p.pre_lse[sidx] = m_ref + ptx::lg2(l);
-      if (hf == 0 && row_valid && piece < 0 && p.lse) p.lse[orow] = (m_ref + ptx::lg2(l)) * 0.6931471805599453f;
-    } else if (row_valid && piece >= 0) {
+      if (hf == 0 && row_valid) p.pre_lse[sidx] = m_ref + ptx::lg2(l);
+    } else if (row_valid) {
       for (int d = 0; d < 64; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
       if (hf == 0) p.pre_lse[sidx] = -INFINITY;
-    } else if (row_valid) {
-      for (int d = 0; d < 64; d += 8) *reinterpret_cast<uint4*>(fdst + d) = make_uint4(0u, 0u, 0u, 0u);
-      if (hf == 0 && p.lse) p.lse[orow] = -INFINITY;
     }
   }
   ptx::tc_fence_before();
@@ -538,7 +495,7 @@ int prefix_max_active_clusters(int cluster) {
 
 cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                           const PrefixParams& p, int kv_dtype, cudaStream_t stream, bool pdl) {
-  const int grid = p.work != nullptr ? p.num_kv_heads * p.n_work : p.num_kv_heads * p.n_splits * p.m_groups * p.cluster;
+  const int grid = p.num_kv_heads * p.n_splits * p.m_groups * p.cluster;
   if (grid <= 0) return cudaSuccess;
   if (kv_dtype != kBF16 && kv_dtype != kF16) return cudaErrorInvalidValue;
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, PrefixParams) =
