@@ -324,6 +324,14 @@ def run_ours(args, world, rank, local):
     nbytes = algorithmic_bytes(b)
     value = world * nbytes / (ms_step * 1e-3) / 1e9
     assert plan.check_device_errors() == 0
+    # host time of one plan (the schedule for this batch into pinned memory),
+    # timed on its own after the timed steps
+    plan_s = []
+    for _ in range(min(K, 50)):
+        t0 = time.perf_counter()
+        do_plan()
+        plan_s.append(time.perf_counter() - t0)
+    torch.cuda.synchronize()
 
     # ---- end to end through the C ABI with host buffers: q and the page table in, out and lse back
     q_h = b.q.cpu().pin_memory()
@@ -378,6 +386,7 @@ def run_ours(args, world, rank, local):
         "ms_per_step": round(ms_step, 5),
         "us_per_call": round(ms_step * 1e3, 2),
         "tokens_per_s": round(world * b.batch / (ms_step * 1e-3), 1),
+        "host_plan_us": round(statistics.median(plan_s) * 1e6, 1),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -408,6 +417,8 @@ def run_ours(args, world, rank, local):
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
             "kernel_us": round(kern_avg_ms * 1e3, 2),
+            # spread of the per-step decode launch (events around each launch)
+            "kernel_us_p10_p50_p90": [round(float(x) * 1e3, 2) for x in np.percentile(kern_ms, [10, 50, 90])],
         },
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "us_per_step": round(e2e_s / K * 1e6, 2)},
