@@ -43,6 +43,9 @@ KERNEL_SOURCES = ["paged_kv_decode_28_gb300/csrc/pkd_decode.cu", "paged_kv_decod
                   "paged_kv_decode_28_gb300/csrc/pkd_internal.h"]
 APPEND_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "append_traffic.json")
 APPEND_SOURCES = ["paged_kv_decode_28_gb300/csrc/pkd_append.cu", "paged_kv_decode_28_gb300/csrc/pkd_internal.h"]
+PREFILL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "prefill_traffic.json")
+PREFILL_SOURCES = ["paged_kv_decode_28_gb300/csrc/pkd_tile2.cu", "paged_kv_decode_28_gb300/csrc/pkd_ptx.cuh",
+                   "paged_kv_decode_28_gb300/csrc/pkd_internal.h"]
 
 
 def parse_args():
@@ -842,6 +845,17 @@ def run_prefill(args, world, rank, local):
     assert plan.check_device_errors() == 0
     flops = prefill_flops(b)
     achieved = flops / (ms_step * 1e-3) / 1e12
+    # DRAM bytes of one launch from an ncu capture of the same kernel source on
+    # the same workload (null for another source or another batch)
+    traffic = None
+    try:
+        with open(PREFILL_TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_hash") == kernel_hash(PREFILL_SOURCES) and tr.get("workload") == b.name and \
+                int(tr.get("query_tokens", -1)) == int(b.q.shape[0]):
+            traffic = int(tr["dram_bytes_per_launch"])
+    except Exception:
+        pass
     peak, peak_kind = measured_tensor_peak()
     e = b.k_cache.element_size()
     nbytes = (int(np.asarray(b.kv_lens, np.int64).sum()) * b.num_kv_heads * b.head_dim * 2 * e
@@ -875,7 +889,7 @@ def run_prefill(args, world, rank, local):
         "roofline": {"bound": "tensor", "kernel": "pkd tile2_kernel (paired query tiles)", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, burst)"
                      if peak_kind == "measured" else "fallback", "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
                      "hbm_gbs": round(nbytes / (ms_step * 1e-3) / 1e9, 1)},
         "cpu_baseline": cpu, "gpu_launches": K, "clocks": clk,
     }
