@@ -486,6 +486,37 @@ pkd_status pkd_plan_host(const int32_t* h_kv_indptr, const int32_t* h_kv_last_pa
                          int max_items, int32_t* cta_item_begin, int32_t* row_item_begin,
                          int32_t* row_item_count, int32_t* merge_rows, int32_t* counts);
 
+/*
+ * The work lists of pkd_plan_prefill and pkd_plan_tree, built on the host only
+ * (no GPU, no plan), for inspection and testing.  Each unit is 12 int32 in the
+ * order (q0, q_end, page_begin, kv_len, t0, t1, piece, level, diag, 0, 0, 0):
+ * query rows (tokens for prefill, requests for the tree) q0 .. min(q0 + 128/g,
+ * q_end) - 1 of one 128-row tile, keys of the page list starting at entry
+ * page_begin (kv_len of them) in 128-key tiles t0 .. t1 - 1, output piece
+ * (-1: final output) of tree level `level`, causal offset diag (token q sees
+ * keys 0 .. q + diag; 2^31 - 1: every key).  Units 2j and 2j + 1 form one CTA's
+ * pair: the same keys, the second tile's rows following the first's (or
+ * q0 = q_end: no rows); pairs are listed longest key range first.
+ *   units_out   int32 [max_units * 12]; *n_units_out the number of units (also
+ *               when it exceeds max_units, which returns PKD_ERR_CAPACITY_EXCEEDED).
+ * pkd_prefill_units_host takes the arguments of pkd_plan_prefill that shape the
+ * list (num_qo_heads / num_kv_heads a group size dividing 128).
+ * pkd_tree_units_host takes those of pkd_plan_tree plus the plan's batch,
+ * head counts, page size, num_ctas (pkd_num_ctas) and max_prefix_splits;
+ * *n_pieces_out receives the pieces per request row over all levels.
+ * Errors: the statuses pkd_plan_prefill / pkd_plan_tree return for the same
+ * arguments.
+ */
+pkd_status pkd_prefill_units_host(const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
+                                  const int32_t* h_kv_last_page_len, int batch, int num_qo_heads,
+                                  int num_kv_heads, int page_size, int causal, int32_t* units_out, int max_units,
+                                  int* n_units_out);
+pkd_status pkd_tree_units_host(int num_levels, const int32_t* const* h_req_indptr,
+                               const int32_t* const* h_kv_indptr, const int32_t* const* h_kv_last_page_len,
+                               const int32_t* h_num_nodes, int batch, int num_qo_heads, int num_kv_heads,
+                               int page_size, int num_ctas, int max_prefix_splits, int32_t* units_out,
+                               int max_units, int* n_units_out, int* n_pieces_out);
+
 #ifdef __cplusplus
 }
 #endif

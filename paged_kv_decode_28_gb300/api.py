@@ -80,6 +80,9 @@ def lib() -> ctypes.CDLL:
         "pkd_decode_noalloc": (i, [_i32p, _vp, _i32p, i, i, i, i, i, i, i, i, _vp, _vp, _vp, i64, i64, _vp, _vp, f,
                                    _vp, _vp, _vp]),
         "pkd_plan_host": (i, [_i32p, _i32p, i, i, i, i, _i32p, i, _i32p, _i32p, _i32p, _i32p, _i32p]),
+        "pkd_prefill_units_host": (i, [_i32p, _i32p, _i32p, i, i, i, i, i, _i32p, i, ctypes.POINTER(ctypes.c_int)]),
+        "pkd_tree_units_host": (i, [i, _vp, _vp, _vp, _i32p, i, i, i, i, i, i, _i32p, i,
+                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -132,6 +135,63 @@ def workspace_bytes(max_batch: int, num_qo_heads: int, num_kv_heads: int, head_d
     if n == 0:
         raise PkdError(1, "invalid workspace limits")
     return int(n)
+
+
+# fields of one work unit, as pkd_prefill_units_host / pkd_tree_units_host return them
+UNIT_FIELDS = ("q0", "q_end", "page_begin", "kv_len", "t0", "t1", "piece", "level", "diag")
+
+
+def _units_call(fn, n_hint: int) -> np.ndarray:
+    """Call a unit-list export with room for n_hint units, retrying once with
+    the size it reports when that is too small."""
+    n = ctypes.c_int(0)
+    for cap in (max(n_hint, 1), None):
+        cap = cap if cap is not None else max(n.value, 1)
+        buf = np.zeros(cap * 12, np.int32)
+        status = fn(buf, cap, n)
+        if status == 0:
+            return buf[: 12 * n.value].reshape(n.value, 12)[:, :9].copy()
+        if status != 4 or n.value <= cap:  # not a capacity shortfall
+            _check(status)
+    _check(status)
+
+
+def prefill_units(qo_indptr, kv_indptr, kv_last_page_len, num_qo_heads: int, num_kv_heads: int, page_size: int,
+                  causal: bool = True) -> np.ndarray:
+    """The work list pkd_plan_prefill uploads, built on the host (no GPU):
+    int32 [n_units, 9] with the columns of UNIT_FIELDS; units 2j and 2j + 1
+    are one CTA's pair."""
+    qi, ki, la = _host_i32(qo_indptr), _host_i32(kv_indptr), _host_i32(kv_last_page_len)
+    B = len(qi) - 1
+    la_arg = la if len(la) else np.zeros(1, np.int32)
+    return _units_call(lambda buf, cap, n: lib().pkd_prefill_units_host(
+        _as_i32p(qi), _as_i32p(ki), _as_i32p(la_arg), B, num_qo_heads, num_kv_heads, page_size, int(bool(causal)),
+        _as_i32p(buf), cap, ctypes.byref(n)), 2 * (int(qi[-1]) + B + 1))
+
+
+def tree_units(levels, batch: int, num_qo_heads: int, num_kv_heads: int, page_size: int, num_ctas_: int,
+               max_prefix_splits: int):
+    """The work list pkd_plan_tree uploads, built on the host (no GPU), and the
+    number of pieces per request row.  ``levels`` as for Plan.plan_tree but
+    without the page indices: ``(req_indptr, kv_indptr, kv_last_page_len)``."""
+    L = len(levels)
+    ri, ki, lp = (ctypes.c_void_p * max(L, 1))(), (ctypes.c_void_p * max(L, 1))(), (ctypes.c_void_p * max(L, 1))()
+    nn = np.zeros(max(L, 1), np.int32)
+    keep = []
+    for l, (req_indptr, kv_indptr, last) in enumerate(levels):
+        r, k, la = _host_i32(req_indptr), _host_i32(kv_indptr), _host_i32(last)
+        if len(la) == 0:
+            la = np.zeros(1, np.int32)
+        keep += [r, k, la]
+        nn[l] = len(r) - 1
+        ri[l], ki[l], lp[l] = r.ctypes.data, k.ctypes.data, la.ctypes.data
+    pieces = ctypes.c_int(0)
+    hint = 2 * max_prefix_splits * (batch + int(nn[:L].sum()) + 1)
+    units = _units_call(lambda buf, cap, n: lib().pkd_tree_units_host(
+        L, ri, ki, lp, _as_i32p(nn), batch, num_qo_heads, num_kv_heads, page_size, num_ctas_, max_prefix_splits,
+        _as_i32p(buf), cap, ctypes.byref(n), ctypes.byref(pieces)), hint)
+    del keep
+    return units, int(pieces.value)
 
 
 def plan_host(kv_indptr, kv_last_page_len, num_kv_heads: int, page_size: int, num_ctas_: int) -> dict:

@@ -613,6 +613,178 @@ std::vector<pkd::TileWork> longest_first(std::vector<UnitPair>& pairs) {
   return w;
 }
 
+// Prefix-tree work units (host): validates the levels, cuts each level into
+// key-range pieces and pairs each node's 128-row query tiles.  Shared by
+// pkd_plan_tree and the host-only pkd_tree_units_host.
+pkd_status tree_units(int num_levels, const int32_t* const* h_req_indptr, const int32_t* const* h_kv_indptr,
+                      const int32_t* const* h_kv_last_page_len, const int32_t* h_num_nodes, int B, int g,
+                      int num_kv_heads, int P, int sms, int max_splits, std::vector<pkd::TileWork>* w,
+                      int* pieces_out) {
+  if (num_levels < 1 || num_levels > pkd::kMaxTreeLevels)
+    return fail(PKD_ERR_UNSUPPORTED, "num_levels %d outside 1..%d", num_levels, pkd::kMaxTreeLevels);
+  if (!h_req_indptr || !h_kv_indptr || !h_kv_last_page_len || !h_num_nodes)
+    return fail(PKD_ERR_INVALID_ARG, "NULL level array");
+  if (max_splits < num_levels)
+    return fail(PKD_ERR_CAPACITY_EXCEEDED, "the plan was created with max_prefix_splits %d < %d levels",
+                max_splits, num_levels);
+  if (g < 1 || pkd::kHeadDim % g != 0) return fail(PKD_ERR_UNSUPPORTED, "group size %d does not divide 128", g);
+  if (P < 1) return fail(PKD_ERR_INVALID_ARG, "page_size must be >= 1");
+  if (sms < 1) return fail(PKD_ERR_INVALID_ARG, "num_ctas must be >= %d", pkd::kCtasPerSm);
+  const int per_tile = 128 / g;  // requests per 128-row query tile
+  // validate the levels and find each level's longest node (in key tiles)
+  std::vector<int> level_max_tiles(num_levels, 0);
+  for (int l = 0; l < num_levels; ++l) {
+    const int nn = h_num_nodes[l];
+    const int32_t* ri = h_req_indptr[l];
+    const int32_t* ki = h_kv_indptr[l];
+    const int32_t* lp = h_kv_last_page_len[l];
+    if (nn < 1 || !ri || !ki || (!lp && nn > 0)) return fail(PKD_ERR_INVALID_ARG, "level %d: bad node arrays", l);
+    if (ri[0] != 0 || ri[nn] != B) return fail(PKD_ERR_INVALID_ARG, "level %d: nodes must cover requests 0..%d", l, B);
+    if (ki[0] != 0) return fail(PKD_ERR_INVALID_ARG, "level %d: kv_indptr[0] must be 0", l);
+    for (int n = 0; n < nn; ++n) {
+      if (ri[n + 1] < ri[n] || ki[n + 1] < ki[n])
+        return fail(PKD_ERR_INVALID_ARG, "level %d node %d: decreasing indptr", l, n);
+      const int pages = ki[n + 1] - ki[n];
+      if (pages > 0 && (lp[n] < 1 || lp[n] > P))
+        return fail(PKD_ERR_INVALID_ARG, "level %d node %d: last_page_len %d outside 1..%d", l, n, lp[n], P);
+      const int64_t len = pages > 0 ? static_cast<int64_t>(pages - 1) * P + lp[n] : 0;
+      if (len > INT32_MAX - 128) return fail(PKD_ERR_INVALID_ARG, "level %d node %d: too many keys", l, n);
+      const int tiles = static_cast<int>((len + 127) / 128);
+      level_max_tiles[l] = tiles > level_max_tiles[l] ? tiles : level_max_tiles[l];
+    }
+  }
+  // key-range pieces per level: one target unit length (in 128-key tiles) for
+  // the whole launch, the work of all levels (CTA-tiles, a CTA per pair of
+  // query tiles) over about one wave of CTAs,
+  // and each level cut into the pieces its longest node needs for it, within
+  // the plan's piece budget (each level keeps one)
+  int64_t work = 0;  // CTA-tiles with one piece per level
+  for (int l = 0; l < num_levels; ++l) {
+    const int32_t* ri = h_req_indptr[l];
+    const int32_t* ki = h_kv_indptr[l];
+    const int32_t* lp = h_kv_last_page_len[l];
+    for (int n = 0; n < h_num_nodes[l]; ++n) {
+      const int pages = ki[n + 1] - ki[n];
+      const int64_t len = pages > 0 ? static_cast<int64_t>(pages - 1) * P + lp[n] : 0;
+      work += static_cast<int64_t>((ri[n + 1] - ri[n] + 2 * per_tile - 1) / (2 * per_tile)) * ((len + 127) / 128);
+    }
+  }
+  work *= num_kv_heads;
+  const int64_t target = (work + sms - 1) / sms > 2 ? (work + sms - 1) / sms : 2;
+  std::vector<int> S(num_levels, 1);
+  int budget = max_splits;
+  for (int l = 0; l < num_levels; ++l) {
+    int want = static_cast<int>((level_max_tiles[l] + target - 1) / target);
+    want = want < 1 ? 1 : want;
+    const int cap = budget - (num_levels - 1 - l);
+    S[l] = want > cap ? cap : want;
+    budget -= S[l];
+  }
+  // units in pairs (two query tiles of one node with the same keys: one CTA
+  // per pair and kv head); a node's lone last tile is paired with a tile
+  // without rows, which the kernel skips
+  std::vector<UnitPair> pairs;
+  int piece = 0;
+  for (int l = 0; l < num_levels; ++l) {
+    const int32_t* ri = h_req_indptr[l];
+    const int32_t* ki = h_kv_indptr[l];
+    const int32_t* lp = h_kv_last_page_len[l];
+    for (int n = 0; n < h_num_nodes[l]; ++n) {
+      const int pages = ki[n + 1] - ki[n];
+      const int len = pages > 0 ? (pages - 1) * P + lp[n] : 0;
+      const int tiles = (len + 127) / 128;
+      const int tps = tiles > 0 ? (tiles + S[l] - 1) / S[l] : 0;
+      for (int r0 = ri[n]; r0 < ri[n + 1]; r0 += 2 * per_tile) {
+        for (int sp = 0; sp < S[l]; ++sp) {
+          pkd::TileWork t{};
+          t.q0 = r0;
+          t.q_end = ri[n + 1];
+          t.page_begin = ki[n];
+          t.kv_len = len;
+          t.t0 = sp * tps < tiles ? sp * tps : tiles;
+          t.t1 = (sp + 1) * tps < tiles ? (sp + 1) * tps : tiles;
+          t.piece = piece + sp;  // every piece of every request is written (empty ranges as empty states)
+          t.level = l;
+          t.diag = pkd::kNoCausal;
+          pkd::TileWork u = t;
+          u.q0 = r0 + per_tile < ri[n + 1] ? r0 + per_tile : ri[n + 1];
+          pairs.push_back({t, u});
+        }
+      }
+    }
+    piece += S[l];
+  }
+  *w = longest_first(pairs);
+  *pieces_out = piece;
+  return PKD_OK;
+}
+
+// Paged-prefill work units (host): validates the requests and pairs each
+// request's 128-row query tiles.  Shared by pkd_plan_prefill and the
+// host-only pkd_prefill_units_host.
+pkd_status prefill_units(const int32_t* h_qo_indptr, const int32_t* h_kv_indptr, const int32_t* h_kv_last_page_len,
+                         int batch, int g, int page_size, bool causal, std::vector<pkd::TileWork>* w) {
+  if (batch < 0) return fail(PKD_ERR_INVALID_ARG, "batch must be >= 0");
+  if (page_size < 1) return fail(PKD_ERR_INVALID_ARG, "page_size must be >= 1");
+  if (g < 1 || pkd::kHeadDim % g != 0) return fail(PKD_ERR_UNSUPPORTED, "group size %d does not divide 128", g);
+  if (!h_qo_indptr || !h_kv_indptr || (batch > 0 && !h_kv_last_page_len))
+    return fail(PKD_ERR_INVALID_ARG, "NULL host array");
+  if (h_qo_indptr[0] != 0 || h_kv_indptr[0] != 0) return fail(PKD_ERR_INVALID_ARG, "indptr[0] must be 0");
+  const int per_tile = 128 / g;  // query tokens per 128-row tile
+  std::vector<UnitPair> pairs;
+  for (int r = 0; r < batch; ++r) {
+    const int q_len = h_qo_indptr[r + 1] - h_qo_indptr[r];
+    const int pages = h_kv_indptr[r + 1] - h_kv_indptr[r];
+    if (q_len < 0 || pages < 0) return fail(PKD_ERR_INVALID_ARG, "request %d: decreasing indptr", r);
+    if (pages > 0 && (h_kv_last_page_len[r] < 1 || h_kv_last_page_len[r] > page_size))
+      return fail(PKD_ERR_INVALID_ARG, "request %d: last_page_len %d outside 1..%d", r, h_kv_last_page_len[r],
+                  page_size);
+    const int64_t len64 = pages > 0 ? static_cast<int64_t>(pages - 1) * page_size + h_kv_last_page_len[r] : 0;
+    if (len64 > INT32_MAX - 128) return fail(PKD_ERR_INVALID_ARG, "request %d: too many keys", r);
+    const int kv_len = static_cast<int>(len64);
+    if (q_len > kv_len)
+      return fail(PKD_ERR_INVALID_ARG, "request %d: %d query tokens but %d keys (the new tokens' keys are in "
+                  "the cache)", r, q_len, kv_len);
+    const int q0 = h_qo_indptr[r], q_end = h_qo_indptr[r + 1];
+    const int diag = kv_len - q_len - q0;  // token q sits at position q + diag
+    // query tiles in pairs (one CTA for both, every key tile read once for
+    // 256 rows): both take the key tiles the later tile's last row sees; a
+    // lone last tile is paired with a tile without rows, which the kernel skips
+    for (int a = q0; a < q_end; a += 2 * per_tile) {
+      const int last_tok = (a + 2 * per_tile < q_end ? a + 2 * per_tile : q_end) - 1;
+      const int keys = causal ? last_tok + diag + 1 : kv_len;  // keys the pair's last row sees
+      pkd::TileWork t{};
+      t.q0 = a;
+      t.q_end = q_end;
+      t.page_begin = h_kv_indptr[r];
+      t.kv_len = kv_len;
+      t.t0 = 0;
+      t.t1 = (keys + 127) / 128;
+      t.piece = -1;
+      t.level = 0;
+      t.diag = causal ? diag : pkd::kNoCausal;
+      pkd::TileWork u = t;
+      u.q0 = a + per_tile < q_end ? a + per_tile : q_end;
+      pairs.push_back({t, u});
+    }
+  }
+  *w = longest_first(pairs);
+  return PKD_OK;
+}
+
+// Copy a unit list out as int32 [n][12] (TileWork's field order).
+pkd_status export_units(const std::vector<pkd::TileWork>& w, int32_t* units_out, int max_units,
+                               int* n_units_out) {
+  static_assert(sizeof(pkd::TileWork) == 12 * sizeof(int32_t), "a unit is 12 int32");
+  if (!n_units_out) return fail(PKD_ERR_INVALID_ARG, "n_units_out is NULL");
+  *n_units_out = static_cast<int>(w.size());
+  if (static_cast<int64_t>(w.size()) > max_units)
+    return fail(PKD_ERR_CAPACITY_EXCEEDED, "%zu units above max_units %d", w.size(), max_units);
+  if (!w.empty() && !units_out) return fail(PKD_ERR_INVALID_ARG, "units_out is NULL");
+  if (!w.empty()) memcpy(units_out, w.data(), sizeof(pkd::TileWork) * w.size());
+  return PKD_OK;
+}
+
 // Upload work-list units into the workspace's work region: copied into the
 // plan's pinned buffer (after the previous upload from it has finished), then
 // one cudaMemcpyAsync on `st`.
@@ -835,112 +1007,56 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
                     sm_scale, d_out, d_lse, stream, nullptr, &cm);
 }
 
+pkd_status pkd_prefill_units_host(const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
+                                  const int32_t* h_kv_last_page_len, int batch, int num_qo_heads,
+                                  int num_kv_heads, int page_size, int causal, int32_t* units_out, int max_units,
+                                  int* n_units_out) {
+  if (num_kv_heads <= 0 || num_qo_heads <= 0 || num_qo_heads % num_kv_heads != 0)
+    return fail(PKD_ERR_INVALID_ARG, "num_qo_heads must be a positive multiple of num_kv_heads");
+  std::vector<pkd::TileWork> w;
+  pkd_status s = prefill_units(h_qo_indptr, h_kv_indptr, h_kv_last_page_len, batch, num_qo_heads / num_kv_heads,
+                               page_size, causal != 0, &w);
+  if (s != PKD_OK) return s;
+  return export_units(w, units_out, max_units, n_units_out);
+}
+
+pkd_status pkd_tree_units_host(int num_levels, const int32_t* const* h_req_indptr,
+                               const int32_t* const* h_kv_indptr, const int32_t* const* h_kv_last_page_len,
+                               const int32_t* h_num_nodes, int batch, int num_qo_heads, int num_kv_heads,
+                               int page_size, int num_ctas, int max_prefix_splits, int32_t* units_out,
+                               int max_units, int* n_units_out, int* n_pieces_out) {
+  if (num_kv_heads <= 0 || num_qo_heads <= 0 || num_qo_heads % num_kv_heads != 0)
+    return fail(PKD_ERR_INVALID_ARG, "num_qo_heads must be a positive multiple of num_kv_heads");
+  if (batch < 0) return fail(PKD_ERR_INVALID_ARG, "batch must be >= 0");
+  if (!n_pieces_out) return fail(PKD_ERR_INVALID_ARG, "n_pieces_out is NULL");
+  std::vector<pkd::TileWork> w;
+  int pieces = 0;
+  pkd_status s = tree_units(num_levels, h_req_indptr, h_kv_indptr, h_kv_last_page_len, h_num_nodes, batch,
+                            num_qo_heads / num_kv_heads, num_kv_heads, page_size, num_ctas / pkd::kCtasPerSm,
+                            max_prefix_splits, &w, &pieces);
+  if (s != PKD_OK) return s;
+  *n_pieces_out = pieces;
+  return export_units(w, units_out, max_units, n_units_out);
+}
+
 pkd_status pkd_plan_tree(pkd_plan_t plan, int num_levels, const int32_t* const* h_req_indptr,
                          const int32_t* const* h_kv_indptr, const int32_t* const* d_kv_page_indices,
                          const int32_t* const* h_kv_last_page_len, const int32_t* h_num_nodes, void* stream) {
   if (!plan) return fail(PKD_ERR_INVALID_ARG, "plan is NULL");
   if (!plan->planned) return fail(PKD_ERR_NO_PLAN, "pkd_plan_tree needs the requests' own pages planned first");
-  if (num_levels < 1 || num_levels > pkd::kMaxTreeLevels)
-    return fail(PKD_ERR_UNSUPPORTED, "num_levels %d outside 1..%d", num_levels, pkd::kMaxTreeLevels);
-  if (!h_req_indptr || !h_kv_indptr || !d_kv_page_indices || !h_kv_last_page_len || !h_num_nodes)
-    return fail(PKD_ERR_INVALID_ARG, "NULL level array");
-  if (plan->max_splits < num_levels)
-    return fail(PKD_ERR_CAPACITY_EXCEEDED, "the plan was created with max_prefix_splits %d < %d levels",
-                plan->max_splits, num_levels);
   const int g = plan->hq / plan->hk;
   const int P = plan->page_size;
   pkd_status s = check_tile_geometry(plan->q_dtype, plan->kv_dtype, g, P, "prefix-tree decode");
   if (s != PKD_OK) return s;
-  const int B = plan->batch;
-  const int per_tile = 128 / g;  // requests per 128-row query tile
-  // validate the levels and count each level's query tiles and key tiles
-  std::vector<int64_t> level_mtiles(num_levels, 0);
-  std::vector<int> level_max_tiles(num_levels, 0);
-  for (int l = 0; l < num_levels; ++l) {
-    const int nn = h_num_nodes[l];
-    const int32_t* ri = h_req_indptr[l];
-    const int32_t* ki = h_kv_indptr[l];
-    const int32_t* lp = h_kv_last_page_len[l];
-    if (nn < 1 || !ri || !ki || (!lp && nn > 0)) return fail(PKD_ERR_INVALID_ARG, "level %d: bad node arrays", l);
-    if (ri[0] != 0 || ri[nn] != B) return fail(PKD_ERR_INVALID_ARG, "level %d: nodes must cover requests 0..%d", l, B);
-    if (ki[0] != 0) return fail(PKD_ERR_INVALID_ARG, "level %d: kv_indptr[0] must be 0", l);
-    if (ki[nn] > 0 && !d_kv_page_indices[l]) return fail(PKD_ERR_INVALID_ARG, "level %d: page indices NULL", l);
-    for (int n = 0; n < nn; ++n) {
-      if (ri[n + 1] < ri[n] || ki[n + 1] < ki[n])
-        return fail(PKD_ERR_INVALID_ARG, "level %d node %d: decreasing indptr", l, n);
-      const int pages = ki[n + 1] - ki[n];
-      if (pages > 0 && (lp[n] < 1 || lp[n] > P))
-        return fail(PKD_ERR_INVALID_ARG, "level %d node %d: last_page_len %d outside 1..%d", l, n, lp[n], P);
-      const int64_t len = pages > 0 ? static_cast<int64_t>(pages - 1) * P + lp[n] : 0;
-      if (len > INT32_MAX - 128) return fail(PKD_ERR_INVALID_ARG, "level %d node %d: too many keys", l, n);
-      level_mtiles[l] += (ri[n + 1] - ri[n] + per_tile - 1) / per_tile;
-      const int tiles = static_cast<int>((len + 127) / 128);
-      level_max_tiles[l] = tiles > level_max_tiles[l] ? tiles : level_max_tiles[l];
-    }
-  }
-  // key-range pieces per level: one target unit length (in 128-key tiles) for
-  // the whole launch, the work of all levels (CTA-tiles, a CTA per pair of
-  // query tiles) over about one wave of CTAs,
-  // and each level cut into the pieces its longest node needs for it, within
-  // the plan's piece budget (each level keeps one)
-  const int sms = plan->G / pkd::kCtasPerSm;
-  int64_t work = 0;  // CTA-tiles with one piece per level
-  for (int l = 0; l < num_levels; ++l) {
-    const int32_t* ri = h_req_indptr[l];
-    const int32_t* ki = h_kv_indptr[l];
-    const int32_t* lp = h_kv_last_page_len[l];
-    for (int n = 0; n < h_num_nodes[l]; ++n) {
-      const int pages = ki[n + 1] - ki[n];
-      const int64_t len = pages > 0 ? static_cast<int64_t>(pages - 1) * P + lp[n] : 0;
-      work += static_cast<int64_t>((ri[n + 1] - ri[n] + 2 * per_tile - 1) / (2 * per_tile)) * ((len + 127) / 128);
-    }
-  }
-  work *= plan->hk;
-  const int64_t target = (work + sms - 1) / sms > 2 ? (work + sms - 1) / sms : 2;
-  std::vector<int> S(num_levels, 1);
-  int budget = plan->max_splits;
-  for (int l = 0; l < num_levels; ++l) {
-    int want = static_cast<int>((level_max_tiles[l] + target - 1) / target);
-    want = want < 1 ? 1 : want;
-    const int cap = budget - (num_levels - 1 - l);
-    S[l] = want > cap ? cap : want;
-    budget -= S[l];
-  }
-  // units in pairs (two query tiles of one node with the same keys: one CTA
-  // per pair and kv head); a node's lone last tile is paired with a tile
-  // without rows, which the kernel skips
-  std::vector<UnitPair> pairs;
+  std::vector<pkd::TileWork> w;
   int piece = 0;
-  for (int l = 0; l < num_levels; ++l) {
-    const int32_t* ri = h_req_indptr[l];
-    const int32_t* ki = h_kv_indptr[l];
-    const int32_t* lp = h_kv_last_page_len[l];
-    for (int n = 0; n < h_num_nodes[l]; ++n) {
-      const int pages = ki[n + 1] - ki[n];
-      const int len = pages > 0 ? (pages - 1) * P + lp[n] : 0;
-      const int tiles = (len + 127) / 128;
-      const int tps = tiles > 0 ? (tiles + S[l] - 1) / S[l] : 0;
-      for (int r0 = ri[n]; r0 < ri[n + 1]; r0 += 2 * per_tile) {
-        for (int sp = 0; sp < S[l]; ++sp) {
-          pkd::TileWork t{};
-          t.q0 = r0;
-          t.q_end = ri[n + 1];
-          t.page_begin = ki[n];
-          t.kv_len = len;
-          t.t0 = sp * tps < tiles ? sp * tps : tiles;
-          t.t1 = (sp + 1) * tps < tiles ? (sp + 1) * tps : tiles;
-          t.piece = piece + sp;  // every piece of every request is written (empty ranges as empty states)
-          t.level = l;
-          t.diag = pkd::kNoCausal;
-          pkd::TileWork u = t;
-          u.q0 = r0 + per_tile < ri[n + 1] ? r0 + per_tile : ri[n + 1];
-          pairs.push_back({t, u});
-        }
-      }
-    }
-    piece += S[l];
-  }
-  std::vector<pkd::TileWork> w = longest_first(pairs);
+  s = tree_units(num_levels, h_req_indptr, h_kv_indptr, h_kv_last_page_len, h_num_nodes, plan->batch, g, plan->hk,
+                 P, plan->G / pkd::kCtasPerSm, plan->max_splits, &w, &piece);
+  if (s != PKD_OK) return s;
+  if (!d_kv_page_indices) return fail(PKD_ERR_INVALID_ARG, "NULL level array");
+  for (int l = 0; l < num_levels; ++l)
+    if (h_kv_indptr[l][h_num_nodes[l]] > 0 && !d_kv_page_indices[l])
+      return fail(PKD_ERR_INVALID_ARG, "level %d: page indices NULL", l);
   s = upload_work(plan, w, static_cast<cudaStream_t>(stream));
   if (s != PKD_OK) return s;
   for (int l = 0; l < pkd::kMaxTreeLevels; ++l) plan->level_pages[l] = l < num_levels ? d_kv_page_indices[l] : nullptr;
@@ -989,49 +1105,10 @@ pkd_status pkd_plan_prefill(pkd_plan_t plan, const int32_t* h_qo_indptr, const i
   const int g = plan->hq / plan->hk;
   pkd_status s = check_tile_geometry(q_dtype, kv_dtype, g, page_size, "prefill");
   if (s != PKD_OK) return s;
-  if (!h_qo_indptr || !h_kv_indptr || (batch > 0 && !h_kv_last_page_len))
-    return fail(PKD_ERR_INVALID_ARG, "NULL host array");
-  if (h_qo_indptr[0] != 0 || h_kv_indptr[0] != 0) return fail(PKD_ERR_INVALID_ARG, "indptr[0] must be 0");
+  std::vector<pkd::TileWork> w;
+  s = prefill_units(h_qo_indptr, h_kv_indptr, h_kv_last_page_len, batch, g, page_size, causal != 0, &w);
+  if (s != PKD_OK) return s;
   if (h_kv_indptr[batch] > 0 && !d_kv_page_indices) return fail(PKD_ERR_INVALID_ARG, "d_kv_page_indices is NULL");
-  const int per_tile = 128 / g;  // query tokens per 128-row tile
-  std::vector<UnitPair> pairs;
-  for (int r = 0; r < batch; ++r) {
-    const int q_len = h_qo_indptr[r + 1] - h_qo_indptr[r];
-    const int pages = h_kv_indptr[r + 1] - h_kv_indptr[r];
-    if (q_len < 0 || pages < 0) return fail(PKD_ERR_INVALID_ARG, "request %d: decreasing indptr", r);
-    if (pages > 0 && (h_kv_last_page_len[r] < 1 || h_kv_last_page_len[r] > page_size))
-      return fail(PKD_ERR_INVALID_ARG, "request %d: last_page_len %d outside 1..%d", r, h_kv_last_page_len[r],
-                  page_size);
-    const int64_t len64 = pages > 0 ? static_cast<int64_t>(pages - 1) * page_size + h_kv_last_page_len[r] : 0;
-    if (len64 > INT32_MAX - 128) return fail(PKD_ERR_INVALID_ARG, "request %d: too many keys", r);
-    const int kv_len = static_cast<int>(len64);
-    if (q_len > kv_len)
-      return fail(PKD_ERR_INVALID_ARG, "request %d: %d query tokens but %d keys (the new tokens' keys are in "
-                  "the cache)", r, q_len, kv_len);
-    const int q0 = h_qo_indptr[r], q_end = h_qo_indptr[r + 1];
-    const int diag = kv_len - q_len - q0;  // token q sits at position q + diag
-    // query tiles in pairs (one CTA for both, every key tile read once for
-    // 256 rows): both take the key tiles the later tile's last row sees; a
-    // lone last tile is paired with a tile without rows, which the kernel skips
-    for (int a = q0; a < q_end; a += 2 * per_tile) {
-      const int last_tok = (a + 2 * per_tile < q_end ? a + 2 * per_tile : q_end) - 1;
-      const int keys = causal ? last_tok + diag + 1 : kv_len;  // keys the pair's last row sees
-      pkd::TileWork t{};
-      t.q0 = a;
-      t.q_end = q_end;
-      t.page_begin = h_kv_indptr[r];
-      t.kv_len = kv_len;
-      t.t0 = 0;
-      t.t1 = (keys + 127) / 128;
-      t.piece = -1;
-      t.level = 0;
-      t.diag = causal ? diag : pkd::kNoCausal;
-      pkd::TileWork u = t;
-      u.q0 = a + per_tile < q_end ? a + per_tile : q_end;
-      pairs.push_back({t, u});
-    }
-  }
-  std::vector<pkd::TileWork> w = longest_first(pairs);
   if (!plan->err_word_zeroed) {  // a plan used for prefill only: the first plan clears the error word
     cudaError_t ez = cudaMemsetAsync(plan->ws, 0, 4, static_cast<cudaStream_t>(stream));
     if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync(error word)");
