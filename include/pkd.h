@@ -517,6 +517,21 @@ pkd_status pkd_tree_units_host(int num_levels, const int32_t* const* h_req_indpt
                                int page_size, int num_ctas, int max_prefix_splits, int32_t* units_out,
                                int max_units, int* n_units_out, int* n_pieces_out);
 
+/*
+ * The key-range split of pkd_mla_decode, built on the host only (no GPU), for
+ * inspection and testing: units of 12 int32 as above with q0 = request,
+ * q_end = request + 1, t0 .. t1 - 1 in 32-key tiles, piece (-1: the request is
+ * one range, written directly) and level = the half of the 512 output dims
+ * (0, 1); the two halves of a range are adjacent, ranges longest first.
+ *   req_piece_begin_out  int32 [batch + 1]: a cut request's pieces are
+ *                        req_piece_begin[b] .. req_piece_begin[b+1] - 1.
+ * Errors: those of pkd_mla_decode for the same page table and num_sms;
+ * PKD_ERR_CAPACITY_EXCEEDED (with *n_units_out set) above max_units.
+ */
+pkd_status pkd_mla_units_host(const int32_t* h_kv_indptr, const int32_t* h_kv_last_page_len, int batch,
+                              int page_size, int num_sms, int32_t* units_out, int max_units, int* n_units_out,
+                              int32_t* req_piece_begin_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
         "pkd_prefill_units_host": (i, [_i32p, _i32p, _i32p, i, i, i, i, i, _i32p, i, ctypes.POINTER(ctypes.c_int)]),
         "pkd_tree_units_host": (i, [i, _vp, _vp, _vp, _i32p, i, i, i, i, i, i, _i32p, i,
                                     ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+        "pkd_mla_units_host": (i, [_i32p, _i32p, i, i, i, _i32p, i, ctypes.POINTER(ctypes.c_int), _i32p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -192,6 +193,20 @@ def tree_units(levels, batch: int, num_qo_heads: int, num_kv_heads: int, page_si
         _as_i32p(buf), cap, ctypes.byref(n), ctypes.byref(pieces)), hint)
     del keep
     return units, int(pieces.value)
+
+
+def mla_units(kv_indptr, kv_last_page_len, page_size: int, num_sms: int):
+    """The key-range split of mla_decode, built on the host (no GPU): units
+    int32 [n_units, 9] (UNIT_FIELDS; t0/t1 in 32-key tiles, level = output
+    half) and the cut requests' piece ranges int32 [batch + 1]."""
+    ki, la = _host_i32(kv_indptr), _host_i32(kv_last_page_len)
+    B = len(ki) - 1
+    la_arg = la if len(la) else np.zeros(1, np.int32)
+    rpb = np.zeros(B + 1, np.int32)
+    units = _units_call(lambda buf, cap, n: lib().pkd_mla_units_host(
+        _as_i32p(ki), _as_i32p(la_arg), B, page_size, num_sms, _as_i32p(buf), cap, ctypes.byref(n),
+        _as_i32p(rpb)), 2 * (B + num_sms))
+    return units, rpb
 
 
 def plan_host(kv_indptr, kv_last_page_len, num_kv_heads: int, page_size: int, num_ctas_: int) -> dict:

@@ -1,6 +1,8 @@
 // pkd_mla_capi.cu -- the C entry points of multi-latent attention decode
 // (declared in include/pkd.h): argument checks, the key-range split, the unit
 // upload, tensor maps and the launch of the kernels in pkd_mla.cu.
+#include <string.h>
+
 #include <algorithm>
 #include <cmath>
 #include <vector>
@@ -15,44 +17,23 @@ using pkd::host::cuda_fail;
 using pkd::host::fail;
 using pkd::host::get_encode;
 
-extern "C" {
+namespace {
 
-size_t pkd_mla_workspace_bytes(int max_batch, int num_heads, int num_sms) {
-  if (max_batch <= 0 || num_heads <= 0 || num_heads > 128 || num_sms <= 0) return 0;
-  const size_t pieces = static_cast<size_t>(max_batch) + num_sms;
-  const size_t units = 2 * pieces;
-  size_t off = 256;  // error word
-  off += align256(sizeof(pkd::TileWork) * units);
-  off += align256(4ull * (max_batch + 1));
-  off += align256(4ull * pieces * num_heads * 512);
-  off += align256(4ull * pieces * num_heads);
-  return off;
-}
-
-pkd_status pkd_mla_decode(const void* d_q_nope, const void* d_q_pe, const void* d_ckv_cache,
-                          const void* d_kpe_cache, const int32_t* h_kv_indptr, const int32_t* d_kv_page_indices,
-                          const int32_t* h_kv_last_page_len, int batch, int num_heads, int page_size,
-                          int64_t num_pages, int64_t ckv_page_stride_elems, int64_t kpe_page_stride_elems,
-                          float sm_scale, void* d_out, float* d_lse, void* d_workspace, size_t workspace_bytes,
-                          int num_sms, void* stream) {
-  if (batch < 0 || num_heads <= 0 || num_heads > 128)
-    return fail(PKD_ERR_UNSUPPORTED, "num_heads %d outside 1..128 (batch %d)", num_heads, batch);
-  if (!(page_size >= 1 && ((page_size <= 32 && 32 % page_size == 0) || page_size % 32 == 0)))
-    return fail(PKD_ERR_UNSUPPORTED, "page_size %d: a divisor of 32 or a multiple of 32", page_size);
+// MLA work units (host): validates the page table, cuts the requests into
+// key ranges and lists two units per range (one per half of the 512 output
+// dims, adjacent), longest first; rpb[b] .. rpb[b+1]-1 are the partial-state
+// pieces of a request that was cut (none for one written directly).  Shared by
+// pkd_mla_decode and the host-only pkd_mla_units_host.
+pkd_status mla_units(const int32_t* h_kv_indptr, const int32_t* h_kv_last_page_len, int batch, int page_size,
+                     int num_sms, std::vector<pkd::TileWork>* w_out, std::vector<int32_t>* rpb_out,
+                     bool* any_split_out) {
+  if (batch < 0) return fail(PKD_ERR_INVALID_ARG, "batch must be >= 0");
+  if (page_size < 1) return fail(PKD_ERR_INVALID_ARG, "page_size must be >= 1");
   if (num_sms <= 0) return fail(PKD_ERR_INVALID_ARG, "num_sms must be > 0");
-  const size_t need = pkd_mla_workspace_bytes(batch > 0 ? batch : 1, num_heads, num_sms);
-  if (!d_workspace || workspace_bytes < need || !aligned16(d_workspace))
-    return fail(PKD_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, need %zu (16-byte aligned)", workspace_bytes,
-                need);
-  if (batch == 0) return PKD_OK;
-  if (!h_kv_indptr || !h_kv_last_page_len || !d_q_nope || !d_q_pe || !d_out)
-    return fail(PKD_ERR_INVALID_ARG, "NULL argument");
-  if (!aligned16(d_q_nope) || !aligned16(d_q_pe) || !aligned16(d_out))
-    return fail(PKD_ERR_INVALID_ARG, "q / out must be 16-byte aligned");
+  if (!h_kv_indptr || (batch > 0 && !h_kv_last_page_len)) return fail(PKD_ERR_INVALID_ARG, "NULL argument");
   if (h_kv_indptr[0] != 0) return fail(PKD_ERR_INVALID_ARG, "kv_indptr[0] must be 0");
   const int P = page_size;
   std::vector<int> lens(batch);
-  int64_t total = 0;
   for (int b = 0; b < batch; ++b) {
     const int pages = h_kv_indptr[b + 1] - h_kv_indptr[b];
     if (pages < 0) return fail(PKD_ERR_INVALID_ARG, "decreasing kv_indptr at %d", b);
@@ -61,16 +42,6 @@ pkd_status pkd_mla_decode(const void* d_q_nope, const void* d_q_pe, const void* 
     const int64_t L = pages > 0 ? static_cast<int64_t>(pages - 1) * P + h_kv_last_page_len[b] : 0;
     if (L > INT32_MAX - 64) return fail(PKD_ERR_INVALID_ARG, "request %d: too many keys", b);
     lens[b] = static_cast<int>(L);
-    total += L;
-  }
-  if (h_kv_indptr[batch] > 0) {
-    if (!d_kv_page_indices || !d_ckv_cache || !d_kpe_cache) return fail(PKD_ERR_INVALID_ARG, "NULL cache");
-    if (!aligned16(d_ckv_cache) || !aligned16(d_kpe_cache))
-      return fail(PKD_ERR_INVALID_ARG, "caches must be 16-byte aligned");
-    if (num_pages <= 0 || num_pages > INT32_MAX) return fail(PKD_ERR_INVALID_ARG, "num_pages out of range");
-    if ((ckv_page_stride_elems * 2) % 16 || ckv_page_stride_elems < static_cast<int64_t>(P) * 512 ||
-        (kpe_page_stride_elems * 2) % 16 || kpe_page_stride_elems < static_cast<int64_t>(P) * 64)
-      return fail(PKD_ERR_INVALID_ARG, "page strides must cover a page and be 16-byte multiples");
   }
   // key ranges: the smallest piece size C (in 32-key tiles, at least 16 =
   // 512 keys) for which cutting every request into pieces of at most C tiles
@@ -95,8 +66,10 @@ pkd_status pkd_mla_decode(const void* d_q_nope, const void* d_q_pe, const void* 
     if (pieces_for(mid) <= num_sms) hi = mid; else lo = mid + 1;
   }
   const int C = lo < 16 ? 16 : lo;
-  std::vector<pkd::TileWork> w;
-  std::vector<int32_t> rpb(batch + 1, 0);
+  std::vector<pkd::TileWork>& w = *w_out;
+  w.clear();
+  std::vector<int32_t>& rpb = *rpb_out;
+  rpb.assign(batch + 1, 0);
   int piece = 0;
   bool any_split = false;
   for (int b = 0; b < batch; ++b) {
@@ -128,6 +101,80 @@ pkd_status pkd_mla_decode(const void* d_q_nope, const void* d_q_pe, const void* 
   std::stable_sort(w.begin(), w.end(), [](const pkd::TileWork& x, const pkd::TileWork& y) {
     return (x.t1 - x.t0) > (y.t1 - y.t0);
   });
+  *any_split_out = any_split;
+  return PKD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkd_mla_workspace_bytes(int max_batch, int num_heads, int num_sms) {
+  if (max_batch <= 0 || num_heads <= 0 || num_heads > 128 || num_sms <= 0) return 0;
+  const size_t pieces = static_cast<size_t>(max_batch) + num_sms;
+  const size_t units = 2 * pieces;
+  size_t off = 256;  // error word
+  off += align256(sizeof(pkd::TileWork) * units);
+  off += align256(4ull * (max_batch + 1));
+  off += align256(4ull * pieces * num_heads * 512);
+  off += align256(4ull * pieces * num_heads);
+  return off;
+}
+
+pkd_status pkd_mla_units_host(const int32_t* h_kv_indptr, const int32_t* h_kv_last_page_len, int batch,
+                              int page_size, int num_sms, int32_t* units_out, int max_units, int* n_units_out,
+                              int32_t* req_piece_begin_out) {
+  static_assert(sizeof(pkd::TileWork) == 12 * sizeof(int32_t), "a unit is 12 int32");
+  if (!n_units_out || !req_piece_begin_out) return fail(PKD_ERR_INVALID_ARG, "NULL output");
+  std::vector<pkd::TileWork> w;
+  std::vector<int32_t> rpb;
+  bool any_split = false;
+  pkd_status s = mla_units(h_kv_indptr, h_kv_last_page_len, batch, page_size, num_sms, &w, &rpb, &any_split);
+  if (s != PKD_OK) return s;
+  *n_units_out = static_cast<int>(w.size());
+  if (static_cast<int64_t>(w.size()) > max_units)
+    return fail(PKD_ERR_CAPACITY_EXCEEDED, "%zu units above max_units %d", w.size(), max_units);
+  if (!w.empty() && !units_out) return fail(PKD_ERR_INVALID_ARG, "units_out is NULL");
+  if (!w.empty()) memcpy(units_out, w.data(), sizeof(pkd::TileWork) * w.size());
+  memcpy(req_piece_begin_out, rpb.data(), sizeof(int32_t) * rpb.size());
+  return PKD_OK;
+}
+
+pkd_status pkd_mla_decode(const void* d_q_nope, const void* d_q_pe, const void* d_ckv_cache,
+                          const void* d_kpe_cache, const int32_t* h_kv_indptr, const int32_t* d_kv_page_indices,
+                          const int32_t* h_kv_last_page_len, int batch, int num_heads, int page_size,
+                          int64_t num_pages, int64_t ckv_page_stride_elems, int64_t kpe_page_stride_elems,
+                          float sm_scale, void* d_out, float* d_lse, void* d_workspace, size_t workspace_bytes,
+                          int num_sms, void* stream) {
+  if (batch < 0 || num_heads <= 0 || num_heads > 128)
+    return fail(PKD_ERR_UNSUPPORTED, "num_heads %d outside 1..128 (batch %d)", num_heads, batch);
+  if (!(page_size >= 1 && ((page_size <= 32 && 32 % page_size == 0) || page_size % 32 == 0)))
+    return fail(PKD_ERR_UNSUPPORTED, "page_size %d: a divisor of 32 or a multiple of 32", page_size);
+  if (num_sms <= 0) return fail(PKD_ERR_INVALID_ARG, "num_sms must be > 0");
+  const size_t need = pkd_mla_workspace_bytes(batch > 0 ? batch : 1, num_heads, num_sms);
+  if (!d_workspace || workspace_bytes < need || !aligned16(d_workspace))
+    return fail(PKD_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, need %zu (16-byte aligned)", workspace_bytes,
+                need);
+  if (batch == 0) return PKD_OK;
+  if (!h_kv_indptr || !h_kv_last_page_len || !d_q_nope || !d_q_pe || !d_out)
+    return fail(PKD_ERR_INVALID_ARG, "NULL argument");
+  if (!aligned16(d_q_nope) || !aligned16(d_q_pe) || !aligned16(d_out))
+    return fail(PKD_ERR_INVALID_ARG, "q / out must be 16-byte aligned");
+  std::vector<pkd::TileWork> w;
+  std::vector<int32_t> rpb;
+  bool any_split = false;
+  pkd_status su = mla_units(h_kv_indptr, h_kv_last_page_len, batch, page_size, num_sms, &w, &rpb, &any_split);
+  if (su != PKD_OK) return su;
+  const int P = page_size;
+  if (h_kv_indptr[batch] > 0) {
+    if (!d_kv_page_indices || !d_ckv_cache || !d_kpe_cache) return fail(PKD_ERR_INVALID_ARG, "NULL cache");
+    if (!aligned16(d_ckv_cache) || !aligned16(d_kpe_cache))
+      return fail(PKD_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+    if (num_pages <= 0 || num_pages > INT32_MAX) return fail(PKD_ERR_INVALID_ARG, "num_pages out of range");
+    if ((ckv_page_stride_elems * 2) % 16 || ckv_page_stride_elems < static_cast<int64_t>(P) * 512 ||
+        (kpe_page_stride_elems * 2) % 16 || kpe_page_stride_elems < static_cast<int64_t>(P) * 64)
+      return fail(PKD_ERR_INVALID_ARG, "page strides must cover a page and be 16-byte multiples");
+  }
   // workspace: error word | units | request piece ranges | partial o | partial lse
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
   const size_t pieces_cap = static_cast<size_t>(batch) + num_sms;

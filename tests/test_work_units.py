@@ -1,9 +1,10 @@
-"""Host logic of the paired-tile work lists (no GPU): the units pkd_plan_prefill
-and pkd_plan_tree upload, built by the library's host-only exports and checked
-against what the kernels rely on -- both units of a pair share their keys,
-every query row is covered exactly once, a node's key-range pieces partition
-its keys, the causal key range is the one the pair's last row sees, and pairs
-come longest first."""
+"""Host logic of the work lists (no GPU): the units pkd_plan_prefill,
+pkd_plan_tree and pkd_mla_decode upload, built by the library's host-only
+exports and checked against what the kernels rely on -- both units of a pair
+share their keys, every query row is covered exactly once, a node's or a
+request's key-range pieces partition its keys, the causal key range is the one
+the pair's last row sees, MLA's piece size is the smallest that fits the SMs,
+and pairs come longest first."""
 import numpy as np
 import pytest
 
@@ -161,3 +162,60 @@ def test_tree_units_errors():
         api.tree_units(lv * 5, 4, 32, 8, 16, 304, 16)
     with pytest.raises(pkd.PkdError):  # last_page_len outside 1..P
         api.tree_units([([0, 4], [0, 2], [17])], 4, 32, 8, 16, 304, 4)
+
+
+def _mla_piece_size(tiles, num_sms):
+    """The rule the split follows, restated: the smallest C >= 16 (32-key
+    tiles) whose pieces -- ceil(tiles / C) per request, at least one -- number
+    at most num_sms, or the longest request's tile count when none does."""
+    def pieces(C):
+        return sum(max(1, -(-t // C)) for t in tiles)
+    top = max(max(tiles), 1)
+    C = next((c for c in range(1, top + 1) if pieces(c) <= num_sms), top)
+    return max(C, 16)
+
+
+@pytest.mark.parametrize("seed,B,P,num_sms", [(1, 64, 16, 152), (2, 7, 1, 148), (3, 200, 64, 152),
+                                              (4, 1, 32, 152), (5, 30, 16, 8)])
+def test_mla_units(seed, B, P, num_sms):
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(0, 9000, size=B)
+    lens[rng.integers(0, B)] = 0  # an empty request
+    pages = (lens + P - 1) // P
+    kvi = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    last = np.where(pages > 0, lens - (pages - 1) * P, 0).astype(np.int32)
+    u, rpb = pkd.mla_units(kvi, last, P, num_sms)
+    tiles = [(int(L) + 31) // 32 for L in lens]
+    C = _mla_piece_size(tiles, num_sms)
+    halves = _pairs(u)
+    for a, b in halves:  # the two output halves of one key range, side by side
+        assert a[LEVEL] == 0 and b[LEVEL] == 1
+        for f in (Q0, QEND, PB, KVLEN, T0, T1, PIECE):
+            assert a[f] == b[f], f
+    lengths = [a[T1] - a[T0] for a, _ in halves]
+    assert lengths == sorted(lengths, reverse=True)
+    assert rpb[0] == 0
+    for r in range(B):
+        ru = sorted((int(a[T0]), int(a[T1]), int(a[PIECE])) for a, _ in halves if a[Q0] == r)
+        np_r = len(ru)
+        assert np_r == max(1, -(-tiles[r] // C))
+        assert all(a[KVLEN] == lens[r] and a[PB] == kvi[r] and a[QEND] == r + 1 for a, _ in halves if a[Q0] == r)
+        # the ranges partition the request's tiles, each at most C long
+        assert ru[0][0] == 0 and ru[-1][1] == tiles[r]
+        for (_, e, _), (s2, _, _) in zip(ru, ru[1:]):
+            assert e == s2
+        assert all(t1 - t0 <= C for t0, t1, _ in ru)
+        if np_r == 1:
+            assert ru[0][2] == -1 and rpb[r + 1] == rpb[r]  # written directly
+        else:
+            assert [p for _, _, p in ru] == list(range(rpb[r], rpb[r + 1]))
+    assert len(halves) <= max(num_sms, B)
+
+
+def test_mla_units_errors():
+    with pytest.raises(pkd.PkdError):  # last_page_len outside 1..P
+        pkd.mla_units([0, 2], [17], 16, 152)
+    with pytest.raises(pkd.PkdError):  # decreasing kv_indptr
+        pkd.mla_units([0, 2, 1], [16, 16], 16, 152)
+    with pytest.raises(pkd.PkdError):  # no SMs
+        pkd.mla_units([0, 2], [16], 16, 0)
