@@ -212,12 +212,13 @@ def cpu_sample_batch(b, n_req: int):
     return q, k, v, np.asarray(indptr, np.int32), idx, np.asarray(last, np.int32), lens
 
 
-def time_cpu_oracle(b, target_s: float, max_req=None):
-    """Run the C fp64 oracle on a bounded sample of requests (all qo heads).
+def time_cpu_oracle(b, target_s: float, max_req=None, threads=None):
+    """Run the C fp64 oracle on a bounded sample of requests (all qo heads),
+    on all host cores or on `threads` of them.
     Returns (GB/s of algorithmic bytes, seconds, requests, threads)."""
     from oracle import c_oracle
 
-    threads = c_oracle.max_threads()
+    threads = c_oracle.max_threads() if threads is None else int(threads)
     e_kv = b.k_cache.element_size()
     ks = None if b.k_scale is None else b.k_scale.cpu()
     vs = None if b.v_scale is None else b.v_scale.cpu()
@@ -462,6 +463,10 @@ def run_ours(args, world, rank, local):
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "sample": f"{n_req} of {b.batch} requests, all {b.num_qo_heads} qo heads "
                                           f"(C fp64 oracle, {secs:.1f} s)"}
+        # the same oracle on one core, over a shorter sample
+        gbs1, secs1, n1, _ = time_cpu_oracle(b, target_s=3.0, threads=1)
+        line["cpu_baseline"]["single_thread"] = {"value": round(gbs1, 4), "unit": UNIT, "cores": 1,
+                                                 "sample": f"{n1} of {b.batch} requests ({secs1:.1f} s)"}
     return line
 
 
