@@ -212,13 +212,18 @@ def cpu_sample_batch(b, n_req: int):
     return q, k, v, np.asarray(indptr, np.int32), idx, np.asarray(last, np.int32), lens
 
 
+_ALL_THREADS = []  # the oracle's thread count before any run narrowed it
+
+
 def time_cpu_oracle(b, target_s: float, max_req=None, threads=None):
     """Run the C fp64 oracle on a bounded sample of requests (all qo heads),
     on all host cores or on `threads` of them.
     Returns (GB/s of algorithmic bytes, seconds, requests, threads)."""
     from oracle import c_oracle
 
-    threads = c_oracle.max_threads() if threads is None else int(threads)
+    if not _ALL_THREADS:  # OpenMP keeps a thread count set by a run for the next ones
+        _ALL_THREADS.append(c_oracle.max_threads())
+    threads = _ALL_THREADS[0] if threads is None else int(threads)
     e_kv = b.k_cache.element_size()
     ks = None if b.k_scale is None else b.k_scale.cpu()
     vs = None if b.v_scale is None else b.v_scale.cpu()
