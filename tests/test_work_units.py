@@ -219,3 +219,22 @@ def test_mla_units_errors():
         pkd.mla_units([0, 2, 1], [16, 16], 16, 152)
     with pytest.raises(pkd.PkdError):  # no SMs
         pkd.mla_units([0, 2], [16], 16, 0)
+
+
+def test_units_call_retries_with_the_reported_size():
+    """A too-small buffer gets PKD_ERR_CAPACITY_EXCEEDED with the needed count,
+    and the binding retries once with that size."""
+    import ctypes
+
+    qo, kvi, last = [0, 500], [0, 40], [16]
+    want = api.prefill_units(qo, kvi, last, 32, 8, 16)
+    qi, ki, la = (np.asarray(x, np.int32) for x in (qo, kvi, last))
+    calls = []
+
+    def fn(buf, cap, n):
+        calls.append(cap)
+        return api.lib().pkd_prefill_units_host(api._as_i32p(qi), api._as_i32p(ki), api._as_i32p(la), 1, 32, 8, 16,
+                                                1, api._as_i32p(buf), cap, ctypes.byref(n))
+
+    got = api._units_call(fn, 1)
+    assert calls == [1, len(want)] and np.array_equal(got, want)
