@@ -11,10 +11,10 @@ is the batch-64 GQA decode batch (64 requests, 32 qo / 8 kv heads, head_dim
 20000-page pool).  Its K/V bytes (0.58 GB) exceed the 129 MB L2, so no flush
 is needed between steps.
 
-Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
-on the host cores instead (the reference arm).  Under torchrun every rank runs
-its own replica of the batch on its own GPU (weak scaling, no collective on the
-data path); the time is the max over ranks.
+Prints ONE JSON line.  ``--impl reference`` times the fp64 CPU oracle on the
+host cores instead (the reference arm).  The path runs on one GPU: launched
+with WORLD_SIZE > 1 (torchrun), the GPU arm refuses with an error, and the
+reference arm runs on rank 0 only (the other ranks exit without work).
 """
 from __future__ import annotations
 
@@ -54,7 +54,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, help="standard workload index (1..5)")
+    ap.add_argument("--config", type=int, default=5,
+                    help="standard workload index (1..5); 5, the long-context fp8 batch, is the largest")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--all-configs", action="store_true", help="also print one line per standard workload")
     ap.add_argument("--batch", type=int, default=None,
@@ -168,27 +169,9 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def dist_init(args):
-    from paged_kv_decode_28_gb300 import replicas
-
-    world, rank, local = replicas.world()
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
-    return world, rank, local
-
-
-def max_over_ranks(x: float, world: int, device) -> float:
-    from paged_kv_decode_28_gb300 import replicas
-
-    return replicas.max_over_ranks(x, world, device)
-
-
-def barrier(world):
-    from paged_kv_decode_28_gb300 import replicas
-
-    replicas.barrier(world)
+def launch_world() -> tuple:
+    """(world_size, rank) from the torchrun environment ((1, 0) when absent)."""
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
 
 
 def cpu_sample_batch(b, n_req: int):
@@ -264,7 +247,7 @@ def l2_note(nbytes: int, l2: int) -> str:
     return f"inputs {nbytes / 1e9:.3f} GB < {l2 / 1e6:.0f} MB L2: L2-resident between steps (no flush)"
 
 
-def run_ours(args, world, rank, local):
+def run_ours(args):
     import torch
 
     import paged_kv_decode_28_gb300 as pkd
@@ -272,8 +255,8 @@ def run_ours(args, world, rank, local):
     from paged_kv_decode_28_gb300 import workloads as wl
 
     _build.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     b = wl.make_config(args.config, device=dev, batch=args.batch)
     if args.kv_layout == "HND":  # the same pages re-laid as [Hk, P, D] blocks
         for name in ("k_cache", "v_cache"):
@@ -338,8 +321,7 @@ def run_ours(args, world, rank, local):
         graphs[i % K].replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        barrier(world)
+    with ClockSampler(0) as clocks:
         torch.cuda.synchronize()
         e0.record(stream)
         for i in range(K):
@@ -347,15 +329,24 @@ def run_ours(args, world, rank, local):
             graphs[i].replay()
         e1.record(stream)
         torch.cuda.synchronize()
-        barrier(world)
     clk = clocks.summary()
     ms_total = e0.elapsed_time(e1)
-    ms_total_max = max_over_ranks(ms_total, world, dev)
+    ms_total_max = ms_total
     ms_step = ms_total_max / K
     kern_ms = [a.elapsed_time(z) for a, z in kev]
     kern_avg_ms = sum(kern_ms) / K
+    # the same replays with a write of 2 x L2 between steps (outside the decode
+    # kernel's events), so that none of a step's input can still be in L2
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    for i in range(K):
+        do_plan()
+        flush.fill_(i & 0xFF)
+        graphs[i].replay()
+    torch.cuda.synchronize()
+    kern_ms_flushed = [a.elapsed_time(z) for a, z in kev]
+    del flush
     nbytes = algorithmic_bytes(b)
-    value = world * nbytes / (ms_step * 1e-3) / 1e9
+    value = nbytes / (ms_step * 1e-3) / 1e9
     assert plan.check_device_errors() == 0
     # host time of one plan (the schedule for this batch into pinned memory),
     # timed on its own after the timed steps
@@ -391,13 +382,12 @@ def run_ours(args, world, rank, local):
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
-    barrier(world)
     t0 = time.perf_counter()
     for _ in range(K):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
-    e2e_value = world * nbytes / (e2e_s / K) / 1e9
+    e2e_s = time.perf_counter() - t0
+    e2e_value = nbytes / (e2e_s / K) / 1e9
     h2d = q_h.numel() * q_h.element_size() + idx_h.numel() * 4 + (b.batch + 1) * 4 + b.batch * 4
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
 
@@ -416,12 +406,12 @@ def run_ours(args, world, rank, local):
         "metric": METRIC,
         "value": round(value, 1),
         "unit": UNIT,
-        "n_gpus": world,
+        "n_gpus": 1,
         "steps": K,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
         "us_per_call": round(ms_step * 1e3, 2),
-        "tokens_per_s": round(world * b.batch / (ms_step * 1e-3), 1),
+        "tokens_per_s": round(b.batch / (ms_step * 1e-3), 1),
         "host_plan_us": round(statistics.median(plan_s) * 1e6, 1),
         "higher_is_better": True,
         "scaling": "weak",
@@ -439,10 +429,11 @@ def run_ours(args, world, rank, local):
             "kv_layout": args.kv_layout,
             "kv_tokens": int(np.asarray(b.kv_lens, np.int64).sum()),
             "algorithmic_bytes_per_step": nbytes,
-            "l2": l2_note(nbytes, l2) if R == 1 else
-                  (f"inputs {nbytes / 1e9:.3f} GB < {l2 / 1e6:.0f} MB L2: {R} copies of q, K and V used in "
-                   f"turn ({R * nbytes / 1e9:.2f} GB), so every step reads from HBM"),
-            "parallelism": f"replicas x{world} (one batch per GPU)",
+            "l2": (l2_note(nbytes, l2) if R == 1 else
+                   (f"inputs {nbytes / 1e9:.3f} GB < {l2 / 1e6:.0f} MB L2: {R} copies of q, K and V used in "
+                    f"turn ({R * nbytes / 1e9:.2f} GB), so every step reads from HBM"))
+                  + "; a second pass writes 2 x L2 before every step (roofline.kernel_us_l2_flushed)",
+            "parallelism": "one GPU",
         },
         "roofline": {
             "bound": "hbm",
@@ -457,13 +448,18 @@ def run_ours(args, world, rank, local):
             "kernel_us": round(kern_avg_ms * 1e3, 2),
             # spread of the per-step decode launch (events around each launch)
             "kernel_us_p10_p50_p90": [round(float(x) * 1e3, 2) for x in np.percentile(kern_ms, [10, 50, 90])],
+            # the decode kernel when a 2 x L2 write precedes every step (same graphs)
+            "kernel_us_l2_flushed": round(sum(kern_ms_flushed) / K * 1e3, 2),
+            "frac_l2_flushed": round(decode_kernel_bytes(b) / (sum(kern_ms_flushed) / K * 1e-3) / 1e9 / peak, 4),
+            # every kernel of the step (host plan included) against the same peak
+            "whole_step": {"achieved": round(value, 1), "frac": round(value / peak, 4)},
         },
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "us_per_step": round(e2e_s / K * 1e6, 2)},
         "gpu_launches": K * (3 if cascade else 2),
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         gbs, secs, n_req, threads = time_cpu_oracle(b, target_s=10.0)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "sample": f"{n_req} of {b.batch} requests, all {b.num_qo_heads} qo heads "
@@ -475,7 +471,7 @@ def run_ours(args, world, rank, local):
     return line
 
 
-def run_reference(args, world, rank, local):
+def run_reference(args):
     """The reference arm: the fp64 CPU oracle on the host cores, on a bounded
     sample of the same workload each step."""
     import torch
@@ -483,8 +479,6 @@ def run_reference(args, world, rank, local):
     from paged_kv_decode_28_gb300 import workloads as wl
     from oracle import c_oracle
 
-    if rank != 0:
-        return None
     c_oracle.build()
     # the same seeded inputs as the GPU arm (generated by the device RNG when a GPU is present)
     b = wl.make_config(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
@@ -518,7 +512,7 @@ def run_reference(args, world, rank, local):
         "metric": METRIC,
         "value": round(value, 4),
         "unit": UNIT,
-        "n_gpus": world,
+        "n_gpus": 1,
         "steps": K,
         "warmup": W,
         "ms_per_step": round(secs * 1e3, 3),
@@ -536,7 +530,7 @@ def run_reference(args, world, rank, local):
     }
 
 
-def run_append(args, world, rank, local):
+def run_append(args):
     """pkd_append_kv on a workload's pool geometry: a bulk append
     (args.append_tokens new tokens per request; bandwidth-bound, reported
     against the HBM peak) and the one-token-per-request append of a decode step
@@ -548,8 +542,8 @@ def run_append(args, world, rank, local):
     from paged_kv_decode_28_gb300 import workloads as wl
 
     _build.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     lens = np.asarray(wl.config_lengths(args.config, args.batch), dtype=np.int64)
     P, _, Hk, _, kvd = wl.config_geometry(args.config)
     row_bytes = Hk * 128 * 2 * (2 + (1 if kvd == "e4m3" else 2))  # K and V of one token, read + written
@@ -595,10 +589,8 @@ def run_append(args, world, rank, local):
         return e0.elapsed_time(e1) / steps
 
     K = args.steps
-    with ClockSampler(local) as clocks:
-        barrier(world)
-        ms_bulk = max_over_ranks(timed(B * A, K), world, dev)
-        barrier(world)
+    with ClockSampler(0) as clocks:
+        ms_bulk = timed(B * A, K)
     clk = clocks.summary()
     # one token per request (the first new token of every request), as in a
     # decode step: device time per append from a captured graph of 16 appends
@@ -656,7 +648,7 @@ def run_append(args, world, rank, local):
         pass
     # the oracle on a bounded sample: 256 of the new tokens into a 512-page pool of the same geometry
     cpu = None
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_cpu_baseline:
         from oracle import kv_append as ka
 
         n_s = min(256, B * A)
@@ -674,13 +666,13 @@ def run_append(args, world, rank, local):
                f"(python oracle, {dt:.2f} s)"}
     return {
         "metric": "kv append (pkd_append_kv): achieved HBM GB/s",
-        "value": round(world * achieved, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "value": round(achieved, 1), "unit": "GB/s", "n_gpus": 1, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_bulk, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": kvd, "data": "synthetic (seeded N(0,1) rows)",
         "config": {"workload": f"append {A} tokens to each request of {wl.CONFIG_NAMES[args.config]}",
                    "batch": B, "num_kv_heads": Hk, "head_dim": 128, "page_size": P, "kv_layout": args.kv_layout,
                    "new_dtype": str(new_dtype),
-                   "bytes_per_step": int(nbytes), "parallelism": f"replicas x{world}",
+                   "bytes_per_step": int(nbytes), "parallelism": "one GPU",
                    "l2": f"{nbytes / 1e9:.2f} GB moved per step "
                    f"{'>' if nbytes > 129e6 else '<'} 129 MB L2; no flush between steps"},
         "roofline": {"bound": "hbm", "kernel": "pkd append_kv_kernel", "achieved": round(achieved, 1),
@@ -727,7 +719,7 @@ def measured_tensor_peak():
         return 1900.0, "fallback"
 
 
-def run_tree(args, world, rank, local):
+def run_tree(args):
     """Prefix-tree decode (pkd_plan_tree / pkd_tree_decode) on the 3-level
     tree workload: run captured in CUDA graphs, both plans on the host before
     every replay."""
@@ -738,8 +730,8 @@ def run_tree(args, world, rank, local):
     from paged_kv_decode_28_gb300 import workloads as wl
 
     _build.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     b = wl.make_config_tree(device=dev, batch=args.batch)
     idx = torch.from_numpy(b.kv_page_indices).to(dev)
     lv = [(ri, ki, torch.from_numpy(np.asarray(ix)).to(dev), last) for ri, ki, ix, last in b.levels]
@@ -771,23 +763,21 @@ def run_tree(args, world, rank, local):
         g.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        barrier(world)
+    with ClockSampler(0) as clocks:
         e0.record(stream)
         for _ in range(K):
             do_plan()
             g.replay()
         e1.record(stream)
         torch.cuda.synchronize()
-        barrier(world)
     clk = clocks.summary()
-    ms_step = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+    ms_step = e0.elapsed_time(e1) / K
     assert plan.check_device_errors() == 0
     nbytes = tree_bytes(b)
     achieved = nbytes / (ms_step * 1e-3) / 1e9
     peak, peak_kind = measured_hbm_peak()
     cpu = None
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_cpu_baseline:
         from oracle import attention as orc
 
         rows = [(r, h) for r in range(0, b.batch, max(1, b.batch // 8)) for h in (0, b.num_qo_heads - 1)]
@@ -801,14 +791,14 @@ def run_tree(args, world, rank, local):
                "sample": f"{len(rows)} of {b.batch * b.num_qo_heads} (request, qo head) rows, bytes scaled by "
                f"that fraction (python fp64 oracle, {dt:.2f} s)"}
     return {
-        "metric": "prefix-tree decode (pkd_tree_decode): achieved HBM GB/s per step", "value": round(world * achieved, 1),
-        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
+        "metric": "prefix-tree decode (pkd_tree_decode): achieved HBM GB/s per step", "value": round(achieved, 1),
+        "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
         "us_per_call": round(ms_step * 1e3, 2), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) values, seeded lengths and page placement)",
         "config": {"workload": b.name, "batch": b.batch, "num_qo_heads": b.num_qo_heads,
                    "num_kv_heads": b.num_kv_heads, "page_size": b.page_size, "bytes_per_step": nbytes,
                    "l2": l2_note(nbytes, l2_bytes(dev)),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": "one GPU"},
         "roofline": {"bound": "hbm", "kernel": "whole step (schedule upload, own-page decode, tree kernel, merge)",
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -817,7 +807,7 @@ def run_tree(args, world, rank, local):
     }
 
 
-def run_prefill(args, world, rank, local):
+def run_prefill(args):
     """Paged append-prefill (pkd_plan_prefill / pkd_prefill_run) on the
     prefill workload: K back-to-back launches timed with CUDA events."""
     import torch
@@ -827,8 +817,8 @@ def run_prefill(args, world, rank, local):
     from paged_kv_decode_28_gb300 import workloads as wl
 
     _build.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     b = wl.make_config_prefill(device=dev, batch=args.batch)
     idx = torch.from_numpy(b.kv_page_indices).to(dev)
     plan = pkd.Plan(b.batch, b.num_qo_heads, b.num_kv_heads, device=dev)
@@ -842,16 +832,14 @@ def run_prefill(args, world, rank, local):
     assert plan.check_device_errors() == 0
     K = args.steps
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        barrier(world)
+    with ClockSampler(0) as clocks:
         e0.record(stream)
         for _ in range(K):
             plan.prefill(b.q, b.k_cache, b.v_cache, sm_scale=b.sm_scale, out=out, lse=lse)
         e1.record(stream)
         torch.cuda.synchronize()
-        barrier(world)
     clk = clocks.summary()
-    ms_step = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+    ms_step = e0.elapsed_time(e1) / K
     assert plan.check_device_errors() == 0
     flops = prefill_flops(b)
     achieved = flops / (ms_step * 1e-3) / 1e12
@@ -871,7 +859,7 @@ def run_prefill(args, world, rank, local):
     nbytes = (int(np.asarray(b.kv_lens, np.int64).sum()) * b.num_kv_heads * b.head_dim * 2 * e
               + 2 * b.q.numel() * b.q.element_size() + lse.numel() * 4)
     cpu = None
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_cpu_baseline:
         from oracle import attention as orc
 
         T = b.q.shape[0]
@@ -887,7 +875,7 @@ def run_prefill(args, world, rank, local):
                f"fraction (python fp64 oracle, {dt:.2f} s)"}
     return {
         "metric": "paged append-prefill attention (pkd_prefill_run): achieved TFLOP/s",
-        "value": round(world * achieved, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "value": round(achieved, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) values, seeded lengths and page placement)",
@@ -895,7 +883,7 @@ def run_prefill(args, world, rank, local):
                    "num_qo_heads": b.num_qo_heads, "num_kv_heads": b.num_kv_heads, "page_size": b.page_size,
                    "causal": True, "flops_per_step": flops, "bytes_per_step": nbytes,
                    "l2": l2_note(nbytes, l2_bytes(dev)),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": "one GPU"},
         "roofline": {"bound": "tensor", "kernel": "pkd tile2_kernel (paired query tiles)", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, burst)"
                      if peak_kind == "measured" else "fallback", "unit": "TFLOP/s",
@@ -913,7 +901,7 @@ def mla_bytes(b) -> int:
     return kv + B * H * (576 * 2 + 512 * 2 + 4)
 
 
-def run_mla(args, world, rank, local):
+def run_mla(args):
     """MLA decode (pkd_mla_decode) on the 64-request DeepSeek-V3 workload: K
     back-to-back calls (host planning and the unit upload included) timed with
     CUDA events."""
@@ -924,8 +912,8 @@ def run_mla(args, world, rank, local):
     from paged_kv_decode_28_gb300 import workloads as wl
 
     _build.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     b = wl.make_config_mla(device=dev, batch=args.batch)
     idx = torch.from_numpy(np.asarray(b.kv_page_indices, np.int32)).to(dev)
     out = torch.empty((b.batch, b.num_heads, 512), dtype=torch.bfloat16, device=dev)
@@ -944,22 +932,20 @@ def run_mla(args, world, rank, local):
     assert int(ws[:4].view(torch.int32).item()) == 0
     K = args.steps
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        barrier(world)
+    with ClockSampler(0) as clocks:
         e0.record(stream)
         for _ in range(K):
             step()
         e1.record(stream)
         torch.cuda.synchronize()
-        barrier(world)
     clk = clocks.summary()
-    ms_step = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+    ms_step = e0.elapsed_time(e1) / K
     nbytes = mla_bytes(b)
     achieved = nbytes / (ms_step * 1e-3) / 1e9
     flops = int(np.asarray(b.kv_lens, np.int64).sum()) * b.num_heads * (576 + 512) * 2
     peak, peak_kind = measured_hbm_peak()
     cpu = None
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_cpu_baseline:
         from oracle import mla as orc
 
         rows = [(r, h) for r in range(0, b.batch, max(1, b.batch // 8)) for h in (0, b.num_heads - 1)]
@@ -972,15 +958,15 @@ def run_mla(args, world, rank, local):
                "sample": f"{len(rows)} of {b.batch * b.num_heads} (request, head) rows, bytes scaled by that "
                f"fraction (python fp64 oracle, {dt:.2f} s, pool copied to the host first)"}
     return {
-        "metric": "MLA decode (pkd_mla_decode): achieved HBM GB/s per call", "value": round(world * achieved, 1),
-        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
+        "metric": "MLA decode (pkd_mla_decode): achieved HBM GB/s per call", "value": round(achieved, 1),
+        "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
         "us_per_call": round(ms_step * 1e3, 2), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) values, seeded lengths and page placement)",
         "config": {"workload": b.name, "batch": b.batch, "num_heads": b.num_heads, "page_size": b.page_size,
                    "kv_tokens": int(np.asarray(b.kv_lens, np.int64).sum()), "bytes_per_step": nbytes,
                    "flops_per_step": flops, "tflops": round(flops / (ms_step * 1e-3) / 1e12, 1),
                    "l2": l2_note(nbytes, l2_bytes(dev)),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": "one GPU"},
         "roofline": {"bound": "hbm", "kernel": "pkd mla_kernel + mla_merge_kernel (whole call)",
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -991,33 +977,35 @@ def run_mla(args, world, rank, local):
 
 def main():
     args = parse_args()
-    world, rank, local = dist_init(args)
+    world, rank = launch_world()
+    if world > 1 or args.gpus != 1:
+        if args.impl == "reference" and args.op == "decode":
+            # the reference arm is the CPU oracle: rank 0 runs it, the others have no work
+            if rank == 0:
+                print(json.dumps(run_reference(args)), flush=True)
+            return
+        print(f"bench.py: this path runs on one GPU only (got --gpus {args.gpus}, WORLD_SIZE {world}); "
+              "its cascade and MLA kernels use cluster-multicast loads that stay within one GPU's memory",
+              file=sys.stderr, flush=True)
+        sys.exit(2)
     if args.op in ("append", "tree", "prefill", "mla"):
-        line = {"append": run_append, "tree": run_tree, "prefill": run_prefill, "mla": run_mla}[args.op](
-            args, world, rank, local)
-        if rank == 0:
-            print(json.dumps(line), flush=True)
+        line = {"append": run_append, "tree": run_tree, "prefill": run_prefill, "mla": run_mla}[args.op](args)
+        print(json.dumps(line), flush=True)
         return
     if args.impl == "reference":
-        line = run_reference(args, world, rank, local)
+        line = run_reference(args)
     else:
-        line = run_ours(args, world, rank, local)
-        if args.all_configs and rank == 0 and world == 1:
+        line = run_ours(args)
+        if args.all_configs:
             for c in (1, 2, 3, 4, 5):
                 if c == args.config:
                     continue
                 a2 = argparse.Namespace(**{**vars(args), "config": c, "no_cpu_baseline": True})
                 try:
-                    print(json.dumps(run_ours(a2, world, rank, local)), flush=True)
+                    print(json.dumps(run_ours(a2)), flush=True)
                 except Exception as exc:  # keep the headline line even if one extra workload fails
                     print(json.dumps({"config": c, "error": str(exc)}), file=sys.stderr, flush=True)
-    if rank == 0 and line is not None:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.barrier()
-        dist.destroy_process_group()
+    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

@@ -451,12 +451,19 @@ pkd_status pkd_plan_set_debug(pkd_plan_t plan, int flags);
  *   - The first call on a device looks up that device's scratch address
  *     (cudaGetSymbolAddress, with the device current); make that first call
  *     before any stream capture on the device.
- *   - All calls share the one scratch area per device and the schedule upload
- *     is a cudaMemcpyAsync on `stream`: calls whose work can overlap on the GPU
- *     (different streams, different threads) race and must be serialised by the
- *     caller.  Each call resets what must start at zero.
- *   - Device error bits (PKD_DEVERR_*) are recorded in the scratch area and are
- *     not reported back; an out-of-range page id is read as page 0.
+ *   - The schedule is uploaded from a host buffer of the library that every
+ *     call rewrites, with a cudaMemcpyAsync on `stream`; the call returns
+ *     PKD_ERR_UNSUPPORTED while `stream` is being captured.
+ *   - All calls share the one scratch area per device: calls whose work can
+ *     overlap on the GPU (different streams, different threads) race and must
+ *     be serialised by the caller.  Each call resets what must start at zero,
+ *     the device error word included.
+ *   - Device error bits (PKD_DEVERR_*) of the last call are kept in the
+ *     scratch area (pkd_noalloc_device_errors reads them); an out-of-range
+ *     page id is read as page 0 and sets PKD_DEVERR_PAGE_INDEX.
+ *   - Two limits, each reported as PKD_ERR_CAPACITY_EXCEEDED with a message
+ *     naming it: the device scratch (PKD_NOALLOC_SCRATCH_BYTES) and the
+ *     library's 256 KiB host buffer for the schedule.
  * Arguments as pkd_plan and pkd_run (h_* are host arrays, d_* device);
  * kv_layout is the pools' page layout (pkd_kv_layout).
  */
@@ -468,6 +475,14 @@ pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32_t* d_kv_pa
                               const void* d_v_cache, int64_t num_pages, int64_t page_stride_elems,
                               const float* d_k_scale, const float* d_v_scale, float sm_scale,
                               void* d_out, float* d_lse, void* stream);
+
+/*
+ * Device error bits (PKD_DEVERR_*) recorded by the last pkd_decode_noalloc
+ * call on the current device, read from its scratch area after synchronising
+ * `stream` (the next call clears them).  *flags_out gets the bits; returns
+ * PKD_ERR_DEVICE_CHECK when a bit was set.  Allocates nothing.
+ */
+pkd_status pkd_noalloc_device_errors(uint32_t* flags_out, void* stream);
 
 /*
  * The split-KV rule of pkd_plan, run on the host only (no GPU), for

@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
                               _vp, _vp]),
         "pkd_decode_noalloc": (i, [_i32p, _vp, _i32p, i, i, i, i, i, i, i, i, _vp, _vp, _vp, i64, i64, _vp, _vp, f,
                                    _vp, _vp, _vp]),
+        "pkd_noalloc_device_errors": (i, [ctypes.POINTER(ctypes.c_uint32), _vp]),
         "pkd_plan_host": (i, [_i32p, _i32p, i, i, i, i, _i32p, i, _i32p, _i32p, _i32p, _i32p, _i32p]),
         "pkd_prefill_units_host": (i, [_i32p, _i32p, _i32p, i, i, i, i, i, _i32p, i, ctypes.POINTER(ctypes.c_int)]),
         "pkd_tree_units_host": (i, [i, _vp, _vp, _vp, _i32p, i, i, i, i, i, i, _i32p, i,
@@ -591,7 +592,8 @@ def decode_noalloc(kv_indptr, kv_page_indices: torch.Tensor, kv_last_page_len, p
     """Plan + run in one call that allocates nothing on the device: the library's
     built-in scratch area replaces the workspace (see ``pkd_decode_noalloc``).
     ``out`` and ``lse`` are caller-provided; the first call on a device must
-    come before any stream capture on it.  ``kv_layout``: 'NHD' or 'HND' pools."""
+    come before any stream capture on it, and no call runs while its stream is
+    being captured.  ``kv_layout``: 'NHD' or 'HND' pools."""
     N, P, Hk, D, stride = _check_pool(q, k_cache, v_cache, kv_layout)
     indptr = _host_i32(kv_indptr)
     last = _host_i32(kv_last_page_len)
@@ -603,3 +605,13 @@ def decode_noalloc(kv_indptr, kv_page_indices: torch.Tensor, kv_last_page_len, p
                                     _ptr(k_cache), _ptr(v_cache), N, stride, _ptr(k_scale), _ptr(v_scale),
                                     float(sm_scale or 0.0), _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
+
+
+def noalloc_device_errors(stream=None) -> int:
+    """PKD_DEVERR_* bits the last ``decode_noalloc`` call on the current device
+    recorded (after synchronising ``stream``)."""
+    flags = ctypes.c_uint32(0)
+    st = lib().pkd_noalloc_device_errors(ctypes.byref(flags), _stream(stream))
+    if st not in (0, 6):
+        _check(st)
+    return int(flags.value)

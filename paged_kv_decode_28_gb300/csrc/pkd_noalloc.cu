@@ -16,9 +16,13 @@
 // cudaGetSymbolAddress (with that device current) and caches it.
 //
 // The schedule is built on the host into a file-scope host buffer (guarded by
-// a mutex) and uploaded with one cudaMemcpyAsync from that pageable buffer,
-// which is staged before the call returns.  The kernels are the same decode
-// and merge kernels the plan/run path launches.
+// a mutex) and uploaded with one cudaMemcpyAsync from that pageable buffer.
+// For a pageable source the runtime copies the bytes into its own staging
+// memory before cudaMemcpyAsync returns, so the host buffer may be reused once
+// the call is back.  A copy captured into a CUDA graph would instead read the
+// host buffer when the graph replays, so the call refuses to run while its
+// stream is capturing.  The kernels are the same decode and merge kernels the
+// plan/run path launches.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -176,14 +180,29 @@ extern "C" pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(MultiProcessorCount)");
   const int G = sms * pkd::kCtasPerSm;
   const NaLayout L = na_layout(batch, num_kv_heads, group, G);
-  if (L.total > kNoAllocScratchBytes || L.meta_end > kHostMetaBytes)
+  if (L.total > kNoAllocScratchBytes)
     return fail(PKD_ERR_CAPACITY_EXCEEDED,
-                "no-alloc decode: batch %d x %d kv heads needs %zu scratch bytes, the fixed scratch holds %zu",
+                "no-alloc decode: batch %d x %d kv heads needs %zu bytes of device scratch, the fixed scratch "
+                "holds %zu",
                 batch, num_kv_heads, L.total, kNoAllocScratchBytes);
+  if (L.meta_end > kHostMetaBytes)
+    return fail(PKD_ERR_CAPACITY_EXCEEDED,
+                "no-alloc decode: batch %d x %d kv heads needs a %zu-byte schedule, the fixed host staging "
+                "buffer holds %zu",
+                batch, num_kv_heads, L.meta_end, kHostMetaBytes);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  {
+    // the schedule upload reads a host buffer that the next call rewrites: a
+    // graph node made of it would replay some later call's schedule
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(PKD_ERR_UNSUPPORTED, "no-alloc decode cannot run while its stream is being captured");
+  }
   uint8_t* ws = nullptr;
   pkd_status s = scratch_for_current_device(&ws);
   if (s != PKD_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   // ---- schedule (host, static buffer) and its upload
   pkd::PlanCounts counts{};
@@ -212,10 +231,10 @@ extern "C" pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32
     }
     if (batch > 0 && h_kv_indptr[batch] > 0 && !d_kv_page_indices)
       return fail(PKD_ERR_INVALID_ARG, "d_kv_page_indices is NULL");
-    std::string unused;  // never written: the checks above cover every rejection of the rule
+    std::string why;
     int r = pkd::compute_plan(h_kv_indptr, h_kv_last_page_len, batch, num_kv_heads, page_size, G, items,
-                              L.max_items, cta_begin, row_begin, row_count, merge_rows, kv_len, &counts, &unused);
-    if (r != pkd::kPlanOk) return fail(static_cast<pkd_status>(r), "no-alloc decode: schedule rejected");
+                              L.max_items, cta_begin, row_begin, row_count, merge_rows, kv_len, &counts, &why);
+    if (r != pkd::kPlanOk) return fail(static_cast<pkd_status>(r), "no-alloc decode: %s", why.c_str());
     for (int i = 0; i < counts.n_items; ++i) items[4 * i + 3] = row_count[items[4 * i]] > 1 ? pkd::kItemSplit : 0;
     for (int b = 0; b < batch; ++b) page_begin[b] = h_kv_indptr[b];
     hdr->err = 0;  // the shared scratch keeps the previous call's bytes: the error word restarts at 0
@@ -223,8 +242,8 @@ extern "C" pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32
     hdr->n_merge_rows = counts.n_merge_rows;
     hdr->batch = batch;
     hdr->zero_page = 0;
-    // pageable source: the bytes are staged before the call returns, so the
-    // static host buffer may be reused as soon as the lock is released
+    // pageable source: the runtime has staged the bytes when cudaMemcpyAsync
+    // returns, so the static host buffer may be reused once the lock is released
     e = cudaMemcpyAsync(ws, h, L.meta_end, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(no-alloc schedule)");
   }
@@ -289,4 +308,19 @@ extern "C" pkd_status pkd_decode_noalloc(const int32_t* h_kv_indptr, const int32
   e = pkd::launch_merge_rows(m, G, st);
   if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
   return PKD_OK;
+}
+
+extern "C" pkd_status pkd_noalloc_device_errors(uint32_t* flags_out, void* stream) {
+  if (!flags_out) return fail(PKD_ERR_INVALID_ARG, "flags_out is NULL");
+  *flags_out = 0;
+  uint8_t* ws = nullptr;
+  pkd_status s = scratch_for_current_device(&ws);
+  if (s != PKD_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned word = 0;
+  e = cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(no-alloc error word)");
+  *flags_out = word;
+  return word ? fail(PKD_ERR_DEVICE_CHECK, "no-alloc decode: device error bits 0x%x", word) : PKD_OK;
 }
