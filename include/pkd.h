@@ -196,8 +196,11 @@ pkd_status pkd_run(pkd_plan_t plan, const void* d_q, const void* d_k_cache, cons
  *   d_prefix_page_indices  device int32 [prefix_num_pages] (prefix_num_pages >= 0).
  *   prefix_last_page_len   valid tokens in the prefix's last page (1..page_size).
  * The prefix is attended once per kv head for all requests (a dense
- * [batch * g, 128] x [128, prefix_len] product on the tensor cores), not once
- * per request.  Other arguments as pkd_run.  The plan must have been created
+ * [batch * g, 128] x [128, prefix_len] product on the tensor cores, 256 query
+ * rows per pair of SMs), not once per request.  Every dtype pair, group size
+ * and page size pkd_plan accepts is supported; E4M3 pools take k_scale /
+ * v_scale as in pkd_run (their codes are widened exactly to q's type for the
+ * products).  Other arguments as pkd_run.  The plan must have been created
  * with max_prefix_splits >= 1.  Enqueues the schedule upload, the suffix
  * decode (every item writes a partial state), the prefix kernel (launched
  * programmatically, so its CTAs take the SMs the decode grid frees as it

@@ -144,19 +144,51 @@ pkd_status encode_kv_map(CUtensorMap* m, const void* base, int kv_dtype, int hk,
 }
 
 
-// Clusters of the prefix kernel that fit on the current device at once
-// (queried once per device and cluster size; 0 when unknown).
-int resident_prefix_clusters(int cluster) {
+// CTA pairs of the shared-prefix kernel that fit on the current device at
+// once (queried once per device and kernel variant; 0 when unknown).
+int resident_prefix_pairs(int q_dtype, int kv_dtype) {
   static std::mutex mu;
-  static int cache[64][9] = {};
+  static int cache[64][2][2] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cluster < 1 || cluster > 8) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int qi = q_dtype == PKD_BF16 ? 1 : 0, ki = kv_dtype == PKD_E4M3 ? 1 : 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (cache[dev][cluster] == 0) {
-    const int n = pkd::prefix_max_active_clusters(cluster);
-    cache[dev][cluster] = n > 0 ? n : -1;
+  if (cache[dev][qi][ki] == 0) {
+    const int n = pkd::prefix_max_active_pairs(q_dtype, kv_dtype);
+    cache[dev][qi][ki] = n > 0 ? n : -1;
   }
-  return cache[dev][cluster] > 0 ? cache[dev][cluster] : 0;
+  return cache[dev][qi][ki] > 0 ? cache[dev][qi][ki] : 0;
+}
+
+// Tensor map over an e4m3 pool whose boxes are `box_cols` codes (128 for K,
+// 64 for one CTA's V columns) x box_tok keys of one head of one page, not
+// swizzled: a box lands as box_tok rows of box_cols bytes.
+pkd_status encode_code_map(CUtensorMap* m, const void* base, int hk, int64_t tok_extent, int64_t num_pages,
+                           int64_t page_stride_elems, int box_tok, int box_cols, bool hnd) {
+  auto enc = get_encode();
+  if (!enc) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t row = static_cast<cuuint64_t>(pkd::kHeadDim);
+  const cuuint64_t n1 = hnd ? static_cast<cuuint64_t>(tok_extent) : static_cast<cuuint64_t>(hk);
+  const cuuint64_t n2 = hnd ? static_cast<cuuint64_t>(hk) : static_cast<cuuint64_t>(tok_extent);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(pkd::kHeadDim), n1, n2, static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {row, n1 * row, static_cast<cuuint64_t>(page_stride_elems)};
+  const cuuint32_t bt = static_cast<cuuint32_t>(box_tok);
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), hnd ? bt : 1u, hnd ? 1u : bt, 1u};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled(codes) failed (CUresult %d)", (int)r);
+  return PKD_OK;
+}
+
+int gcd_int(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
 }
 
 }  // namespace
@@ -549,8 +581,8 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
     cudaError_t e = cascade->pp.work
                         ? pkd::launch_tile2(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->kv_dtype, st,
                                             true)
-                        : pkd::launch_prefix(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->kv_dtype,
-                                             st, true);
+                        : pkd::launch_prefix(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->q_dtype,
+                                             plan->kv_dtype, st, true);
     if (e != cudaSuccess) return cuda_fail(e, "prefix kernel launch");
   }
   // plain decode merges its split rows and writes its empty rows in the decode
@@ -901,18 +933,15 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
   if (!plan->planned) return fail(PKD_ERR_NO_PLAN, "cascade_decode before a successful plan");
   if (plan->max_splits < 1)
     return fail(PKD_ERR_CAPACITY_EXCEEDED, "the plan was created with max_prefix_splits = 0");
-  if (plan->kv_dtype == PKD_E4M3)
-    return fail(PKD_ERR_UNSUPPORTED, "cascade decode is built for f16/bf16 caches only");
   const int g = plan->hq / plan->hk;
-  if (pkd::kHeadDim % g != 0) return fail(PKD_ERR_UNSUPPORTED, "cascade decode needs a group size dividing 128");
   const int P = plan->page_size;
-  if (P <= pkd::kChunkKeys ? (128 % P != 0) : (P % pkd::kChunkKeys != 0))
-    return fail(PKD_ERR_UNSUPPORTED, "cascade decode needs a page size dividing 128 or a multiple of 64");
+  const bool fp8 = plan->kv_dtype == PKD_E4M3;
   if (prefix_num_pages < 0) return fail(PKD_ERR_INVALID_ARG, "prefix_num_pages must be >= 0");
   if (prefix_num_pages > 0 && (prefix_last_page_len < 1 || prefix_last_page_len > P))
     return fail(PKD_ERR_INVALID_ARG, "prefix_last_page_len %d outside 1..page_size", prefix_last_page_len);
   if (prefix_num_pages > 0 && !d_prefix_page_indices)
     return fail(PKD_ERR_INVALID_ARG, "d_prefix_page_indices is NULL");
+  if (fp8 && (!d_k_scale || !d_v_scale)) return fail(PKD_ERR_INVALID_ARG, "an E4M3 cache needs k_scale and v_scale");
   const int64_t prefix_len64 = prefix_num_pages > 0 ? static_cast<int64_t>(prefix_num_pages - 1) * P + prefix_last_page_len : 0;
   if (prefix_len64 > INT32_MAX) return fail(PKD_ERR_INVALID_ARG, "prefix longer than 2^31 - 1 keys");
   const int prefix_len = static_cast<int>(prefix_len64);
@@ -927,52 +956,48 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
     if ((page_stride_elems * elem_bytes(plan->kv_dtype)) % 16 != 0 ||
         page_stride_elems < static_cast<int64_t>(P) * plan->hk * plan->d)
       return fail(PKD_ERR_INVALID_ARG, "page_stride_elems must cover a page and be a 16-byte multiple");
+    // Each CTA of the prefix kernel holds R = floor(128 / g) requests (R * g
+    // query rows) of one kv head; two CTAs form a pair.  Key-range splits fill
+    // the pairs that fit on the GPU at once.
+    const int R = pkd::kHeadDim / g;
     const int n_tiles = (prefix_len + 127) / 128;
-    const int m_tiles = (B * g + 127) / 128;
-    // clusters of C query tiles share each K/V tile (multicast)
-    // (C divides the tile count, so every CTA of a cluster owns a real tile).
-    // Key-range splits fill the clusters that fit on the GPU at once; among
-    // the sizes, take the one that keeps the most CTAs busy, then the largest.
-    int C = 1, best_ctas = -1, splits = 1;
-    for (int c = 1; c <= 8; c *= 2) {
-      if (m_tiles % c != 0) continue;
-      int resident = resident_prefix_clusters(c);
-      if (resident <= 0) resident = (plan->G / pkd::kCtasPerSm) / c;
-      int sp = resident / (plan->hk * (m_tiles / c));
-      sp = sp < 1 ? 1 : sp;
-      sp = sp > plan->max_splits ? plan->max_splits : sp;
-      sp = sp > n_tiles ? n_tiles : sp;
-      const int ctas = plan->hk * m_tiles * sp;
-      const int busy = ctas < resident * c ? ctas : resident * c;
-      if (busy >= best_ctas) {
-        best_ctas = busy;
-        C = c;
-        splits = sp;
-      }
-    }
-    const int m_groups = m_tiles / C;
+    const int m_tiles = (B + R - 1) / R;
+    const int m_pairs = (m_tiles + 1) / 2;
+    int resident = resident_prefix_pairs(plan->q_dtype, plan->kv_dtype);
+    if (resident <= 0) resident = plan->G / (2 * pkd::kCtasPerSm);
+    int splits = resident / (plan->hk * m_pairs);
+    splits = splits < 1 ? 1 : splits;
+    splits = splits > plan->max_splits ? plan->max_splits : splits;
+    splits = splits > n_tiles ? n_tiles : splits;
     const int tps = (n_tiles + splits - 1) / splits;
     splits = (n_tiles + tps - 1) / tps;
-    // Q viewed as [B][Hk][g][128]: a box of 128 / g requests x g heads is one 128-row tile
+    // boxes of gcd(P, 64) keys never cross a page, whatever the page size
+    const int box_tok = gcd_int(P, 64);
     auto enc = get_encode();
     if (!enc) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     CUtensorMap tmq, tmk, tmv;
+    // q viewed as [B][Hk][g][128]: a box of R requests x g heads of one kv head
     cuuint64_t qdims[4] = {static_cast<cuuint64_t>(pkd::kHeadDim), static_cast<cuuint64_t>(g),
                            static_cast<cuuint64_t>(plan->hk), static_cast<cuuint64_t>(B)};
     cuuint64_t qstr[3] = {static_cast<cuuint64_t>(pkd::kHeadDim) * 2, static_cast<cuuint64_t>(g) * pkd::kHeadDim * 2,
                           static_cast<cuuint64_t>(plan->hq) * pkd::kHeadDim * 2};
-    cuuint32_t qbox[4] = {64u, static_cast<cuuint32_t>(g), 1u, static_cast<cuuint32_t>(128 / g)};
+    cuuint32_t qbox[4] = {64u, static_cast<cuuint32_t>(g), 1u, static_cast<cuuint32_t>(R)};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(&tmq, plan->q_dtype == PKD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                      4, const_cast<void*>(d_q), qdims, qstr, qbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKD_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed (CUresult %d)", (int)r);
-    const int box_tok = P <= pkd::kChunkKeys ? P : pkd::kChunkKeys;
     const bool hnd = plan->kv_layout == PKD_LAYOUT_HND;
-    pkd_status s = encode_kv_map(&tmk, d_k_cache, plan->kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok,
-                                 hnd);
-    if (s != PKD_OK) return s;
-    s = encode_kv_map(&tmv, d_v_cache, plan->kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok, hnd);
+    pkd_status s;
+    if (fp8) {
+      s = encode_code_map(&tmk, d_k_cache, plan->hk, P, num_pages, page_stride_elems, box_tok, 128, hnd);
+      if (s != PKD_OK) return s;
+      s = encode_code_map(&tmv, d_v_cache, plan->hk, P, num_pages, page_stride_elems, box_tok, 64, hnd);
+    } else {
+      s = encode_kv_map(&tmk, d_k_cache, plan->kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok, hnd);
+      if (s != PKD_OK) return s;
+      s = encode_kv_map(&tmv, d_v_cache, plan->kv_dtype, plan->hk, P, num_pages, page_stride_elems, box_tok, hnd);
+    }
     if (s != PKD_OK) return s;
     const float scale = (sm_scale > 0.f) ? sm_scale : 1.0f / std::sqrt(static_cast<float>(plan->d));
     pkd::PrefixParams pp{};
@@ -988,11 +1013,14 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
     pp.n_splits = splits;
     pp.tiles_per_split = tps;
     pp.m_tiles = m_tiles;
-    pp.cluster = C;
-    pp.m_groups = m_groups;
+    pp.cluster = 2;
+    pp.m_groups = m_pairs;
+    pp.req_per_tile = R;
     pp.scale_log2 = scale * 1.4426950408889634f;
     pp.pre_o = reinterpret_cast<float*>(plan->ws + plan->lay.pre_o);
     pp.pre_lse = reinterpret_cast<float*>(plan->ws + plan->lay.pre_lse);
+    pp.k_scale = d_k_scale;
+    pp.v_scale = d_v_scale;
     pp.err = reinterpret_cast<unsigned*>(plan->ws);
     pp.kv_hnd = hnd ? 1 : 0;
     pp.rows_per_piece = B * plan->hq;

@@ -123,9 +123,10 @@ struct PrefixParams {
   int box_tok;              // keys per TMA box (min(page_size, 64))
   int n_splits;             // key-range pieces
   int tiles_per_split;      // 128-key tiles per piece
-  int m_tiles;              // 128-row query tiles per kv head
-  int cluster;              // CTAs per cluster sharing K/V tiles (1, 2, 4 or 8)
-  int m_groups;             // ceil(m_tiles / cluster)
+  int m_tiles;              // query tiles per kv head (one per CTA)
+  int cluster;              // CTAs per cluster (2: a pair of the shared-prefix kernel)
+  int m_groups;             // shared-prefix kernel: CTA pairs per kv head, ceil(m_tiles / 2)
+  int req_per_tile;         // shared-prefix kernel: requests per CTA, floor(128 / group)
   float scale_log2;
   float* pre_o;             // [split, B * Hq, D]
   float* pre_lse;           // [split, B * Hq] base 2
@@ -206,14 +207,16 @@ cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, 
                                cudaStream_t stream);
 cudaError_t launch_merge_states(const void* v, const float* s, int64_t n, int k, int heads, int dim,
                                 int dtype, void* vo, float* so, cudaStream_t stream);
+// shared-prefix attention on CTA pairs (pkd_prefix.cu); e4m3 pools take maps
+// of unswizzled code boxes (128 codes of K, 64 of V per row)
 cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                          const PrefixParams& p, int kv_dtype, cudaStream_t stream, bool pdl);
+                          const PrefixParams& p, int q_dtype, int kv_dtype, cudaStream_t stream, bool pdl);
 // work-list units in pairs (p.work, p.n_work even): one CTA per pair and kv head
 cudaError_t launch_tile2(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                          const PrefixParams& p, int kv_dtype, cudaStream_t stream, bool pdl);
 int decode_smem_bytes(int kv_dtype);
-int prefix_smem_bytes();
+int prefix_smem_bytes(int kv_dtype);
 int tile2_smem_bytes();
-int prefix_max_active_clusters(int cluster);  // 0 if the query fails
+int prefix_max_active_pairs(int q_dtype, int kv_dtype);  // resident CTA pairs, 0 if the query fails
 
 }  // namespace pkd

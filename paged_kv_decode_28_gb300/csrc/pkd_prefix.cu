@@ -1,91 +1,109 @@
-// pkd_prefix.cu -- tile attention on the sm_103a tensor cores (tcgen05 +
-// TMEM): a 128-row query tile of one kv head against a range of 128-key tiles
-// of the shared prefix's page list.
+// pkd_prefix.cu -- shared-prefix (cascade level 0) attention on pairs of SMs:
+// tcgen05 MMAs of cta_group::2 with TMEM accumulators, for sm_103a.
 //
 // Cascade decode attends one shared prefix for every request and merges that
 // state with each request's own (2026 guide, "Cascade attention for shared
 // prefixes"; deep dive, "Why This Design Works": the shared prefix is read once
 // but counted as if each request owns it).  For one kv head h the prefix part
-// is a dense product: the B * g query rows of the group (row r = b * g + j is
-// qo head h * g + j of request b) against the prefix keys.  One CTA takes a
-// 128-row query tile and a contiguous range of 128-key tiles of the prefix and
-// writes an fp32 partial state (o, base-2 lse) per row; the merge pass folds
-// these partials into each request's suffix states.
+// is a dense product: the B * g query rows of the group against the prefix
+// keys.  A CTA holds R = floor(128 / g) requests, i.e. R * g query rows (row r
+// is qo head h * g + r % g of request b0 + r / g; the rows past R * g are
+// zero); the two CTAs of a cluster form a pair and compute a 256-row product:
+// the MMA, issued by the even CTA, takes each CTA's 128 query rows and each
+// CTA's half of every key tile's K rows (keys 64 c .. 64 c + 63 of CTA c) and
+// V columns (head dims 64 c .. 64 c + 63), and leaves each CTA's rows of S and
+// of O in that CTA's TMEM.  So every SM receives half of each K/V tile it
+// multiplies, and no load is shared between CTAs (no multicast).  A pair takes
+// a contiguous range of 128-key tiles of the prefix and writes an fp32 partial
+// state (o, base-2 lse) per row; the merge pass folds these into each
+// request's suffix state.
 //
-// (The prefix tree's levels and paged prefill are work lists of query tiles in
-// pairs, run by the paired-tile kernel of pkd_tile2.cu.)
-//
-// CTAs run in clusters of C (1, 2, 4 or 8): the C query tiles of one kv head
-// and key range read the same K/V tiles, so each CTA fetches 1/C of every
-// tile's TMA boxes and multicasts them to the whole cluster, and a K or V slot
-// is reused only after all C CTAs have released it (their tcgen05.commit
-// arrives on the slot's "empty" barrier in every CTA).
-//
-// Per CTA (384 threads, one CTA per SM):
-//   warp 0      TMA producer of Q (once) and of the K ring; warp 2 producer of
-//               the V ring: key tiles page by page into two 3-stage rings
-//               (128-byte swizzled, K-major for K, MN-major for V); a K slot is
-//               freed as soon as its S product is done, a V slot when its P V
-//               product is done, so K loads run ahead of V;
-//   warp 1      allocates 512 TMEM columns and issues the MMAs from one thread:
-//               S = Q K^T into one of three S buffers (two tiles ahead of the
-//               P V product), then O += P_hi V + P_lo V with both parts of P
-//               read from TMEM; tcgen05.commit signals the mbarriers;
-//   warps 4..11 softmax, two threads per query row: warps 4 + q and 8 + q
-//               share TMEM lanes 32q .. 32q+31 (query rows), the first taking
-//               keys 0..63 of each tile and the second keys 64..127.  The two
-//               halves of a row swap their partial maxima through shared
-//               memory, keep one running reference max (rescaling O in TMEM,
-//               each its 64 columns, only when the tile max exceeds it by more
-//               than 8 in log2 units, which leaves the result exact), write P
-//               as two bf16/f16 parts (P_hi = round(P), P_lo = round(P - P_hi),
-//               so P reaches the product to ~2^-17 instead of the 16-bit type's
-//               2^-9 / 2^-11) into TMEM and keep partial row sums, added at the
-//               end.
-// TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512).  Tile
-// i uses S (i mod 3): once its scores are in registers, P_hi overwrites its
-// columns [0,64) and P_lo [64,128), so S u is rewritten (for tile i + 3) only
-// after the P V product of tile i is done.
+// Per CTA (384 threads; 512 with e4m3 pools):
+//   warp 0      Q (once) and the K ring, page by page: boxes of gcd(P, 64)
+//               keys, 128-byte swizzled, K-major.  16-bit pools load straight
+//               into the K slots and signal the even CTA's "K full" barrier
+//               (cta_group::2 loads), so it fires when both halves landed;
+//   warp 2      the V ring, this CTA's 64 head dims of all 128 keys, MN-major,
+//               signalled on this CTA's own "V full" barrier;
+//   warp 1      allocates the pair's 512 TMEM columns (both CTAs); in the even
+//               CTA one thread issues every MMA: S = Q K^T into one of three S
+//               buffers two tiles ahead of O += P_hi V + P_lo V, and commits
+//               to both CTAs' barriers;
+//   warps 4..11 softmax, two threads per query row (keys 0..63 / 64..127 of
+//               each tile): maximum with the row's other half through shared
+//               memory, a running reference max (O is rescaled in TMEM only
+//               when the tile max exceeds it by more than 8 in log2 units),
+//               P = 2^(s * scale - m) written over the scores as two 16-bit
+//               parts (P_hi = round(P), P_lo = round(P - P_hi), so P enters
+//               the product to ~2^-17); then, once this CTA's V tile has
+//               landed (zeroing V rows past the prefix end), one arrival per
+//               warp on the even CTA's "P full" barrier: the P V product of a
+//               tile waits for all 16 softmax warps of the pair;
+//   warps 12..15 (e4m3 pools only) widen the K and V codes, loaded by warps
+//               0 and 2 into staging slots, exactly into q's 16-bit type in the
+//               slots the MMAs read; the per-kv-head scales are folded into
+//               the score scale and the output.
+// TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512).  P of a
+// tile's keys 16k .. 16k + 15: P_hi of keys 16k + 2e, 16k + 2e + 1 in column
+// 16k + e, P_lo in column 16k + 8 + e (e = 0..7), over the scores of those keys.
 #include "pkd_internal.h"
 #include "pkd_ptx.cuh"
 
 namespace pkd {
 namespace {
 
-constexpr int kRows = 128;  // query rows per CTA
-constexpr int kKeys = 128;  // keys per tile
-constexpr int kThreads = 384;
+constexpr int kRows = 128;      // query rows per CTA (a pair computes 256)
+constexpr int kKeys = 128;      // keys per key tile (the S product's N)
+constexpr int kHalfKeys = 64;   // keys of a K tile one CTA holds
+constexpr int kStages = 3;      // ring depth of K and of V
 constexpr int kSoftmaxWarps = 8;
+constexpr int kConvWarps = 4;
 constexpr float kRescaleThreshold = 8.0f;
 
-constexpr int kHalf = 16384;   // one 64-element (128-byte) column half of a 128-row tile
-constexpr int kStage = 32768;  // a K (or V) tile: two halves
-constexpr int kStages = 3;     // ring depth of K and of V
-constexpr int kQ = 0;
-constexpr int kK = kQ + kStage;
-constexpr int kV = kK + kStages * kStage;
-constexpr int kBars = kV + kStages * kStage;
+template <bool FP8>
+struct PCfg {
+  static constexpr int kThreads = (4 + kSoftmaxWarps + (FP8 ? kConvWarps : 0)) * 32;
+  static constexpr int kQHalf = kRows * 128;      // [128 rows][128 B]: 64 of q's dims
+  static constexpr int kKHalf = kHalfKeys * 128;  // [64 keys][128 B]: 64 dims of this CTA's keys
+  static constexpr int kKStage = 2 * kKHalf;
+  static constexpr int kVStage = kKeys * 128;     // [128 keys][128 B]: this CTA's 64 dims
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + 2 * kQHalf;
+  static constexpr int kV = kK + kStages * kKStage;
+  // e4m3 codes as loaded: K [64 keys][128 B], V [128 keys][64 B] (this CTA's dims)
+  static constexpr int kK8Stage = kHalfKeys * 128;
+  static constexpr int kV8Stage = kKeys * 64;
+  static constexpr int kK8 = kV + kStages * kVStage;
+  static constexpr int kV8 = kK8 + (FP8 ? kStages * kK8Stage : 0);
+  static constexpr int kBars = kV8 + (FP8 ? kStages * kV8Stage : 0);
+  static constexpr int kTmemSlot = kBars + 64 * 8;
+  static constexpr int kAbort = kTmemSlot + 8;
+  static constexpr int kXchg = kAbort + 8;  // fp32 [buffer][half][row]: the halves' partial maxima / sums
+  static constexpr int kTotal = kXchg + 4 * 2 * 2 * kRows;
+  static constexpr int kAlloc = kTotal + 1024;
+  static_assert(kAlloc <= 227 * 1024, "dynamic shared memory above the 227 KB a CTA may use");
+};
+
 enum {
-  B_Q = 0,
-  B_KF = 1,                  // K full  [kStages]
-  B_KE = B_KF + kStages,     // K empty [kStages]
-  B_VF = B_KE + kStages,     // V full  [kStages]
-  B_VE = B_VF + kStages,     // V empty [kStages]
-  B_SF = B_VE + kStages,     // S full  [3]
-  B_PF = B_SF + 3,           // P full  [3]
-  B_OD = B_PF + 3,           // P V done [3]
-  B_DRAIN = B_OD + 3,
+  B_Q = 0,                   // Q of both CTAs landed (even CTA)
+  B_KF = 1,                  // K tile of both CTAs ready (even CTA) [kStages]
+  B_KE = B_KF + kStages,     // K slot free (each CTA) [kStages]
+  B_VF = B_KE + kStages,     // this CTA's V tile ready [kStages]
+  B_VE = B_VF + kStages,     // V slot free (each CTA) [kStages]
+  B_SF = B_VE + kStages,     // S ready (each CTA) [3]
+  B_PF = B_SF + 3,           // P of both CTAs written (even CTA) [3]
+  B_OD = B_PF + 3,           // P V done (each CTA) [3]
+  B_K8F = B_OD + 3,          // e4m3: codes landed [kStages]
+  B_K8E = B_K8F + kStages,   // e4m3: staging slot free [kStages]
+  B_V8F = B_K8E + kStages,
+  B_V8E = B_V8F + kStages,
+  B_DRAIN = B_V8E + kStages,
   kNumBars = B_DRAIN + 1
 };
-constexpr int kTmemSlot = kBars + kNumBars * 8;
-constexpr int kAbort = kTmemSlot + 8;
-constexpr int kXchg = kAbort + 16;  // fp32 [2 halves][128 rows]: the softmax halves' partial maxima / sums
-constexpr int kTotal = kXchg + 4 * 2 * kRows;
-constexpr int kAlloc = kTotal + 1024;
-static_assert(kAlloc <= 227 * 1024, "dynamic shared memory above the 227 KB a CTA may use");
+static_assert(kNumBars <= 64, "barrier area");
 
 constexpr uint32_t kColO = 384, kTmemCols = 512;
-__device__ __forceinline__ uint32_t col_s(int u) { return static_cast<uint32_t>(u) * 128u; }  // S buffer u
+__device__ __forceinline__ uint32_t col_s(int u) { return static_cast<uint32_t>(u) * 128u; }
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, unsigned* err, volatile int* abort_flag) {
   if (*abort_flag) return false;
@@ -101,68 +119,109 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigne
   return __all_sync(0xffffffffu, r);
 }
 
+// Eight E4M3 codes (bytes of w0, w1) -> eight 16-bit values (bf16 when BF,
+// else f16) as four packed pairs, exact: every E4M3 value is an f16 and a bf16.
 template <bool BF>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefix_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv, const PrefixParams p) {
+__device__ __forceinline__ void widen8(uint32_t w0, uint32_t w1, uint32_t (&o)[4]) {
+  const uint32_t w[2] = {w0, w1};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w[i]));
+    if constexpr (BF) {
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+      lo = ptx::pack2<true>(a.x, a.y);
+      hi = ptx::pack2<true>(b.x, b.y);
+    }
+    o[2 * i] = lo;
+    o[2 * i + 1] = hi;
+  }
+}
+
+template <bool BF, bool FP8>
+__global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
+    prefix_pair_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, const PrefixParams p) {
+  using C = PCfg<FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + kAbort);
-  auto bar = [&](int i) { return base + kBars + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kAbort);
+  auto bar = [&](int i) { return base + C::kBars + 8u * i; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   const int Hq = p.num_kv_heads * G;
-  const int C = p.cluster;
-  const int rank = static_cast<int>(ptx::cluster_ctarank());
-  const uint16_t cta_mask = static_cast<uint16_t>((1u << C) - 1u);
-  // this CTA's unit: kv head h, query rows from request b0 (requests past
-  // the batch are not written), prefix keys in tiles t0 .. t0+n-1, piece
-  // `split`; blockIdx.x = ((h * n_splits + split) * m_groups + mgroup) * C + rank
-  const int cl = blockIdx.x / C;
-  const int mgroup = cl % p.m_groups;
-  const int hs = cl / p.m_groups;
+  const int R = p.req_per_tile;  // requests per CTA
+  const uint32_t rank = ptx::cluster_ctarank() & 1u;
+  const bool lead = rank == 0;
+  // this pair's unit: kv head h, CTA rows from request b0, prefix keys in
+  // tiles t0 .. t0 + n - 1, piece `split`;
+  // blockIdx.x = ((h * n_splits + split) * m_groups + mpair) * 2 + rank
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int mpair = pair % p.m_groups;
+  const int hs = pair / p.m_groups;
   const int split = hs % p.n_splits;
   const int h = hs / p.n_splits;
-  const int mt = mgroup * C + rank;  // may pass m_tiles: such a CTA only helps load
-  const int b0 = mt * (kRows / G);
-  const int row_end = p.batch;
+  const int b0 = (2 * mpair + static_cast<int>(rank)) * R;  // may pass the batch: the CTA then only loads its halves
   const int kv_len = p.prefix_len;
   const int* pages = p.prefix_pages;
   const int n_tiles_all = (kv_len + kKeys - 1) / kKeys;
   const int t0 = split * p.tiles_per_split;
   const int n = max(min(t0 + p.tiles_per_split, n_tiles_all) - t0, 0);
-  const int piece = split;
+  const int used_rows = R * G;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(B_Q), 1);
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(bar(B_KF + s), 1);
-      ptx::mbar_init(bar(B_KE + s), C);
-      ptx::mbar_init(bar(B_VF + s), 1);
-      ptx::mbar_init(bar(B_VE + s), C);
+      // 16-bit pools: the even CTA's producer arrives with the pair's bytes;
+      // e4m3: the widening warps of both CTAs arrive
+      ptx::mbar_init(bar(B_KF + s), FP8 ? 2 * kConvWarps : 1);
+      ptx::mbar_init(bar(B_KE + s), 1);
+      ptx::mbar_init(bar(B_VF + s), FP8 ? kConvWarps : 1);
+      ptx::mbar_init(bar(B_VE + s), 1);
+      ptx::mbar_init(bar(B_K8F + s), 1);
+      ptx::mbar_init(bar(B_K8E + s), kConvWarps);
+      ptx::mbar_init(bar(B_V8F + s), 1);
+      ptx::mbar_init(bar(B_V8E + s), kConvWarps);
     }
-    for (int s = 0; s < 3; ++s) {
-      ptx::mbar_init(bar(B_SF + s), 1);
-      ptx::mbar_init(bar(B_PF + s), kSoftmaxWarps * 32);
-      ptx::mbar_init(bar(B_OD + s), 1);
+    for (int u = 0; u < 3; ++u) {
+      ptx::mbar_init(bar(B_SF + u), 1);
+      ptx::mbar_init(bar(B_PF + u), 2 * kSoftmaxWarps);
+      ptx::mbar_init(bar(B_OD + u), 1);
     }
     ptx::mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
+  // the odd CTA of the last pair may hold no request at all: it loads no Q
+  const bool has_q = b0 < p.batch;
+  if (warp == 0 && (used_rows < kRows || !has_q)) {
+    // query rows that get no box (past R * g, or all of them) are zero in both column halves
+    for (int i = (has_q ? used_rows : 0) * 8 + lane; i < kRows * 8; i += 32) {
+      const int r = i >> 3, c = i & 7;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(base_ptr + C::kQ + r * 128 + c * 16) = z;
+      *reinterpret_cast<uint4*>(base_ptr + C::kQ + C::kQHalf + r * 128 + c * 16) = z;
+    }
+    ptx::fence_proxy_async_smem();
+  }
   if (warp == 1) {
-    ptx::tmem_alloc(base + kTmemSlot, kTmemCols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair(base + C::kTmemSlot, kTmemCols);
+    ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before();
   __syncthreads();
-  ptx::cluster_sync();  // every CTA's barriers exist before any multicast reaches them
+  ptx::cluster_sync();  // both CTAs' barriers exist (and Q's zero rows are written) before any signal crosses
   ptx::tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base_ptr + kTmemSlot);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base_ptr + C::kTmemSlot);
+  const int box = p.box_tok;
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ TMA producers (K: warp 0, V: warp 2)
@@ -172,99 +231,107 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmq);
         ptx::prefetch_tensormap(&tmk);
         ptx::prefetch_tensormap(&tmv);
-        ptx::mbar_arrive_expect_tx(bar(B_Q), 2u * kHalf);
-        ptx::tma_load_4d(base + kQ, &tmq, bar(B_Q), 0, 0, h, b0);
-        ptx::tma_load_4d(base + kQ + kHalf, &tmq, bar(B_Q), 64, 0, h, b0);
+        // q viewed as [B][Hk][g][128]: a box of R requests x g heads of kv head h
+        // (the even CTA always holds requests; it expects the odd CTA's box bytes when that one does)
+        const uint32_t qbytes = static_cast<uint32_t>(used_rows) * 128u * 2u;
+        if (lead) ptx::mbar_arrive_expect_tx(bar(B_Q), (b0 + R < p.batch ? 2u : 1u) * qbytes);
+        if (has_q) {
+          const uint32_t lead_q = ptx::mapa(bar(B_Q), 0);  // the even CTA's barrier
+          ptx::tma_load_4d_pair(base + C::kQ, &tmq, lead_q, 0, 0, h, b0);
+          ptx::tma_load_4d_pair(base + C::kQ + C::kQHalf, &tmq, lead_q, 64, 0, h, b0);
+        }
       }
-      const int box = p.box_tok;
-      // this CTA's boxes of a tile are bx = rank + C * (lane + 32 * r); page ids
-      // are fetched two tiles ahead of their use
-      auto fetch = [&](int i, int (&pg)[4], int (&tk)[4]) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          pg[r] = 0;
-          tk[r] = 0;
-          if (i >= n) continue;
-          const int key0 = (t0 + i) * kKeys;
-          const int boxes = (min(kKeys, kv_len - key0) + box - 1) / box;
-          const int bx = rank + C * (lane + 32 * r);
-          if (bx < boxes) {
-            const int key = key0 + bx * box;
-            const int pi = key / p.page_size;
-            pg[r] = __ldg(pages + pi);  // checked at use, so the load stays in flight
-            tk[r] = key - pi * p.page_size;
-          }
+      // this CTA's keys of tile i: K rows key0 + 64 rank .. (kside), or all
+      // 128 keys of the tile (V side); boxes of `box` keys never cross a page
+      auto span = [&](int i, int& first, int& cnt) {
+        const int key0 = (t0 + i) * kKeys;
+        if (kside) {
+          first = key0 + kHalfKeys * static_cast<int>(rank);
+          cnt = min(max(kv_len - first, 0), kHalfKeys);
+        } else {
+          first = key0;
+          cnt = min(kv_len - key0, kKeys);
         }
       };
-      const int eb = kside ? B_KE : B_VE;
-      const int fb = kside ? B_KF : B_VF;
+      const int fb = FP8 ? (kside ? B_K8F : B_V8F) : (kside ? B_KF : B_VF);
+      const int eb = FP8 ? (kside ? B_K8E : B_V8E) : (kside ? B_KE : B_VE);
       const CUtensorMap* map = kside ? &tmk : &tmv;
-      const uint32_t ring = kside ? kK : kV;
-      auto issue = [&](int i, const int (&pg)[4], const int (&tk)[4]) -> bool {
+      // bytes one box puts in shared memory: K 128-byte rows (per column half
+      // for 16-bit pools), V rows of this CTA's 64 dims (64 B of codes, or 128 B)
+      const uint32_t row_bytes = FP8 ? (kside ? 128u : 64u) : 128u;
+      const uint32_t slot = FP8 ? (kside ? C::kK8 : C::kV8) : (kside ? C::kK : C::kV);
+      const uint32_t slot_bytes = FP8 ? (kside ? C::kK8Stage : C::kV8Stage) : (kside ? C::kKStage : C::kVStage);
+      const int vcol = FP8 ? 0 : 64 * static_cast<int>(rank);  // 16-bit V: this CTA's column half of the map
+      for (int i = 0; i < n; ++i) {
         const int s = i % kStages;
         const uint32_t par = ((i / kStages) & 1) ^ 1;
-        const int key0 = (t0 + i) * kKeys;
-        const int boxes = (min(kKeys, kv_len - key0) + box - 1) / box;
-        const uint32_t tile_bytes = static_cast<uint32_t>(boxes) * box * 128u * 2u;  // all CTAs' boxes
-        if (!warp_wait(bar(eb + s), par, p.err, abort_flag)) return false;
-        if (lane == 0) ptx::mbar_arrive_expect_tx(bar(fb + s), tile_bytes);
+        int first, cnt;
+        span(i, first, cnt);
+        const int boxes = (cnt + box - 1) / box;
+        if (!warp_wait(bar(eb + s), par, p.err, abort_flag)) break;
+        const uint32_t dst0 = base + slot + s * slot_bytes;
+        uint32_t full;  // the barrier the loads signal
+        if (!FP8 && kside) {
+          // the even CTA expects both CTAs' K bytes of this tile (its own cnt
+          // keys and the odd CTA's, from key0 + 64 on), two column halves each
+          if (lead && lane == 0) {
+            const int c1 = min(max(kv_len - ((t0 + i) * kKeys + kHalfKeys), 0), kHalfKeys);
+            const uint32_t bytes = static_cast<uint32_t>(((cnt + box - 1) / box + (c1 + box - 1) / box) * box) * 256u;
+            ptx::mbar_arrive_expect_tx(bar(B_KF + s), bytes);
+          }
+          full = ptx::mapa(bar(B_KF + s), 0);
+        } else {
+          if (lane == 0) {
+            const uint32_t per_box = static_cast<uint32_t>(box) * row_bytes * ((!FP8 && kside) ? 2u : 1u);
+            ptx::mbar_arrive_expect_tx(bar(fb + s), static_cast<uint32_t>(boxes) * per_box);
+          }
+          full = bar(fb + s);
+        }
         __syncwarp();
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int bx = rank + C * (lane + 32 * r);
-          if (bx < boxes) {
-            int page = pg[r];
-            if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
-              atomicOr(p.err, kDevErrPageIndex);
-              page = 0;
-            }
-            const uint32_t d = base + ring + s * kStage + static_cast<uint32_t>(bx * box) * 128u;
-            // map coordinates (dim, head, key, page) for NHD pages, (dim, key, head, page) for HND
-            const int c1 = p.kv_hnd ? tk[r] : h, c2 = p.kv_hnd ? h : tk[r];
-            ptx::tma_load_4d_mc(d, map, bar(fb + s), 0, c1, c2, page, cta_mask);
-            ptx::tma_load_4d_mc(d + kHalf, map, bar(fb + s), 64, c1, c2, page, cta_mask);
+        for (int j = lane; j < boxes; j += 32) {
+          const int key = first + j * box;
+          const int pi = key / p.page_size;
+          int page = __ldg(pages + pi);
+          if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
+            atomicOr(p.err, kDevErrPageIndex);
+            page = 0;
+          }
+          const int tk = key - pi * p.page_size;
+          // map coordinates (dim, head, key, page) for NHD pages, (dim, key, head, page) for HND
+          const int c1 = p.kv_hnd ? tk : h, c2 = p.kv_hnd ? h : tk;
+          const uint32_t d = dst0 + static_cast<uint32_t>(j * box) * row_bytes;
+          if (!FP8 && kside) {
+            ptx::tma_load_4d_pair(d, map, full, 0, c1, c2, page);
+            ptx::tma_load_4d_pair(d + C::kKHalf, map, full, 64, c1, c2, page);
+          } else if (!FP8) {
+            ptx::tma_load_4d(d, map, full, vcol, c1, c2, page);
+          } else {
+            ptx::tma_load_4d(d, map, full, kside ? 0 : 64 * static_cast<int>(rank), c1, c2, page);
           }
         }
-        return true;
-      };
-      // three register sets in rotation, unrolled so that no set is copied
-      // while its loads are in flight: tile i's ids were requested two tiles earlier
-      int pgA[4], tkA[4], pgB[4], tkB[4], pgC[4], tkC[4];
-      fetch(0, pgA, tkA);
-      fetch(1, pgB, tkB);
-      for (int i = 0; i < n; i += 3) {
-        fetch(i + 2, pgC, tkC);
-        if (!issue(i, pgA, tkA)) break;
-        if (i + 1 >= n) break;
-        fetch(i + 3, pgA, tkA);
-        if (!issue(i + 1, pgB, tkB)) break;
-        if (i + 2 >= n) break;
-        fetch(i + 4, pgB, tkB);
-        if (!issue(i + 2, pgC, tkC)) break;
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
-      constexpr uint32_t idesc_s = ptx::idesc_f16(BF, false, kRows, kKeys);
-      constexpr uint32_t idesc_pv = ptx::idesc_f16(BF, true, kRows, kHeadDim);
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lead && lane == 0 && n > 0) {
+      constexpr uint32_t idesc_s = ptx::idesc_f16(BF, false, 2 * kRows, kKeys);
+      constexpr uint32_t idesc_pv = ptx::idesc_f16(BF, true, 2 * kRows, kHeadDim);
       bool ok = wait_or_abort(bar(B_Q), 0, p.err, abort_flag);
       auto pv = [&](int t) -> bool {
         const int u = t % 3;
         const int sv = t % kStages;
+        // P of both CTAs written, and both CTAs' V tiles landed
         if (!wait_or_abort(bar(B_PF + u), (t / 3) & 1, p.err, abort_flag)) return false;
-        if (!wait_or_abort(bar(B_VF + sv), (t / kStages) & 1, p.err, abort_flag)) return false;
         ptx::tc_fence_after();
-        const uint32_t pcol = col_s(u);       // P_hi
-        const uint32_t lcol = col_s(u) + 64;  // P_lo
+        const uint32_t pcol = col_s(u);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t bdesc = ptx::smem_desc_sw128(base + kV + sv * kStage + k * 2048, kHalf, 1024);
-          ptx::umma_ts(tmem + kColO, tmem + pcol + 8 * k, bdesc, idesc_pv, (t > 0 || k > 0) ? 1u : 0u);
-          ptx::umma_ts(tmem + kColO, tmem + lcol + 8 * k, bdesc, idesc_pv, 1u);
+          const uint64_t bdesc = ptx::smem_desc_sw128(base + C::kV + sv * C::kVStage + k * 2048, C::kVStage, 1024);
+          ptx::umma_ts_pair(tmem + kColO, tmem + pcol + 16 * k, bdesc, idesc_pv, (t > 0 || k > 0) ? 1u : 0u);
+          ptx::umma_ts_pair(tmem + kColO, tmem + pcol + 16 * k + 8, bdesc, idesc_pv, 1u);
         }
-        ptx::tc_commit(bar(B_OD + u));
-        if (t + kStages < n) ptx::tc_commit_mc(bar(B_VE + sv), cta_mask);
+        ptx::tc_commit_pair(bar(B_OD + u), 3);
+        if (t + kStages < n) ptx::tc_commit_pair(bar(B_VE + sv), 3);
         return true;
       };
       for (int i = 0; i < n && ok; ++i) {
@@ -272,19 +339,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sk = i % kStages;
         if (!wait_or_abort(bar(B_KF + sk), (i / kStages) & 1, p.err, abort_flag)) break;
         // S u holds P of tile i - 3 until that tile's P V product is done
-        // (issued by this thread in the previous iteration)
         if (i >= 3 && !wait_or_abort(bar(B_OD + u), ((i - 3) / 3) & 1, p.err, abort_flag)) break;
         ptx::tc_fence_after();
-        const uint32_t scol = col_s(u);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
-          const uint64_t adesc = ptx::smem_desc_sw128(base + kQ + koff, 16, 1024);
-          const uint64_t bdesc = ptx::smem_desc_sw128(base + kK + sk * kStage + koff, 16, 1024);
-          ptx::umma_ss(tmem + scol, adesc, bdesc, idesc_s, k > 0 ? 1u : 0u);
+          const uint64_t adesc =
+              ptx::smem_desc_sw128(base + C::kQ + (k >> 2) * C::kQHalf + (k & 3) * 32, 16, 1024);
+          const uint64_t bdesc =
+              ptx::smem_desc_sw128(base + C::kK + sk * C::kKStage + (k >> 2) * C::kKHalf + (k & 3) * 32, 16, 1024);
+          ptx::umma_ss_pair(tmem + col_s(u), adesc, bdesc, idesc_s, k > 0 ? 1u : 0u);
         }
-        ptx::tc_commit(bar(B_SF + u));
-        if (i + kStages < n) ptx::tc_commit_mc(bar(B_KE + sk), cta_mask);
+        ptx::tc_commit_pair(bar(B_SF + u), 3);
+        if (i + kStages < n) ptx::tc_commit_pair(bar(B_KE + sk), 3);
         // the P V product runs two tiles behind S
         if (i >= 2 && !pv(i - 2)) {
           ok = false;
@@ -294,63 +360,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && !*abort_flag && n >= 2) ok = pv(n - 2);
       if (ok && !*abort_flag) pv(n - 1);
       // drain: every MMA issued above has finished before TMEM is released
-      ptx::tc_commit(bar(B_DRAIN));
+      ptx::tc_commit_pair_local(bar(B_DRAIN));
       ptx::mbar_wait(bar(B_DRAIN), 0, p.err);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 4 + kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax
     const int wq = warp & 3;
     const int hf = (warp - 4) >> 2;  // keys [64 hf, 64 hf + 64) of each tile
     const int row = wq * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
-    float* xchg = reinterpret_cast<float*>(base_ptr + kXchg);  // [half][row]
-    const float sl2 = p.scale_log2;
+    const int bar_id = 1 + wq;  // the row's two halves
+    float* xchg = reinterpret_cast<float*>(base_ptr + C::kXchg);  // [buffer][half][row]
+    const float ksc = FP8 ? __ldg(p.k_scale + h) : 1.f;
+    const float sl2 = p.scale_log2 * ksc;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    // this thread's query row: request tok, qo head h * G + jj
-    const int tok = b0 + row / G;
+    // this thread's query row: request b, qo head h * G + jj
+    const int b = b0 + row / G;
     const int jj = row - (row / G) * G;
-    // Each iteration passes the pair's named barrier exactly twice, also after
-    // a failed wait (ok false: the rest of the work is skipped, and every later
+    const uint32_t scol_base = tmem + lanes + 64 * hf;
+    const uint32_t ocol = tmem + lanes + kColO + 64 * hf;
+    // Each iteration passes the row's named barrier exactly once, also after a
+    // failed wait (ok false: the rest of the work is skipped, and every later
     // wait returns at once on the abort flag), so the two halves never wait at
     // barriers the other does not reach.
     for (int i = 0; i < n; ++i) {
       const int u = i % 3;
       ok = ok && warp_wait(bar(B_SF + u), (i / 3) & 1, p.err, abort_flag);
-      const uint32_t scol = tmem + lanes + col_s(u);
-      uint32_t sr[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) sr[c] = __float_as_uint(-INFINITY);
-      if (ok) {
-        ptx::tc_fence_after();
-        ptx::tmem_ld32(scol + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        ptx::tmem_ld32(scol + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        ptx::tmem_ld_wait();
-      }
+      const uint32_t scol = scol_base + col_s(u);
       const int key0 = (t0 + i) * kKeys;
       const int nv = min(kKeys, kv_len - key0);
-      // the tile's keys before the prefix's end, counted within this thread's half
-      const int vr = min(max(nv - 64 * hf, 0), 64);
-      // mask, then a tree max of the raw scores (the scale is positive, so it
-      // commutes with max): 8 independent chains, then the other half's
+      const int vr = min(max(nv - 64 * hf, 0), 64);  // keys before the prefix end in this half
+      // the maximum of the raw scores (the scale is positive, so it commutes
+      // with max): 8 independent chains, then the other half's
       float m8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
-      if (vr < 64) {
+      if (ok) {
+        ptx::tc_fence_after();
+        uint32_t sr[64];
+        ptx::tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        ptx::tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        ptx::tmem_ld_wait();
+        if (vr < 64) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c >= vr) sr[c] = __float_as_uint(-INFINITY);
+          for (int e = 0; e < 64; ++e)
+            if (e >= vr) sr[e] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int e = 0; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sr[e]));
       }
-#pragma unroll
-      for (int c = 0; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
       const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                              fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      xchg[hf * kRows + row] = mh;
-      // both halves' scores are in registers past this barrier, so P may
-      // overwrite any column of S u
-      ptx::named_bar_sync(1 + wq, 64);
-      const float mo = xchg[(hf ^ 1) * kRows + row];
-      ptx::named_bar_sync(1 + wq, 64);  // both have read before the next tile writes
+      // one barrier per tile: tile i uses buffer i % 2, and a half writes that
+      // buffer again (tile i + 2) only after passing tile i + 1's barrier,
+      // which its partner reaches after reading tile i's value
+      float* xb = xchg + (i & 1) * 2 * kRows;
+      xb[hf * kRows + row] = mh;
+      ptx::named_bar_sync(bar_id, 64);
+      const float mo = xb[(hf ^ 1) * kRows + row];
       if (!ok) continue;
       const float mx = sl2 * fmaxf(mh, mo);
       const bool need = (i > 0) && (mx > m_ref + kRescaleThreshold);
@@ -365,11 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          ptx::tmem_ld32(tmem + lanes + kColO + 64 * hf + 32 * c, o);
+          ptx::tmem_ld32(ocol + 32 * c, o);
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          ptx::tmem_st32(tmem + lanes + kColO + 64 * hf + 32 * c, o);
+          ptx::tmem_st32(ocol + 32 * c, o);
         }
         ptx::tmem_st_wait();
         if (need) {
@@ -377,72 +445,83 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mx;
         }
       }
-      // P goes into S u itself: P_hi of keys 2c, 2c + 1 in column c, P_lo in
-      // column 64 + c (this half: columns 32 hf .. 32 hf + 31 of each)
-      const uint32_t pcol = scol + 32 * hf;
-      const uint32_t lcol = scol + 64 + 32 * hf;
+      // P over the scores, sixteen keys at a time: P_hi of the block's keys
+      // in its first 8 columns, P_lo in the last 8
       float rs[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) rs[e] = 0.f;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16], pl[16];
+        uint32_t sr[32];
+        ptx::tmem_ld32(scol + 32 * c, sr);
+        ptx::tmem_ld_wait();
+        const int vc = vr - 32 * c;
+        if (vc < 32) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e]), sl2, -m_ref));
-          const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e + 1]), sl2, -m_ref));
-          rs[e & 7] += p0 + p1;
-          ptx::split2<BF>(p0, p1, pk[e], pl[e]);
+          for (int e = 0; e < 32; ++e)
+            if (e >= vc) sr[e] = __float_as_uint(-INFINITY);
         }
-        ptx::tmem_st16(pcol + 16 * c, pk);
-        ptx::tmem_st16(lcol + 16 * c, pl);
+#pragma unroll
+        for (int bk = 0; bk < 2; ++bk) {
+          uint32_t pp[16];  // P_hi pairs, then P_lo pairs
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[16 * bk + 2 * e]), sl2, -m_ref));
+            const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[16 * bk + 2 * e + 1]), sl2, -m_ref));
+            rs[e] += p0 + p1;
+            ptx::split2<BF>(p0, p1, pp[e], pp[8 + e]);
+          }
+          ptx::tmem_st16(scol + 32 * c + 16 * bk, pp);
+        }
       }
       l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-      if (nv < kKeys) {
-        // keys past the prefix's end: their P is 0, and their V rows must be
-        // finite for the product, so zero them (each half one column half)
-        // once the tile's V has landed
-        if (!warp_wait(bar(B_VF + i % kStages), (i / kStages) & 1, p.err, abort_flag)) {
-          ok = false;
-          continue;
-        }
+      // this CTA's V tile must have landed before the pair's P V product; keys
+      // past the prefix end have P = 0 and their V rows must be finite, so the
+      // first half's threads zero them (16-bit pools; the widening warps do it
+      // for e4m3 pools)
+      const int sv = i % kStages;
+      if (!warp_wait(bar(B_VF + sv), (i / kStages) & 1, p.err, abort_flag)) {
+        ok = false;
+        continue;
       }
-      if (nv < kKeys && row >= nv) {
-        uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        uint8_t* vrow = base_ptr + kV + (i % kStages) * kStage + hf * kHalf + row * 128;
+      if (!FP8 && hf == 0 && row >= nv) {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        uint8_t* vrow_p = base_ptr + C::kV + sv * C::kVStage + row * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + 16 * c) = z;
+        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow_p + 16 * c) = z;
         ptx::fence_proxy_async_smem();
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(B_PF + u));
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(bar(B_PF + u), 0));
     }
-    // ---- epilogue: o = O / l, lse2 = m_ref + log2(l) into piece `piece` as
+    // ---- epilogue: o = O / l, lse2 = m_ref + log2(l) into piece `split` as
     // an fp32 partial state; each half writes its 64 columns, the first half
     // the lse
-    const bool row_valid = tok < row_end;
-    const size_t orow = static_cast<size_t>(tok) * Hq + h * G + jj;
-    const size_t sidx = static_cast<size_t>(piece) * p.rows_per_piece + orow;
+    const bool row_valid = row < used_rows && b < p.batch;
+    const size_t orow = static_cast<size_t>(b) * Hq + h * G + jj;
+    const size_t sidx = static_cast<size_t>(split) * p.rows_per_piece + orow;
     float* dst = p.pre_o + sidx * kHeadDim + 64 * hf;
     // the row sum is the two halves' partial sums (every thread arrives here,
     // also after a failed wait, so the barrier is always complete)
-    xchg[hf * kRows + row] = l;
-    ptx::named_bar_sync(1 + wq, 64);
-    l += xchg[(hf ^ 1) * kRows + row];
+    float* xe = xchg + (n & 1) * 2 * kRows;  // the buffer a tile n would use
+    xe[hf * kRows + row] = l;
+    ptx::named_bar_sync(bar_id, 64);
+    l += xe[(hf ^ 1) * kRows + row];
     if (n > 0 && ok && warp_wait(bar(B_OD + (n - 1) % 3), ((n - 1) / 3) & 1, p.err, abort_flag)) {
       ptx::tc_fence_after();
-      const float inv = 1.f / l;
+      const float inv = (FP8 ? __ldg(p.v_scale + h) : 1.f) / l;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        ptx::tmem_ld32(tmem + lanes + kColO + 64 * hf + 32 * c, o);
+        ptx::tmem_ld32(ocol + 32 * c, o);
         ptx::tmem_ld_wait();
         if (row_valid) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            float4 v = make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                                   __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            const float4 v = make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                                         __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
             *reinterpret_cast<float4*>(dst + 32 * c + e) = v;
           }
         }
@@ -452,14 +531,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int d = 0; d < 64; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
       if (hf == 0) p.pre_lse[sidx] = -INFINITY;
     }
+  } else if (FP8 && warp >= 4 + kSoftmaxWarps) {
+    // ------------------------------------------------------------ e4m3 widening (K and V)
+    const int ct = threadIdx.x - (4 + kSoftmaxWarps) * 32;  // 0..127
+    for (int i = 0; i < n; ++i) {
+      const int s = i % kStages;
+      const uint32_t ph = (i / kStages) & 1;
+      const uint32_t freep = ph ^ 1u;
+      const int key0 = (t0 + i) * kKeys;
+      const int nv = min(kKeys, kv_len - key0);
+      // K: [64 keys][128 codes] -> [2 halves][64 keys][128 B], swizzled
+      if (!warp_wait(bar(B_K8F + s), ph, p.err, abort_flag) || !warp_wait(bar(B_KE + s), freep, p.err, abort_flag))
+        break;
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int item = ct + 128 * it;  // (key, 16-code chunk)
+        const int key = item >> 3, c = item & 7;
+        const uint4 raw = *reinterpret_cast<const uint4*>(base_ptr + C::kK8 + s * C::kK8Stage + key * 128 + c * 16);
+        uint32_t a[4], bq[4];
+        widen8<BF>(raw.x, raw.y, a);
+        widen8<BF>(raw.z, raw.w, bq);
+        const uint32_t half = static_cast<uint32_t>(c >> 2), ch = 2u * static_cast<uint32_t>(c & 3);
+        const uint32_t kb = base + C::kK + s * C::kKStage + half * C::kKHalf;
+        ptx::sts128(kb + ptx::sw128(key, ch), a[0], a[1], a[2], a[3]);
+        ptx::sts128(kb + ptx::sw128(key, ch + 1), bq[0], bq[1], bq[2], bq[3]);
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive_cluster(ptx::mapa(bar(B_KF + s), 0));  // the pair's K tile: both CTAs' widening warps
+        ptx::mbar_arrive(bar(B_K8E + s));
+      }
+      // V: [128 keys][64 codes] (this CTA's dims) -> [128 keys][128 B], swizzled; rows past the end zero
+      if (!warp_wait(bar(B_V8F + s), ph, p.err, abort_flag) || !warp_wait(bar(B_VE + s), freep, p.err, abort_flag))
+        break;
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int item = ct + 128 * it;
+        const int key = item >> 2, c = item & 3;
+        uint32_t a[4] = {0u, 0u, 0u, 0u}, bq[4] = {0u, 0u, 0u, 0u};
+        if (key < nv) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(base_ptr + C::kV8 + s * C::kV8Stage + key * 64 + c * 16);
+          widen8<BF>(raw.x, raw.y, a);
+          widen8<BF>(raw.z, raw.w, bq);
+        }
+        const uint32_t vb = base + C::kV + s * C::kVStage;
+        ptx::sts128(vb + ptx::sw128(key, 2u * c), a[0], a[1], a[2], a[3]);
+        ptx::sts128(vb + ptx::sw128(key, 2u * c + 1u), bq[0], bq[1], bq[2], bq[3]);
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(bar(B_VF + s));
+        ptx::mbar_arrive(bar(B_V8E + s));
+      }
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
-  // no CTA leaves while a peer may still deliver into its shared memory
+  // neither CTA leaves (or frees TMEM) while the pair's MMAs or loads may still
+  // touch its shared memory or TMEM
   ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    ptx::tmem_dealloc_pair(tmem, kTmemCols);
   }
   // This grid is launched programmatically behind the decode grid and reads
   // nothing it writes; it does not finish before that grid has, so the merge
@@ -467,56 +602,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) ptx::pdl_wait_prior_grid();
 }
 
+template <bool BF, bool FP8>
+void* kernel_ptr() {
+  return reinterpret_cast<void*>(prefix_pair_kernel<BF, FP8>);
+}
+
+void* pick(int q_dtype, int kv_dtype) {
+  const bool bf = q_dtype == kBF16;
+  if (kv_dtype == kE4M3) return bf ? kernel_ptr<true, true>() : kernel_ptr<false, true>();
+  return bf ? kernel_ptr<true, false>() : kernel_ptr<false, false>();
+}
+
+int smem_of(int kv_dtype) { return kv_dtype == kE4M3 ? PCfg<true>::kAlloc : PCfg<false>::kAlloc; }
+int threads_of(int kv_dtype) { return kv_dtype == kE4M3 ? PCfg<true>::kThreads : PCfg<false>::kThreads; }
+
 }  // namespace
 
-int prefix_smem_bytes() { return kAlloc; }
+int prefix_smem_bytes(int kv_dtype) { return smem_of(kv_dtype); }
 
-int prefix_max_active_clusters(int cluster) {
-  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, PrefixParams) = prefix_kernel<true>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc) != cudaSuccess) return 0;
+int prefix_max_active_pairs(int q_dtype, int kv_dtype) {
+  const void* kern = pick(q_dtype, kv_dtype);
+  const int smem = smem_of(kv_dtype);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cluster);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kAlloc;
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(threads_of(kv_dtype));
+  cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+  int nclusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  return n;
+  return nclusters;
 }
 
 cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                          const PrefixParams& p, int kv_dtype, cudaStream_t stream, bool pdl) {
-  const int grid = p.num_kv_heads * p.n_splits * p.m_groups * p.cluster;
+                          const PrefixParams& p, int q_dtype, int kv_dtype, cudaStream_t stream, bool pdl) {
+  const int grid = p.num_kv_heads * p.n_splits * p.m_groups * 2;
   if (grid <= 0) return cudaSuccess;
-  if (kv_dtype != kBF16 && kv_dtype != kF16) return cudaErrorInvalidValue;
-  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, PrefixParams) =
-      kv_dtype == kBF16 ? prefix_kernel<true> : prefix_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+  if (!(q_dtype == kBF16 || q_dtype == kF16) || !(kv_dtype == q_dtype || kv_dtype == kE4M3))
+    return cudaErrorInvalidValue;
+  const void* kern = pick(q_dtype, kv_dtype);
+  const int smem = smem_of(kv_dtype);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kAlloc;
+  cfg.blockDim = dim3(threads_of(kv_dtype));
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.cluster;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, kern, tmq, tmk, tmv, p);
+  void* args[] = {const_cast<CUtensorMap*>(&tmq), const_cast<CUtensorMap*>(&tmk), const_cast<CUtensorMap*>(&tmv),
+                  const_cast<PrefixParams*>(&p)};
+  e = cudaLaunchKernelExC(&cfg, kern, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -21,7 +21,8 @@ def _gpu_cascade(b, plan=None):
     if plan is None:
         plan = pkd.Plan(b.batch, b.num_qo_heads, b.num_kv_heads, max_prefix_splits=16)
     plan.plan(b.kv_indptr, idx, b.kv_last_page_len, b.page_size, q_dtype=b.q.dtype, kv_dtype=b.k_cache.dtype)
-    out, lse = plan.cascade_decode(pre, b.prefix_last_page_len, b.q, b.k_cache, b.v_cache, sm_scale=b.sm_scale)
+    out, lse = plan.cascade_decode(pre, b.prefix_last_page_len, b.q, b.k_cache, b.v_cache, sm_scale=b.sm_scale,
+                                   k_scale=b.k_scale, v_scale=b.v_scale)
     torch.cuda.synchronize()
     assert plan.check_device_errors() == 0
     return out, lse
@@ -30,7 +31,8 @@ def _gpu_cascade(b, plan=None):
 def _oracle(b, rows=None):
     pre = b.prefix_page_indices if b.prefix_page_indices is not None else np.zeros(0, np.int32)
     return orc.cascade_decode(b.q, b.k_cache, b.v_cache, pre, b.prefix_last_page_len, b.kv_indptr,
-                              b.kv_page_indices, b.kv_last_page_len, sm_scale=b.sm_scale, rows=rows)
+                              b.kv_page_indices, b.kv_last_page_len, sm_scale=b.sm_scale, k_scale=b.k_scale,
+                              v_scale=b.v_scale, rows=rows)
 
 
 @pytest.mark.parametrize("prefix_len", [1, 15, 63, 64, 65, 127, 128, 129, 191, 1000])
@@ -53,6 +55,76 @@ def test_cascade_few_prefix_keys_many_requests(prefix_len):
     lengths = rng.integers(0, 3, size=300).tolist()
     b = wl.make_paged(seed=620 + prefix_len, lengths=lengths, num_qo_heads=16, num_kv_heads=2, page_size=16,
                       prefix_len=prefix_len, device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+@pytest.mark.parametrize("prefix_len", [1, 2, 63, 64, 65, 128, 129, 1000])
+@pytest.mark.parametrize("q_dtype", ["bf16", "f16"])
+def test_cascade_e4m3_pool(prefix_len, q_dtype):
+    """E4M3 K/V with per-kv-head scales: the prefix codes are widened exactly
+    to q's type before the tensor-core products."""
+    b = wl.make_paged(seed=700 + prefix_len, lengths=[0, 1, 17, 300, 64, 5, 129], num_qo_heads=16,
+                      num_kv_heads=4, page_size=16, q_dtype=q_dtype, kv_dtype="e4m3", prefix_len=prefix_len,
+                      device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+@pytest.mark.parametrize("prefix_len", [1, 3])
+def test_cascade_e4m3_few_prefix_keys_many_requests(prefix_len):
+    rng = np.random.default_rng(72 + prefix_len)
+    lengths = rng.integers(0, 3, size=300).tolist()
+    b = wl.make_paged(seed=720 + prefix_len, lengths=lengths, num_qo_heads=16, num_kv_heads=2, page_size=64,
+                      q_dtype="bf16", kv_dtype="e4m3", prefix_len=prefix_len, device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+def test_cascade_e4m3_long_context_sampled():
+    """The long-context fp8 geometry (64 / 8 heads, page 64) with a shared
+    prefix of 8192 keys and 160 requests, sampled rows."""
+    rng = np.random.default_rng(73)
+    lengths = rng.integers(64, 2048, size=160).tolist()
+    b = wl.make_paged(seed=730, lengths=lengths, num_qo_heads=64, num_kv_heads=8, page_size=64,
+                      q_dtype="bf16", kv_dtype="e4m3", prefix_len=8192, device="cuda")
+    out, lse = _gpu_cascade(b)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    rows = sample_rows(b, 40, seed=73)
+    o_ref, l_ref = _oracle(b, rows)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+@pytest.mark.parametrize("g", [3, 5, 6, 7])
+@pytest.mark.parametrize("prefix_len", [1, 200, 1000])
+def test_cascade_odd_groups(g, prefix_len):
+    """Group sizes that do not divide 128: a CTA holds floor(128 / g) requests
+    and its last rows stay empty; batches leave the last pair half empty."""
+    rng = np.random.default_rng(g * 10 + prefix_len)
+    B = 2 * (128 // g) + 5  # three CTA row tiles: the second pair's odd CTA is past the batch
+    lens = rng.integers(0, 300, size=B)
+    b = wl.make_paged(seed=740 + g + prefix_len, lengths=lens, num_qo_heads=2 * g, num_kv_heads=2, page_size=16,
+                      prefix_len=prefix_len, device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
+@pytest.mark.parametrize("prefix_len", [1, 47, 48, 49, 130, 1000])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_cascade_page_48(prefix_len, kv_dtype):
+    """A page size that is neither a divisor of the 128-key tile nor a multiple
+    of 64: boxes of gcd(48, 64) = 16 keys, tiles straddling pages."""
+    b = wl.make_paged(seed=760 + prefix_len, lengths=[0, 1, 47, 48, 49, 500], num_qo_heads=32, num_kv_heads=8,
+                      page_size=48, q_dtype="bf16", kv_dtype=kv_dtype, prefix_len=prefix_len, device="cuda")
     out, lse = _gpu_cascade(b)
     o_ref, l_ref = _oracle(b)
     assert_o_close(out, o_ref)
