@@ -146,7 +146,7 @@ pkd_status encode_kv_map(CUtensorMap* m, const void* base, int kv_dtype, int hk,
 
 // CTA pairs of the shared-prefix kernel that fit on the current device at
 // once (queried once per device and kernel variant; 0 when unknown).
-int resident_prefix_pairs(int q_dtype, int kv_dtype) {
+int resident_prefix_clusters(int q_dtype, int kv_dtype) {
   static std::mutex mu;
   static int cache[64][2][2] = {};
   int dev = 0;
@@ -154,7 +154,7 @@ int resident_prefix_pairs(int q_dtype, int kv_dtype) {
   const int qi = q_dtype == PKD_BF16 ? 1 : 0, ki = kv_dtype == PKD_E4M3 ? 1 : 0;
   std::lock_guard<std::mutex> lock(mu);
   if (cache[dev][qi][ki] == 0) {
-    const int n = pkd::prefix_max_active_pairs(q_dtype, kv_dtype);
+    const int n = pkd::prefix_max_active_clusters(q_dtype, kv_dtype);
     cache[dev][qi][ki] = n > 0 ? n : -1;
   }
   return cache[dev][qi][ki] > 0 ? cache[dev][qi][ki] : 0;
@@ -963,7 +963,7 @@ pkd_status pkd_cascade_decode(pkd_plan_t plan, const int32_t* d_prefix_page_indi
     const int n_tiles = (prefix_len + 127) / 128;
     const int m_tiles = (B + R - 1) / R;
     const int m_pairs = (m_tiles + 1) / 2;
-    int resident = resident_prefix_pairs(plan->q_dtype, plan->kv_dtype);
+    int resident = resident_prefix_clusters(plan->q_dtype, plan->kv_dtype);
     if (resident <= 0) resident = plan->G / (2 * pkd::kCtasPerSm);
     int splits = resident / (plan->hk * m_pairs);
     splits = splits < 1 ? 1 : splits;

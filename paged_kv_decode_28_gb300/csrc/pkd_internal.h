@@ -217,6 +217,6 @@ cudaError_t launch_tile2(const CUtensorMap& tmq, const CUtensorMap& tmk, const C
 int decode_smem_bytes(int kv_dtype);
 int prefix_smem_bytes(int kv_dtype);
 int tile2_smem_bytes();
-int prefix_max_active_pairs(int q_dtype, int kv_dtype);  // resident CTA pairs, 0 if the query fails
+int prefix_max_active_clusters(int q_dtype, int kv_dtype);  // resident CTA pairs (clusters of 2), 0 if unknown
 
 }  // namespace pkd

@@ -46,6 +46,7 @@ __device__ __forceinline__ float load_elem(const void* in, size_t idx, int dtype
 // stream the states' fp32 partial outputs as float4.  Partial log-sum-exps are
 // base 2 (the decode kernels' convention); the output lse is natural log.
 constexpr int kMergeWarps = 8;
+constexpr int kFewStates = 8;  // rows with at most this many states take the single-round-trip path
 
 __device__ __forceinline__ void store4(void* out, size_t idx, float4 v, int dtype) {
   if (dtype == kBF16) {
@@ -99,14 +100,50 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const Merg
       return reinterpret_cast<const float4*>(base) + lane;
     };
     float M = -INFINITY;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    if (n_states <= kFewStates) {
+      // few states (a cascade row: the prefix pieces and one or two items):
+      // every load is issued before any result is used, so the row costs one
+      // memory round trip; the states are folded in the same slot order
+      const float x = (lane < n_states) ? lse_of(lane) : -INFINITY;
+      float4 o[kFewStates];
+#pragma unroll
+      for (int s = 0; s < kFewStates; ++s) o[s] = (s < n_states) ? *o_of(s) : make_float4(0.f, 0.f, 0.f, 0.f);
+      M = x;
+#pragma unroll
+      for (int k = 16; k > 0; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
+      if (M != -INFINITY) {
+        const float w = (x == -INFINITY) ? 0.f : ptx::ex2(x - M);
+        L = w;
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1) L += __shfl_xor_sync(0xffffffffu, L, k);
+#pragma unroll
+        for (int s = 0; s < kFewStates; ++s) {
+          const float ws = __shfl_sync(0xffffffffu, w, s);
+          if (s < n_states) {
+            acc.x += ws * o[s].x;
+            acc.y += ws * o[s].y;
+            acc.z += ws * o[s].z;
+            acc.w += ws * o[s].w;
+          }
+        }
+        const float inv = 1.f / L;
+        acc.x *= inv;
+        acc.y *= inv;
+        acc.z *= inv;
+        acc.w *= inv;
+      }
+      store4(p.out, bq * kHeadDim + 4 * lane, acc, p.out_dtype);
+      if (lane == 0 && p.lse) p.lse[bq] = (M == -INFINITY) ? -INFINITY : (M + ptx::lg2(L)) * kLn2;
+      continue;
+    }
     for (int s0 = 0; s0 < n_states; s0 += 32) {
       const float x = (s0 + lane < n_states) ? lse_of(s0 + lane) : -INFINITY;
       M = fmaxf(M, x);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = 0.f;
     if (M != -INFINITY) {
       for (int s0 = 0; s0 < n_states; s0 += 32) {
         const int ns = min(32, n_states - s0);

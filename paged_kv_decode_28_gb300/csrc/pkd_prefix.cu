@@ -18,31 +18,35 @@
 // state (o, base-2 lse) per row; the merge pass folds these into each
 // request's suffix state.
 //
-// Per CTA (384 threads; 512 with e4m3 pools):
+// Per CTA (384 threads):
 //   warp 0      Q (once) and the K ring, page by page: boxes of gcd(P, 64)
 //               keys, 128-byte swizzled, K-major.  16-bit pools load straight
 //               into the K slots and signal the even CTA's "K full" barrier
 //               (cta_group::2 loads), so it fires when both halves landed;
 //   warp 2      the V ring, this CTA's 64 head dims of all 128 keys, MN-major,
-//               signalled on this CTA's own "V full" barrier;
+//               signalled on this CTA's own "V full" barrier.  For e4m3 pools
+//               warps 0 and 2 load the codes into a two-slot staging ring and
+//               widen them exactly into q's 16-bit type in the slots the MMAs
+//               read (every E4M3 value is an f16 and a bf16) while the next
+//               tile's codes are in flight; the per-kv-head scales are folded
+//               into the score scale and the output;
 //   warp 1      allocates the pair's 512 TMEM columns (both CTAs); in the even
 //               CTA one thread issues every MMA: S = Q K^T into one of three S
 //               buffers two tiles ahead of O += P_hi V + P_lo V, and commits
 //               to both CTAs' barriers;
+//   warp 3      in the odd CTA, relays its softmax warps' "P written" to the
+//               even CTA with one cluster-scope arrival per tile;
 //   warps 4..11 softmax, two threads per query row (keys 0..63 / 64..127 of
-//               each tile): maximum with the row's other half through shared
-//               memory, a running reference max (O is rescaled in TMEM only
-//               when the tile max exceeds it by more than 8 in log2 units),
-//               P = 2^(s * scale - m) written over the scores as two 16-bit
-//               parts (P_hi = round(P), P_lo = round(P - P_hi), so P enters
-//               the product to ~2^-17); then, once this CTA's V tile has
-//               landed (zeroing V rows past the prefix end), one arrival per
-//               warp on the even CTA's "P full" barrier: the P V product of a
-//               tile waits for all 16 softmax warps of the pair;
-//   warps 12..15 (e4m3 pools only) widen the K and V codes, loaded by warps
-//               0 and 2 into staging slots, exactly into q's 16-bit type in the
-//               slots the MMAs read; the per-kv-head scales are folded into
-//               the score scale and the output.
+//               each tile), the 64 scores of a tile read from TMEM once (the
+//               next tile's read is issued as soon as P is written): maximum
+//               with the row's other half through shared memory, a running
+//               reference max (O is rescaled in TMEM only when the tile max
+//               exceeds it by more than 8 in log2 units), P = 2^(s * scale - m)
+//               written over the scores as two 16-bit parts (P_hi = round(P),
+//               P_lo = round(P - P_hi), so P enters the product to ~2^-17);
+//               then, once this CTA's V tile has landed (16-bit pools: zeroing
+//               V rows past the prefix end), one arrival per warp: the P V
+//               product of a tile waits for the softmax of both CTAs.
 // TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512).  P of a
 // tile's keys 16k .. 16k + 15: P_hi of keys 16k + 2e, 16k + 2e + 1 in column
 // 16k + e, P_lo in column 16k + 8 + e (e = 0..7), over the scores of those keys.
@@ -55,27 +59,30 @@ namespace {
 constexpr int kRows = 128;      // query rows per CTA (a pair computes 256)
 constexpr int kKeys = 128;      // keys per key tile (the S product's N)
 constexpr int kHalfKeys = 64;   // keys of a K tile one CTA holds
-constexpr int kStages = 3;      // ring depth of K and of V
+constexpr int kKStages = 3;     // ring depth of K
+constexpr int kVStages = 4;     // ring depth of V (a V slot is freed two tiles after its K slot)
 constexpr int kSoftmaxWarps = 8;
-constexpr int kConvWarps = 4;
+constexpr int kStaging = 2;     // e4m3: staging slots of codes per side
+constexpr int kCluster = 2;     // one pair
 constexpr float kRescaleThreshold = 8.0f;
 
 template <bool FP8>
 struct PCfg {
-  static constexpr int kThreads = (4 + kSoftmaxWarps + (FP8 ? kConvWarps : 0)) * 32;
+  static constexpr int kThreads = (4 + kSoftmaxWarps) * 32;
   static constexpr int kQHalf = kRows * 128;      // [128 rows][128 B]: 64 of q's dims
   static constexpr int kKHalf = kHalfKeys * 128;  // [64 keys][128 B]: 64 dims of this CTA's keys
   static constexpr int kKStage = 2 * kKHalf;
   static constexpr int kVStage = kKeys * 128;     // [128 keys][128 B]: this CTA's 64 dims
+  static constexpr int kVSt = FP8 ? kVStages - 1 : kVStages;  // e4m3: one slot less, for the staging ring
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + 2 * kQHalf;
-  static constexpr int kV = kK + kStages * kKStage;
+  static constexpr int kV = kK + kKStages * kKStage;
   // e4m3 codes as loaded: K [64 keys][128 B], V [128 keys][64 B] (this CTA's dims)
   static constexpr int kK8Stage = kHalfKeys * 128;
   static constexpr int kV8Stage = kKeys * 64;
-  static constexpr int kK8 = kV + kStages * kVStage;
-  static constexpr int kV8 = kK8 + (FP8 ? kStages * kK8Stage : 0);
-  static constexpr int kBars = kV8 + (FP8 ? kStages * kV8Stage : 0);
+  static constexpr int kK8 = kV + kVSt * kVStage;
+  static constexpr int kV8 = kK8 + (FP8 ? kStaging * kK8Stage : 0);
+  static constexpr int kBars = kV8 + (FP8 ? kStaging * kV8Stage : 0);
   static constexpr int kTmemSlot = kBars + 64 * 8;
   static constexpr int kAbort = kTmemSlot + 8;
   static constexpr int kXchg = kAbort + 8;  // fp32 [buffer][half][row]: the halves' partial maxima / sums
@@ -86,18 +93,17 @@ struct PCfg {
 
 enum {
   B_Q = 0,                   // Q of both CTAs landed (even CTA)
-  B_KF = 1,                  // K tile of both CTAs ready (even CTA) [kStages]
-  B_KE = B_KF + kStages,     // K slot free (each CTA) [kStages]
-  B_VF = B_KE + kStages,     // this CTA's V tile ready [kStages]
-  B_VE = B_VF + kStages,     // V slot free (each CTA) [kStages]
-  B_SF = B_VE + kStages,     // S ready (each CTA) [3]
+  B_KF = 1,                  // K tile of both CTAs ready (even CTA) [kKStages]
+  B_KE = B_KF + kKStages,    // K slot free (each CTA) [kKStages]
+  B_VF = B_KE + kKStages,    // this CTA's V tile ready [kVStages]
+  B_VE = B_VF + kVStages,    // V slot free (each CTA) [kVStages]
+  B_SF = B_VE + kVStages,    // S ready (each CTA) [3]
   B_PF = B_SF + 3,           // P of both CTAs written (even CTA) [3]
   B_OD = B_PF + 3,           // P V done (each CTA) [3]
-  B_K8F = B_OD + 3,          // e4m3: codes landed [kStages]
-  B_K8E = B_K8F + kStages,   // e4m3: staging slot free [kStages]
-  B_V8F = B_K8E + kStages,
-  B_V8E = B_V8F + kStages,
-  B_DRAIN = B_V8E + kStages,
+  B_K8F = B_OD + 3,          // e4m3: codes landed in a staging slot [kStaging]
+  B_V8F = B_K8F + kStaging,
+  B_PL = B_V8F + kStaging,   // odd CTA: its softmax warps' P written [3] (relayed by warp 3)
+  B_DRAIN = B_PL + 3,        // even CTA: every MMA done
   kNumBars = B_DRAIN + 1
 };
 static_assert(kNumBars <= 64, "barrier area");
@@ -108,6 +114,15 @@ __device__ __forceinline__ uint32_t col_s(int u) { return static_cast<uint32_t>(
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, unsigned* err, volatile int* abort_flag) {
   if (*abort_flag) return false;
   if (ptx::mbar_wait(bar, parity, err)) return true;
+  *abort_flag = 1;
+  return false;
+}
+
+// The same for a barrier that the other CTA of the pair arrives on.
+__device__ __forceinline__ bool wait_or_abort_cluster(uint32_t bar, uint32_t parity, unsigned* err,
+                                                      volatile int* abort_flag) {
+  if (*abort_flag) return false;
+  if (ptx::mbar_wait_cluster(bar, parity, err)) return true;
   *abort_flag = 1;
   return false;
 }
@@ -159,8 +174,12 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
   const int G = p.group;
   const int Hq = p.num_kv_heads * G;
   const int R = p.req_per_tile;  // requests per CTA
+  // cluster rank c (0 or 1): K keys 64 c .. 64 c + 63 and V dims 64 c ..
+  // 64 c + 63 of every tile; rank 0 issues the pair's MMAs
   const uint32_t rank = ptx::cluster_ctarank() & 1u;
+  const uint32_t leader = 0;
   const bool lead = rank == 0;
+  const uint16_t pair_mask = 3;
   // this pair's unit: kv head h, CTA rows from request b0, prefix keys in
   // tiles t0 .. t0 + n - 1, piece `split`;
   // blockIdx.x = ((h * n_splits + split) * m_groups + mpair) * 2 + rank
@@ -179,22 +198,26 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(B_Q), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       // 16-bit pools: the even CTA's producer arrives with the pair's bytes;
-      // e4m3: the widening warps of both CTAs arrive
-      ptx::mbar_init(bar(B_KF + s), FP8 ? 2 * kConvWarps : 1);
+      // e4m3: the K producer of each CTA arrives once it has widened its half
+      ptx::mbar_init(bar(B_KF + s), FP8 ? 2 : 1);
       ptx::mbar_init(bar(B_KE + s), 1);
-      ptx::mbar_init(bar(B_VF + s), FP8 ? kConvWarps : 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      ptx::mbar_init(bar(B_VF + s), 1);
       ptx::mbar_init(bar(B_VE + s), 1);
+    }
+    for (int s = 0; s < kStaging; ++s) {
       ptx::mbar_init(bar(B_K8F + s), 1);
-      ptx::mbar_init(bar(B_K8E + s), kConvWarps);
       ptx::mbar_init(bar(B_V8F + s), 1);
-      ptx::mbar_init(bar(B_V8E + s), kConvWarps);
     }
     for (int u = 0; u < 3; ++u) {
       ptx::mbar_init(bar(B_SF + u), 1);
-      ptx::mbar_init(bar(B_PF + u), 2 * kSoftmaxWarps);
+      // the even CTA's softmax warps, and one relayed arrival for the odd CTA's
+      ptx::mbar_init(bar(B_PF + u), kSoftmaxWarps + 1);
       ptx::mbar_init(bar(B_OD + u), 1);
+      ptx::mbar_init(bar(B_PL + u), kSoftmaxWarps);
     }
     ptx::mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
@@ -232,11 +255,12 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
         ptx::prefetch_tensormap(&tmk);
         ptx::prefetch_tensormap(&tmv);
         // q viewed as [B][Hk][g][128]: a box of R requests x g heads of kv head h
-        // (the even CTA always holds requests; it expects the odd CTA's box bytes when that one does)
+        // (the even CTA expects the box bytes of both CTAs that hold requests)
         const uint32_t qbytes = static_cast<uint32_t>(used_rows) * 128u * 2u;
-        if (lead) ptx::mbar_arrive_expect_tx(bar(B_Q), (b0 + R < p.batch ? 2u : 1u) * qbytes);
+        if (lead)
+          ptx::mbar_arrive_expect_tx(bar(B_Q), (has_q ? qbytes : 0u) + (b0 + R < p.batch ? qbytes : 0u));
         if (has_q) {
-          const uint32_t lead_q = ptx::mapa(bar(B_Q), 0);  // the even CTA's barrier
+          const uint32_t lead_q = ptx::mapa(bar(B_Q), leader);  // the even CTA's barrier
           ptx::tma_load_4d_pair(base + C::kQ, &tmq, lead_q, 0, 0, h, b0);
           ptx::tma_load_4d_pair(base + C::kQ + C::kQHalf, &tmq, lead_q, 64, 0, h, b0);
         }
@@ -253,62 +277,166 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
           cnt = min(kv_len - key0, kKeys);
         }
       };
-      const int fb = FP8 ? (kside ? B_K8F : B_V8F) : (kside ? B_KF : B_VF);
-      const int eb = FP8 ? (kside ? B_K8E : B_V8E) : (kside ? B_KE : B_VE);
       const CUtensorMap* map = kside ? &tmk : &tmv;
-      // bytes one box puts in shared memory: K 128-byte rows (per column half
-      // for 16-bit pools), V rows of this CTA's 64 dims (64 B of codes, or 128 B)
-      const uint32_t row_bytes = FP8 ? (kside ? 128u : 64u) : 128u;
-      const uint32_t slot = FP8 ? (kside ? C::kK8 : C::kV8) : (kside ? C::kK : C::kV);
-      const uint32_t slot_bytes = FP8 ? (kside ? C::kK8Stage : C::kV8Stage) : (kside ? C::kKStage : C::kVStage);
-      const int vcol = FP8 ? 0 : 64 * static_cast<int>(rank);  // 16-bit V: this CTA's column half of the map
-      for (int i = 0; i < n; ++i) {
-        const int s = i % kStages;
-        const uint32_t par = ((i / kStages) & 1) ^ 1;
+      const int vst = kside ? kKStages : C::kVSt;  // ring depth of this side
+      // page ids and in-page offsets of tile i's boxes that this lane issues
+      // (box j = lane + 32 r; at most 128 boxes of a 128-key tile), read two
+      // tiles ahead of their use so that the table's latency stays off the loads
+      auto fetch = [&](int i, int (&pg)[4], int (&tk)[4]) {
+        int first = 0, cnt = 0;
+        if (i < n) span(i, first, cnt);
+        const int boxes = (cnt + box - 1) / box;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          pg[r] = 0;
+          tk[r] = 0;
+          const int j = lane + 32 * r;
+          if (j < boxes) {
+            const int key = first + j * box;
+            const int pi = key / p.page_size;
+            pg[r] = __ldg(pages + pi);  // checked at use, so the load stays in flight
+            tk[r] = key - pi * p.page_size;
+          }
+        }
+      };
+      // issue the boxes of tile i into dst0 (rows of row_bytes), completing on
+      // `full`; pair loads (16-bit K) signal the even CTA's barrier
+      auto issue = [&](int i, const int (&pg)[4], const int (&tk)[4], uint32_t dst0, uint32_t row_bytes, uint32_t full,
+                       int c0, bool pair_load) {
         int first, cnt;
         span(i, first, cnt);
         const int boxes = (cnt + box - 1) / box;
-        if (!warp_wait(bar(eb + s), par, p.err, abort_flag)) break;
-        const uint32_t dst0 = base + slot + s * slot_bytes;
-        uint32_t full;  // the barrier the loads signal
-        if (!FP8 && kside) {
-          // the even CTA expects both CTAs' K bytes of this tile (its own cnt
-          // keys and the odd CTA's, from key0 + 64 on), two column halves each
-          if (lead && lane == 0) {
-            const int c1 = min(max(kv_len - ((t0 + i) * kKeys + kHalfKeys), 0), kHalfKeys);
-            const uint32_t bytes = static_cast<uint32_t>(((cnt + box - 1) / box + (c1 + box - 1) / box) * box) * 256u;
-            ptx::mbar_arrive_expect_tx(bar(B_KF + s), bytes);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int j = lane + 32 * r;
+          if (j < boxes) {
+            int page = pg[r];
+            if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
+              atomicOr(p.err, kDevErrPageIndex);
+              page = 0;
+            }
+            // map coordinates (dim, head, key, page) for NHD pages, (dim, key, head, page) for HND
+            const int c1 = p.kv_hnd ? tk[r] : h, c2 = p.kv_hnd ? h : tk[r];
+            const uint32_t d = dst0 + static_cast<uint32_t>(j * box) * row_bytes;
+            if (pair_load) {
+              ptx::tma_load_4d_pair(d, map, full, c0, c1, c2, page);
+              ptx::tma_load_4d_pair(d + C::kKHalf, map, full, c0 + 64, c1, c2, page);
+            } else {
+              ptx::tma_load_4d(d, map, full, c0, c1, c2, page);
+            }
           }
-          full = ptx::mapa(bar(B_KF + s), 0);
-        } else {
-          if (lane == 0) {
-            const uint32_t per_box = static_cast<uint32_t>(box) * row_bytes * ((!FP8 && kside) ? 2u : 1u);
-            ptx::mbar_arrive_expect_tx(bar(fb + s), static_cast<uint32_t>(boxes) * per_box);
-          }
-          full = bar(fb + s);
         }
-        __syncwarp();
-        for (int j = lane; j < boxes; j += 32) {
-          const int key = first + j * box;
-          const int pi = key / p.page_size;
-          int page = __ldg(pages + pi);
-          if (static_cast<unsigned>(page) >= static_cast<unsigned>(p.num_pages)) {
-            atomicOr(p.err, kDevErrPageIndex);
-            page = 0;
-          }
-          const int tk = key - pi * p.page_size;
-          // map coordinates (dim, head, key, page) for NHD pages, (dim, key, head, page) for HND
-          const int c1 = p.kv_hnd ? tk : h, c2 = p.kv_hnd ? h : tk;
-          const uint32_t d = dst0 + static_cast<uint32_t>(j * box) * row_bytes;
-          if (!FP8 && kside) {
-            ptx::tma_load_4d_pair(d, map, full, 0, c1, c2, page);
-            ptx::tma_load_4d_pair(d + C::kKHalf, map, full, 64, c1, c2, page);
-          } else if (!FP8) {
-            ptx::tma_load_4d(d, map, full, vcol, c1, c2, page);
+      };
+      // the side's loads of tile i with its fetched page ids; false once a wait gave up
+      auto step = [&](int i, const int (&pg)[4], const int (&tk)[4]) -> bool {
+        if constexpr (!FP8) {
+          // 16-bit pools: straight into the K / V slots
+          const int s = i % vst;
+          if (!warp_wait(bar((kside ? B_KE : B_VE) + s), ((i / vst) & 1) ^ 1, p.err, abort_flag)) return false;
+          int first, cnt;
+          span(i, first, cnt);
+          const uint32_t bytes_here = static_cast<uint32_t>((cnt + box - 1) / box * box) * 128u;
+          if (kside) {
+            // the even CTA expects both CTAs' K bytes of this tile (its own
+            // keys and the odd CTA's, from key0 + 64 on), two column halves each
+            if (lead && lane == 0) {
+              const int c1 = min(max(kv_len - ((t0 + i) * kKeys + kHalfKeys), 0), kHalfKeys);
+              ptx::mbar_arrive_expect_tx(bar(B_KF + s),
+                                         2u * bytes_here + static_cast<uint32_t>((c1 + box - 1) / box * box) * 256u);
+            }
+            __syncwarp();
+            issue(i, pg, tk, base + C::kK + s * C::kKStage, 128u, ptx::mapa(bar(B_KF + s), leader), 0, true);
           } else {
-            ptx::tma_load_4d(d, map, full, kside ? 0 : 64 * static_cast<int>(rank), c1, c2, page);
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(B_VF + s), bytes_here);
+            __syncwarp();
+            issue(i, pg, tk, base + C::kV + s * C::kVStage, 128u, bar(B_VF + s), 64 * static_cast<int>(rank), false);
           }
+          return true;
+        } else {
+          // e4m3 pools: the codes of tile i go to a two-slot staging ring; this
+          // warp then widens tile i - 1 into its K / V slot (V rows past the
+          // prefix end as zeros) while tile i's codes are in flight
+          const int f8 = kside ? B_K8F : B_V8F;
+          const uint32_t stg = base + (kside ? C::kK8 : C::kV8);
+          const uint32_t stg_bytes = kside ? C::kK8Stage : C::kV8Stage;
+          const uint32_t row_bytes = kside ? 128u : 64u;
+          if (i < n) {
+            const int s8 = i % kStaging;
+            int first, cnt;
+            span(i, first, cnt);
+            // the widening reads of this slot (tile i - 2) come before the copy into it
+            ptx::fence_proxy_async_smem();
+            if (lane == 0)
+              ptx::mbar_arrive_expect_tx(bar(f8 + s8), static_cast<uint32_t>((cnt + box - 1) / box * box) * row_bytes);
+            __syncwarp();
+            issue(i, pg, tk, stg + s8 * stg_bytes, row_bytes, bar(f8 + s8), kside ? 0 : 64 * static_cast<int>(rank),
+                  false);
+          }
+          if (i == 0) return true;
+          const int w = i - 1;  // the tile to widen
+          const int s8 = w % kStaging, s = w % vst;
+          if (!warp_wait(bar(f8 + s8), (w / kStaging) & 1, p.err, abort_flag)) return false;
+          if (!warp_wait(bar((kside ? B_KE : B_VE) + s), ((w / vst) & 1) ^ 1, p.err, abort_flag)) return false;
+          const uint8_t* src = base_ptr + (stg - base) + s8 * stg_bytes;
+          if (kside) {
+            // [64 keys][128 codes] -> [2 halves][64 keys][128 B]
+            const uint32_t kb = base + C::kK + s * C::kKStage;
+#pragma unroll 4
+            for (int item = lane; item < kHalfKeys * 8; item += 32) {
+              const int key = item >> 3, c = item & 7;  // 16 codes = head dims 16 c .. 16 c + 15
+              const uint4 raw = *reinterpret_cast<const uint4*>(src + key * 128 + c * 16);
+              uint32_t a[4], bq[4];
+              widen8<BF>(raw.x, raw.y, a);
+              widen8<BF>(raw.z, raw.w, bq);
+              const uint32_t half = static_cast<uint32_t>(c >> 2), ch = 2u * static_cast<uint32_t>(c & 3);
+              ptx::sts128(kb + half * C::kKHalf + ptx::sw128(key, ch), a[0], a[1], a[2], a[3]);
+              ptx::sts128(kb + half * C::kKHalf + ptx::sw128(key, ch + 1), bq[0], bq[1], bq[2], bq[3]);
+            }
+          } else {
+            // [128 keys][64 codes] -> [128 keys][128 B]
+            const int nv = min(kKeys, kv_len - (t0 + w) * kKeys);
+            const uint32_t vb = base + C::kV + s * C::kVStage;
+#pragma unroll 4
+            for (int item = lane; item < kKeys * 4; item += 32) {
+              const int key = item >> 2, c = item & 3;
+              uint32_t a[4] = {0u, 0u, 0u, 0u}, bq[4] = {0u, 0u, 0u, 0u};
+              if (key < nv) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(src + key * 64 + c * 16);
+                widen8<BF>(raw.x, raw.y, a);
+                widen8<BF>(raw.z, raw.w, bq);
+              }
+              ptx::sts128(vb + ptx::sw128(key, 2u * c), a[0], a[1], a[2], a[3]);
+              ptx::sts128(vb + ptx::sw128(key, 2u * c + 1u), bq[0], bq[1], bq[2], bq[3]);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (kside) {
+              ptx::mbar_arrive_cluster(ptx::mapa(bar(B_KF + s), leader));  // the pair's K tile: both CTAs' halves
+            } else {
+              ptx::mbar_arrive(bar(B_VF + s));
+            }
+          }
+          return true;
         }
+      };
+      // three register sets of page ids in rotation, unrolled so that no set is
+      // copied while its loads are in flight: tile i's ids were requested two
+      // tiles earlier.  e4m3 pools run one step past the last tile (its widening).
+      const int steps = FP8 ? n + 1 : n;
+      int pgA[4], tkA[4], pgB[4], tkB[4], pgC[4], tkC[4];
+      fetch(0, pgA, tkA);
+      fetch(1, pgB, tkB);
+      for (int i = 0; i < steps; i += 3) {
+        fetch(i + 2, pgC, tkC);
+        if (!step(i, pgA, tkA)) break;
+        if (i + 1 >= steps) break;
+        fetch(i + 3, pgA, tkA);
+        if (!step(i + 1, pgB, tkB)) break;
+        if (i + 2 >= steps) break;
+        fetch(i + 4, pgB, tkB);
+        if (!step(i + 2, pgC, tkC)) break;
       }
     }
   } else if (warp == 1) {
@@ -317,11 +445,12 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
       constexpr uint32_t idesc_s = ptx::idesc_f16(BF, false, 2 * kRows, kKeys);
       constexpr uint32_t idesc_pv = ptx::idesc_f16(BF, true, 2 * kRows, kHeadDim);
       bool ok = wait_or_abort(bar(B_Q), 0, p.err, abort_flag);
+      // O += P_hi V + P_lo V of tile t once both CTAs' softmax has written P
+      // and seen its V tile land
       auto pv = [&](int t) -> bool {
         const int u = t % 3;
-        const int sv = t % kStages;
-        // P of both CTAs written, and both CTAs' V tiles landed
-        if (!wait_or_abort(bar(B_PF + u), (t / 3) & 1, p.err, abort_flag)) return false;
+        const int sv = t % C::kVSt;
+        if (!wait_or_abort_cluster(bar(B_PF + u), (t / 3) & 1, p.err, abort_flag)) return false;
         ptx::tc_fence_after();
         const uint32_t pcol = col_s(u);
 #pragma unroll
@@ -330,15 +459,17 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
           ptx::umma_ts_pair(tmem + kColO, tmem + pcol + 16 * k, bdesc, idesc_pv, (t > 0 || k > 0) ? 1u : 0u);
           ptx::umma_ts_pair(tmem + kColO, tmem + pcol + 16 * k + 8, bdesc, idesc_pv, 1u);
         }
-        ptx::tc_commit_pair(bar(B_OD + u), 3);
-        if (t + kStages < n) ptx::tc_commit_pair(bar(B_VE + sv), 3);
+        ptx::tc_commit_pair(bar(B_OD + u), pair_mask);
+        if (t + C::kVSt < n) ptx::tc_commit_pair(bar(B_VE + sv), pair_mask);
         return true;
       };
+      // S = Q K^T of tile i into S buffer i mod 3 once the pair's K tile has
+      // landed and the P V product of tile i - 3 (whose P the buffer holds) is
+      // done; the P V product runs two tiles behind
       for (int i = 0; i < n && ok; ++i) {
         const int u = i % 3;
-        const int sk = i % kStages;
-        if (!wait_or_abort(bar(B_KF + sk), (i / kStages) & 1, p.err, abort_flag)) break;
-        // S u holds P of tile i - 3 until that tile's P V product is done
+        const int sk = i % kKStages;
+        if (!wait_or_abort_cluster(bar(B_KF + sk), (i / kKStages) & 1, p.err, abort_flag)) break;
         if (i >= 3 && !wait_or_abort(bar(B_OD + u), ((i - 3) / 3) & 1, p.err, abort_flag)) break;
         ptx::tc_fence_after();
 #pragma unroll
@@ -349,9 +480,8 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
               ptx::smem_desc_sw128(base + C::kK + sk * C::kKStage + (k >> 2) * C::kKHalf + (k & 3) * 32, 16, 1024);
           ptx::umma_ss_pair(tmem + col_s(u), adesc, bdesc, idesc_s, k > 0 ? 1u : 0u);
         }
-        ptx::tc_commit_pair(bar(B_SF + u), 3);
-        if (i + kStages < n) ptx::tc_commit_pair(bar(B_KE + sk), 3);
-        // the P V product runs two tiles behind S
+        ptx::tc_commit_pair(bar(B_SF + u), pair_mask);
+        if (i + kKStages < n) ptx::tc_commit_pair(bar(B_KE + sk), pair_mask);
         if (i >= 2 && !pv(i - 2)) {
           ok = false;
           break;
@@ -362,6 +492,17 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
       // drain: every MMA issued above has finished before TMEM is released
       ptx::tc_commit_pair_local(bar(B_DRAIN));
       ptx::mbar_wait(bar(B_DRAIN), 0, p.err);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ odd CTA: P-full relay
+    // its softmax warps arrive on a local barrier; one cluster-scope arrival
+    // per tile reaches the even CTA
+    if (!lead && lane == 0) {
+      for (int i = 0; i < n; ++i) {
+        const int u = i % 3;
+        if (!wait_or_abort(bar(B_PL + u), (i / 3) & 1, p.err, abort_flag)) break;
+        ptx::mbar_arrive_cluster(ptx::mapa(bar(B_PF + u), leader));
+      }
     }
   } else if (warp >= 4 && warp < 4 + kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax
@@ -380,13 +521,24 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
     const int jj = row - (row / G) * G;
     const uint32_t scol_base = tmem + lanes + 64 * hf;
     const uint32_t ocol = tmem + lanes + kColO + 64 * hf;
+    const int pf = lead ? B_PF : B_PL;  // where this CTA's "P written" arrivals go
+    // this thread's 64 scores of a tile, loaded once; the next tile's load is
+    // issued as soon as this tile's P is in TMEM
+    uint32_t sr[64];
+    if (n > 0) {
+      ok = warp_wait(bar(B_SF), 0, p.err, abort_flag);
+      if (ok) {
+        ptx::tc_fence_after();
+        ptx::tmem_ld32(scol_base, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        ptx::tmem_ld32(scol_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      }
+    }
     // Each iteration passes the row's named barrier exactly once, also after a
     // failed wait (ok false: the rest of the work is skipped, and every later
     // wait returns at once on the abort flag), so the two halves never wait at
     // barriers the other does not reach.
     for (int i = 0; i < n; ++i) {
       const int u = i % 3;
-      ok = ok && warp_wait(bar(B_SF + u), (i / 3) & 1, p.err, abort_flag);
       const uint32_t scol = scol_base + col_s(u);
       const int key0 = (t0 + i) * kKeys;
       const int nv = min(kKeys, kv_len - key0);
@@ -397,18 +549,17 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
       if (ok) {
-        ptx::tc_fence_after();
-        uint32_t sr[64];
-        ptx::tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        ptx::tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         ptx::tmem_ld_wait();
+        ptx::reg_fence32(&sr[0]);
+        ptx::reg_fence32(&sr[32]);
         if (vr < 64) {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
             if (e >= vr) sr[e] = __float_as_uint(-INFINITY);
         }
 #pragma unroll
-        for (int e = 0; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sr[e]));
+        for (int e = 0; e < 32; ++e)
+          m8[e & 7] = ptx::fmax3(m8[e & 7], __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
       }
       const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                              fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
@@ -435,6 +586,7 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
           uint32_t o[32];
           ptx::tmem_ld32(ocol + 32 * c, o);
           ptx::tmem_ld_wait();
+          ptx::reg_fence32(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           ptx::tmem_st32(ocol + 32 * c, o);
@@ -446,41 +598,60 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
         }
       }
       // P over the scores, sixteen keys at a time: P_hi of the block's keys
-      // in its first 8 columns, P_lo in the last 8
-      float rs[8];
+      // in its first 8 columns, P_lo in the last 8; pairs of scores go through
+      // the two-wide fp32 instructions (scale and shift, sums, residuals)
+      const uint64_t sl2x2 = ptx::f2pack(sl2, sl2), negm = ptx::f2pack(-m_ref, -m_ref);
+      uint64_t rs2[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) rs[e] = 0.f;
+      for (int e = 0; e < 4; ++e) rs2[e] = ptx::f2pack(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sr[32];
-        ptx::tmem_ld32(scol + 32 * c, sr);
-        ptx::tmem_ld_wait();
-        const int vc = vr - 32 * c;
-        if (vc < 32) {
+      for (int bk = 0; bk < 4; bk += 2) {
+        uint32_t pp[32];  // blocks bk, bk + 1: P_hi pairs, P_lo pairs, P_hi pairs, P_lo pairs
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (e >= vc) sr[e] = __float_as_uint(-INFINITY);
-        }
-#pragma unroll
-        for (int bk = 0; bk < 2; ++bk) {
-          uint32_t pp[16];  // P_hi pairs, then P_lo pairs
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[16 * bk + 2 * e]), sl2, -m_ref));
-            const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[16 * bk + 2 * e + 1]), sl2, -m_ref));
-            rs[e] += p0 + p1;
-            ptx::split2<BF>(p0, p1, pp[e], pp[8 + e]);
+        for (int e = 0; e < 16; ++e) {
+          const uint64_t x = ptx::f2fma(ptx::f2pack(__uint_as_float(sr[16 * bk + 2 * e]),
+                                                    __uint_as_float(sr[16 * bk + 2 * e + 1])),
+                                        sl2x2, negm);
+          float x0, x1;
+          ptx::f2unpack(x, x0, x1);
+          const uint64_t pv = ptx::f2pack(ptx::ex2(x0), ptx::ex2(x1));
+          rs2[e & 3] = ptx::f2add(rs2[e & 3], pv);
+          const int slot = (e >> 3) * 16 + (e & 7);
+          if constexpr (BF) {
+            ptx::split2_bf16_packed(pv, pp[slot], pp[slot + 8]);
+          } else {
+            float q0, q1;
+            ptx::f2unpack(pv, q0, q1);
+            ptx::split2<false>(q0, q1, pp[slot], pp[slot + 8]);
           }
-          ptx::tmem_st16(scol + 32 * c + 16 * bk, pp);
         }
+        ptx::tmem_st32(scol + 16 * bk, pp);
       }
-      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+      {
+        float a0, a1, b0s, b1s, c0, c1, d0, d1;
+        ptx::f2unpack(rs2[0], a0, a1);
+        ptx::f2unpack(rs2[1], b0s, b1s);
+        ptx::f2unpack(rs2[2], c0, c1);
+        ptx::f2unpack(rs2[3], d0, d1);
+        l += ((a0 + a1) + (b0s + b1s)) + ((c0 + c1) + (d0 + d1));
+      }
+      // the next tile's scores (another S buffer) while this tile's tail runs
+      if (i + 1 < n) {
+        const int un = (i + 1) % 3;
+        if (!warp_wait(bar(B_SF + un), ((i + 1) / 3) & 1, p.err, abort_flag)) {
+          ok = false;
+          continue;
+        }
+        ptx::tc_fence_after();
+        ptx::tmem_ld32(scol_base + col_s(un), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        ptx::tmem_ld32(scol_base + col_s(un) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      }
       // this CTA's V tile must have landed before the pair's P V product; keys
       // past the prefix end have P = 0 and their V rows must be finite, so the
       // first half's threads zero them (16-bit pools; the widening warps do it
       // for e4m3 pools)
-      const int sv = i % kStages;
-      if (!warp_wait(bar(B_VF + sv), (i / kStages) & 1, p.err, abort_flag)) {
+      const int sv = i % C::kVSt;
+      if (!warp_wait(bar(B_VF + sv), (i / C::kVSt) & 1, p.err, abort_flag)) {
         ok = false;
         continue;
       }
@@ -494,8 +665,9 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(bar(B_PF + u), 0));
+      if (lane == 0) ptx::mbar_arrive(bar(pf + u));
     }
+    if (ok) ptx::tmem_ld_wait();  // no load is left in flight
     // ---- epilogue: o = O / l, lse2 = m_ref + log2(l) into piece `split` as
     // an fp32 partial state; each half writes its 64 columns, the first half
     // the lse
@@ -531,61 +703,6 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
       for (int d = 0; d < 64; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
       if (hf == 0) p.pre_lse[sidx] = -INFINITY;
     }
-  } else if (FP8 && warp >= 4 + kSoftmaxWarps) {
-    // ------------------------------------------------------------ e4m3 widening (K and V)
-    const int ct = threadIdx.x - (4 + kSoftmaxWarps) * 32;  // 0..127
-    for (int i = 0; i < n; ++i) {
-      const int s = i % kStages;
-      const uint32_t ph = (i / kStages) & 1;
-      const uint32_t freep = ph ^ 1u;
-      const int key0 = (t0 + i) * kKeys;
-      const int nv = min(kKeys, kv_len - key0);
-      // K: [64 keys][128 codes] -> [2 halves][64 keys][128 B], swizzled
-      if (!warp_wait(bar(B_K8F + s), ph, p.err, abort_flag) || !warp_wait(bar(B_KE + s), freep, p.err, abort_flag))
-        break;
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int item = ct + 128 * it;  // (key, 16-code chunk)
-        const int key = item >> 3, c = item & 7;
-        const uint4 raw = *reinterpret_cast<const uint4*>(base_ptr + C::kK8 + s * C::kK8Stage + key * 128 + c * 16);
-        uint32_t a[4], bq[4];
-        widen8<BF>(raw.x, raw.y, a);
-        widen8<BF>(raw.z, raw.w, bq);
-        const uint32_t half = static_cast<uint32_t>(c >> 2), ch = 2u * static_cast<uint32_t>(c & 3);
-        const uint32_t kb = base + C::kK + s * C::kKStage + half * C::kKHalf;
-        ptx::sts128(kb + ptx::sw128(key, ch), a[0], a[1], a[2], a[3]);
-        ptx::sts128(kb + ptx::sw128(key, ch + 1), bq[0], bq[1], bq[2], bq[3]);
-      }
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive_cluster(ptx::mapa(bar(B_KF + s), 0));  // the pair's K tile: both CTAs' widening warps
-        ptx::mbar_arrive(bar(B_K8E + s));
-      }
-      // V: [128 keys][64 codes] (this CTA's dims) -> [128 keys][128 B], swizzled; rows past the end zero
-      if (!warp_wait(bar(B_V8F + s), ph, p.err, abort_flag) || !warp_wait(bar(B_VE + s), freep, p.err, abort_flag))
-        break;
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int item = ct + 128 * it;
-        const int key = item >> 2, c = item & 3;
-        uint32_t a[4] = {0u, 0u, 0u, 0u}, bq[4] = {0u, 0u, 0u, 0u};
-        if (key < nv) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(base_ptr + C::kV8 + s * C::kV8Stage + key * 64 + c * 16);
-          widen8<BF>(raw.x, raw.y, a);
-          widen8<BF>(raw.z, raw.w, bq);
-        }
-        const uint32_t vb = base + C::kV + s * C::kVStage;
-        ptx::sts128(vb + ptx::sw128(key, 2u * c), a[0], a[1], a[2], a[3]);
-        ptx::sts128(vb + ptx::sw128(key, 2u * c + 1u), bq[0], bq[1], bq[2], bq[3]);
-      }
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(bar(B_VF + s));
-        ptx::mbar_arrive(bar(B_V8E + s));
-      }
-    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -620,17 +737,17 @@ int threads_of(int kv_dtype) { return kv_dtype == kE4M3 ? PCfg<true>::kThreads :
 
 int prefix_smem_bytes(int kv_dtype) { return smem_of(kv_dtype); }
 
-int prefix_max_active_pairs(int q_dtype, int kv_dtype) {
+int prefix_max_active_clusters(int q_dtype, int kv_dtype) {
   const void* kern = pick(q_dtype, kv_dtype);
   const int smem = smem_of(kv_dtype);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2);
+  cfg.gridDim = dim3(kCluster);
   cfg.blockDim = dim3(threads_of(kv_dtype));
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = kCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -645,7 +762,7 @@ int prefix_max_active_pairs(int q_dtype, int kv_dtype) {
 
 cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                           const PrefixParams& p, int q_dtype, int kv_dtype, cudaStream_t stream, bool pdl) {
-  const int grid = p.num_kv_heads * p.n_splits * p.m_groups * 2;
+  const int grid = p.num_kv_heads * p.n_splits * p.m_groups * kCluster;
   if (grid <= 0) return cudaSuccess;
   if (!(q_dtype == kBF16 || q_dtype == kF16) || !(kv_dtype == q_dtype || kv_dtype == kE4M3))
     return cudaErrorInvalidValue;
@@ -660,7 +777,7 @@ cudaError_t launch_prefix(const CUtensorMap& tmq, const CUtensorMap& tmk, const 
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = kCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

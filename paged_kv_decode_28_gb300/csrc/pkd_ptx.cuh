@@ -223,6 +223,55 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   lo = pack2<BF16>(a - ha, b - hb);
 }
 
+// Packed pairs of fp32 values (Blackwell's two-wide fp32 instructions).
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ void f2unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+
+// a * b + c on both halves, round to nearest even.
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// max of three fp32 values (NaN-free inputs).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// split2<true> for a packed pair (p0, p1): hi = bf16x2 round of the pair, lo =
+// bf16x2 round of the residuals, the residuals taken with one two-wide subtract.
+__device__ __forceinline__ void split2_bf16_packed(uint64_t pv, uint32_t& hi, uint32_t& lo) {
+  float p0, p1;
+  f2unpack(pv, p0, p1);
+  hi = pack2<true>(p0, p1);
+  const uint64_t hv = f2pack(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
+  float r0, r1;
+  f2unpack(f2sub(pv, hv), r0, r1);
+  lo = pack2<true>(r0, r1);
+}
+
 // Two E4M3 codes (lo byte = first element) -> f16x2, exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
@@ -359,6 +408,43 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+
+// mbar_wait with acquire semantics at cluster scope: for barriers that other
+// CTAs of the cluster arrive on with release semantics at cluster scope.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned* err) {
+  auto try_wait = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_wait()) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t spin = 0;; ++spin) {
+    if (try_wait()) return true;
+    if ((spin & 63u) == 63u) {
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        atomicOr(err, kDevErrWaitTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Registers just written by tcgen05.ld: an empty statement that the compiler
+// must treat as redefining them, placed after tcgen05.wait::ld so that no use
+// of the loaded values is scheduled before the wait.
+__device__ __forceinline__ void reg_fence32(uint32_t* r) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 8)
+    asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]),
+                 "+r"(r[i + 6]), "+r"(r[i + 7]));
 }
 
 // Arrive once on an mbarrier of (possibly) another CTA of the cluster, with
