@@ -399,8 +399,10 @@ def run_ours(args):
     try:
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
-        if tr.get("kernel_hash") == kernel_hash() and tr.get("config") == args.config and args.kv_layout == "NHD":
-            traffic = tr.get("dram_bytes_per_launch")
+        ent = tr.get("configs", {}).get(str(args.config))
+        # the record holds only for the kernel sources it was captured on, the full batch and NHD pages
+        if ent and tr.get("kernel_hash") == kernel_hash() and args.batch is None and args.kv_layout == "NHD":
+            traffic = ent.get("dram_bytes_per_launch")
     except Exception:
         pass
 

@@ -24,6 +24,10 @@ namespace pkd {
 namespace {
 
 constexpr int kConsumerWarps = 4;
+// row stride (floats) of the shared buffer the consumer warps combine their
+// states through: 8 floats of padding put the float2 accesses of a half-warp
+// (4 head rows x 4 column pairs) on distinct banks
+constexpr int kCombStride = kHeadDim + 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -41,8 +45,8 @@ struct Cfg {
   // [2 halves][16][128 B] per warp
   static constexpr int kV16Bytes = (KVT == kE4M3) ? 4 * 4096 : 0;
   static constexpr int kV16 = kStages * kStageBytes;
-  static constexpr int kCombO = kV16 + kV16Bytes;                               // f32 [3][8][128]
-  static constexpr int kCombML = kCombO + 3 * kMaxGroup * kHeadDim * 4;         // f32 [3][8][2]
+  static constexpr int kCombO = kV16 + kV16Bytes;                               // f32 [3][8][kCombStride]
+  static constexpr int kCombML = kCombO + 3 * kMaxGroup * kCombStride * 4;      // f32 [3][8][2]
   static constexpr int kBars = kCombML + 3 * kMaxGroup * 2 * 4;                 // u64 [2][stages]
   static constexpr int kAbort = kBars + 2 * kStages * 8;                        // int
   static constexpr int kTotal = kAbort + 16;
@@ -244,14 +248,16 @@ __device__ __forceinline__ void qk_e4m3(uint32_t kb, int w, int lane, const uint
 #pragma unroll
     for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.f;
     const uint32_t tok = 16 * w + 8 * nt + gid;
-    const uint4 c0 = ptx::lds128(kb + ptx::sw128(tok, 2 * t));
-    const uint4 c1 = ptx::lds128(kb + ptx::sw128(tok, 2 * t + 1));
-    const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t b0, b1;
-      e4m3x4_to_f16x2x2(wd[j], b0, b1);
-      ptx::mma_16816<false>(sacc[nt], qa0[j], 0u, qa2[j], 0u, b0, b1);
+    for (int hc = 0; hc < 2; ++hc) {  // the row's 16-byte chunks 2t and 2t + 1, one at a time
+      const uint4 c = ptx::lds128(kb + ptx::sw128(tok, 2 * t + hc));
+      const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t b0, b1;
+        e4m3x4_to_f16x2x2(wd[j], b0, b1);
+        ptx::mma_16816<false>(sacc[nt], qa0[4 * hc + j], 0u, qa2[4 * hc + j], 0u, b0, b1);
+      }
     }
   }
 }
@@ -305,18 +311,25 @@ __device__ __forceinline__ void tile32_e4m3(uint32_t kbA, uint32_t vbA, int vali
                                             float& m_run, float& l_run, float (&o)[16][4]) {
   const int t = lane & 3;
   convert_v16(vbA, v16, w, lane);
-  float sA[2][4], sB[2][4];
-  qk_e4m3(kbA, w, lane, qa0, qa2, sA);
-  qk_e4m3(kbB, w, lane, qa0, qa2, sB);
+  // the scaled scores of A's and then B's keys (each S product's accumulators
+  // are dead once its four scores of this thread's head row are taken)
   float x[8];
-  x[0] = (2 * t < validA) ? sA[0][0] * sl2 : -INFINITY;
-  x[1] = (2 * t + 1 < validA) ? sA[0][1] * sl2 : -INFINITY;
-  x[2] = (2 * t + 8 < validA) ? sA[1][0] * sl2 : -INFINITY;
-  x[3] = (2 * t + 9 < validA) ? sA[1][1] * sl2 : -INFINITY;
-  x[4] = (2 * t < validB) ? sB[0][0] * sl2 : -INFINITY;
-  x[5] = (2 * t + 1 < validB) ? sB[0][1] * sl2 : -INFINITY;
-  x[6] = (2 * t + 8 < validB) ? sB[1][0] * sl2 : -INFINITY;
-  x[7] = (2 * t + 9 < validB) ? sB[1][1] * sl2 : -INFINITY;
+  {
+    float sA[2][4];
+    qk_e4m3(kbA, w, lane, qa0, qa2, sA);
+    x[0] = (2 * t < validA) ? sA[0][0] * sl2 : -INFINITY;
+    x[1] = (2 * t + 1 < validA) ? sA[0][1] * sl2 : -INFINITY;
+    x[2] = (2 * t + 8 < validA) ? sA[1][0] * sl2 : -INFINITY;
+    x[3] = (2 * t + 9 < validA) ? sA[1][1] * sl2 : -INFINITY;
+  }
+  {
+    float sB[2][4];
+    qk_e4m3(kbB, w, lane, qa0, qa2, sB);
+    x[4] = (2 * t < validB) ? sB[0][0] * sl2 : -INFINITY;
+    x[5] = (2 * t + 1 < validB) ? sB[0][1] * sl2 : -INFINITY;
+    x[6] = (2 * t + 8 < validB) ? sB[1][0] * sl2 : -INFINITY;
+    x[7] = (2 * t + 9 < validB) ? sB[1][1] * sl2 : -INFINITY;
+  }
   float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -639,12 +652,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     ptx::named_bar_sync(1, kConsumerWarps * 32);
     if (w > 0 && hv) {
-      float* dst = comb_o + ((w - 1) * kMaxGroup + gid) * kHeadDim;
+      float* dst = comb_o + ((w - 1) * kMaxGroup + gid) * kCombStride;
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        dst[o_dim<KVT>(nt, 0, t)] = o[nt][0];
-        dst[o_dim<KVT>(nt, 1, t)] = o[nt][1];
-      }
+      for (int nt = 0; nt < 16; ++nt)
+        *reinterpret_cast<float2*>(dst + o_dim<KVT>(nt, 0, t)) = make_float2(o[nt][0], o[nt][1]);
       if (t == 0) {
         comb_ml[((w - 1) * kMaxGroup + gid) * 2 + 0] = m_run;
         comb_ml[((w - 1) * kMaxGroup + gid) * 2 + 1] = l_run;
@@ -672,30 +683,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const float vsc = p.v_scale ? __ldg(p.v_scale + h) : 1.f;
       const float lse2 = M + ptx::lg2(Ls);
       const bool partial = (item.w & kItemSplit) || p.force_partial;
-      const float* c1 = comb_o + (0 * kMaxGroup + gid) * kHeadDim;
-      const float* c2 = comb_o + (1 * kMaxGroup + gid) * kHeadDim;
-      const float* c3 = comb_o + (2 * kMaxGroup + gid) * kHeadDim;
+      const float* c1 = comb_o + (0 * kMaxGroup + gid) * kCombStride;
+      const float* c2 = comb_o + (1 * kMaxGroup + gid) * kCombStride;
+      const float* c3 = comb_o + (2 * kMaxGroup + gid) * kCombStride;
+      // this thread's two columns 8 nt + 2t, 8 nt + 2t + 1 of the combined row
+      auto comb2 = [&](int nt) {
+        const int d = o_dim<KVT>(nt, 0, t);
+        const float2 a = *reinterpret_cast<const float2*>(c1 + d);
+        const float2 bb = *reinterpret_cast<const float2*>(c2 + d);
+        const float2 c = *reinterpret_cast<const float2*>(c3 + d);
+        return make_float2((o[nt][0] * sc[0] + a.x * sc[1] + bb.x * sc[2] + c.x * sc[3]) * inv * vsc,
+                           (o[nt][1] * sc[0] + a.y * sc[1] + bb.y * sc[2] + c.y * sc[3]) * inv * vsc);
+      };
       if (partial) {
         float* po = p.part_o + (static_cast<size_t>(it) * G + gid) * kHeadDim;
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int d = o_dim<KVT>(nt, e, t);
-            po[d] = (o[nt][e] * sc[0] + c1[d] * sc[1] + c2[d] * sc[2] + c3[d] * sc[3]) * inv * vsc;
-          }
-        }
+        for (int nt = 0; nt < 16; ++nt) *reinterpret_cast<float2*>(po + o_dim<KVT>(nt, 0, t)) = comb2(nt);
         if (t == 0) p.part_lse[static_cast<size_t>(it) * G + gid] = lse2;
       } else {
         const size_t orow = (static_cast<size_t>(b) * Hq + qo) * kHeadDim;
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int d = o_dim<KVT>(nt, e, t);
-            const float v = (o[nt][e] * sc[0] + c1[d] * sc[1] + c2[d] * sc[2] + c3[d] * sc[3]) * inv * vsc;
-            store_out<QT>(p.out, orow + d, v);
-          }
+          const float2 v = comb2(nt);
+          *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + orow + o_dim<KVT>(nt, 0, t)) =
+              ptx::pack2<QT == kBF16>(v.x, v.y);
         }
         if (t == 0 && p.lse) p.lse[static_cast<size_t>(b) * Hq + qo] = lse2 * kLn2;
       }
