@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
   const int t0 = split * p.tiles_per_split;
   const int n = max(min(t0 + p.tiles_per_split, n_tiles_all) - t0, 0);
   const int used_rows = R * G;
+  auto tile_of = [&](int i) { return t0 + i; };  // the i-th tile processed
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(B_Q), 1);
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
       // this CTA's keys of tile i: K rows key0 + 64 rank .. (kside), or all
       // 128 keys of the tile (V side); boxes of `box` keys never cross a page
       auto span = [&](int i, int& first, int& cnt) {
-        const int key0 = (t0 + i) * kKeys;
+        const int key0 = tile_of(i) * kKeys;
         if (kside) {
           first = key0 + kHalfKeys * static_cast<int>(rank);
           cnt = min(max(kv_len - first, 0), kHalfKeys);
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
             // the even CTA expects both CTAs' K bytes of this tile (its own
             // keys and the odd CTA's, from key0 + 64 on), two column halves each
             if (lead && lane == 0) {
-              const int c1 = min(max(kv_len - ((t0 + i) * kKeys + kHalfKeys), 0), kHalfKeys);
+              const int c1 = min(max(kv_len - (tile_of(i) * kKeys + kHalfKeys), 0), kHalfKeys);
               ptx::mbar_arrive_expect_tx(bar(B_KF + s),
                                          2u * bytes_here + static_cast<uint32_t>((c1 + box - 1) / box * box) * 256u);
             }
@@ -394,7 +395,7 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
             }
           } else {
             // [128 keys][64 codes] -> [128 keys][128 B]
-            const int nv = min(kKeys, kv_len - (t0 + w) * kKeys);
+            const int nv = min(kKeys, kv_len - tile_of(w) * kKeys);
             const uint32_t vb = base + C::kV + s * C::kVStage;
 #pragma unroll 4
             for (int item = lane; item < kKeys * 4; item += 32) {
@@ -540,7 +541,7 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
     for (int i = 0; i < n; ++i) {
       const int u = i % 3;
       const uint32_t scol = scol_base + col_s(u);
-      const int key0 = (t0 + i) * kKeys;
+      const int key0 = tile_of(i) * kKeys;
       const int nv = min(kKeys, kv_len - key0);
       const int vr = min(max(nv - 64 * hf, 0), 64);  // keys before the prefix end in this half
       // the maximum of the raw scores (the scale is positive, so it commutes
