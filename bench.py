@@ -60,9 +60,10 @@ def parse_args():
     ap.add_argument("--all-configs", action="store_true", help="also print one line per standard workload")
     ap.add_argument("--batch", type=int, default=None,
                     help="shrink the workload to its first N requests (small cases for profiling)")
-    ap.add_argument("--op", choices=["decode", "append", "tree", "prefill", "mla"], default="decode",
+    ap.add_argument("--op", choices=["decode", "append", "tree", "prefill", "mla", "merge"], default="decode",
                     help="append: pkd_append_kv (new tokens written into the workload's pool); tree: "
-                    "prefix-tree decode on the 3-level tree workload; prefill: append-prefill attention; mla: MLA decode")
+                    "prefix-tree decode on the 3-level tree workload; prefill: append-prefill attention; mla: MLA "
+                    "decode; merge: the standalone pkd_merge_state / pkd_merge_states on cascade-shaped states")
     ap.add_argument("--kv-layout", choices=["NHD", "HND"], default="NHD",
                     help="page layout of the K/V pools: NHD [P, Hk, D] pages or HND [Hk, P, D] pages")
     ap.add_argument("--append-tokens", type=int, default=0,
@@ -979,6 +980,61 @@ def run_mla(args):
     }
 
 
+def run_merge(args):
+    """The standalone merge_state (two states) and merge_states (k = 4 states)
+    calls: n = 16384 rows x 32 qo heads x 128 dims of bf16 values with fp32
+    log-sum-exps (each input well above L2), K back-to-back calls each, timed
+    with CUDA events.  Bytes: every input and output once."""
+    import torch
+
+    import paged_kv_decode_28_gb300 as pkd
+    from paged_kv_decode_28_gb300 import _build
+
+    _build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    n, H, D, k = (args.batch or 16384), 32, 128, 4
+    va = torch.randn((n, H, D), generator=gen, device=dev).to(torch.bfloat16)
+    vb = torch.randn((n, H, D), generator=gen, device=dev).to(torch.bfloat16)
+    sa = torch.randn((n, H), generator=gen, device=dev) * 4
+    sb = torch.randn((n, H), generator=gen, device=dev) * 4
+    vk = torch.randn((n, k, H, D), generator=gen, device=dev).to(torch.bfloat16)
+    sk = torch.randn((n, k, H), generator=gen, device=dev) * 4
+    out = torch.empty_like(va)
+    s_out = torch.empty_like(sa)
+    K = args.steps
+    peak, peak_kind = measured_hbm_peak()
+    res = {}
+    for name, fn, nbytes in (
+            ("merge_state", lambda: pkd.merge_state(va, sa, vb, sb, out=out, s_out=s_out),
+             3 * va.numel() * 2 + 3 * sa.numel() * 4),
+            ("merge_states", lambda: pkd.merge_states(vk, sk),
+             vk.numel() * 2 + sk.numel() * 4 + va.numel() * 2 + sa.numel() * 4)):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(0) as clocks:
+            e0.record()
+            for _ in range(K):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / K * 1e3
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[name] = {"us_per_call": round(us, 2), "bytes_per_call": int(nbytes), "achieved": round(gbs, 1),
+                     "frac": round(gbs / peak, 4), "clocks": clocks.summary()}
+    return {"metric": "standalone merge_state / merge_states: achieved HBM GB/s per call",
+            "value": res["merge_state"]["achieved"], "unit": "GB/s", "n_gpus": 1, "steps": K,
+            "warmup": max(args.warmup, 3), "higher_is_better": True, "dtype": "bf16 values, f32 lse",
+            "data": "synthetic (seeded N(0,1) values)",
+            "config": {"workload": f"n={n} x {H} heads x {D} dims; merge_states over k={k} states",
+                       "l2": l2_note(3 * va.numel() * 2, l2_bytes(dev)), "parallelism": "one GPU"},
+            "roofline": {"bound": "hbm", "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", **res}}
+
+
 def main():
     args = parse_args()
     world, rank = launch_world()
@@ -992,8 +1048,9 @@ def main():
               "its cascade and MLA kernels use cluster-multicast loads that stay within one GPU's memory",
               file=sys.stderr, flush=True)
         sys.exit(2)
-    if args.op in ("append", "tree", "prefill", "mla"):
-        line = {"append": run_append, "tree": run_tree, "prefill": run_prefill, "mla": run_mla}[args.op](args)
+    if args.op in ("append", "tree", "prefill", "mla", "merge"):
+        line = {"append": run_append, "tree": run_tree, "prefill": run_prefill, "mla": run_mla,
+                "merge": run_merge}[args.op](args)
         print(json.dumps(line), flush=True)
         return
     if args.impl == "reference":
