@@ -181,25 +181,96 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const Merg
   }
 }
 
-// One warp per (index, head) row; lanes stride over head_dim.
+// Weights of two states of log-sum-exps a, b (natural log) and the merged one.
+__device__ __forceinline__ void pair_weights(float a, float b, float& wa, float& wb, float& s) {
+  const float M = fmaxf(a, b);
+  wa = 0.f;
+  wb = 0.f;
+  s = -INFINITY;
+  if (M != -INFINITY) {
+    const float ea = (a == -INFINITY) ? 0.f : ptx::ex2((a - M) * kLog2e);
+    const float eb = (b == -INFINITY) ? 0.f : ptx::ex2((b - M) * kLog2e);
+    const float tot = ea + eb;
+    wa = ea / tot;
+    wb = eb / tot;
+    s = M + ptx::lg2(tot) * kLn2;
+  }
+}
+
+// 16 bytes of values (8 16-bit or 4 fp32 elements) as fp32, and back.
+struct Chunk {
+  float f[8];
+};
+
+__device__ __forceinline__ Chunk load_chunk(const void* in, size_t idx, int dtype) {
+  Chunk c;
+  const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(in) + idx * (dtype == kF32 ? 4 : 2));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  if (dtype == kF32) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      c.f[e] = __uint_as_float(w[e]);
+      c.f[4 + e] = 0.f;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 v = dtype == kBF16 ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]))
+                                      : __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+      c.f[2 * e] = v.x;
+      c.f[2 * e + 1] = v.y;
+    }
+  }
+  return c;
+}
+
+__device__ __forceinline__ void store_chunk(void* out, size_t idx, const Chunk& c, int dtype) {
+  uint4 u;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+  if (dtype == kF32) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[e] = __float_as_uint(c.f[e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[e] = dtype == kBF16 ? ptx::pack2<true>(c.f[2 * e], c.f[2 * e + 1])
+                                                      : ptx::pack2<false>(c.f[2 * e], c.f[2 * e + 1]);
+  }
+  *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + idx * (dtype == kF32 ? 4 : 2)) = u;
+}
+
+// Pairwise merge.  flat: one thread per 16-byte chunk of the values (dim a
+// multiple of the chunk, 16-byte aligned arrays, s_out not one of the inputs),
+// each thread taking its row's weights from the (cached) log-sum-exps; else
+// one warp per (index, head) row, lanes striding over head_dim (the order that
+// lets s_out overwrite an input in place).
 __global__ void merge_state_kernel(const void* va, const float* sa, const void* vb, const float* sb,
-                                   void* vo, float* so, int64_t rows, int dim, int dtype) {
+                                   void* vo, float* so, int64_t rows, int dim, int dtype, int flat) {
+  if (flat) {
+    const int ce = dtype == kF32 ? 4 : 8;  // elements per chunk
+    const int per_row = dim / ce;
+    const int64_t chunks = rows * per_row;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < chunks;
+         j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t r = j / per_row;
+      const size_t idx = static_cast<size_t>(j) * ce;
+      const Chunk x = load_chunk(va, idx, dtype), y = load_chunk(vb, idx, dtype);
+      float wa, wb, st;
+      pair_weights(__ldg(sa + r), __ldg(sb + r), wa, wb, st);
+      Chunk o;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o.f[e] = x.f[e] * wa + y.f[e] * wb;
+      store_chunk(vo, idx, o, dtype);
+      if (j - r * per_row == 0) so[r] = st;
+    }
+    return;
+  }
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
 #pragma unroll 1
   for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
        r += warps) {
-    const float a = sa[r], b = sb[r];
-    const float M = fmaxf(a, b);
-    float wa = 0.f, wb = 0.f, s = -INFINITY;
-    if (M != -INFINITY) {
-      const float ea = (a == -INFINITY) ? 0.f : ptx::ex2((a - M) * kLog2e);
-      const float eb = (b == -INFINITY) ? 0.f : ptx::ex2((b - M) * kLog2e);
-      const float tot = ea + eb;
-      wa = ea / tot;
-      wb = eb / tot;
-      s = M + ptx::lg2(tot) * kLn2;
-    }
+    float wa, wb, s;
+    pair_weights(sa[r], sb[r], wa, wb, s);
     __syncwarp();  // every lane has read sa/sb before lane 0 may overwrite them
 #pragma unroll 1
     for (int c = lane; c < dim; c += 32) {
@@ -211,11 +282,62 @@ __global__ void merge_state_kernel(const void* va, const float* sa, const void* 
   }
 }
 
-// One warp per (index, head): merges k states in order.
+// k-way merge, states folded in order.  flat (as above, values 16-byte
+// aligned, dim a multiple of the chunk): one thread per 16-byte chunk of the
+// output, up to four states' chunks loaded before they are used; else one
+// warp per (index, head) row.
 __global__ void merge_states_kernel(const void* v, const float* s, int64_t n, int k, int heads,
-                                    int dim, int dtype, void* vo, float* so) {
-  const int lane = threadIdx.x & 31;
+                                    int dim, int dtype, void* vo, float* so, int flat) {
   const int64_t rows = n * heads;
+  if (flat) {
+    const int ce = dtype == kF32 ? 4 : 8;
+    const int per_row = dim / ce;
+    const int64_t chunks = rows * per_row;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < chunks;
+         j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t r = j / per_row;
+      const int64_t i = r / heads;
+      const int hh = static_cast<int>(r - i * heads);
+      const int64_t off = (j - r * per_row) * ce;
+      // the first four states' chunks are requested before the maximum is known
+      Chunk x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (e < k) x[e] = load_chunk(v, ((i * k + e) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
+      float M = -INFINITY;
+      for (int c = 0; c < k; ++c) M = fmaxf(M, __ldg(s + (i * k + c) * heads + hh));
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float L = 0.f;
+      if (M != -INFINITY) {
+        for (int c0 = 0; c0 < k; c0 += 4) {
+          if (c0 > 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (c0 + e < k)
+                x[e] = load_chunk(v, ((i * k + c0 + e) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (c0 + e < k) {
+              const float sc = __ldg(s + (i * k + c0 + e) * heads + hh);
+              const float w = (sc == -INFINITY) ? 0.f : ptx::ex2((sc - M) * kLog2e);
+              L += w;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) acc[q] += w * x[e].f[q];
+            }
+          }
+        }
+      }
+      const float inv = M != -INFINITY ? 1.f / L : 0.f;
+      Chunk o;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o.f[q] = acc[q] * inv;
+      store_chunk(vo, static_cast<size_t>(r) * dim + off, o, dtype);
+      if (off == 0) so[r] = (M == -INFINITY) ? -INFINITY : M + ptx::lg2(L) * kLn2;
+    }
+    return;
+  }
+  const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
 #pragma unroll 1
   for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
@@ -255,13 +377,25 @@ __global__ void merge_states_kernel(const void* v, const float* s, int64_t n, in
 // is itself launched programmatically: it may become resident while the
 // previous step's merge drains, and waits for that grid before it overwrites
 // the schedule the merge reads.
+// The reads of the first four words per thread are issued before the wait, so
+// that their latency (the staging buffer is host memory) overlaps the tail of
+// the previous grid.
 __global__ void copy_words_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t n16) {
   ptx::pdl_launch_dependents();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  uint4 w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (i0 + e * stride < n16) w[e] = src[i0 + e * stride];
   ptx::pdl_wait_prior_grid();
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    dst[i] = src[i];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (i0 + e * stride < n16) dst[i0 + e * stride] = w[e];
+  for (int64_t i = i0 + 4 * stride; i < n16; i += stride) dst[i] = src[i];
 }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int grid_for_rows(int64_t rows) {
   const int64_t per_block = 8;  // warps per 256-thread block
@@ -316,7 +450,16 @@ cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, 
                                cudaStream_t stream) {
   const int64_t rows = n * heads;
   if (rows == 0) return cudaSuccess;
-  merge_state_kernel<<<grid_for_rows(rows), 256, 0, stream>>>(va, sa, vb, sb, vo, so, rows, dim, dtype);
+  const int ce = dtype == kF32 ? 4 : 8;
+  const bool flat = dim % ce == 0 && aligned16(va) && aligned16(vb) && aligned16(vo) && so != sa && so != sb;
+  if (flat) {
+    const int64_t chunks = rows * (dim / ce);
+    const int64_t blocks = (chunks + 255) / 256;
+    merge_state_kernel<<<static_cast<int>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(va, sa, vb, sb, vo, so,
+                                                                                          rows, dim, dtype, 1);
+  } else {
+    merge_state_kernel<<<grid_for_rows(rows), 256, 0, stream>>>(va, sa, vb, sb, vo, so, rows, dim, dtype, 0);
+  }
   return cudaGetLastError();
 }
 
@@ -324,7 +467,16 @@ cudaError_t launch_merge_states(const void* v, const float* s, int64_t n, int k,
                                 int dtype, void* vo, float* so, cudaStream_t stream) {
   const int64_t rows = n * heads;
   if (rows == 0) return cudaSuccess;
-  merge_states_kernel<<<grid_for_rows(rows), 256, 0, stream>>>(v, s, n, k, heads, dim, dtype, vo, so);
+  const int ce = dtype == kF32 ? 4 : 8;
+  const bool flat = dim % ce == 0 && aligned16(v) && aligned16(vo);
+  if (flat) {
+    const int64_t chunks = rows * (dim / ce);
+    const int64_t blocks = (chunks + 255) / 256;
+    merge_states_kernel<<<static_cast<int>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(v, s, n, k, heads, dim,
+                                                                                           dtype, vo, so, 1);
+  } else {
+    merge_states_kernel<<<grid_for_rows(rows), 256, 0, stream>>>(v, s, n, k, heads, dim, dtype, vo, so, 0);
+  }
   return cudaGetLastError();
 }
 

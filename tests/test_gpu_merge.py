@@ -11,7 +11,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
-@pytest.mark.parametrize("D", [128, 64, 8, 1024])
+@pytest.mark.parametrize("D", [128, 64, 8, 1024, 24])
 def test_merge_state(dtype, D):
     g = torch.Generator(device="cuda").manual_seed(D)
     n, H = 257, 5
@@ -41,7 +41,23 @@ def test_merge_state_in_place():
     assert_lse_close(sa, s_ref)
 
 
-@pytest.mark.parametrize("k", [0, 1, 3, 9])
+def test_merge_state_unaligned_rows():
+    """Views that start 2 elements into their storage: the kernel takes its
+    scalar path (the four-wide one needs 16-byte aligned arrays)."""
+    g = torch.Generator(device="cuda").manual_seed(5)
+    base_a = torch.randn(40 * 3 * 128 + 2, device="cuda", generator=g).bfloat16()
+    base_b = torch.randn(40 * 3 * 128 + 2, device="cuda", generator=g).bfloat16()
+    va = base_a[2:].view(40, 3, 128)
+    vb = base_b[2:].view(40, 3, 128)
+    sa = torch.randn(40, 3, device="cuda", generator=g)
+    sb = torch.randn(40, 3, device="cuda", generator=g)
+    v, s = pkd.merge_state(va, sa, vb, sb)
+    v_ref, s_ref = orc.merge_state(va.cpu(), sa.cpu(), vb.cpu(), sb.cpu())
+    assert_o_close(v, v_ref)
+    assert_lse_close(s, s_ref)
+
+
+@pytest.mark.parametrize("k", [0, 1, 3, 4, 5, 9])
 def test_merge_states(k):
     g = torch.Generator(device="cuda").manual_seed(k)
     n, H, D = 33, 6, 128
