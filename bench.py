@@ -105,11 +105,13 @@ def algorithmic_bytes(b) -> int:
 
 
 def decode_kernel_bytes(b) -> int:
-    """Algorithmic bytes of the decode kernel alone: as algorithmic_bytes, but
-    without the shared prefix, which the cascade's prefix kernel reads."""
+    """Algorithmic bytes of the kernels between the library's timing events:
+    the decode kernel (all of algorithmic_bytes) or, for the cascade, the
+    prefix kernel and the suffix decode that overlaps it (every K/V byte, q and
+    the scales; the merge after them writes out and lse)."""
     n = algorithmic_bytes(b)
     if b.prefix_page_indices is not None:
-        n -= b.prefix_len * b.num_kv_heads * b.head_dim * 2 * b.k_cache.element_size()
+        n -= b.batch * b.num_qo_heads * (b.head_dim * b.q.element_size() + 4)
     return n
 
 
@@ -442,7 +444,9 @@ def run_ours(args):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "pkd decode_kernel" + (" (suffix pages; the shared prefix is the prefix kernel's)" if cascade else ""),
+            "kernel": ("pkd prefix_pair_kernel + decode_kernel (the suffix decode starts on the SMs the prefix "
+                       "kernel leaves free; events from before the prefix kernel to the end of the decode grid)"
+                       if cascade else "pkd decode_kernel"),
             "bytes_per_launch": decode_kernel_bytes(b),
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -461,7 +465,8 @@ def run_ours(args):
         },
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "us_per_step": round(e2e_s / K * 1e6, 2)},
-        "gpu_launches": K * (3 if cascade else 2),
+        # upload copy + decode (+ prefix kernel + merge for the cascade)
+        "gpu_launches": K * (4 if cascade else 2),
         "clocks": clk,
     }
     if not args.no_cpu_baseline:

@@ -541,6 +541,10 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
     if (e != cudaSuccess) return cuda_fail(e, "upload fork");
     joined = false;
   }
+  // A single shared prefix (the pair kernel, one CTA per SM on most of the
+  // GPU, bound by its MMA chain) goes ahead of the suffix decode, whose CTAs
+  // start on the SMs it leaves free and read HBM meanwhile.
+  const bool prefix_first = cascade && cascade->n_pre_splits > 0 && !cascade->pp.work && plan->counts.n_items > 0;
   if (plan->counts.n_items > 0) {
     if (!d_k_cache || !d_v_cache) return fail(PKD_ERR_INVALID_ARG, "k/v cache is NULL");
     if (!aligned16(d_k_cache) || !aligned16(d_v_cache))
@@ -560,6 +564,12 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
       cudaError_t er = cudaEventRecordWithFlags(plan->ev_start, st, rec_flags);
       if (er != cudaSuccess) return cuda_fail(er, "cudaEventRecord(timing start)");
     }
+    if (prefix_first) {
+      cudaError_t e = pkd::launch_prefix(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->q_dtype,
+                                         plan->kv_dtype, st, true);
+      if (e != cudaSuccess) return cuda_fail(e, "prefix kernel launch");
+      p.behind_prefix = 1;
+    }
     cudaError_t e = pkd::launch_decode(tmk, tmv, p, plan->q_dtype, plan->kv_dtype, plan->G, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     if (plan->ev_stop) {
@@ -575,9 +585,9 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
       joined = false;
     }
   }
-  if (cascade && cascade->n_pre_splits > 0) {
-    // a prefix tree's levels are work-list pairs; a single shared prefix is
-    // the tile kernel's cluster mode
+  if (cascade && cascade->n_pre_splits > 0 && !prefix_first) {
+    // a prefix tree's levels are work-list pairs (after the decode grid); a
+    // single shared prefix runs here only when there is no decode grid
     cudaError_t e = cascade->pp.work
                         ? pkd::launch_tile2(cascade->tmq, cascade->tmk, cascade->tmv, cascade->pp, plan->kv_dtype, st,
                                             true)

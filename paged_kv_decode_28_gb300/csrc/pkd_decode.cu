@@ -51,6 +51,8 @@ struct Cfg {
   static constexpr int kAbort = kBars + 2 * kStages * 8;                        // int
   static constexpr int kTotal = kAbort + 16;
   static constexpr int kAlloc = kTotal + 1024;  // slack for the 1024-byte alignment of stages
+  // two CTAs per SM: 228 KB of shared memory, 1 KB of it reserved per CTA
+  static_assert(kCtasPerSm * (kAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
 __device__ __forceinline__ int load_page(const DecodeParams& p, int idx) {
@@ -468,11 +470,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   __syncthreads();
 
-  // this grid may have been launched before the schedule upload finished
-  ptx::pdl_wait_prior_grid();
-  // the next grid (the merge, or the cascade's prefix kernel) may be scheduled
-  // now: everything enqueued before this step is complete, so it may read the
-  // step's inputs; it waits for this grid before reading this grid's output
+  // This grid may have been launched before the schedule upload finished.  A
+  // grid launched behind the cascade's prefix kernel is launched only once
+  // every CTA of that kernel has waited for the upload, so the schedule and
+  // the caller's inputs were complete before its launch; it reads nothing the
+  // prefix kernel writes, and must not wait for that kernel to end: it waits
+  // for it at its own end instead, so that the grid behind it finds both done.
+  if (!p.behind_prefix) ptx::pdl_wait_prior_grid();
+  // the next grid (the merge, or the prefix kernel of a prefix tree) may be
+  // scheduled now: everything enqueued before this step is complete, so it may
+  // read the step's inputs; it waits for this grid before reading its output
   ptx::pdl_launch_dependents();
   const int it0 = p.cta_begin[blockIdx.x];
   const int it1 = p.cta_begin[blockIdx.x + 1];
@@ -727,6 +734,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     }
   }
+  // see the top: the grid does not end before the prefix kernel ahead of it
+  if (p.behind_prefix && threadIdx.x == 0) ptx::pdl_wait_prior_grid();
 }
 
 template <int QT, int KVT>

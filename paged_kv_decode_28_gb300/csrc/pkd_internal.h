@@ -70,6 +70,11 @@ struct DecodeParams {
   const WsHeader* header;
   int debug_stall;            // test hook: the producer issues nothing (waits run out)
   int kv_hnd;                 // pages are [Hk, P, D] (HND) instead of [P, Hk, D] (NHD)
+  // launched behind the cascade's prefix kernel, once that kernel has waited
+  // for the upload: everything this grid reads was complete before it was
+  // launched, so it skips griddepcontrol.wait at the start (which would wait
+  // for the prefix kernel) and waits at its end instead
+  int behind_prefix;
 };
 
 struct MergeParams {

@@ -223,6 +223,10 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
     ptx::mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
+    // launched programmatically behind the schedule upload, which itself
+    // waits for the previous step's merge (a reader of pre_o) and for the
+    // kernels that wrote this step's inputs
+    ptx::pdl_wait_prior_grid();
   }
   // the odd CTA of the last pair may hold no request at all: it loads no Q
   const bool has_q = b0 < p.batch;
@@ -242,6 +246,10 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // The suffix decode grid behind this one may start now, on the SMs this grid
+  // leaves free: it reads nothing this grid writes, and it ends only after
+  // this grid has, so the merge grid behind it finds both done.
+  ptx::pdl_launch_dependents();
   ptx::cluster_sync();  // both CTAs' barriers exist (and Q's zero rows are written) before any signal crosses
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base_ptr + C::kTmemSlot);
@@ -714,10 +722,6 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc_pair(tmem, kTmemCols);
   }
-  // This grid is launched programmatically behind the decode grid and reads
-  // nothing it writes; it does not finish before that grid has, so the merge
-  // grid behind it, which waits for this one, sees the decode's partials too.
-  if (threadIdx.x == 0) ptx::pdl_wait_prior_grid();
 }
 
 template <bool BF, bool FP8>
