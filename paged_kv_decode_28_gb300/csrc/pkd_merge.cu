@@ -202,9 +202,12 @@ struct Chunk {
   float f[8];
 };
 
-__device__ __forceinline__ Chunk load_chunk(const void* in, size_t idx, int dtype) {
+__device__ __forceinline__ uint4 load_raw(const void* in, size_t idx, int dtype) {
+  return *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(in) + idx * (dtype == kF32 ? 4 : 2));
+}
+
+__device__ __forceinline__ Chunk to_chunk(const uint4& u, int dtype) {
   Chunk c;
-  const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(in) + idx * (dtype == kF32 ? 4 : 2));
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
   if (dtype == kF32) {
 #pragma unroll
@@ -222,6 +225,10 @@ __device__ __forceinline__ Chunk load_chunk(const void* in, size_t idx, int dtyp
     }
   }
   return c;
+}
+
+__device__ __forceinline__ Chunk load_chunk(const void* in, size_t idx, int dtype) {
+  return to_chunk(load_raw(in, idx, dtype), dtype);
 }
 
 __device__ __forceinline__ void store_chunk(void* out, size_t idx, const Chunk& c, int dtype) {
@@ -249,18 +256,36 @@ __global__ void merge_state_kernel(const void* va, const float* sa, const void* 
     const int ce = dtype == kF32 ? 4 : 8;  // elements per chunk
     const int per_row = dim / ce;
     const int64_t chunks = rows * per_row;
-    for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < chunks;
-         j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-      const int64_t r = j / per_row;
-      const size_t idx = static_cast<size_t>(j) * ce;
-      const Chunk x = load_chunk(va, idx, dtype), y = load_chunk(vb, idx, dtype);
-      float wa, wb, st;
-      pair_weights(__ldg(sa + r), __ldg(sb + r), wa, wb, st);
-      Chunk o;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    // chunks j and j + stride per iteration, all four loads issued first
+    for (int64_t j0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j0 < chunks; j0 += 2 * stride) {
+      uint4 xa[2], xb[2];
+      float la[2], lb[2];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o.f[e] = x.f[e] * wa + y.f[e] * wb;
-      store_chunk(vo, idx, o, dtype);
-      if (j - r * per_row == 0) so[r] = st;
+      for (int u = 0; u < 2; ++u) {
+        const int64_t j = j0 + u * stride;
+        if (j < chunks) {
+          const int64_t r = j / per_row;
+          xa[u] = load_raw(va, static_cast<size_t>(j) * ce, dtype);
+          xb[u] = load_raw(vb, static_cast<size_t>(j) * ce, dtype);
+          la[u] = __ldg(sa + r);
+          lb[u] = __ldg(sb + r);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int64_t j = j0 + u * stride;
+        if (j >= chunks) continue;
+        const int64_t r = j / per_row;
+        const Chunk x = to_chunk(xa[u], dtype), y = to_chunk(xb[u], dtype);
+        float wa, wb, st;
+        pair_weights(la[u], lb[u], wa, wb, st);
+        Chunk o;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o.f[e] = x.f[e] * wa + y.f[e] * wb;
+        store_chunk(vo, static_cast<size_t>(j) * ce, o, dtype);
+        if (j - r * per_row == 0) so[r] = st;
+      }
     }
     return;
   }
@@ -293,47 +318,71 @@ __global__ void merge_states_kernel(const void* v, const float* s, int64_t n, in
     const int ce = dtype == kF32 ? 4 : 8;
     const int per_row = dim / ce;
     const int64_t chunks = rows * per_row;
-    for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < chunks;
-         j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-      const int64_t r = j / per_row;
-      const int64_t i = r / heads;
-      const int hh = static_cast<int>(r - i * heads);
-      const int64_t off = (j - r * per_row) * ce;
-      // the first four states' chunks are requested before the maximum is known
-      Chunk x[4];
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    // chunks j and j + stride per iteration: the first four states' chunks and
+    // log-sum-exps of both are requested before any is used
+    for (int64_t j0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j0 < chunks; j0 += 2 * stride) {
+      uint4 x[2][4];
+      float sc[2][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (e < k) x[e] = load_chunk(v, ((i * k + e) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
-      float M = -INFINITY;
-      for (int c = 0; c < k; ++c) M = fmaxf(M, __ldg(s + (i * k + c) * heads + hh));
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float L = 0.f;
-      if (M != -INFINITY) {
-        for (int c0 = 0; c0 < k; c0 += 4) {
-          if (c0 > 0) {
+      for (int u = 0; u < 2; ++u) {
+        const int64_t j = j0 + u * stride;
+        if (j >= chunks) continue;
+        const int64_t r = j / per_row;
+        const int64_t i = r / heads;
+        const int hh = static_cast<int>(r - i * heads);
+        const int64_t off = (j - r * per_row) * ce;
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (c0 + e < k)
-                x[e] = load_chunk(v, ((i * k + c0 + e) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (c0 + e < k) {
-              const float sc = __ldg(s + (i * k + c0 + e) * heads + hh);
-              const float w = (sc == -INFINITY) ? 0.f : ptx::ex2((sc - M) * kLog2e);
-              L += w;
-#pragma unroll
-              for (int q = 0; q < 8; ++q) acc[q] += w * x[e].f[q];
-            }
+        for (int e = 0; e < 4; ++e) {
+          if (e < k) {
+            x[u][e] = load_raw(v, ((i * k + e) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
+            sc[u][e] = __ldg(s + (i * k + e) * heads + hh);
           }
         }
       }
-      const float inv = M != -INFINITY ? 1.f / L : 0.f;
-      Chunk o;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) o.f[q] = acc[q] * inv;
-      store_chunk(vo, static_cast<size_t>(r) * dim + off, o, dtype);
-      if (off == 0) so[r] = (M == -INFINITY) ? -INFINITY : M + ptx::lg2(L) * kLn2;
+      for (int u = 0; u < 2; ++u) {
+        const int64_t j = j0 + u * stride;
+        if (j >= chunks) continue;
+        const int64_t r = j / per_row;
+        const int64_t i = r / heads;
+        const int hh = static_cast<int>(r - i * heads);
+        const int64_t off = (j - r * per_row) * ce;
+        float M = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (e < k) M = fmaxf(M, sc[u][e]);
+        for (int c = 4; c < k; ++c) M = fmaxf(M, __ldg(s + (i * k + c) * heads + hh));
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (e < k) {
+              const float w = (sc[u][e] == -INFINITY) ? 0.f : ptx::ex2((sc[u][e] - M) * kLog2e);
+              const Chunk c = to_chunk(x[u][e], dtype);
+              L += w;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) acc[q] += w * c.f[q];
+            }
+          }
+          // states past the fourth, in order
+          for (int c0 = 4; c0 < k; ++c0) {
+            const float scc = __ldg(s + (i * k + c0) * heads + hh);
+            const float w = (scc == -INFINITY) ? 0.f : ptx::ex2((scc - M) * kLog2e);
+            const Chunk c = load_chunk(v, ((i * k + c0) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
+            L += w;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] += w * c.f[q];
+          }
+        }
+        const float inv = M != -INFINITY ? 1.f / L : 0.f;
+        Chunk o;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) o.f[q] = acc[q] * inv;
+        store_chunk(vo, static_cast<size_t>(r) * dim + off, o, dtype);
+        if (off == 0) so[r] = (M == -INFINITY) ? -INFINITY : M + ptx::lg2(L) * kLn2;
+      }
     }
     return;
   }
