@@ -655,6 +655,33 @@ std::vector<pkd::TileWork> longest_first(std::vector<UnitPair>& pairs) {
   return w;
 }
 
+// Paged prefill: the pairs of one request together (its K/V then stays in L2
+// while its query tiles run; spread over the launch, a request's pages were
+// read from DRAM 1.29 times on the append-prefill workload), requests in
+// order of their longest pair and each request's pairs longest first, so the
+// long ones still do not start last.  A request's pairs are contiguous in
+// `pairs` (built request by request).
+std::vector<pkd::TileWork> by_request_longest_first(std::vector<UnitPair>& pairs) {
+  auto len = [](const UnitPair& x) { return x.a.t1 - x.a.t0; };
+  auto same_request = [](const UnitPair& x, const UnitPair& y) { return x.a.page_begin == y.a.page_begin && x.a.q_end == y.a.q_end; };
+  std::vector<std::vector<UnitPair>> groups;
+  for (const UnitPair& q : pairs) {
+    if (groups.empty() || !same_request(groups.back().front(), q)) groups.emplace_back();
+    groups.back().push_back(q);
+  }
+  for (auto& g : groups) std::stable_sort(g.begin(), g.end(), [&](const UnitPair& x, const UnitPair& y) { return len(x) > len(y); });
+  std::stable_sort(groups.begin(), groups.end(),
+                   [&](const std::vector<UnitPair>& x, const std::vector<UnitPair>& y) { return len(x.front()) > len(y.front()); });
+  std::vector<pkd::TileWork> w;
+  w.reserve(2 * pairs.size());
+  for (const auto& g : groups)
+    for (const UnitPair& q : g) {
+      w.push_back(q.a);
+      w.push_back(q.b);
+    }
+  return w;
+}
+
 // Prefix-tree work units (host): validates the levels, cuts each level into
 // key-range pieces and pairs each node's 128-row query tiles.  Shared by
 // pkd_plan_tree and the host-only pkd_tree_units_host.
@@ -810,7 +837,7 @@ pkd_status prefill_units(const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
       pairs.push_back({t, u});
     }
   }
-  *w = longest_first(pairs);
+  *w = by_request_longest_first(pairs);
   return PKD_OK;
 }
 

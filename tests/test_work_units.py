@@ -4,7 +4,8 @@ exports and checked against what the kernels rely on -- both units of a pair
 share their keys, every query row is covered exactly once, a node's or a
 request's key-range pieces partition its keys, the causal key range is the one
 the pair's last row sees, MLA's piece size is the smallest that fits the SMs,
-and pairs come longest first."""
+and pairs come longest first (prefill: a request's pairs together, longest
+first, requests in order of their longest pair)."""
 import numpy as np
 import pytest
 
@@ -29,14 +30,29 @@ def _rows(a, per_tile):
     return range(a[Q0], min(a[Q0] + per_tile, a[QEND]))
 
 
-def _check_pair_invariants(u, per_tile):
+def _check_pair_invariants(u, per_tile, by_request=False):
     for a, b in _pairs(u):
         for f in (QEND, PB, KVLEN, T0, T1, PIECE, LEVEL, DIAG):
             assert a[f] == b[f], f
         assert a[Q0] < a[QEND]  # the first tile always has rows
         assert b[Q0] == min(a[Q0] + per_tile, a[QEND])
     lengths = [a[T1] - a[T0] for a, _ in _pairs(u)]
-    assert lengths == sorted(lengths, reverse=True)
+    if not by_request:
+        assert lengths == sorted(lengths, reverse=True)
+        return
+    # a request's pairs are contiguous and longest first; the requests come in
+    # order of their longest pair
+    groups = []
+    for a, _ in _pairs(u):
+        key = (a[PB], a[QEND])
+        if not groups or groups[-1][0] != key:
+            assert all(g[0] != key for g in groups), "a request's pairs are split"
+            groups.append((key, []))
+        groups[-1][1].append(a[T1] - a[T0])
+    for _, ls in groups:
+        assert ls == sorted(ls, reverse=True)
+    firsts = [ls[0] for _, ls in groups]
+    assert firsts == sorted(firsts, reverse=True)
 
 
 def _prefill_case(rng, B, P):
@@ -58,7 +74,7 @@ def test_prefill_units(causal, g, P):
     qo, kvi, last, kv_lens = _prefill_case(rng, B, P)
     per_tile = 128 // g
     u = api.prefill_units(qo, kvi, last, 8 * g, 8, P, causal=causal)
-    _check_pair_invariants(u, per_tile)
+    _check_pair_invariants(u, per_tile, by_request=True)
     seen = np.zeros(int(qo[-1]), np.int32)
     for a, b in _pairs(u):
         r = int(np.searchsorted(qo, a[Q0], side="right")) - 1
