@@ -53,6 +53,21 @@ def test_prefill_matches_oracle(causal, P, g):
     assert_lse_close(lse, l_ref)
 
 
+@pytest.mark.parametrize("g", [1, 4])
+def test_lone_tiles_split_over_key_tiles(g):
+    """A request's lone last query tile with two or more key tiles takes its
+    even and odd key tiles in two halves and combines them: rows that see no
+    key of the odd tiles (causal rows before key 128), three key tiles, a tile
+    cut by the sequence end."""
+    b = wl.make_prefill(seed=1240 + g, q_lens=[100, 20, 3, 30, 1], kv_lens=[150, 140, 300, 140, 257],
+                        num_qo_heads=2 * g, num_kv_heads=2, page_size=16, device="cuda")
+    for causal in (True, False):
+        out, lse = _gpu_prefill(b, causal)
+        o_ref, l_ref = _oracle(b, causal)
+        assert_o_close(out, o_ref, what=f"causal={causal}")
+        assert_lse_close(lse, l_ref, what=f"causal={causal}")
+
+
 def test_prefill_f16_and_hnd():
     from tests.test_gpu_hnd import to_hnd
 
