@@ -245,47 +245,60 @@ __device__ __forceinline__ void store_chunk(void* out, size_t idx, const Chunk& 
   *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + idx * (dtype == kF32 ? 4 : 2)) = u;
 }
 
+// The flat pairwise merge with chunk indices of type I (32-bit when the
+// chunk count allows: the index arithmetic is most of the instructions).
+template <typename I>
+__device__ __forceinline__ void merge_state_flat(const void* va, const float* sa, const void* vb, const float* sb,
+                                                 void* vo, float* so, int64_t rows, int dim, int dtype) {
+  const int ce = dtype == kF32 ? 4 : 8;  // elements per chunk
+  const int per_row = dim / ce;
+  const I chunks = static_cast<I>(rows) * per_row;
+  const I stride = static_cast<I>(gridDim.x) * blockDim.x;
+  // chunks j and j + stride per iteration, all four loads issued first
+  for (I j0 = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; j0 < chunks; j0 += 2 * stride) {
+    uint4 xa[2], xb[2];
+    float la[2], lb[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const I j = j0 + u * stride;
+      if (j < chunks) {
+        const I r = j / per_row;
+        xa[u] = load_raw(va, static_cast<size_t>(j) * ce, dtype);
+        xb[u] = load_raw(vb, static_cast<size_t>(j) * ce, dtype);
+        la[u] = __ldg(sa + r);
+        lb[u] = __ldg(sb + r);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const I j = j0 + u * stride;
+      if (j >= chunks) continue;
+      const I r = j / per_row;
+      const Chunk x = to_chunk(xa[u], dtype), y = to_chunk(xb[u], dtype);
+      float wa, wb, st;
+      pair_weights(la[u], lb[u], wa, wb, st);
+      Chunk o;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o.f[e] = x.f[e] * wa + y.f[e] * wb;
+      store_chunk(vo, static_cast<size_t>(j) * ce, o, dtype);
+      if (j - r * per_row == 0) so[r] = st;
+    }
+  }
+}
+
 // Pairwise merge.  flat: one thread per 16-byte chunk of the values (dim a
 // multiple of the chunk, 16-byte aligned arrays, s_out not one of the inputs),
 // each thread taking its row's weights from the (cached) log-sum-exps; else
 // one warp per (index, head) row, lanes striding over head_dim (the order that
 // lets s_out overwrite an input in place).
+
 __global__ void merge_state_kernel(const void* va, const float* sa, const void* vb, const float* sb,
                                    void* vo, float* so, int64_t rows, int dim, int dtype, int flat) {
   if (flat) {
-    const int ce = dtype == kF32 ? 4 : 8;  // elements per chunk
-    const int per_row = dim / ce;
-    const int64_t chunks = rows * per_row;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    // chunks j and j + stride per iteration, all four loads issued first
-    for (int64_t j0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j0 < chunks; j0 += 2 * stride) {
-      uint4 xa[2], xb[2];
-      float la[2], lb[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int64_t j = j0 + u * stride;
-        if (j < chunks) {
-          const int64_t r = j / per_row;
-          xa[u] = load_raw(va, static_cast<size_t>(j) * ce, dtype);
-          xb[u] = load_raw(vb, static_cast<size_t>(j) * ce, dtype);
-          la[u] = __ldg(sa + r);
-          lb[u] = __ldg(sb + r);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int64_t j = j0 + u * stride;
-        if (j >= chunks) continue;
-        const int64_t r = j / per_row;
-        const Chunk x = to_chunk(xa[u], dtype), y = to_chunk(xb[u], dtype);
-        float wa, wb, st;
-        pair_weights(la[u], lb[u], wa, wb, st);
-        Chunk o;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o.f[e] = x.f[e] * wa + y.f[e] * wb;
-        store_chunk(vo, static_cast<size_t>(j) * ce, o, dtype);
-        if (j - r * per_row == 0) so[r] = st;
-      }
+    if (flat == 2) {
+      merge_state_flat<uint32_t>(va, sa, vb, sb, vo, so, rows, dim, dtype);
+    } else {
+      merge_state_flat<int64_t>(va, sa, vb, sb, vo, so, rows, dim, dtype);
     }
     return;
   }
@@ -307,82 +320,94 @@ __global__ void merge_state_kernel(const void* va, const float* sa, const void* 
   }
 }
 
-// k-way merge, states folded in order.  flat (as above, values 16-byte
-// aligned, dim a multiple of the chunk): one thread per 16-byte chunk of the
-// output, up to four states' chunks loaded before they are used; else one
-// warp per (index, head) row.
-__global__ void merge_states_kernel(const void* v, const float* s, int64_t n, int k, int heads,
-                                    int dim, int dtype, void* vo, float* so, int flat) {
-  const int64_t rows = n * heads;
-  if (flat) {
-    const int ce = dtype == kF32 ? 4 : 8;
-    const int per_row = dim / ce;
-    const int64_t chunks = rows * per_row;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    // chunks j and j + stride per iteration: the first four states' chunks and
-    // log-sum-exps of both are requested before any is used
-    for (int64_t j0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j0 < chunks; j0 += 2 * stride) {
-      uint4 x[2][4];
-      float sc[2][4];
+// The flat k-way merge with chunk indices of type I (see merge_state_flat).
+template <typename I>
+__device__ __forceinline__ void merge_states_flat(const void* v, const float* s, int64_t rows, int k, int heads,
+                                                  int dim, int dtype, void* vo, float* so) {
+  const int ce = dtype == kF32 ? 4 : 8;
+  const int per_row = dim / ce;
+  const I chunks = static_cast<I>(rows) * per_row;
+  const I stride = static_cast<I>(gridDim.x) * blockDim.x;
+  // chunks j and j + stride per iteration: the first four states' chunks and
+  // log-sum-exps of both are requested before any is used
+  for (I j0 = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; j0 < chunks; j0 += 2 * stride) {
+    uint4 x[2][4];
+    float sc[2][4];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int64_t j = j0 + u * stride;
-        if (j >= chunks) continue;
-        const int64_t r = j / per_row;
-        const int64_t i = r / heads;
-        const int hh = static_cast<int>(r - i * heads);
-        const int64_t off = (j - r * per_row) * ce;
+    for (int u = 0; u < 2; ++u) {
+      const I j = j0 + u * stride;
+      if (j >= chunks) continue;
+      const I r = j / per_row;
+      const int64_t i = static_cast<int64_t>(r / static_cast<I>(heads));
+      const int hh = static_cast<int>(r - static_cast<I>(i) * heads);
+      const int64_t off = static_cast<int64_t>(j - r * per_row) * ce;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (e < k) {
+          x[u][e] = load_raw(v, ((i * k + e) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
+          sc[u][e] = __ldg(s + (i * k + e) * heads + hh);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const I j = j0 + u * stride;
+      if (j >= chunks) continue;
+      const I r = j / per_row;
+      const int64_t i = static_cast<int64_t>(r / static_cast<I>(heads));
+      const int hh = static_cast<int>(r - static_cast<I>(i) * heads);
+      const int64_t off = static_cast<int64_t>(j - r * per_row) * ce;
+      float M = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (e < k) M = fmaxf(M, sc[u][e]);
+      for (int c = 4; c < k; ++c) M = fmaxf(M, __ldg(s + (i * k + c) * heads + hh));
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float L = 0.f;
+      if (M != -INFINITY) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           if (e < k) {
-            x[u][e] = load_raw(v, ((i * k + e) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
-            sc[u][e] = __ldg(s + (i * k + e) * heads + hh);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int64_t j = j0 + u * stride;
-        if (j >= chunks) continue;
-        const int64_t r = j / per_row;
-        const int64_t i = r / heads;
-        const int hh = static_cast<int>(r - i * heads);
-        const int64_t off = (j - r * per_row) * ce;
-        float M = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (e < k) M = fmaxf(M, sc[u][e]);
-        for (int c = 4; c < k; ++c) M = fmaxf(M, __ldg(s + (i * k + c) * heads + hh));
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        float L = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (e < k) {
-              const float w = (sc[u][e] == -INFINITY) ? 0.f : ptx::ex2((sc[u][e] - M) * kLog2e);
-              const Chunk c = to_chunk(x[u][e], dtype);
-              L += w;
-#pragma unroll
-              for (int q = 0; q < 8; ++q) acc[q] += w * c.f[q];
-            }
-          }
-          // states past the fourth, in order
-          for (int c0 = 4; c0 < k; ++c0) {
-            const float scc = __ldg(s + (i * k + c0) * heads + hh);
-            const float w = (scc == -INFINITY) ? 0.f : ptx::ex2((scc - M) * kLog2e);
-            const Chunk c = load_chunk(v, ((i * k + c0) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
+            const float w = (sc[u][e] == -INFINITY) ? 0.f : ptx::ex2((sc[u][e] - M) * kLog2e);
+            const Chunk c = to_chunk(x[u][e], dtype);
             L += w;
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[q] += w * c.f[q];
           }
         }
-        const float inv = M != -INFINITY ? 1.f / L : 0.f;
-        Chunk o;
+        // states past the fourth, in order
+        for (int c0 = 4; c0 < k; ++c0) {
+          const float scc = __ldg(s + (i * k + c0) * heads + hh);
+          const float w = (scc == -INFINITY) ? 0.f : ptx::ex2((scc - M) * kLog2e);
+          const Chunk c = load_chunk(v, ((i * k + c0) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
+          L += w;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) o.f[q] = acc[q] * inv;
-        store_chunk(vo, static_cast<size_t>(r) * dim + off, o, dtype);
-        if (off == 0) so[r] = (M == -INFINITY) ? -INFINITY : M + ptx::lg2(L) * kLn2;
+          for (int q = 0; q < 8; ++q) acc[q] += w * c.f[q];
+        }
       }
+      const float inv = M != -INFINITY ? 1.f / L : 0.f;
+      Chunk o;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o.f[q] = acc[q] * inv;
+      store_chunk(vo, static_cast<size_t>(r) * dim + off, o, dtype);
+      if (off == 0) so[r] = (M == -INFINITY) ? -INFINITY : M + ptx::lg2(L) * kLn2;
+    }
+  }
+}
+
+// k-way merge, states folded in order.  flat (as above, values 16-byte
+// aligned, dim a multiple of the chunk): one thread per 16-byte chunk of the
+// output, up to four states' chunks loaded before they are used; else one
+// warp per (index, head) row.
+
+__global__ void merge_states_kernel(const void* v, const float* s, int64_t n, int k, int heads,
+                                    int dim, int dtype, void* vo, float* so, int flat) {
+  const int64_t rows = n * heads;
+  if (flat) {
+    if (flat == 2) {
+      merge_states_flat<uint32_t>(v, s, rows, k, heads, dim, dtype, vo, so);
+    } else {
+      merge_states_flat<int64_t>(v, s, rows, k, heads, dim, dtype, vo, so);
     }
     return;
   }
@@ -504,8 +529,8 @@ cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, 
   if (flat) {
     const int64_t chunks = rows * (dim / ce);
     const int64_t blocks = (chunks + 255) / 256;
-    merge_state_kernel<<<static_cast<int>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(va, sa, vb, sb, vo, so,
-                                                                                          rows, dim, dtype, 1);
+    merge_state_kernel<<<static_cast<int>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(
+        va, sa, vb, sb, vo, so, rows, dim, dtype, chunks < (int64_t(1) << 31) ? 2 : 1);
   } else {
     merge_state_kernel<<<grid_for_rows(rows), 256, 0, stream>>>(va, sa, vb, sb, vo, so, rows, dim, dtype, 0);
   }
@@ -521,8 +546,8 @@ cudaError_t launch_merge_states(const void* v, const float* s, int64_t n, int k,
   if (flat) {
     const int64_t chunks = rows * (dim / ce);
     const int64_t blocks = (chunks + 255) / 256;
-    merge_states_kernel<<<static_cast<int>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(v, s, n, k, heads, dim,
-                                                                                           dtype, vo, so, 1);
+    merge_states_kernel<<<static_cast<int>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(
+        v, s, n, k, heads, dim, dtype, vo, so, chunks < (int64_t(1) << 31) ? 2 : 1);
   } else {
     merge_states_kernel<<<grid_for_rows(rows), 256, 0, stream>>>(v, s, n, k, heads, dim, dtype, vo, so, 0);
   }
