@@ -30,6 +30,8 @@ constexpr int kConsumerWarps = 4;
 constexpr int kCombStride = kHeadDim + 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr float kLn2 = 0.693147180559945309f;
+// a split row of at most this many items is merged with one round trip of loads
+constexpr int kFewStates = 8;
 
 template <int KVT>
 struct Cfg {
@@ -400,42 +402,74 @@ __device__ __forceinline__ void merge_split_row(const DecodeParams& p, int row, 
     return __ldcg(reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(beg + s) * G + j) * kHeadDim) + lane);
   };
   float M = -INFINITY;
-  for (int s0 = 0; s0 < cnt; s0 += 32) M = fmaxf(M, (s0 + lane < cnt) ? lse_of(s0 + lane) : -INFINITY);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
-  if (M != -INFINITY) {
-    for (int s0 = 0; s0 < cnt; s0 += 32) {
-      const int ns = min(32, cnt - s0);
-      const float x = (lane < ns) ? lse_of(s0 + lane) : -INFINITY;
-      const float wgt = (x == -INFINITY) ? 0.f : ptx::ex2(x - M);
-      L += wgt;
-      int s = 0;
-      for (; s + 2 <= ns; s += 2) {
-        const float w0 = __shfl_sync(0xffffffffu, wgt, s), w1 = __shfl_sync(0xffffffffu, wgt, s + 1);
-        const float4 a = o_of(s0 + s), c = o_of(s0 + s + 1);
-        acc.x += w0 * a.x + w1 * c.x;
-        acc.y += w0 * a.y + w1 * c.y;
-        acc.z += w0 * a.z + w1 * c.z;
-        acc.w += w0 * a.w + w1 * c.w;
-      }
-      if (s < ns) {
-        const float w0 = __shfl_sync(0xffffffffu, wgt, s);
-        const float4 a = o_of(s0 + s);
-        acc.x += w0 * a.x;
-        acc.y += w0 * a.y;
-        acc.z += w0 * a.z;
-        acc.w += w0 * a.w;
-      }
-    }
+  if (cnt <= kFewStates) {
+    // every state's lse and o requested at once: one memory round trip
+    float4 ov[kFewStates];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    const float inv = 1.f / L;
-    acc.x *= inv;
-    acc.y *= inv;
-    acc.z *= inv;
-    acc.w *= inv;
+    for (int s = 0; s < kFewStates; ++s) ov[s] = s < cnt ? o_of(s) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float x = lane < cnt ? lse_of(lane) : -INFINITY;
+    M = x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (M != -INFINITY) {
+      const float wgt = (x == -INFINITY) ? 0.f : ptx::ex2(x - M);
+      L = wgt;
+#pragma unroll
+      for (int s = 0; s < kFewStates; ++s) {
+        const float w = __shfl_sync(0xffffffffu, wgt, s);
+        if (s < cnt) {
+          acc.x += w * ov[s].x;
+          acc.y += w * ov[s].y;
+          acc.z += w * ov[s].z;
+          acc.w += w * ov[s].w;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      const float inv = 1.f / L;
+      acc.x *= inv;
+      acc.y *= inv;
+      acc.z *= inv;
+      acc.w *= inv;
+    }
+  } else {
+    for (int s0 = 0; s0 < cnt; s0 += 32) M = fmaxf(M, (s0 + lane < cnt) ? lse_of(s0 + lane) : -INFINITY);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (M != -INFINITY) {
+      for (int s0 = 0; s0 < cnt; s0 += 32) {
+        const int ns = min(32, cnt - s0);
+        const float x = (lane < ns) ? lse_of(s0 + lane) : -INFINITY;
+        const float wgt = (x == -INFINITY) ? 0.f : ptx::ex2(x - M);
+        L += wgt;
+        int s = 0;
+        for (; s + 2 <= ns; s += 2) {
+          const float w0 = __shfl_sync(0xffffffffu, wgt, s), w1 = __shfl_sync(0xffffffffu, wgt, s + 1);
+          const float4 a = o_of(s0 + s), c = o_of(s0 + s + 1);
+          acc.x += w0 * a.x + w1 * c.x;
+          acc.y += w0 * a.y + w1 * c.y;
+          acc.z += w0 * a.z + w1 * c.z;
+          acc.w += w0 * a.w + w1 * c.w;
+        }
+        if (s < ns) {
+          const float w0 = __shfl_sync(0xffffffffu, wgt, s);
+          const float4 a = o_of(s0 + s);
+          acc.x += w0 * a.x;
+          acc.y += w0 * a.y;
+          acc.z += w0 * a.z;
+          acc.w += w0 * a.w;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      const float inv = 1.f / L;
+      acc.x *= inv;
+      acc.y *= inv;
+      acc.z *= inv;
+      acc.w *= inv;
+    }
   }
   const size_t bq = static_cast<size_t>(b) * Hq + h * G + j;
   store_out4<QT>(p.out, bq * kHeadDim + 4 * lane, acc);
