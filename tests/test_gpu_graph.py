@@ -149,3 +149,49 @@ def test_cascade_replan_then_replay_matches_oracle(kv_dtype):
                                           k_scale=pool.k_scale, v_scale=pool.v_scale)
         assert_o_close(out, o_ref, what=f"cascade replay {trial} out")
         assert_lse_close(lse, l_ref, what=f"cascade replay {trial} lse")
+
+
+def test_cascade_back_to_back_without_sync():
+    """Cascade steps of alternating suffix tables with no host synchronization:
+    the prefix grid of a step must not overwrite the prefix pieces the previous
+    step's merge still reads, and the suffix decode behind it must read its own
+    step's schedule; every step equals its isolated run bit for bit."""
+    B, Hq, Hk, P = 40, 32, 8, 16
+    pool = wl.make_paged(seed=33, lengths=[512] * B, num_qo_heads=Hq, num_kv_heads=Hk, page_size=P,
+                         prefix_len=1000, q_dtype="bf16", kv_dtype="bf16", device="cuda")
+    rng = np.random.default_rng(3)
+    own = pool.kv_page_indices.copy()
+    pre = torch.from_numpy(pool.prefix_page_indices.copy()).cuda()
+    plan = pkd.Plan(B, Hq, Hk, max_prefix_splits=16)
+
+    def table(lens):
+        n = (lens + P - 1) // P
+        indptr = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+        pages = np.concatenate([own[32 * r:32 * r + n[r]] for r in range(B)]).astype(np.int32)
+        last = np.where(n > 0, lens - (n - 1) * P, 0).astype(np.int32)
+        return indptr, torch.from_numpy(np.ascontiguousarray(pages)).cuda(), last
+
+    tables = [table(rng.integers(1, 513, size=B)), table(rng.integers(0, 65, size=B))]
+    kw = dict(sm_scale=pool.sm_scale)
+    ref = []
+    for indptr, pages, last in tables:  # each alone, synchronized, against the oracle
+        plan.plan(indptr, pages, last, P, q_dtype=pool.q.dtype, kv_dtype=pool.k_cache.dtype)
+        o, l = plan.cascade_decode(pre, pool.prefix_last_page_len, pool.q, pool.k_cache, pool.v_cache, **kw)
+        torch.cuda.synchronize()
+        o_ref, l_ref = orc.cascade_decode(pool.q, pool.k_cache, pool.v_cache, pool.prefix_page_indices,
+                                          pool.prefix_last_page_len, indptr, pages.cpu().numpy(), last,
+                                          sm_scale=pool.sm_scale)
+        assert_o_close(o, o_ref)
+        assert_lse_close(l, l_ref)
+        ref.append((o.clone(), l.clone()))
+    outs = [(torch.empty_like(pool.q), torch.empty(B, Hq, device="cuda")) for _ in range(8)]
+    for i, (o, l) in enumerate(outs):
+        indptr, pages, last = tables[i % 2]
+        plan.plan(indptr, pages, last, P, q_dtype=pool.q.dtype, kv_dtype=pool.k_cache.dtype)
+        plan.cascade_decode(pre, pool.prefix_last_page_len, pool.q, pool.k_cache, pool.v_cache, out=o, lse=l, **kw)
+    torch.cuda.synchronize()
+    assert plan.check_device_errors() == 0
+    for i, (o, l) in enumerate(outs):
+        ro, rl = ref[i % 2]
+        assert torch.equal(o, ro), f"step {i}: output differs from the isolated run"
+        assert torch.equal(l, rl), f"step {i}: lse differs from the isolated run"
