@@ -35,8 +35,10 @@ class PkdError(RuntimeError):
 
 _lib = None
 
-_i32p = ctypes.POINTER(ctypes.c_int32)
 _vp = ctypes.c_void_p
+# int32 host arrays are passed as plain addresses (an int per call is cheaper
+# to marshal than a ctypes pointer object)
+_i32p = _vp
 
 
 def lib() -> ctypes.CDLL:
@@ -100,13 +102,19 @@ def _check(status: int):
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream) -> ctypes.c_void_p:
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream) -> int:
+    """The CUDA stream handle: the given torch stream's, or the current one."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _host_i32(x) -> np.ndarray:
@@ -115,8 +123,8 @@ def _host_i32(x) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
 
 
-def _as_i32p(a: np.ndarray):
-    return a.ctypes.data_as(_i32p)
+def _as_i32p(a: np.ndarray) -> int:
+    return a.ctypes.data
 
 
 def version() -> str:
