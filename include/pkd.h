@@ -201,11 +201,13 @@ pkd_status pkd_run(pkd_plan_t plan, const void* d_q, const void* d_k_cache, cons
  * and page size pkd_plan accepts is supported; E4M3 pools take k_scale /
  * v_scale as in pkd_run (their codes are widened exactly to q's type for the
  * products).  Other arguments as pkd_run.  The plan must have been created
- * with max_prefix_splits >= 1.  Enqueues the schedule upload, the suffix
- * decode (every item writes a partial state), the prefix kernel (launched
- * programmatically, so its CTAs take the SMs the decode grid frees as it
- * drains; it finishes only after the decode grid has) and the merge of the
- * prefix and suffix states.  Capturable like pkd_run.
+ * with max_prefix_splits >= 1.  Enqueues the schedule upload, the prefix
+ * kernel (it waits for the upload, then lets the next grid launch), the
+ * suffix decode (launched programmatically behind it: its first CTAs start on
+ * the SMs the prefix kernel leaves free, every item writes a partial state,
+ * and the grid finishes only after the prefix kernel has) and the merge of the
+ * prefix and suffix states.  With no suffix keys the decode grid is left out.
+ * Capturable like pkd_run.
  */
 pkd_status pkd_cascade_decode(pkd_plan_t suffix_plan, const int32_t* d_prefix_page_indices,
                               int prefix_num_pages, int prefix_last_page_len, const void* d_q,
