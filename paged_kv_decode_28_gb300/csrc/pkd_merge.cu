@@ -254,35 +254,21 @@ __device__ __forceinline__ void merge_state_flat(const void* va, const float* sa
   const int per_row = dim / ce;
   const I chunks = static_cast<I>(rows) * per_row;
   const I stride = static_cast<I>(gridDim.x) * blockDim.x;
-  // chunks j and j + stride per iteration, all four loads issued first
-  for (I j0 = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; j0 < chunks; j0 += 2 * stride) {
-    uint4 xa[2], xb[2];
-    float la[2], lb[2];
+  // one chunk per iteration, its four loads issued first; the grid is one wave
+  // of resident blocks, so the latency is covered by the many threads
+  for (I j = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; j < chunks; j += stride) {
+    const I r = j / per_row;
+    const uint4 xa = load_raw(va, static_cast<size_t>(j) * ce, dtype);
+    const uint4 xb = load_raw(vb, static_cast<size_t>(j) * ce, dtype);
+    const float la = __ldg(sa + r), lb = __ldg(sb + r);
+    const Chunk x = to_chunk(xa, dtype), y = to_chunk(xb, dtype);
+    float wa, wb, st;
+    pair_weights(la, lb, wa, wb, st);
+    Chunk o;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const I j = j0 + u * stride;
-      if (j < chunks) {
-        const I r = j / per_row;
-        xa[u] = load_raw(va, static_cast<size_t>(j) * ce, dtype);
-        xb[u] = load_raw(vb, static_cast<size_t>(j) * ce, dtype);
-        la[u] = __ldg(sa + r);
-        lb[u] = __ldg(sb + r);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const I j = j0 + u * stride;
-      if (j >= chunks) continue;
-      const I r = j / per_row;
-      const Chunk x = to_chunk(xa[u], dtype), y = to_chunk(xb[u], dtype);
-      float wa, wb, st;
-      pair_weights(la[u], lb[u], wa, wb, st);
-      Chunk o;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o.f[e] = x.f[e] * wa + y.f[e] * wb;
-      store_chunk(vo, static_cast<size_t>(j) * ce, o, dtype);
-      if (j - r * per_row == 0) so[r] = st;
-    }
+    for (int e = 0; e < 8; ++e) o.f[e] = x.f[e] * wa + y.f[e] * wb;
+    store_chunk(vo, static_cast<size_t>(j) * ce, o, dtype);
+    if (j - r * per_row == 0) so[r] = st;
   }
 }
 
@@ -325,43 +311,50 @@ template <typename I>
 __device__ __forceinline__ void merge_states_flat(const void* v, const float* s, int64_t rows, int k, int heads,
                                                   int dim, int dtype, void* vo, float* so) {
   const int ce = dtype == kF32 ? 4 : 8;
+  const int esz = dtype == kF32 ? 4 : 2;
   const int per_row = dim / ce;
   const I chunks = static_cast<I>(rows) * per_row;
   const I stride = static_cast<I>(gridDim.x) * blockDim.x;
-  // chunks j and j + stride per iteration: the first four states' chunks and
-  // log-sum-exps of both are requested before any is used
-  for (I j0 = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; j0 < chunks; j0 += 2 * stride) {
-    uint4 x[2][4];
-    float sc[2][4];
+  // bytes from one state's values to the next state's, and the same for lse
+  const size_t vstep = static_cast<size_t>(heads) * dim * esz;
+  const uint8_t* vbytes = static_cast<const uint8_t*>(v);
+  // one output chunk per iteration (more resident threads beat more chunks per
+  // thread here): the first four states' chunks and log-sum-exps are
+  // requested before any is used
+  for (I j0 = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; j0 < chunks; j0 += stride) {
+    uint4 x[1][4];
+    float sc[1][4];
+    const uint8_t* vp[1];
+    const float* sp[1];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < 1; ++u) {
       const I j = j0 + u * stride;
       if (j >= chunks) continue;
       const I r = j / per_row;
-      const int64_t i = static_cast<int64_t>(r / static_cast<I>(heads));
-      const int hh = static_cast<int>(r - static_cast<I>(i) * heads);
-      const int64_t off = static_cast<int64_t>(j - r * per_row) * ce;
+      const I i = r / static_cast<I>(heads);
+      const I hh = r - i * static_cast<I>(heads);
+      const I c = j - r * per_row;
+      // state 0 of (index i, head hh), this thread's chunk
+      const size_t row0 = static_cast<size_t>(i) * k * heads + hh;
+      vp[u] = vbytes + (row0 * dim + static_cast<size_t>(c) * ce) * esz;
+      sp[u] = s + row0;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         if (e < k) {
-          x[u][e] = load_raw(v, ((i * k + e) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
-          sc[u][e] = __ldg(s + (i * k + e) * heads + hh);
+          x[u][e] = *reinterpret_cast<const uint4*>(vp[u] + e * vstep);
+          sc[u][e] = __ldg(sp[u] + static_cast<size_t>(e) * heads);
         }
       }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < 1; ++u) {
       const I j = j0 + u * stride;
       if (j >= chunks) continue;
-      const I r = j / per_row;
-      const int64_t i = static_cast<int64_t>(r / static_cast<I>(heads));
-      const int hh = static_cast<int>(r - static_cast<I>(i) * heads);
-      const int64_t off = static_cast<int64_t>(j - r * per_row) * ce;
       float M = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         if (e < k) M = fmaxf(M, sc[u][e]);
-      for (int c = 4; c < k; ++c) M = fmaxf(M, __ldg(s + (i * k + c) * heads + hh));
+      for (int c = 4; c < k; ++c) M = fmaxf(M, __ldg(sp[u] + static_cast<size_t>(c) * heads));
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       float L = 0.f;
       if (M != -INFINITY) {
@@ -377,9 +370,9 @@ __device__ __forceinline__ void merge_states_flat(const void* v, const float* s,
         }
         // states past the fourth, in order
         for (int c0 = 4; c0 < k; ++c0) {
-          const float scc = __ldg(s + (i * k + c0) * heads + hh);
+          const float scc = __ldg(sp[u] + static_cast<size_t>(c0) * heads);
           const float w = (scc == -INFINITY) ? 0.f : ptx::ex2((scc - M) * kLog2e);
-          const Chunk c = load_chunk(v, ((i * k + c0) * heads + hh) * static_cast<int64_t>(dim) + off, dtype);
+          const Chunk c = to_chunk(*reinterpret_cast<const uint4*>(vp[u] + c0 * vstep), dtype);
           L += w;
 #pragma unroll
           for (int q = 0; q < 8; ++q) acc[q] += w * c.f[q];
@@ -389,8 +382,9 @@ __device__ __forceinline__ void merge_states_flat(const void* v, const float* s,
       Chunk o;
 #pragma unroll
       for (int q = 0; q < 8; ++q) o.f[q] = acc[q] * inv;
-      store_chunk(vo, static_cast<size_t>(r) * dim + off, o, dtype);
-      if (off == 0) so[r] = (M == -INFINITY) ? -INFINITY : M + ptx::lg2(L) * kLn2;
+      store_chunk(vo, static_cast<size_t>(j) * ce, o, dtype);
+      const I r = j / per_row;
+      if (j - r * per_row == 0) so[r] = (M == -INFINITY) ? -INFINITY : M + ptx::lg2(L) * kLn2;
     }
   }
 }
@@ -471,6 +465,18 @@ __global__ void copy_words_kernel(uint4* __restrict__ dst, const uint4* __restri
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Blocks of `threads` threads of `kernel` resident on the whole GPU at once
+// (SM count x occupancy), for a grid-stride kernel sized to run in one wave.
+int64_t resident_blocks(const void* kernel, int threads) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess) {
+    cudaGetLastError();  // a failed query falls back to a fixed grid
+    return 8192;
+  }
+  return static_cast<int64_t>(sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+}
+
 int grid_for_rows(int64_t rows) {
   const int64_t per_block = 8;  // warps per 256-thread block
   int64_t g = (rows + per_block - 1) / per_block;
@@ -529,7 +535,8 @@ cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, 
   if (flat) {
     const int64_t chunks = rows * (dim / ce);
     const int64_t blocks = (chunks + 255) / 256;
-    merge_state_kernel<<<static_cast<int>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(
+    const int64_t cap = resident_blocks(reinterpret_cast<const void*>(merge_state_kernel), 256);
+    merge_state_kernel<<<static_cast<int>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
         va, sa, vb, sb, vo, so, rows, dim, dtype, chunks < (int64_t(1) << 31) ? 2 : 1);
   } else {
     merge_state_kernel<<<grid_for_rows(rows), 256, 0, stream>>>(va, sa, vb, sb, vo, so, rows, dim, dtype, 0);
@@ -546,7 +553,8 @@ cudaError_t launch_merge_states(const void* v, const float* s, int64_t n, int k,
   if (flat) {
     const int64_t chunks = rows * (dim / ce);
     const int64_t blocks = (chunks + 255) / 256;
-    merge_states_kernel<<<static_cast<int>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(
+    const int64_t cap = resident_blocks(reinterpret_cast<const void*>(merge_states_kernel), 256);
+    merge_states_kernel<<<static_cast<int>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
         v, s, n, k, heads, dim, dtype, vo, so, chunks < (int64_t(1) << 31) ? 2 : 1);
   } else {
     merge_states_kernel<<<grid_for_rows(rows), 256, 0, stream>>>(v, s, n, k, heads, dim, dtype, vo, so, 0);
