@@ -10,7 +10,8 @@
 // e4m3(x / scale[h]), the quotient in fp32 (IEEE division), rounded to nearest
 // even and saturated to +-448.
 //
-// One warp per token: after one page lookup the warp moves the token's Hk * 256
+// One warp per token (the grid one wave of resident blocks, warps striding over
+// the tokens): after one page lookup the warp moves the token's Hk * 256
 // bytes of K and of V with independent 16-byte loads and stores (8-byte stores
 // of codes for e4m3).  The token's rows are contiguous in the new-token tensor
 // ([Hk, 128]); in an NHD page they are contiguous too ((slot * Hk + h) * 128),
@@ -63,7 +64,7 @@ __device__ __forceinline__ uint2 quantise8(const float (&f)[8], float scale) {
 }
 
 template <int NT, int KVT>
-__global__ void __launch_bounds__(kAppendWarps * 32, KVT == kE4M3 ? 4 : 6) append_kv_kernel(const AppendParams p) {
+__global__ void __launch_bounds__(kAppendWarps * 32, 6) append_kv_kernel(const AppendParams p) {
   const int lane = threadIdx.x & 31;
   const int Hk = p.num_kv_heads;
   const int chunks = Hk * (kHeadDim / 8);  // 16-byte chunks of 16-bit source per token
@@ -100,16 +101,25 @@ __global__ void __launch_bounds__(kAppendWarps * 32, KVT == kE4M3 ? 4 : 6) appen
     if constexpr (KVT == kE4M3) {
       uint8_t* kd = static_cast<uint8_t*>(p.k_cache) + dst;
       uint8_t* vd = static_cast<uint8_t*>(p.v_cache) + dst;
-#pragma unroll 4
+      // two chunks in flight per lane and K, then V, quantised in turn: 40
+      // registers (a few bytes of spill) for six blocks per SM, whose warps
+      // hide the latency that the divisions leave exposed
+#pragma unroll 2
       for (int c = lane; c < chunks; c += 32) {
         const int h = c >> 4;
         const uint4 ku = __ldg(ks + c), vu = __ldg(vs + c);
-        float kf[8], vf[8];
-        unpack8<NT>(ku, kf);
-        unpack8<NT>(vu, vf);
+        const float ksc = __ldg(p.k_scale + h), vsc = __ldg(p.v_scale + h);
         const uint32_t o = chunk_off(c);
-        *reinterpret_cast<uint2*>(kd + o) = quantise8(kf, __ldg(p.k_scale + h));
-        *reinterpret_cast<uint2*>(vd + o) = quantise8(vf, __ldg(p.v_scale + h));
+        {
+          float f[8];
+          unpack8<NT>(ku, f);
+          *reinterpret_cast<uint2*>(kd + o) = quantise8(f, ksc);
+        }
+        {
+          float f[8];
+          unpack8<NT>(vu, f);
+          *reinterpret_cast<uint2*>(vd + o) = quantise8(f, vsc);
+        }
       }
     } else {
       uint16_t* kd = static_cast<uint16_t*>(p.k_cache) + dst;
@@ -127,8 +137,19 @@ __global__ void __launch_bounds__(kAppendWarps * 32, KVT == kE4M3 ? 4 : 6) appen
 
 template <int NT, int KVT>
 cudaError_t launch_t(const AppendParams& p, cudaStream_t stream) {
+  // one wave of resident blocks (SM count x occupancy), warps striding over
+  // the tokens: no block launches past the first wave
   int64_t grid = (static_cast<int64_t>(p.n_tokens) + kAppendWarps - 1) / kAppendWarps;
-  grid = grid < 1 ? 1 : (grid > 8192 ? 8192 : grid);
+  int64_t cap = 8192;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, append_kv_kernel<NT, KVT>, kAppendWarps * 32, 0) == cudaSuccess &&
+      sms > 0 && per_sm > 0) {
+    cap = static_cast<int64_t>(sms) * per_sm;
+  } else {
+    cudaGetLastError();  // a failed query falls back to a fixed grid
+  }
+  grid = grid < 1 ? 1 : (grid > cap ? cap : grid);
   append_kv_kernel<NT, KVT><<<static_cast<int>(grid), kAppendWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
