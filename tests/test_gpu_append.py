@@ -85,6 +85,33 @@ def test_e4m3_codes_of_every_16_bit_value(newd, scale):
     assert torch.equal(b.v_cache.cpu().view(torch.uint8), vr.view(torch.uint8))
 
 
+@pytest.mark.parametrize("kvd", ["bf16", "e4m3"])
+def test_append_more_tokens_than_resident_warps(kvd):
+    """More new tokens than the one-wave grid has warps (each warp strides over
+    several tokens), appended at the end of a few long requests."""
+    P, Hk = 16, 2
+    reqs, per = 4, 2503
+    lens = np.full(reqs, per, dtype=np.int64)
+    b = wl.make_paged(seed=870, lengths=lens.tolist(), num_qo_heads=4, num_kv_heads=Hk, page_size=P, kv_dtype=kvd,
+                      q_dtype="bf16", device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(9)
+    n = reqs * per
+    k_new = (torch.randn(n, Hk, 128, device="cuda", generator=gen) * 3).to(torch.bfloat16)
+    v_new = (torch.randn(n, Hk, 128, device="cuda", generator=gen) * 3).to(torch.bfloat16)
+    bi = np.repeat(np.arange(reqs), per)
+    pos = np.tile(np.arange(per), reqs)  # every slot of every request, rewritten
+    kr, vr, skipped = ka.append_kv(b.k_cache, b.v_cache, k_new, v_new, bi, pos, b.kv_indptr, b.kv_page_indices, P,
+                                   b.k_scale, b.v_scale)
+    assert skipped == 0
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkd.append_kv(k_new, v_new, _cuda_i32(bi), _cuda_i32(pos), _cuda_i32(b.kv_indptr), _cuda_i32(b.kv_page_indices),
+                  b.k_cache, b.v_cache, k_scale=b.k_scale, v_scale=b.v_scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    view = (lambda t: t.view(torch.uint8)) if kvd == "e4m3" else (lambda t: t)
+    assert torch.equal(view(b.k_cache.cpu()), view(kr)) and torch.equal(view(b.v_cache.cpu()), view(vr))
+
+
 def test_append_then_decode_equals_oracle():
     lens = np.array([1, 17, 300, 64, 1000])
     for kvd in ("bf16", "e4m3"):

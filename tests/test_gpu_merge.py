@@ -72,3 +72,35 @@ def test_merge_states(k):
     v_ref, s_ref = orc.merge_states(v.cpu(), s.cpu())
     assert_o_close(vo, v_ref)
     assert_lse_close(so, s_ref)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_merge_state_more_chunks_than_resident_threads(dtype):
+    """A few times more 16-byte chunks than the one-wave grid has threads, so
+    every thread strides over several, with a ragged last pass."""
+    g = torch.Generator(device="cuda").manual_seed(41)
+    n, H, D = 1031, 32, 128
+    va = torch.randn(n, H, D, device="cuda", generator=g).to(dtype)
+    vb = torch.randn(n, H, D, device="cuda", generator=g).to(dtype)
+    sa = torch.randn(n, H, device="cuda", generator=g) * 4
+    sb = torch.randn(n, H, device="cuda", generator=g) * 4
+    sa[-1, -1] = -float("inf")
+    v, s = pkd.merge_state(va, sa, vb, sb)
+    v_ref, s_ref = orc.merge_state(va.cpu(), sa.cpu(), vb.cpu(), sb.cpu())
+    assert_o_close(v, v_ref)
+    assert_lse_close(s, s_ref)
+
+
+@pytest.mark.parametrize("k,dtype", [(4, torch.bfloat16), (6, torch.bfloat16), (3, torch.float32)])
+def test_merge_states_more_chunks_than_resident_threads(k, dtype):
+    g = torch.Generator(device="cuda").manual_seed(43 + k)
+    n, H, D = 517, 32, 128
+    v = torch.randn(n, k, H, D, device="cuda", generator=g).to(dtype)
+    s = torch.randn(n, k, H, device="cuda", generator=g) * 3
+    s[-1, :, -1] = -float("inf")
+    s[5, 0, 7] = -float("inf")
+    vo, so = pkd.merge_states(v, s)
+    v_ref, s_ref = orc.merge_states(v.cpu(), s.cpu())
+    assert_o_close(vo, v_ref)
+    assert_lse_close(so, s_ref)
+    assert torch.all(vo[-1, -1] == 0) and torch.isneginf(so[-1, -1])
