@@ -365,9 +365,14 @@ pkd_status pkd_append_kv(const void* d_k_new, const void* d_v_new, int new_dtype
  *   d_q [num_qo_heads, 128]; d_k, d_v [kv_len, num_kv_heads, 128] (kv_len >= 0);
  *   d_out [num_qo_heads, 128] (q dtype); d_lse fp32 [num_qo_heads] or NULL.
  *   q_dtype / kv_dtype as for pkd_plan; d_k_scale / d_v_scale for E4M3.
- * Plans internally (one cudaMemcpyAsync of the schedule into d_workspace, so not
- * capturable) and runs the batched path on it.  d_workspace must hold
- * pkd_workspace_bytes(1, num_qo_heads, num_kv_heads, 128, num_ctas, 0) bytes.
+ * Plans internally and runs the batched path on it.  The schedule (a few KB
+ * for one request) is carried in the parameters of the kernel that writes it
+ * into d_workspace, so the call allocates nothing, never touches a copy engine
+ * and can be captured in a CUDA graph (the graph replays the kv_len it was
+ * captured with); only a schedule above 16 KB (num_kv_heads + num_ctas above
+ * ~900) falls back to one cudaMemcpyAsync, which is not capturable.
+ * d_workspace must hold pkd_workspace_bytes(1, num_qo_heads, num_kv_heads,
+ * 128, num_ctas, 0) bytes.
  */
 pkd_status pkd_single_decode(const void* d_q, const void* d_k, const void* d_v, int kv_len,
                              int num_qo_heads, int num_kv_heads, int head_dim, int q_dtype,

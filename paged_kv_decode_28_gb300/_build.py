@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkd.so")
 SOURCES = ["pkd_capi.cu", "pkd_plan.cpp", "pkd_decode.cu", "pkd_merge.cu", "pkd_prefix.cu", "pkd_tile2.cu", "pkd_noalloc.cu",
-           "pkd_append.cu", "pkd_mla.cu", "pkd_mla_capi.cu"]
+           "pkd_append.cu", "pkd_mla.cu", "pkd_mla_capi.cu", "pkd_upload.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

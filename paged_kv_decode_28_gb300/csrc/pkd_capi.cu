@@ -16,6 +16,7 @@
 #include "pkd.h"
 #include "pkd_host.h"
 #include "pkd_internal.h"
+#include "pkd_upload.h"
 #include "pkd_plan.h"
 
 namespace {
@@ -212,6 +213,9 @@ struct pkd_plan_s {
   // the latest plan on each replay); stage_done fires after each such copy and
   // plan waits for it before overwriting the buffer
   bool use_pinned = true;
+  // one-shot plans (single-request decode): the schedule travels in the
+  // upload kernel's parameters instead (no copy engine: capturable)
+  bool upload_by_blob = false;
   uint8_t* staging = nullptr;
   uint8_t* staging_dev = nullptr;  // device mapping of the staging buffer
   cudaEvent_t stage_done = nullptr;
@@ -426,6 +430,8 @@ pkd_status pkd_plan(pkd_plan_t plan, const int32_t* h_kv_indptr, const int32_t* 
       if (ea != cudaSuccess) return cuda_fail(ea, "cudaEventSynchronize(plan staging)");
     }
     memcpy(plan->staging + 16, h + 16, L.meta_end - 16);
+  } else if (plan->upload_by_blob) {
+    // run_common launches the upload with the host copy as its parameter
   } else {
     cudaError_t e = cudaMemcpyAsync(plan->ws + 4, h + 4, L.meta_end - 4, cudaMemcpyHostToDevice,
                                     static_cast<cudaStream_t>(stream));
@@ -540,6 +546,9 @@ pkd_status run_common(pkd_plan_t plan, const void* d_q, const void* d_k_cache, c
     if (e == cudaSuccess && plan->ev_start) e = cudaEventRecordWithFlags(plan->ev_start, plan->side, rec_flags);
     if (e != cudaSuccess) return cuda_fail(e, "upload fork");
     joined = false;
+  } else if (plan->upload_by_blob) {
+    cudaError_t e = pkd::launch_copy_blob(ws + 16, plan->host.data() + 16, L.meta_end - 16, st);
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload");
   }
   // A single shared prefix (the pair kernel, one CTA per SM on most of the
   // GPU, bound by its MMA chain) goes ahead of the suffix decode, whose CTAs
@@ -1293,7 +1302,10 @@ pkd_status pkd_single_decode(const void* d_q, const void* d_k, const void* d_v, 
   const int32_t last[1] = {kv_len > 0 ? kv_len : 0};
   const int32_t* zero_page = reinterpret_cast<const int32_t*>(
       static_cast<uint8_t*>(d_workspace) + offsetof(pkd::WsHeader, zero_page));
-  plan->use_pinned = false;  // a one-shot plan: the pageable copy is staged before return
+  // a one-shot plan: the schedule goes in the upload kernel's parameters when
+  // it fits (capturable), else by a pageable copy staged before return
+  plan->use_pinned = false;
+  plan->upload_by_blob = plan->lay.meta_end - 16 <= static_cast<size_t>(pkd::kBlobBytes);
   s = pkd_plan(plan, indptr, zero_page, last, 1, num_qo_heads, num_kv_heads, head_dim, P, q_dtype,
                kv_dtype, stream);
   if (s == PKD_OK) {

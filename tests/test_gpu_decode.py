@@ -133,6 +133,35 @@ def test_single_decode_lengths_gqa(L):
     assert_lse_close(lse, l_ref)
 
 
+@pytest.mark.parametrize("L", [1, 65, 2048])
+def test_single_decode_captured_in_a_graph(L):
+    """The schedule of single-request decode travels in its upload kernel's
+    parameters, so the call captures into a CUDA graph; replays after the
+    inputs change in place follow the new values."""
+    g = torch.Generator(device="cuda").manual_seed(300 + L)
+    q = torch.randn(32, 128, device="cuda", generator=g).half()
+    k = torch.randn(L, 8, 128, device="cuda", generator=g).half()
+    v = torch.randn(L, 8, 128, device="cuda", generator=g).half()
+    ws = torch.empty(pkd.workspace_bytes(1, 32, 8, 128, pkd.num_ctas(0), 0), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pkd.single_decode(q, k, v, workspace=ws)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        o, lse = pkd.single_decode(q, k, v, workspace=ws)
+    for rep in range(3):
+        q.copy_(torch.randn(32, 128, device="cuda", generator=g).half())
+        k.copy_(torch.randn(L, 8, 128, device="cuda", generator=g).half())
+        v.copy_(torch.randn(L, 8, 128, device="cuda", generator=g).half())
+        graph.replay()
+        torch.cuda.synchronize()
+        o_ref, l_ref = orc.single_decode(q, k, v)
+        assert_o_close(o, o_ref)
+        assert_lse_close(lse, l_ref)
+
+
 def test_out_of_range_page_index_sets_flag():
     """A page id past the pool is read as page 0 and flagged; nothing faults."""
     b = wl.make_paged(seed=10, lengths=[40, 40], num_qo_heads=8, num_kv_heads=2, page_size=16,
