@@ -731,12 +731,16 @@ pkd_status tree_units(int num_levels, const int32_t* const* h_req_indptr, const 
       level_max_tiles[l] = tiles > level_max_tiles[l] ? tiles : level_max_tiles[l];
     }
   }
-  // key-range pieces per level: one target unit length (in 128-key tiles) for
-  // the whole launch, the work of all levels (CTA-tiles, a CTA per pair of
-  // query tiles) over about one wave of CTAs,
-  // and each level cut into the pieces its longest node needs for it, within
-  // the plan's piece budget (each level keeps one)
-  int64_t work = 0;  // CTA-tiles with one piece per level
+  // key-range pieces per level.  A CTA's cost per 128-key tile: its pair of
+  // query tiles takes ~1.43 times as long as a lone tile (the last, odd tile
+  // of a node; ~3.9 against ~2.75 us on GB300).  The launch's cost over the
+  // SMs is the average load; each level is cut so that its longest unit's
+  // pieces cost at most 3/4 of it (pieces as long as the average next to
+  // short ones leave SMs idle at the end), within the plan's piece budget
+  // (each level keeps one).
+  constexpr int64_t kCostPair = 143, kCostLone = 100;  // per key tile
+  int64_t cost = 0;                                    // the launch, with one piece per level
+  std::vector<int64_t> level_max_cost(num_levels, 0);  // the costliest unit of each level
   for (int l = 0; l < num_levels; ++l) {
     const int32_t* ri = h_req_indptr[l];
     const int32_t* ki = h_kv_indptr[l];
@@ -744,18 +748,23 @@ pkd_status tree_units(int num_levels, const int32_t* const* h_req_indptr, const 
     for (int n = 0; n < h_num_nodes[l]; ++n) {
       const int pages = ki[n + 1] - ki[n];
       const int64_t len = pages > 0 ? static_cast<int64_t>(pages - 1) * P + lp[n] : 0;
-      work += static_cast<int64_t>((ri[n + 1] - ri[n] + 2 * per_tile - 1) / (2 * per_tile)) * ((len + 127) / 128);
+      const int64_t tiles = (len + 127) / 128;
+      const int64_t qt = (ri[n + 1] - ri[n] + per_tile - 1) / per_tile;  // query tiles of the node
+      cost += ((qt / 2) * kCostPair + (qt % 2) * kCostLone) * tiles;
+      const int64_t unit = (qt >= 2 ? kCostPair : kCostLone) * tiles;
+      level_max_cost[l] = unit > level_max_cost[l] ? unit : level_max_cost[l];
     }
   }
-  work *= num_kv_heads;
-  const int64_t target = (work + sms - 1) / sms > 2 ? (work + sms - 1) / sms : 2;
+  cost *= num_kv_heads;
+  int64_t target = (3 * cost) / (4 * static_cast<int64_t>(sms));
+  target = target > 2 * kCostLone ? target : 2 * kCostLone;
   std::vector<int> S(num_levels, 1);
   int budget = max_splits;
   for (int l = 0; l < num_levels; ++l) {
-    int want = static_cast<int>((level_max_tiles[l] + target - 1) / target);
-    want = want < 1 ? 1 : want;
+    int64_t want = (level_max_cost[l] + target - 1) / target;
+    want = want < 1 ? 1 : (want > level_max_tiles[l] && level_max_tiles[l] > 0 ? level_max_tiles[l] : want);
     const int cap = budget - (num_levels - 1 - l);
-    S[l] = want > cap ? cap : want;
+    S[l] = want > cap ? cap : static_cast<int>(want);
     budget -= S[l];
   }
   // units in pairs (two query tiles of one node with the same keys: one CTA
