@@ -21,6 +21,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "pkd_internal.h"
 #include "pkd_ptx.cuh"
 
@@ -139,15 +141,28 @@ template <int NT, int KVT>
 cudaError_t launch_t(const AppendParams& p, cudaStream_t stream) {
   // one wave of resident blocks (SM count x occupancy), warps striding over
   // the tokens: no block launches past the first wave
+  // (queried once per device and instantiation; a failed query falls back
+  // to a fixed grid)
+  static std::atomic<int> cached[64];
   int64_t grid = (static_cast<int64_t>(p.n_tokens) + kAppendWarps - 1) / kAppendWarps;
   int64_t cap = 8192;
-  int dev = 0, sms = 0, per_sm = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, append_kv_kernel<NT, KVT>, kAppendWarps * 32, 0) == cudaSuccess &&
-      sms > 0 && per_sm > 0) {
-    cap = static_cast<int64_t>(sms) * per_sm;
-  } else {
-    cudaGetLastError();  // a failed query falls back to a fixed grid
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+    int c = cached[dev].load(std::memory_order_relaxed);
+    if (c == 0) {
+      int sms = 0, per_sm = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, append_kv_kernel<NT, KVT>, kAppendWarps * 32, 0) ==
+              cudaSuccess &&
+          sms > 0 && per_sm > 0) {
+        c = sms * per_sm;
+      } else {
+        cudaGetLastError();
+        c = -1;
+      }
+      cached[dev].store(c, std::memory_order_relaxed);
+    }
+    if (c > 0) cap = c;
   }
   grid = grid < 1 ? 1 : (grid > cap ? cap : grid);
   append_kv_kernel<NT, KVT><<<static_cast<int>(grid), kAppendWarps * 32, 0, stream>>>(p);

@@ -14,6 +14,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "pkd_internal.h"
 #include "pkd_ptx.cuh"
 
@@ -315,77 +317,65 @@ __device__ __forceinline__ void merge_states_flat(const void* v, const float* s,
   const int per_row = dim / ce;
   const I chunks = static_cast<I>(rows) * per_row;
   const I stride = static_cast<I>(gridDim.x) * blockDim.x;
-  // bytes from one state's values to the next state's, and the same for lse
+  // bytes from one state's values to the next state's (the log-sum-exps are
+  // `heads` floats apart)
   const size_t vstep = static_cast<size_t>(heads) * dim * esz;
   const uint8_t* vbytes = static_cast<const uint8_t*>(v);
   // one output chunk per iteration (more resident threads beat more chunks per
   // thread here): the first four states' chunks and log-sum-exps are
   // requested before any is used
-  for (I j0 = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; j0 < chunks; j0 += stride) {
-    uint4 x[1][4];
-    float sc[1][4];
-    const uint8_t* vp[1];
-    const float* sp[1];
+  for (I j = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; j < chunks; j += stride) {
+    const I r = j / per_row;
+    const I i = r / static_cast<I>(heads);
+    const I hh = r - i * static_cast<I>(heads);
+    const I c = j - r * per_row;
+    // state 0 of (index i, head hh): this thread's chunk and the lse
+    const size_t row0 = static_cast<size_t>(i) * k * heads + hh;
+    const uint8_t* vp = vbytes + (row0 * dim + static_cast<size_t>(c) * ce) * esz;
+    const float* sp = s + row0;
+    uint4 x[4];
+    float sc[4];
 #pragma unroll
-    for (int u = 0; u < 1; ++u) {
-      const I j = j0 + u * stride;
-      if (j >= chunks) continue;
-      const I r = j / per_row;
-      const I i = r / static_cast<I>(heads);
-      const I hh = r - i * static_cast<I>(heads);
-      const I c = j - r * per_row;
-      // state 0 of (index i, head hh), this thread's chunk
-      const size_t row0 = static_cast<size_t>(i) * k * heads + hh;
-      vp[u] = vbytes + (row0 * dim + static_cast<size_t>(c) * ce) * esz;
-      sp[u] = s + row0;
+    for (int e = 0; e < 4; ++e) {
+      if (e < k) {
+        x[e] = *reinterpret_cast<const uint4*>(vp + e * vstep);
+        sc[e] = __ldg(sp + static_cast<size_t>(e) * heads);
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < k) M = fmaxf(M, sc[e]);
+    for (int e = 4; e < k; ++e) M = fmaxf(M, __ldg(sp + static_cast<size_t>(e) * heads));
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float L = 0.f;
+    if (M != -INFINITY) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         if (e < k) {
-          x[u][e] = *reinterpret_cast<const uint4*>(vp[u] + e * vstep);
-          sc[u][e] = __ldg(sp[u] + static_cast<size_t>(e) * heads);
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 1; ++u) {
-      const I j = j0 + u * stride;
-      if (j >= chunks) continue;
-      float M = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (e < k) M = fmaxf(M, sc[u][e]);
-      for (int c = 4; c < k; ++c) M = fmaxf(M, __ldg(sp[u] + static_cast<size_t>(c) * heads));
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float L = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (e < k) {
-            const float w = (sc[u][e] == -INFINITY) ? 0.f : ptx::ex2((sc[u][e] - M) * kLog2e);
-            const Chunk c = to_chunk(x[u][e], dtype);
-            L += w;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] += w * c.f[q];
-          }
-        }
-        // states past the fourth, in order
-        for (int c0 = 4; c0 < k; ++c0) {
-          const float scc = __ldg(sp[u] + static_cast<size_t>(c0) * heads);
-          const float w = (scc == -INFINITY) ? 0.f : ptx::ex2((scc - M) * kLog2e);
-          const Chunk c = to_chunk(*reinterpret_cast<const uint4*>(vp[u] + c0 * vstep), dtype);
+          const float w = (sc[e] == -INFINITY) ? 0.f : ptx::ex2((sc[e] - M) * kLog2e);
+          const Chunk ch = to_chunk(x[e], dtype);
           L += w;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] += w * c.f[q];
+          for (int q = 0; q < 8; ++q) acc[q] += w * ch.f[q];
         }
       }
-      const float inv = M != -INFINITY ? 1.f / L : 0.f;
-      Chunk o;
+      // states past the fourth, in order
+      for (int e = 4; e < k; ++e) {
+        const float sce = __ldg(sp + static_cast<size_t>(e) * heads);
+        const float w = (sce == -INFINITY) ? 0.f : ptx::ex2((sce - M) * kLog2e);
+        const Chunk ch = to_chunk(*reinterpret_cast<const uint4*>(vp + e * vstep), dtype);
+        L += w;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) o.f[q] = acc[q] * inv;
-      store_chunk(vo, static_cast<size_t>(j) * ce, o, dtype);
-      const I r = j / per_row;
-      if (j - r * per_row == 0) so[r] = (M == -INFINITY) ? -INFINITY : M + ptx::lg2(L) * kLn2;
+        for (int q = 0; q < 8; ++q) acc[q] += w * ch.f[q];
+      }
     }
+    const float inv = M != -INFINITY ? 1.f / L : 0.f;
+    Chunk o;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o.f[q] = acc[q] * inv;
+    store_chunk(vo, static_cast<size_t>(j) * ce, o, dtype);
+    if (c == 0) so[r] = (M == -INFINITY) ? -INFINITY : M + ptx::lg2(L) * kLn2;
   }
 }
 
@@ -466,15 +456,29 @@ __global__ void copy_words_kernel(uint4* __restrict__ dst, const uint4* __restri
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Blocks of `threads` threads of `kernel` resident on the whole GPU at once
-// (SM count x occupancy), for a grid-stride kernel sized to run in one wave.
-int64_t resident_blocks(const void* kernel, int threads) {
-  int dev = 0, sms = 0, per_sm = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess) {
-    cudaGetLastError();  // a failed query falls back to a fixed grid
+// (SM count x occupancy), for a grid-stride kernel sized to run in one wave;
+// `cache` holds the answer per device (0: not asked yet, -1: the query
+// failed, and a fixed grid is used).
+int64_t resident_blocks(const void* kernel, int threads, std::atomic<int> (&cache)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
     return 8192;
   }
-  return static_cast<int64_t>(sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+  int c = cache[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) == cudaSuccess && sms > 0 &&
+        per_sm > 0) {
+      c = sms * per_sm;
+    } else {
+      cudaGetLastError();
+      c = -1;
+    }
+    cache[dev].store(c, std::memory_order_relaxed);
+  }
+  return c > 0 ? c : 8192;
 }
 
 int grid_for_rows(int64_t rows) {
@@ -535,7 +539,8 @@ cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, 
   if (flat) {
     const int64_t chunks = rows * (dim / ce);
     const int64_t blocks = (chunks + 255) / 256;
-    const int64_t cap = resident_blocks(reinterpret_cast<const void*>(merge_state_kernel), 256);
+    static std::atomic<int> cache[64];
+    const int64_t cap = resident_blocks(reinterpret_cast<const void*>(merge_state_kernel), 256, cache);
     merge_state_kernel<<<static_cast<int>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
         va, sa, vb, sb, vo, so, rows, dim, dtype, chunks < (int64_t(1) << 31) ? 2 : 1);
   } else {
@@ -553,7 +558,8 @@ cudaError_t launch_merge_states(const void* v, const float* s, int64_t n, int k,
   if (flat) {
     const int64_t chunks = rows * (dim / ce);
     const int64_t blocks = (chunks + 255) / 256;
-    const int64_t cap = resident_blocks(reinterpret_cast<const void*>(merge_states_kernel), 256);
+    static std::atomic<int> cache[64];
+    const int64_t cap = resident_blocks(reinterpret_cast<const void*>(merge_states_kernel), 256, cache);
     merge_states_kernel<<<static_cast<int>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
         v, s, n, k, heads, dim, dtype, vo, so, chunks < (int64_t(1) << 31) ? 2 : 1);
   } else {
