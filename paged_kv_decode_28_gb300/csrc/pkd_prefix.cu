@@ -77,9 +77,12 @@ struct PCfg {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + 2 * kQHalf;
   static constexpr int kV = kK + kKStages * kKStage;
-  // e4m3 codes as loaded: K [64 keys][128 B], V [128 keys][64 B] (this CTA's dims)
+  // e4m3 codes as loaded: K [64 keys][128 B], V [128 keys][64 B] (this CTA's
+  // dims).  A copy's shared-memory destination must be 128-byte aligned, so
+  // when the boxes are single keys (odd page sizes) the V rows sit 128 bytes
+  // apart: the V slot has room for that.
   static constexpr int kK8Stage = kHalfKeys * 128;
-  static constexpr int kV8Stage = kKeys * 64;
+  static constexpr int kV8Stage = kKeys * 128;
   static constexpr int kK8 = kV + kVSt * kVStage;
   static constexpr int kV8 = kK8 + (FP8 ? kStaging * kK8Stage : 0);
   static constexpr int kBars = kV8 + (FP8 ? kStaging * kV8Stage : 0);
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
           }
         }
       };
-      // issue the boxes of tile i into dst0 (rows of row_bytes), completing on
+      // issue the boxes of tile i into dst0 (rows row_bytes apart), completing on
       // `full`; pair loads (16-bit K) signal the even CTA's barrier
       auto issue = [&](int i, const int (&pg)[4], const int (&tk)[4], uint32_t dst0, uint32_t row_bytes, uint32_t full,
                        int c0, bool pair_load) {
@@ -369,6 +372,8 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
           const uint32_t stg = base + (kside ? C::kK8 : C::kV8);
           const uint32_t stg_bytes = kside ? C::kK8Stage : C::kV8Stage;
           const uint32_t row_bytes = kside ? 128u : 64u;
+          // where the rows land: V rows of single-key boxes 128 bytes apart
+          const uint32_t row_stride = kside || box > 1 ? row_bytes : 128u;
           if (i < n) {
             const int s8 = i % kStaging;
             int first, cnt;
@@ -378,7 +383,7 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
             if (lane == 0)
               ptx::mbar_arrive_expect_tx(bar(f8 + s8), static_cast<uint32_t>((cnt + box - 1) / box * box) * row_bytes);
             __syncwarp();
-            issue(i, pg, tk, stg + s8 * stg_bytes, row_bytes, bar(f8 + s8), kside ? 0 : 64 * static_cast<int>(rank),
+            issue(i, pg, tk, stg + s8 * stg_bytes, row_stride, bar(f8 + s8), kside ? 0 : 64 * static_cast<int>(rank),
                   false);
           }
           if (i == 0) return true;
@@ -410,7 +415,7 @@ __global__ void __launch_bounds__(PCfg<FP8>::kThreads, 1)
               const int key = item >> 2, c = item & 3;
               uint32_t a[4] = {0u, 0u, 0u, 0u}, bq[4] = {0u, 0u, 0u, 0u};
               if (key < nv) {
-                const uint4 raw = *reinterpret_cast<const uint4*>(src + key * 64 + c * 16);
+                const uint4 raw = *reinterpret_cast<const uint4*>(src + key * row_stride + c * 16);
                 widen8<BF>(raw.x, raw.y, a);
                 widen8<BF>(raw.z, raw.w, bq);
               }

@@ -238,3 +238,19 @@ def test_cascade_back_to_back_without_sync():
     for i, (o, l) in enumerate(outs):
         ro, rl = refs[i % 2]
         assert torch.equal(o, ro) and torch.equal(l, rl), f"step {i} differs from the isolated run"
+
+
+@pytest.mark.parametrize("P", [1, 3, 7, 23, 33, 63])
+@pytest.mark.parametrize("q_dtype", ["bf16", "f16"])
+def test_cascade_e4m3_odd_page_sizes(P, q_dtype):
+    """Odd page sizes give single-key copy boxes in the prefix kernel: its e4m3
+    V rows (64 codes) then land 128 bytes apart, each copy's destination
+    128-byte aligned."""
+    rng = np.random.default_rng(990 + P)
+    lengths = rng.integers(0, 70, size=37).tolist()
+    b = wl.make_paged(seed=995 + P, lengths=lengths, num_qo_heads=12, num_kv_heads=4, page_size=P, q_dtype=q_dtype,
+                      kv_dtype="e4m3", prefix_len=300 + P, device="cuda")
+    out, lse = _gpu_cascade(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
