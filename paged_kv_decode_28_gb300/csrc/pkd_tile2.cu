@@ -27,13 +27,14 @@
 //               runs;
 //   warps 4..19 softmax: tile t = (warp - 4) / 8, key half hf =
 //               ((warp - 4) / 4) % 2, TMEM lane quarter warp % 4; two threads
-//               per query row, each reading its 64 scores of a tile twice:
-//               first for the row maximum (swapped with the row's other half
-//               through shared memory), then again to form, sixteen keys at a time,
-//               P = 2^(s * scale_log2 - m), written as two 16-bit parts (P_hi
-//               = round(P), P_lo = round(P - P_hi)) over the columns just
-//               read.  O is rescaled in TMEM only when the row maximum grows
-//               by more than 8 in log2 units (exact either way).
+//               per query row, each reading its 64 scores of a tile from TMEM
+//               once and keeping them in registers: first the row maximum
+//               (swapped with the row's other half through shared memory),
+//               then, sixteen keys at a time and two scores per two-wide fp32
+//               instruction, P = 2^(s * scale_log2 - m), written as two 16-bit
+//               parts (P_hi = round(P), P_lo = round(P - P_hi)) over the
+//               columns read.  O is rescaled in TMEM only when the row
+//               maximum grows by more than 8 in log2 units (exact either way).
 // TMEM columns: O_A [0,128), O_B [128,256), S_A [256,384), S_B [384,512).
 // P of a tile's keys 16k .. 16k + 15 (k = 0..7): P_hi of keys 16k + 2e and
 // 16k + 2e + 1 in column 16k + e, P_lo in column 16k + 8 + e (e = 0..7).
@@ -76,6 +77,23 @@ constexpr int kAlloc = kTotal + 1024;
 static_assert(kAlloc <= 227 * 1024, "dynamic shared memory above the 227 KB a CTA may use");
 
 constexpr uint32_t kTmemCols = 512;
+
+// 32 lanes x 16 consecutive 32-bit columns -> 16 registers per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+               : "r"(taddr));
+}
+
+// Registers just written by tcgen05.ld, redefined after tcgen05.wait::ld so
+// that no use of them is scheduled before the wait.
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; i += 8)
+    asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]),
+                 "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
 __device__ __forceinline__ uint32_t col_o(int t) { return static_cast<uint32_t>(t) * 128u; }
 __device__ __forceinline__ uint32_t col_s(int t) { return 256u + static_cast<uint32_t>(t) * 128u; }
 
@@ -349,26 +367,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vrow = diag == kNoCausal ? nv : max(0, min(nv, tok + diag + 1 - key0));
         const int vr = min(max(vrow - 64 * hf, 0), 64);
         // the maximum of the raw scores (the scale is positive, so it commutes
-        // with max): 8 independent chains, then the other half's
-        float m8[8];
+        // with max): 4 independent chains of three-way maxima, then the other half's
+        float m4[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
+        for (int e = 0; e < 4; ++e) m4[e] = -INFINITY;
+        uint32_t sr[64];  // this half's 64 scores, both chunks in one round trip, kept for P
         if (ok) {
           ptx::tc_fence_after();
-          uint32_t sr[64];  // both chunks in one round trip
           ptx::tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
           ptx::tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
           ptx::tmem_ld_wait();
+          ptx::reg_fence32(&sr[0]);
+          ptx::reg_fence32(&sr[32]);
           if (vr < 64) {
 #pragma unroll
             for (int e = 0; e < 64; ++e)
               if (e >= vr) sr[e] = __float_as_uint(-INFINITY);
           }
 #pragma unroll
-          for (int e = 0; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sr[e]));
+          for (int e = 0; e < 32; ++e)
+            m4[e & 3] = ptx::fmax3(m4[e & 3], __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
         }
-        const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        const float mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         // one barrier per tile: tile i uses buffer i % 2, and a half writes
         // that buffer again (tile i + 2) only after passing tile i + 1's
         // barrier, which its partner reaches after reading tile i's value
@@ -387,14 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::tc_fence_after();
           const float alpha = need ? ptx::ex2(m_ref - mx) : 1.f;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o[32];
-            ptx::tmem_ld32(ocol + 32 * c, o);
+          // sixteen columns at a time: the scores stay in registers meanwhile
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[16];
+            tmem_ld16(ocol + 16 * c, o);
             ptx::tmem_ld_wait();
+            reg_fence16(o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            ptx::tmem_st32(ocol + 32 * c, o);
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st16(ocol + 16 * c, o);
           }
           ptx::tmem_st_wait();
           if (need) {
@@ -403,35 +425,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // P over the scores, sixteen keys at a time: P_hi of the block's keys
-        // in its first 8 columns, P_lo in the last 8
-        float rs[8];
+        // in its first 8 columns, P_lo in the last 8; pairs of scores go
+        // through the two-wide fp32 instructions (scale and shift, sums,
+        // residuals)
+        const uint64_t sl2x2 = ptx::f2pack(sl2, sl2), negm = ptx::f2pack(-m_ref, -m_ref);
+        uint64_t rs2[2];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) rs[e] = 0.f;
+        for (int e = 0; e < 2; ++e) rs2[e] = ptx::f2pack(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t sr[32];
-          ptx::tmem_ld32(scol + 32 * c, sr);
-          ptx::tmem_ld_wait();
-          const int vc = vr - 32 * c;
-          if (vc < 32) {
+        for (int bk = 0; bk < 4; ++bk) {
+          uint32_t pp[16];  // P_hi pairs, then P_lo pairs
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (e >= vc) sr[e] = __float_as_uint(-INFINITY);
-          }
-#pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            uint32_t pp[16];  // P_hi pairs, then P_lo pairs
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[16 * b + 2 * e]), sl2, -m_ref));
-              const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[16 * b + 2 * e + 1]), sl2, -m_ref));
-              rs[e] += p0 + p1;
-              ptx::split2<BF>(p0, p1, pp[e], pp[8 + e]);
+          for (int e = 0; e < 8; ++e) {
+            const uint64_t x = ptx::f2fma(ptx::f2pack(__uint_as_float(sr[16 * bk + 2 * e]),
+                                                      __uint_as_float(sr[16 * bk + 2 * e + 1])),
+                                          sl2x2, negm);
+            float x0, x1;
+            ptx::f2unpack(x, x0, x1);
+            const uint64_t pv = ptx::f2pack(ptx::ex2(x0), ptx::ex2(x1));
+            rs2[e & 1] = ptx::f2add(rs2[e & 1], pv);
+            if constexpr (BF) {
+              ptx::split2_bf16_packed(pv, pp[e], pp[8 + e]);
+            } else {
+              float q0, q1;
+              ptx::f2unpack(pv, q0, q1);
+              ptx::split2<false>(q0, q1, pp[e], pp[8 + e]);
             }
-            ptx::tmem_st16(scol + 32 * c + 16 * b, pp);
           }
+          ptx::tmem_st16(scol + 16 * bk, pp);
         }
-        l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+        {
+          float a0, a1, b0s, b1s;
+          ptx::f2unpack(rs2[0], a0, a1);
+          ptx::f2unpack(rs2[1], b0s, b1s);
+          l += (a0 + a1) + (b0s + b1s);
+        }
         if (t == 0 && nv < kKeys) {
           // keys past the list's end: their P is 0, and their V rows must be
           // finite for both tiles' products, so tile A's threads zero them
