@@ -68,6 +68,25 @@ def test_lone_tiles_split_over_key_tiles(g):
         assert_lse_close(lse, l_ref, what=f"causal={causal}")
 
 
+def test_prefill_growing_scores():
+    """Keys whose norm grows page by page along each sequence, so a row's
+    running maximum rises by more than the lazy-rescale threshold many times
+    over its key tiles (O rescaled in TMEM between products), causal and not,
+    bf16 and f16."""
+    for dt in ("bf16", "f16"):
+        b = wl.make_prefill(seed=1290, q_lens=[40, 130, 7, 256], kv_lens=[700, 520, 900, 300], num_qo_heads=8,
+                            num_kv_heads=2, page_size=16, q_dtype=dt, kv_dtype=dt, device="cuda")
+        ip = b.kv_indptr
+        for r in range(len(ip) - 1):
+            for pos, pid in enumerate(b.kv_page_indices[ip[r]:ip[r + 1]].tolist()):
+                b.k_cache[pid] *= 1.0 + 0.25 * pos
+        for causal in (True, False):
+            out, lse = _gpu_prefill(b, causal)
+            o_ref, l_ref = _oracle(b, causal)
+            assert_o_close(out, o_ref, what=f"{dt} causal={causal}")
+            assert_lse_close(lse, l_ref, what=f"{dt} causal={causal}")
+
+
 def test_prefill_f16_and_hnd():
     from tests.test_gpu_hnd import to_hnd
 

@@ -63,6 +63,24 @@ def test_tree_matches_oracle(P, g):
     assert_lse_close(lse, l_ref)
 
 
+def test_tree_growing_scores():
+    """A root whose keys grow in norm page by page, so the shared level's
+    running maximum rises by more than the lazy-rescale threshold many times
+    within one key-range piece (O rescaled in TMEM), next to branches and
+    own pages of ordinary scale."""
+    b = _tree(1160, 16, 4)
+    ri, ki, idx, last = b.levels[0]
+    for pos, pid in enumerate(np.asarray(idx)[ki[0]:ki[1]].tolist()):
+        b.k_cache[pid] *= 1.0 + 0.5 * pos
+    # one key-range piece per level (three levels), so the root's three key
+    # tiles run in one CTA
+    plan = pkd.Plan(b.batch, b.num_qo_heads, b.num_kv_heads, max_prefix_splits=3)
+    out, lse = _gpu_tree(b, plan=plan)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref)
+    assert_lse_close(lse, l_ref)
+
+
 def test_tree_f16_and_one_level():
     b = _tree(1150, 16, 4, q_dtype="f16")
     out, lse = _gpu_tree(b)
