@@ -94,6 +94,26 @@ def test_tree_f16_and_one_level():
     assert_lse_close(lse, l_ref)
 
 
+@pytest.mark.parametrize("root", ["two nodes", "no keys", "no own pages"])
+def test_tree_root_variants(root):
+    """Root levels of other shapes: a first level of two nodes, a batch-wide
+    root without keys (a level of empty states), and a batch-wide root over
+    requests without own pages (no decode grid: the tree kernel and the merge
+    alone)."""
+    B = 13
+    rng = np.random.default_rng(1170)
+    lengths = rng.integers(0, 150, size=B).tolist()
+    lv0 = ([6, 7], [300, 200]) if root == "two nodes" else ([B], [0 if root == "no keys" else 300])
+    if root == "no own pages":
+        lengths = [0] * B
+    b = wl.make_tree(seed=1170, levels=[lv0, ([5, 0, 8], [129, 7, 64])], lengths=lengths, num_qo_heads=8,
+                     num_kv_heads=2, page_size=16, device="cuda")
+    out, lse = _gpu_tree(b)
+    o_ref, l_ref = _oracle(b)
+    assert_o_close(out, o_ref, what=root)
+    assert_lse_close(lse, l_ref, what=root)
+
+
 def test_tree_with_empty_level_and_many_query_tiles():
     """300 requests x g = 8 rows: a node spans several 128-row tiles, and a
     level whose nodes have no keys merges as the identity."""
