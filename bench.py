@@ -60,7 +60,7 @@ def parse_args():
     ap.add_argument("--all-configs", action="store_true", help="also print one line per standard workload")
     ap.add_argument("--batch", type=int, default=None,
                     help="shrink the workload to its first N requests (small cases for profiling)")
-    ap.add_argument("--op", choices=["decode", "append", "tree", "prefill", "mla", "merge"], default="decode",
+    ap.add_argument("--op", choices=["decode", "append", "tree", "prefill", "mla", "merge", "single"], default="decode",
                     help="append: pkd_append_kv (new tokens written into the workload's pool); tree: "
                     "prefix-tree decode on the 3-level tree workload; prefill: append-prefill attention; mla: MLA "
                     "decode; merge: the standalone pkd_merge_state / pkd_merge_states on cascade-shaped states")
@@ -1040,6 +1040,58 @@ def run_merge(args):
             "roofline": {"bound": "hbm", "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", **res}}
 
 
+def run_single(args):
+    """One request through pkd_single_decode (q [32, 128], contiguous f16 K/V
+    [2048, 32, 128]: the single-request workload's shape): host plan, the
+    schedule in the upload kernel's parameters and the decode, K back-to-back
+    calls timed with CUDA events.  The calls rotate over enough input copies
+    (4 x L2 in all) that every call reads its K/V from HBM."""
+    import torch
+
+    import paged_kv_decode_28_gb300 as pkd
+    from paged_kv_decode_28_gb300 import _build
+
+    _build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(21)
+    L, Hq, Hk, D = 2048, 32, 32, 128
+    nbytes = 2 * L * Hk * D * 2 + 2 * Hq * D * 2 + Hq * 4
+    R = max(1, int(math.ceil(4 * l2_bytes(dev) / nbytes)))
+    inputs = [(torch.randn((Hq, D), generator=gen, device=dev).half(),
+               torch.randn((L, Hk, D), generator=gen, device=dev).half(),
+               torch.randn((L, Hk, D), generator=gen, device=dev).half()) for _ in range(R)]
+    ws = torch.empty(pkd.workspace_bytes(1, Hq, Hk, D, pkd.num_ctas(0), 0), dtype=torch.uint8, device=dev)
+    for i in range(max(args.warmup, 3)):
+        pkd.single_decode(*inputs[i % R], workspace=ws)
+    torch.cuda.synchronize()
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clocks:
+        e0.record()
+        for i in range(K):
+            pkd.single_decode(*inputs[i % R], workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+    clk = clocks.summary()
+    ms = e0.elapsed_time(e1) / K
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    return {"metric": "single-request decode (pkd_single_decode): achieved HBM GB/s per call",
+            "value": round(achieved, 1), "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": max(args.warmup, 3),
+            "ms_per_step": round(ms, 5), "us_per_call": round(ms * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic (seeded N(0,1) values)",
+            "config": {"workload": f"one request, {L} keys, {Hq}/{Hk} heads, f16, contiguous K/V",
+                       "bytes_per_call": nbytes, "input_copies": R,
+                       "l2": f"{R} input copies ({R * nbytes / 1e6:.0f} MB) used in turn", "parallelism": "one GPU"},
+            "roofline": {"bound": "hbm", "kernel": "whole call (host plan, schedule upload kernel, decode)",
+                         "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None},
+            "cpu_baseline": None, "gpu_launches": 2 * K, "clocks": clk}
+
+
 def main():
     args = parse_args()
     world, rank = launch_world()
@@ -1053,9 +1105,9 @@ def main():
               "its cascade and MLA kernels use cluster-multicast loads that stay within one GPU's memory",
               file=sys.stderr, flush=True)
         sys.exit(2)
-    if args.op in ("append", "tree", "prefill", "mla", "merge"):
+    if args.op in ("append", "tree", "prefill", "mla", "merge", "single"):
         line = {"append": run_append, "tree": run_tree, "prefill": run_prefill, "mla": run_mla,
-                "merge": run_merge}[args.op](args)
+                "merge": run_merge, "single": run_single}[args.op](args)
         print(json.dumps(line), flush=True)
         return
     if args.impl == "reference":
