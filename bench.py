@@ -1063,15 +1063,17 @@ def run_single(args):
                torch.randn((L, Hk, D), generator=gen, device=dev).half(),
                torch.randn((L, Hk, D), generator=gen, device=dev).half()) for _ in range(R)]
     ws = torch.empty(pkd.workspace_bytes(1, Hq, Hk, D, pkd.num_ctas(0), 0), dtype=torch.uint8, device=dev)
+    out = torch.empty((Hq, D), dtype=torch.float16, device=dev)
+    lse = torch.empty(Hq, dtype=torch.float32, device=dev)
     for i in range(max(args.warmup, 3)):
-        pkd.single_decode(*inputs[i % R], workspace=ws)
+        pkd.single_decode(*inputs[i % R], workspace=ws, out=out, lse=lse)
     torch.cuda.synchronize()
     K = args.steps
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clocks:
         e0.record()
         for i in range(K):
-            pkd.single_decode(*inputs[i % R], workspace=ws)
+            pkd.single_decode(*inputs[i % R], workspace=ws, out=out, lse=lse)
         e1.record()
         torch.cuda.synchronize()
     clk = clocks.summary()

@@ -131,11 +131,17 @@ def version() -> str:
     return lib().pkd_version().decode()
 
 
+_num_ctas = {}  # per device: the SM count times the decode kernel's CTAs per SM, fixed for a device
+
+
 def num_ctas(device: Optional[int] = None) -> int:
     dev = torch.cuda.current_device() if device is None else int(device)
-    out = ctypes.c_int(0)
-    _check(lib().pkd_num_ctas(dev, ctypes.byref(out)))
-    return out.value
+    n = _num_ctas.get(dev)
+    if n is None:
+        out = ctypes.c_int(0)
+        _check(lib().pkd_num_ctas(dev, ctypes.byref(out)))
+        n = _num_ctas[dev] = out.value
+    return n
 
 
 def workspace_bytes(max_batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int = 128,
@@ -542,21 +548,32 @@ def mla_decode(q_nope: torch.Tensor, q_pe: torch.Tensor, ckv_cache: torch.Tensor
     return out, lse, workspace
 
 
+_single_ws = {}  # (device, Hq, Hk, D) -> workspace bytes of a one-request plan
+
+
 def single_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, sm_scale: Optional[float] = None,
-                  k_scale=None, v_scale=None, workspace: Optional[torch.Tensor] = None, stream=None):
-    """Quickstart call: q ``[Hq, D]``, contiguous K/V ``[kv_len, Hk, D]`` -> ``(o [Hq, D], lse [Hq])``."""
+                  k_scale=None, v_scale=None, workspace: Optional[torch.Tensor] = None,
+                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, stream=None):
+    """Quickstart call: q ``[Hq, D]``, contiguous K/V ``[kv_len, Hk, D]`` -> ``(o [Hq, D], lse [Hq])``
+    (into ``out`` / ``lse`` when given)."""
     if q.dim() != 2 or k.dim() != 3 or k.shape != v.shape:
         raise ValueError("q [Hq, D] and k, v [kv_len, Hk, D] expected")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
     Hq, D = q.shape
     L, Hk, _ = k.shape
-    G = num_ctas(q.device.index)
-    nbytes = workspace_bytes(1, Hq, Hk, D, G, 0)
+    key = (q.device.index, Hq, Hk, D)
+    nbytes = _single_ws.get(key)
+    if nbytes is None:
+        nbytes = _single_ws[key] = workspace_bytes(1, Hq, Hk, D, num_ctas(q.device.index), 0)
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    out = torch.empty_like(q)
-    lse = torch.empty(Hq, dtype=torch.float32, device=q.device)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(Hq, dtype=torch.float32, device=q.device) if lse is None else lse
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of q's shape and dtype")
+    if lse.shape != (Hq,) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [Hq]")
     _check(lib().pkd_single_decode(_ptr(q), _ptr(k), _ptr(v), L, Hq, Hk, D, _DTYPE_CODE[q.dtype],
                                    _DTYPE_CODE[k.dtype], _ptr(k_scale), _ptr(v_scale), float(sm_scale or 0.0),
                                    _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)))

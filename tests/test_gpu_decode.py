@@ -118,6 +118,27 @@ def test_single_decode_quickstart():
     assert_lse_close(lse, l_ref)
 
 
+def test_single_decode_into_given_outputs():
+    """out / lse given: written in place, two calls in a row with different
+    inputs; wrong output shapes are refused."""
+    g = torch.Generator(device="cuda").manual_seed(2)
+    out = torch.full((32, 128), float("nan"), device="cuda").half()
+    lse = torch.full((32,), float("nan"), device="cuda")
+    for L in (300, 77):
+        q = torch.randn(32, 128, device="cuda", generator=g).half()
+        k = torch.randn(L, 8, 128, device="cuda", generator=g).half()
+        v = torch.randn(L, 8, 128, device="cuda", generator=g).half()
+        o, s = pkd.single_decode(q, k, v, out=out, lse=lse)
+        assert o.data_ptr() == out.data_ptr() and s.data_ptr() == lse.data_ptr()
+        o_ref, l_ref = orc.single_decode(q, k, v)
+        assert_o_close(out, o_ref)
+        assert_lse_close(lse, l_ref)
+    with pytest.raises(ValueError):
+        pkd.single_decode(q, k, v, out=torch.empty(16, 128, device="cuda").half())
+    with pytest.raises(ValueError):
+        pkd.single_decode(q, k, v, lse=torch.empty(32, device="cuda").half())
+
+
 @pytest.mark.parametrize("L", [0, 1, 63, 64, 65, 100, 1000])
 def test_single_decode_lengths_gqa(L):
     g = torch.Generator(device="cuda").manual_seed(L)
